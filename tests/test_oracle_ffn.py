@@ -1,0 +1,110 @@
+"""Pins of the oracle's expert FFN, combine and INT4 dequantisation: a worked
+example, an independent library computation (torch fp64), algebraic
+invariants and a closed form.  CPU only."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from conftest import read_golden
+
+
+def _vec(s):
+    return np.array([float(v) for v in s.split()], np.float64)
+
+
+def test_swiglu_worked_example():
+    g = read_golden("swiglu_hand.txt")
+    x = _vec(g["x"])
+    wg = _vec(g["w_gate"]).reshape(2, 3)
+    wu = _vec(g["w_up"]).reshape(2, 3)
+    wd = _vec(g["w_down"]).reshape(3, 2)
+    y = oracle.expert_ffn(x, wg, wu, wd)
+    assert np.allclose(y, _vec(g["y"]), rtol=0, atol=1e-15)
+
+
+def torch_expert(x, wg, wu, wd):
+    """The same expert through torch's fp64 matmul and SiLU (a library routine)."""
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    h = torch.nn.functional.silu(t(wg) @ t(x)) * (t(wu) @ t(x))
+    return (t(wd) @ h).numpy()
+
+
+@pytest.mark.parametrize("d,F", [(8, 5), (64, 128), (96, 40)])
+def test_expert_matches_library_fp64(d, F):
+    rng = np.random.default_rng(d * F)
+    x = rng.standard_normal(d).astype(np.float32)
+    wg, wu = (rng.standard_normal((2, F, d)) / np.sqrt(d)).astype(np.float32)
+    wd = (rng.standard_normal((d, F)) / np.sqrt(F)).astype(np.float32)
+    y = oracle.expert_ffn(x, wg, wu, wd)
+    ref = torch_expert(x, wg, wu, wd)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_expert_algebra():
+    """Linear in W_down and in W_up, not in W_gate; invariant under a shared
+    permutation of the hidden units; W_down = I gives silu(g) * u."""
+    rng = np.random.default_rng(1)
+    d, F = 24, 24
+    x = rng.standard_normal(d).astype(np.float32)
+    wg, wu = rng.standard_normal((2, F, d)).astype(np.float32) * 0.2
+    wd = rng.standard_normal((d, F)).astype(np.float32) * 0.2
+    y = oracle.expert_ffn(x, wg, wu, wd)
+    assert np.allclose(oracle.expert_ffn(x, wg, wu * 2, wd), 2 * y, rtol=1e-12, atol=1e-14)
+    assert np.allclose(oracle.expert_ffn(x, wg, wu, wd * 4), 4 * y, rtol=1e-12, atol=1e-14)
+    assert not np.allclose(oracle.expert_ffn(x, wg * 2, wu, wd), 2 * y, rtol=1e-3)
+    pf = rng.permutation(F)
+    assert np.allclose(oracle.expert_ffn(x, wg[pf], wu[pf], wd[:, pf]), y, rtol=1e-12, atol=1e-14)
+    g = wg.astype(np.float64) @ x
+    u = wu.astype(np.float64) @ x
+    eye = np.eye(d, dtype=np.float32)
+    closed = g / (1.0 + np.exp(-g)) * u
+    assert np.allclose(oracle.expert_ffn(x, wg, wu, eye), closed, rtol=1e-12, atol=1e-14)
+
+
+def test_combine_is_weighted_sum_in_slot_order():
+    """out_i = sum_j w_ij y_{e_ij}(x_i) (kept, renormalised scores weight the
+    expert outputs; OEA page, section 2 Q2); unused slots (-1) add nothing."""
+    rng = np.random.default_rng(2)
+    B, N, d, F = 3, 5, 16, 12
+    x = rng.standard_normal((B, d)).astype(np.float32)
+    wg, wu = rng.standard_normal((2, N, F, d)).astype(np.float32) * 0.3
+    wd = rng.standard_normal((N, d, F)).astype(np.float32) * 0.3
+    idx = np.array([[4, 0, -1], [1, 1, 2], [3, -1, -1]], np.int32)
+    w = np.array([[0.7, 0.3, 0.0], [0.5, 0.25, 0.25], [1.0, 0.0, 0.0]])
+    out = oracle.moe_experts(x, wg, wu, wd, idx, w)
+    for i in range(B):
+        ref = np.zeros(d)
+        for j in range(3):
+            if idx[i, j] >= 0:
+                e = idx[i, j]
+                ref += w[i, j] * torch_expert(x[i], wg[e], wu[e], wd[e])
+        assert np.allclose(out[i], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_router_logits_match_library():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((7, 40)).astype(np.float32)
+    wr = rng.standard_normal((9, 40)).astype(np.float32)
+    b = rng.standard_normal(9).astype(np.float32)
+    lg = oracle.router_logits(x, wr, b)
+    ref = (torch.from_numpy(x.astype(np.float64)) @ torch.from_numpy(wr.astype(np.float64)).T
+           + torch.from_numpy(b.astype(np.float64))).numpy()
+    assert np.allclose(lg, ref, rtol=1e-13, atol=1e-13)
+    assert np.allclose(oracle.router_logits(x, wr), ref - b, rtol=1e-13, atol=1e-13)
+
+
+def test_dequant_int4_codes_and_layout():
+    """Every code -8..7 in both nibble positions, two groups with their own
+    scale: w = q * s (DynaExq page, section 3.2, INT4 tier)."""
+    rows, cols, group = 2, 256, 128
+    q = np.tile(np.arange(-8, 8), cols // 16 * rows).reshape(rows, cols)
+    q[1] = q[1][::-1]
+    nib = (q & 0xF).astype(np.uint8)
+    packed = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    s = np.array([[0.5, 2.0], [0.25, 1.5]], np.float32)
+    sbits = synth.to_bf16_bits(s)
+    out = oracle.dequant_int4(packed, sbits, rows, cols, group)
+    want = q * np.repeat(s, group, axis=1)
+    assert np.array_equal(out, want.astype(np.float32))
