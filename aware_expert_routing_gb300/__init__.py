@@ -1,0 +1,248 @@
+"""Python binding of the OEA MoE decode-layer library (libaware_moe.so).
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  PyTorch supplies device memory (tensors) and streams; the
+functions below take torch tensors, check dtypes/devices, and pass raw
+pointers to the C ABI declared in include/moe.h under the same names.
+
+There is no fallback: if the shared library is missing or fails to load,
+importing the functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libaware_moe.so")
+
+MOE_OK, MOE_ERR_ARG, MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_WORKSPACE, MOE_ERR_UNSUPPORTED = range(6)
+MODE_TOPK, MODE_OEA = 0, 1
+DTYPE_BF16, DTYPE_F32 = 0, 1
+FLAG_NONFINITE_SCORE, FLAG_WAIT_TIMEOUT, FLAG_BAD_INDEX = 0x1, 0x2, 0x4
+MAX_TOKENS, MAX_EXPERTS, MAX_SLOTS = 256, 1024, 32
+
+EXPORTED = ["moe_num_slots", "moe_workspace_bytes", "moe_route", "moe_expert_ffn",
+            "moe_decode_layer", "moe_device_status", "moe_synth_normal",
+            "moe_status_string", "moe_last_error"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: status {status}: {detail}")
+        self.status = status
+
+
+class _Params(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("B_valid", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("N", ctypes.c_int32), ("k", ctypes.c_int32), ("mode", ctypes.c_int32),
+                ("k0", ctypes.c_int32), ("p", ctypes.c_float), ("maxP", ctypes.c_int32),
+                ("kmax", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class _Routing(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("expert_idx", "weights", "T", "active", "counts", "offsets", "perm",
+                 "n_base", "logits")]
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load the shared library (once).  Raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"{p} is missing: build it with aware_expert_routing_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    V, P = ctypes.c_void_p, ctypes.POINTER
+    lib.moe_num_slots.argtypes = [P(_Params)]
+    lib.moe_num_slots.restype = ctypes.c_int32
+    lib.moe_workspace_bytes.argtypes = [P(_Params), ctypes.c_int32]
+    lib.moe_workspace_bytes.restype = ctypes.c_size_t
+    lib.moe_route.argtypes = [V, V, V, P(_Params), P(_Routing), V, ctypes.c_size_t, V]
+    lib.moe_route.restype = ctypes.c_int
+    lib.moe_expert_ffn.argtypes = [V, V, V, V, ctypes.c_int32, P(_Params), P(_Routing), V, V,
+                                   ctypes.c_size_t, V]
+    lib.moe_expert_ffn.restype = ctypes.c_int
+    lib.moe_decode_layer.argtypes = [V, V, V, V, V, V, ctypes.c_int32, P(_Params), P(_Routing), V,
+                                     V, ctypes.c_size_t, V]
+    lib.moe_decode_layer.restype = ctypes.c_int
+    lib.moe_device_status.argtypes = [V, V, P(ctypes.c_uint32)]
+    lib.moe_device_status.restype = ctypes.c_int
+    lib.moe_synth_normal.argtypes = [V, ctypes.c_int32, ctypes.c_uint64, ctypes.c_uint64,
+                                     ctypes.c_uint64, ctypes.c_float, V]
+    lib.moe_synth_normal.restype = ctypes.c_int
+    lib.moe_status_string.argtypes = [ctypes.c_int]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_last_error.argtypes = []
+    lib.moe_last_error.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+@dataclasses.dataclass
+class RouteParams:
+    """Mirror of moe_route_params (include/moe.h)."""
+    B: int
+    d: int
+    N: int
+    k: int
+    mode: int = MODE_TOPK
+    k0: int = 0
+    p: float = 1.0
+    maxP: int = 0
+    kmax: int = 0
+    B_valid: int = -1
+    dtype: int = DTYPE_BF16
+
+    def c(self) -> _Params:
+        return _Params(self.B, self.B_valid, self.d, self.N, self.k, self.mode,
+                       self.k0 if self.mode == MODE_OEA else self.k, self.p, self.maxP,
+                       self.kmax, self.dtype)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == DTYPE_BF16 else torch.float32
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        lib = load()
+        raise MoeError(status, where, lib.moe_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def moe_num_slots(params: RouteParams) -> int:
+    n = load().moe_num_slots(ctypes.byref(params.c()))
+    if n < 0:
+        raise MoeError(MOE_ERR_ARG, "moe_num_slots", load().moe_last_error().decode())
+    return n
+
+
+def moe_workspace_bytes(params: RouteParams, d_ff: int = 0) -> int:
+    n = load().moe_workspace_bytes(ctypes.byref(params.c()), d_ff)
+    if n == 0:
+        raise MoeError(MOE_ERR_ARG, "moe_workspace_bytes", load().moe_last_error().decode())
+    return n
+
+
+def alloc_workspace(params: RouteParams, d_ff: int, device) -> torch.Tensor:
+    """A zero-filled workspace tensor of the required size (torch allocates
+    with at least 256-byte alignment)."""
+    return torch.zeros(moe_workspace_bytes(params, d_ff), dtype=torch.uint8, device=device)
+
+
+class Routing:
+    """Device buffers of moe_routing, allocated with torch."""
+
+    def __init__(self, params: RouteParams, device, with_logits: bool = False,
+                 with_n_base: bool = True):
+        B, N = params.B, params.N
+        ks = moe_num_slots(params)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.kslots = ks
+        self.expert_idx = torch.empty(B, ks, **i32)
+        self.weights = torch.empty(B, ks, dtype=torch.float32, device=device)
+        self.T = torch.empty(1, **i32)
+        self.active = torch.empty(N, **i32)
+        self.counts = torch.empty(N, **i32)
+        self.offsets = torch.empty(N + 1, **i32)
+        self.perm = torch.empty(max(B * ks, 1), **i32)
+        self.n_base = torch.empty(max(B, 1), **i32) if with_n_base else None
+        self.logits = torch.empty(B, N, dtype=torch.float32, device=device) if with_logits else None
+
+    def c(self) -> _Routing:
+        return _Routing(*[_ptr(getattr(self, n)) for n in
+                          ("expert_idx", "weights", "T", "active", "counts", "offsets", "perm",
+                           "n_base", "logits")])
+
+
+def _need(t, dtype, name):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}")
+
+
+def moe_route(hidden, w_router, router_bias, params: RouteParams, routing: Routing,
+              workspace: torch.Tensor, stream=None):
+    dt = params.torch_dtype
+    _need(hidden, dt, "hidden")
+    _need(w_router, dt, "w_router")
+    if router_bias is not None:
+        _need(router_bias, torch.float32, "router_bias")
+    st = load().moe_route(_ptr(hidden), _ptr(w_router), _ptr(router_bias), ctypes.byref(params.c()),
+                          ctypes.byref(routing.c()), _ptr(workspace), workspace.numel(),
+                          _stream(stream))
+    _check(st, "moe_route")
+    return routing
+
+
+def moe_expert_ffn(hidden, w_gate, w_up, w_down, d_ff: int, params: RouteParams, routing: Routing,
+                   out, workspace: torch.Tensor, stream=None):
+    dt = params.torch_dtype
+    for t, n in ((hidden, "hidden"), (w_gate, "w_gate"), (w_up, "w_up"), (w_down, "w_down"),
+                 (out, "out")):
+        _need(t, dt, n)
+    st = load().moe_expert_ffn(_ptr(hidden), _ptr(w_gate), _ptr(w_up), _ptr(w_down), d_ff,
+                               ctypes.byref(params.c()), ctypes.byref(routing.c()), _ptr(out),
+                               _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "moe_expert_ffn")
+    return out
+
+
+def moe_decode_layer(hidden, w_router, router_bias, w_gate, w_up, w_down, d_ff: int,
+                     params: RouteParams, routing: Routing, out, workspace: torch.Tensor,
+                     stream=None):
+    dt = params.torch_dtype
+    for t, n in ((hidden, "hidden"), (w_router, "w_router"), (w_gate, "w_gate"), (w_up, "w_up"),
+                 (w_down, "w_down"), (out, "out")):
+        _need(t, dt, n)
+    if router_bias is not None:
+        _need(router_bias, torch.float32, "router_bias")
+    st = load().moe_decode_layer(_ptr(hidden), _ptr(w_router), _ptr(router_bias), _ptr(w_gate),
+                                 _ptr(w_up), _ptr(w_down), d_ff, ctypes.byref(params.c()),
+                                 ctypes.byref(routing.c()), _ptr(out), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(st, "moe_decode_layer")
+    return out
+
+
+def moe_device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream; returns and clears the device flag word."""
+    f = ctypes.c_uint32(0)
+    load().moe_device_status(_ptr(workspace), _stream(stream), ctypes.byref(f))
+    return int(f.value)
+
+
+def moe_synth_normal(dst: torch.Tensor, seed: int, scale: float, start: int = 0, stream=None):
+    """Fill `dst` (bf16 or fp32) with the seeded synthetic stream."""
+    if dst.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif dst.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise ValueError("dst must be bf16 or fp32")
+    if not dst.is_cuda or not dst.is_contiguous():
+        raise ValueError("dst must be a contiguous CUDA tensor")
+    st = load().moe_synth_normal(_ptr(dst), dt, dst.numel(), start, seed & ((1 << 64) - 1),
+                                 ctypes.c_float(scale), _stream(stream))
+    _check(st, "moe_synth_normal")
+    return dst

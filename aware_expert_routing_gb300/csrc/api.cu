@@ -1,0 +1,369 @@
+// api.cu -- the C ABI declared in include/moe.h: argument checks, workspace
+// layout, TMA descriptor encoding and the launch sequence of the layer.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+
+namespace moe {
+size_t ffn_bf16_smem_bytes();
+}
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+moe_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct Params {
+    int B, B_valid, d, N, k, mode, k0, maxP, kmax, kslots, dtype;
+    float p;
+};
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status resolve(const moe_route_params* in, Params& P) {
+    if (!in) return fail(MOE_ERR_ARG, "params is NULL");
+    P.B = in->B;
+    P.B_valid = in->B_valid < 0 ? in->B : in->B_valid;
+    P.d = in->d;
+    P.N = in->N;
+    P.k = in->k;
+    P.mode = in->mode;
+    P.dtype = in->dtype;
+    P.k0 = in->k0;
+    P.p = in->p;
+    if (P.B < 0 || P.B > MOE_MAX_TOKENS) return fail(MOE_ERR_ARG, "B=%d outside 0..%d", P.B, MOE_MAX_TOKENS);
+    if (P.B_valid > P.B) return fail(MOE_ERR_ARG, "B_valid=%d > B=%d", P.B_valid, P.B);
+    if (P.d < 64 || P.d % 64 != 0 || P.d > 16384)
+        return fail(MOE_ERR_ARG, "d=%d must be a multiple of 64 in 64..16384", P.d);
+    if (P.N < 1 || P.N > MOE_MAX_EXPERTS) return fail(MOE_ERR_ARG, "N=%d outside 1..%d", P.N, MOE_MAX_EXPERTS);
+    const int slot_cap = P.N < MOE_MAX_SLOTS ? P.N : MOE_MAX_SLOTS;
+    if (P.k < 1 || P.k > slot_cap) return fail(MOE_ERR_ARG, "k=%d outside 1..%d", P.k, slot_cap);
+    if (P.dtype != MOE_DTYPE_BF16 && P.dtype != MOE_DTYPE_F32) return fail(MOE_ERR_ARG, "unknown dtype %d", P.dtype);
+    if (P.mode == MOE_MODE_TOPK) {
+        P.k0 = P.k;
+        P.p = 1.f;
+        P.maxP = P.N;
+        P.kmax = P.k;
+        P.kslots = P.k;
+    } else if (P.mode == MOE_MODE_OEA) {
+        if (P.k0 < 1 || P.k0 > P.k) return fail(MOE_ERR_ARG, "k0=%d outside 1..k=%d", P.k0, P.k);
+        if (!(P.p > 0.f) || !(P.p <= 1.f)) return fail(MOE_ERR_ARG, "p=%g outside (0, 1]", (double)P.p);
+        P.maxP = (in->maxP <= 0 || in->maxP >= P.N) ? P.N : in->maxP;
+        P.kmax = in->kmax <= 0 ? P.k : in->kmax;
+        if (P.kmax < P.k0 || P.kmax > slot_cap)
+            return fail(MOE_ERR_ARG, "kmax=%d outside k0..%d", P.kmax, slot_cap);
+        P.kslots = P.kmax;
+    } else {
+        return fail(MOE_ERR_ARG, "unknown mode %d", P.mode);
+    }
+    return MOE_OK;
+}
+
+WsLayout layout(const Params& P, int F) {
+    return ws_layout(P.B, P.N, P.d, P.kslots, F, P.dtype == MOE_DTYPE_BF16 ? 2 : 4);
+}
+
+moe_status check_ws(void* ws, size_t bytes, size_t need) {
+    if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(MOE_ERR_WORKSPACE, "workspace not 256-byte aligned");
+    if (bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", bytes, need);
+    return MOE_OK;
+}
+
+// Buffers sized by B may be NULL when B == 0.
+moe_status check_routing(const moe_routing* r, bool for_route, int B) {
+    if (!r) return fail(MOE_ERR_ARG, "routing is NULL");
+    const void* req[] = {r->T, r->active, r->counts, r->offsets, r->expert_idx, r->weights, r->perm};
+    for (int i = 0; i < 7; ++i) {
+        const void* q = req[i];
+        if (!q && (i < 4 || B > 0)) return fail(MOE_ERR_ARG, "a required routing buffer is NULL");
+        if (!aligned(q, 4)) return fail(MOE_ERR_ARG, "routing buffer not 4-byte aligned");
+    }
+    if (for_route) {
+        if (r->n_base && !aligned(r->n_base, 4)) return fail(MOE_ERR_ARG, "n_base not 4-byte aligned");
+        if (r->logits && !aligned(r->logits, 4)) return fail(MOE_ERR_ARG, "logits not 4-byte aligned");
+    }
+    return MOE_OK;
+}
+
+// ---- TMA descriptors for the expert matrices (cached per weight set) -------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void *g, *u, *dn;
+    int N, F, d, dev;
+    bool operator==(const MapKey& o) const {
+        return g == o.g && u == o.u && dn == o.dn && N == o.N && F == o.F && d == o.d && dev == o.dev;
+    }
+};
+
+struct MapEntry {
+    MapKey key;
+    CUtensorMap maps[3];
+    bool used;
+};
+
+std::mutex g_map_mu;
+MapEntry g_maps[64];
+int g_map_next = 0;
+
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+moe_status expert_maps(const void* g, const void* u, const void* dn, int N, int F, int d, int dev,
+                       CUtensorMap* out) {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    MapKey key{g, u, dn, N, F, d, dev};
+    for (auto& e : g_maps)
+        if (e.used && e.key == key) {
+            memcpy(out, e.maps, sizeof e.maps);
+            return MOE_OK;
+        }
+    MapEntry& e = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % 64;
+    e.key = key;
+    e.used = false;
+    if (!encode_2d(&e.maps[0], g, d, (uint64_t)N * F, 16) || !encode_2d(&e.maps[1], u, d, (uint64_t)N * F, 16) ||
+        !encode_2d(&e.maps[2], dn, F, (uint64_t)N * d, 32))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    e.used = true;
+    memcpy(out, e.maps, sizeof e.maps);
+    return MOE_OK;
+}
+
+int num_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_num_slots(const moe_route_params* params) {
+    Params P;
+    if (resolve(params, P) != MOE_OK) return -1;
+    return P.kslots;
+}
+
+size_t moe_workspace_bytes(const moe_route_params* params, int32_t d_ff) {
+    Params P;
+    if (resolve(params, P) != MOE_OK) return 0;
+    if (d_ff < 0 || d_ff % 64 != 0 || d_ff > 16384) return 0;
+    const WsLayout L = layout(P, d_ff);
+    return d_ff == 0 ? L.hbuf : L.total;
+}
+
+moe_status moe_route(const void* hidden, const void* w_router, const float* router_bias,
+                     const moe_route_params* params, const moe_routing* routing, void* workspace,
+                     size_t workspace_bytes, moe_stream_t stream) {
+    Params P;
+    moe_status st = resolve(params, P);
+    if (st != MOE_OK) return st;
+    if ((st = check_routing(routing, true, P.B)) != MOE_OK) return st;
+    if ((!hidden && P.B > 0) || !w_router) return fail(MOE_ERR_ARG, "hidden or w_router is NULL");
+    if (!aligned(hidden, 16) || !aligned(w_router, 16)) return fail(MOE_ERR_ARG, "hidden/w_router not 16-byte aligned");
+    if (router_bias && !aligned(router_bias, 4)) return fail(MOE_ERR_ARG, "router_bias not 4-byte aligned");
+    const WsLayout L = layout(P, 0);
+    if ((st = check_ws(workspace, workspace_bytes, L.hbuf)) != MOE_OK) return st;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    RouterArgs ra{};
+    ra.x = hidden;
+    ra.w = w_router;
+    ra.bias = router_bias;
+    ra.logits = routing->logits ? routing->logits : reinterpret_cast<float*>(ws + L.logits);
+    ra.B = P.B;
+    ra.N = P.N;
+    ra.d = P.d;
+    cudaError_t e = launch_router(ra, P.dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e, "router launch");
+
+    RouteArgs a{};
+    a.logits = ra.logits;
+    a.B = P.B;
+    a.B_valid = P.B_valid;
+    a.N = P.N;
+    a.k = P.k;
+    a.mode = P.mode;
+    a.k0 = P.k0;
+    a.maxP = P.maxP;
+    a.kmax = P.kmax;
+    a.kslots = P.kslots;
+    a.p = P.p;
+    a.idx = routing->expert_idx;
+    a.w = routing->weights;
+    a.T = routing->T;
+    a.active = routing->active;
+    a.counts = routing->counts;
+    a.offsets = routing->offsets;
+    a.perm = routing->perm;
+    a.pos_of = reinterpret_cast<int32_t*>(ws + L.pos_of);
+    a.n_base = routing->n_base;
+    a.flags = &reinterpret_cast<WsHeader*>(ws + L.header)->flags;
+    e = launch_route(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const void* hidden, const void* w_gate, const void* w_up, const void* w_down,
+                          int32_t d_ff, const moe_route_params* params, const moe_routing* routing, void* out,
+                          void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    Params P;
+    moe_status st = resolve(params, P);
+    if (st != MOE_OK) return st;
+    if ((st = check_routing(routing, false, P.B)) != MOE_OK) return st;
+    if (d_ff < 64 || d_ff % 64 != 0 || d_ff > 16384)
+        return fail(MOE_ERR_ARG, "d_ff=%d must be a multiple of 64 in 64..16384", d_ff);
+    const void* req[] = {w_gate, w_up, w_down, hidden, out};
+    for (int i = 0; i < 5; ++i) {
+        if (!req[i] && (i < 3 || P.B > 0)) return fail(MOE_ERR_ARG, "a tensor pointer is NULL");
+        if (!aligned(req[i], 16)) return fail(MOE_ERR_ARG, "a tensor pointer is not 16-byte aligned");
+    }
+    const WsLayout L = layout(P, d_ff);
+    if ((st = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return st;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    FfnArgs a{};
+    a.x = hidden;
+    a.T = routing->T;
+    a.active = routing->active;
+    a.counts = routing->counts;
+    a.offsets = routing->offsets;
+    a.perm = routing->perm;
+    a.pos_of = reinterpret_cast<const int32_t*>(ws + L.pos_of);
+    a.w = routing->weights;
+    a.hbuf = ws + L.hbuf;
+    a.ybuf = reinterpret_cast<float*>(ws + L.ybuf);
+    a.out = out;
+    a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone);
+    a.ydone = reinterpret_cast<uint32_t*>(ws + L.ydone);
+    a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
+    a.w_gate = w_gate;
+    a.w_up = w_up;
+    a.w_down = w_down;
+    a.B = P.B;
+    a.N = P.N;
+    a.d = P.d;
+    a.F = d_ff;
+    a.kslots = P.kslots;
+
+    cudaError_t e;
+    if (P.dtype == MOE_DTYPE_F32) {
+        e = launch_ffn_f32(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 expert launch");
+        return MOE_OK;
+    }
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    CUtensorMap maps[3];
+    if ((st = expert_maps(w_gate, w_up, w_down, P.N, d_ff, P.d, dev, maps)) != MOE_OK) return st;
+    const int sms = num_sms();
+    if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
+    e = launch_ffn_bf16(a, maps, sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
+    return MOE_OK;
+}
+
+moe_status moe_decode_layer(const void* hidden, const void* w_router, const float* router_bias,
+                            const void* w_gate, const void* w_up, const void* w_down, int32_t d_ff,
+                            const moe_route_params* params, const moe_routing* routing, void* out,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+    moe_status st = moe_route(hidden, w_router, router_bias, params, routing, workspace, workspace_bytes, stream);
+    if (st != MOE_OK) return st;
+    return moe_expert_ffn(hidden, w_gate, w_up, w_down, d_ff, params, routing, out, workspace, workspace_bytes,
+                          stream);
+}
+
+moe_status moe_device_status(void* workspace, moe_stream_t stream, uint32_t* flags) {
+    if (!workspace || !aligned(workspace, 256)) return fail(MOE_ERR_WORKSPACE, "bad workspace");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t f = 0;
+    WsHeader* h = static_cast<WsHeader*>(workspace);
+    cudaError_t e = cudaMemcpyAsync(&f, &h->flags, sizeof f, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(&h->flags, 0, sizeof f, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device flags");
+    if (flags) *flags = f;
+    if (f) return fail(MOE_ERR_DEVICE_CHECK, "device flags 0x%x", f);
+    return MOE_OK;
+}
+
+moe_status moe_synth_normal(void* dst, int32_t dtype, uint64_t n, uint64_t start, uint64_t seed, float scale,
+                            moe_stream_t stream) {
+    if (!dst && n) return fail(MOE_ERR_ARG, "dst is NULL");
+    if (dtype != MOE_DTYPE_BF16 && dtype != MOE_DTYPE_F32) return fail(MOE_ERR_ARG, "unknown dtype %d", dtype);
+    if (!std::isfinite(scale)) return fail(MOE_ERR_ARG, "scale is not finite");
+    cudaError_t e = launch_synth(dst, dtype, n, start, seed, scale, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "synth launch");
+    return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_ARG: return "MOE_ERR_ARG";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    }
+    return "unknown status";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,229 @@
+// common.cuh -- internal definitions shared by the kernels of the library:
+// argument structs, the workspace layout and inline-PTX wrappers for
+// sm_103a (mbarrier, TMA, warp-level bf16 MMA, cluster shared memory).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr uint32_t kFlagNonFinite = MOE_FLAG_NONFINITE_SCORE;
+constexpr uint32_t kFlagTimeout = MOE_FLAG_WAIT_TIMEOUT;
+constexpr uint32_t kFlagBadIndex = MOE_FLAG_BAD_INDEX;
+
+// ---------------------------------------------------------------------------
+// Workspace layout.  Offsets are 256-byte aligned; the header holds the flag
+// word and the counters that the expert kernel uses to order its two phases.
+// ---------------------------------------------------------------------------
+struct WsHeader {
+    uint32_t flags;       // MOE_FLAG_* raised by kernels
+    uint32_t ctas_done;   // expert kernel: CTAs finished (last one resets)
+    uint32_t pad[62];
+};
+
+struct WsLayout {
+    size_t header, hdone, ydone, pos_of, logits, hbuf, ybuf, total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// B, N, d, kslots, F: see moe.h.  elt = bytes per element of the FFN width
+// buffer H (bf16 or fp32).
+inline WsLayout ws_layout(int B, int N, int d, int kslots, int F, int h_elt) {
+    WsLayout L;
+    size_t o = 0;
+    L.header = o; o += align256(sizeof(WsHeader));
+    L.hdone = o;  o += align256(sizeof(uint32_t) * N);
+    L.ydone = o;  o += align256(sizeof(uint32_t) * (d / 32 + 1));
+    L.pos_of = o; o += align256(sizeof(int32_t) * (size_t)B * kslots + 4);
+    L.logits = o; o += align256(sizeof(float) * (size_t)B * N + 4);
+    L.hbuf = o;   o += align256((size_t)B * kslots * F * h_elt);
+    L.ybuf = o;   o += align256(sizeof(float) * (size_t)B * kslots * d);
+    L.total = o;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel argument structs.
+// ---------------------------------------------------------------------------
+struct RouterArgs {
+    const void* x;          // [B][d]
+    const void* w;          // [N][d]
+    const float* bias;      // [N] or null
+    float* logits;          // [B][N]
+    int B, N, d;
+    int ks;                 // cluster size along K
+};
+
+struct RouteArgs {
+    const float* logits;    // [B][N]
+    int B, B_valid, N, k, mode, k0, maxP, kmax, kslots;
+    float p;
+    int32_t* idx;           // [B][kslots]
+    float* w;               // [B][kslots]
+    int32_t* T;
+    int32_t* active;        // [N]
+    int32_t* counts;        // [N]
+    int32_t* offsets;       // [N+1]
+    int32_t* perm;          // [B*kslots]
+    int32_t* pos_of;        // [B*kslots]
+    int32_t* n_base;        // [B] or null
+    uint32_t* flags;
+};
+
+struct FfnArgs {
+    const void* x;          // [B][d] hidden
+    const int32_t* T;
+    const int32_t* active;
+    const int32_t* counts;
+    const int32_t* offsets;
+    const int32_t* perm;
+    const int32_t* pos_of;
+    const float* w;         // [B][kslots] routing weights
+    void* hbuf;             // [pairs][F]
+    float* ybuf;            // [pairs][d]
+    void* out;              // [B][d]
+    uint32_t* hdone;        // [N]
+    uint32_t* ydone;        // [d/32]
+    WsHeader* hdr;
+    const void* w_gate;     // [N][F][d]   (fp32 path)
+    const void* w_up;
+    const void* w_down;     // [N][d][F]
+    int B, N, d, F, kslots;
+};
+
+// Launchers (defined in the .cu files).
+cudaError_t launch_router(const RouterArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+cudaError_t launch_ffn_bf16(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s);
+cudaError_t launch_ffn_f32(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_synth(void* dst, int dtype, uint64_t n, uint64_t start, uint64_t seed,
+                         float scale, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Device helpers.
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void raise_flag(uint32_t* flags, uint32_t bits) {
+    atomicOr(flags, bits);
+}
+
+// mbarrier ------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after `limit` polls (each poll may suspend the
+// thread for a hardware-defined interval), returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 24)) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// TMA ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+          "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Warp-level MMA: D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col) ------
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Cluster ----------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+    uint32_t raddr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
+    return v;
+}
+
+// Global memory ordering -------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Named barrier for a subset of warps.
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace moe

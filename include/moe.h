@@ -1,0 +1,223 @@
+/*
+ * moe.h -- C ABI of the OEA MoE decode layer for one GB300 (sm_103a).
+ *
+ * The layer is the decode-time Mixture-of-Experts block described on the
+ * page "Opportunistic Expert Activation (OEA)" (zhaifeiyue.github.io,
+ * papers/2511.02237/detail.html):
+ *   1. router scores and per-token top-k (section 2, Q1/Q2);
+ *   2. optionally the OEA two-phase re-route: each token keeps its top-n_i
+ *      experts, n_i = min(k0, t_i) with t_i an adaptive top-p count, the
+ *      batch union S_base of those baselines is formed, and each token then
+ *      adds experts from its own ranked list only if they are already in
+ *      S_base, so T = |S_base| does not grow; kept scores are renormalised
+ *      (section 2 Q2, section 3);
+ *   3. grouping of (token, slot) pairs by expert (the per-expert loads
+ *      cnt_e of the cost model, section 4);
+ *   4. the expert FFN of every activated expert, each expert's weights read
+ *      from HBM once (section 2 Q1, section 4 check 4), in the SwiGLU form
+ *      of the Qwen3 experts the page measures:
+ *      y = W_down (silu(W_gate x) * (W_up x));
+ *   5. the weighted combine out_i = sum_j w_ij y_{e_ij}(x_i).
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, 16-byte
+ *     aligned, row-major and densely packed.  Buffers whose size is a
+ *     multiple of B may be NULL when B == 0.  The library allocates no
+ *     device memory; per-call scratch lives in the caller's workspace.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default
+ *     stream).  Nothing synchronises except moe_device_status().
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns MOE_ERR_ARG and launches nothing.  Conditions only
+ *     the GPU can see (a non-finite router score, a wait that timed out)
+ *     set bits in a flag word in the workspace and never trap; read them
+ *     with moe_device_status().
+ *   - Results are deterministic: the same inputs give the same bits.
+ *   - Not thread-safe per workspace: calls that share a workspace must be
+ *     ordered on one stream.
+ */
+#ifndef OEA_MOE_H
+#define OEA_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_ARG = 1,          /* invalid argument; nothing was launched       */
+    MOE_ERR_CUDA = 2,         /* a CUDA runtime call failed                   */
+    MOE_ERR_DEVICE_CHECK = 3, /* the GPU raised a flag (moe_device_status)    */
+    MOE_ERR_WORKSPACE = 4,    /* workspace missing, misaligned or too small   */
+    MOE_ERR_UNSUPPORTED = 5   /* valid but not supported on this device       */
+} moe_status;
+
+typedef enum { MOE_MODE_TOPK = 0, MOE_MODE_OEA = 1 } moe_mode;
+
+/* Element type of hidden states, router and expert weights and output. */
+typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
+
+/* Device flag bits reported by moe_device_status(). */
+#define MOE_FLAG_NONFINITE_SCORE 0x1u  /* a router score was NaN or +-inf     */
+#define MOE_FLAG_WAIT_TIMEOUT 0x2u     /* an in-kernel wait gave up           */
+#define MOE_FLAG_BAD_INDEX 0x4u        /* an index failed its range check     */
+
+/* Size limits. */
+#define MOE_MAX_TOKENS 256
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_SLOTS 32
+
+/*
+ * Routing parameters (OEA page, section 2 Q2; sections 4-5 and 7 for maxP,
+ * k^max and the padding mask).
+ *   B        tokens in the batch, 0..MOE_MAX_TOKENS.
+ *   B_valid  tokens 0..B_valid-1 are real; tokens B_valid..B-1 are padding
+ *            and select no expert, so they cannot enlarge T (OEA page,
+ *            section 7, implementation detail 1).  Negative: B.
+ *   d        hidden size; a multiple of 64.
+ *   N        experts, 1..MOE_MAX_EXPERTS.
+ *   k        experts per token of the plain router, 1..min(N, 32).
+ *   mode     MOE_MODE_TOPK or MOE_MODE_OEA.
+ *   k0       OEA baseline cap, 1..k.
+ *   p        OEA top-p threshold in (0, 1]; p >= 1 switches top-p off
+ *            (t_i = N), as in the simplified router of section 5.
+ *   maxP     OEA: deepest rank of the token's own list that phase 2 may
+ *            take an expert from; <= 0 or >= N means N (no limit).
+ *   kmax     OEA: experts per token after phase 2 (k^max); <= 0 means k;
+ *            otherwise k0..min(N, 32).
+ *   dtype    moe_dtype of hidden, router weights, expert weights and output.
+ * Slots per token: kslots = k for MOE_MODE_TOPK, kmax for MOE_MODE_OEA
+ * (moe_num_slots()).
+ */
+typedef struct {
+    int32_t B;
+    int32_t B_valid;
+    int32_t d;
+    int32_t N;
+    int32_t k;
+    int32_t mode;
+    int32_t k0;
+    float p;
+    int32_t maxP;
+    int32_t kmax;
+    int32_t dtype;
+} moe_route_params;
+
+/*
+ * Routing results: device buffers owned by the caller, written by
+ * moe_route().  Ranks and ties: experts are ranked by score, larger first,
+ * equal scores by the lower expert id.
+ *   expert_idx [B][kslots] int32  chosen experts in rank order, -1 in unused
+ *                                 slots (a token keeps min(kmax, T) experts
+ *                                 in OEA mode; padding tokens keep none).
+ *   weights    [B][kslots] fp32   renormalised scores (softmax over the kept
+ *                                 scores), 0 in unused slots.
+ *   T          [1] int32          number of distinct activated experts.
+ *   active     [N] int32          activated experts, ascending id; entries
+ *                                 T..N-1 are -1.
+ *   counts     [N] int32          cnt_e, tokens routed to expert e.
+ *   offsets    [N+1] int32        exclusive prefix sum of counts.
+ *   perm       [B*kslots] int32   token*kslots+slot grouped by expert
+ *                                 (ascending id), tokens ascending within an
+ *                                 expert; entries offsets[N].. are unused.
+ *   n_base     [B] int32          nullable; n_i (k in top-k mode, 0 for
+ *                                 padding tokens).
+ *   logits     [B][N] fp32        nullable; router scores (bias included).
+ */
+typedef struct {
+    int32_t *expert_idx;
+    float *weights;
+    int32_t *T;
+    int32_t *active;
+    int32_t *counts;
+    int32_t *offsets;
+    int32_t *perm;
+    int32_t *n_base;
+    float *logits;
+} moe_routing;
+
+/* Slots per token for these parameters (k or kmax), or -1 if invalid. */
+int32_t moe_num_slots(const moe_route_params *params);
+
+/*
+ * Bytes of device workspace needed by moe_route / moe_expert_ffn /
+ * moe_decode_layer for these parameters and expert FFN width d_ff (pass
+ * d_ff = 0 when only moe_route is used).  Returns 0 if the parameters are
+ * invalid.  The workspace must be 256-byte aligned and zero-filled once
+ * before its first use; the library leaves it ready for the next call.
+ */
+size_t moe_workspace_bytes(const moe_route_params *params, int32_t d_ff);
+
+/*
+ * Router + routing (steps 1-3 above).
+ *   hidden      [B][d]  dtype   token hidden states.
+ *   w_router    [N][d]  dtype   router (gate) weights.
+ *   router_bias [N]     fp32    nullable; added to every score.
+ *   routing                     outputs, see moe_routing.
+ * Scores are accumulated in fp32.  Routing decisions compare those fp32
+ * scores exactly; the top-p prefix is computed in fp32.
+ */
+moe_status moe_route(const void *hidden, const void *w_router, const float *router_bias,
+                     const moe_route_params *params, const moe_routing *routing,
+                     void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Expert FFN + weighted combine (steps 4-5) for a batch routed by
+ * moe_route() with the same params.  Reads only activated experts, each
+ * expert's three matrices once from HBM.
+ *   hidden  [B][d]        dtype  the hidden states given to moe_route.
+ *   w_gate  [N][d_ff][d]  dtype  expert gate projections.
+ *   w_up    [N][d_ff][d]  dtype  expert up projections.
+ *   w_down  [N][d][d_ff]  dtype  expert down projections.
+ *   d_ff    expert FFN width, a multiple of 64.
+ *   routing the results of moe_route (expert_idx, weights, T, active,
+ *           counts, offsets, perm are read).
+ *   out     [B][d]        dtype  written; padding tokens get zeros.
+ * bf16: products in fp32 on tensor cores, the SwiGLU activation h rounded
+ * to bf16 before the down projection, sums in fp32, output rounded once.
+ * fp32: all arithmetic in fp32 on CUDA cores.
+ */
+moe_status moe_expert_ffn(const void *hidden, const void *w_gate, const void *w_up,
+                          const void *w_down, int32_t d_ff, const moe_route_params *params,
+                          const moe_routing *routing, void *out, void *workspace,
+                          size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_route followed by moe_expert_ffn on the same stream. */
+moe_status moe_decode_layer(const void *hidden, const void *w_router, const float *router_bias,
+                            const void *w_gate, const void *w_up, const void *w_down,
+                            int32_t d_ff, const moe_route_params *params,
+                            const moe_routing *routing, void *out, void *workspace,
+                            size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Synchronises `stream`, returns the device flag word (MOE_FLAG_*) that the
+ * calls on this workspace raised since the last read, and clears it.
+ * Returns MOE_ERR_DEVICE_CHECK if any flag was set.
+ */
+moe_status moe_device_status(void *workspace, moe_stream_t stream, uint32_t *flags);
+
+/*
+ * Seeded synthetic tensor fill (for benchmarks and tests; not part of the
+ * layer).  Writes elements start..start+n-1 of the counter-based stream:
+ * SplitMix64 (Steele, Lea & Flood, OOPSLA 2014) output i for initial state
+ * `seed`, its four 16-bit fields summed and centred (an Irwin-Hall sum),
+ * times `scale` in fp32, rounded to bf16 (nearest even) when dtype is bf16.
+ * dst must hold n elements of dtype.
+ */
+moe_status moe_synth_normal(void *dst, int32_t dtype, uint64_t n, uint64_t start, uint64_t seed,
+                            float scale, moe_stream_t stream);
+
+/* Human-readable name of a status, and the last error detail on this thread. */
+const char *moe_status_string(moe_status status);
+const char *moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OEA_MOE_H */

@@ -1,0 +1,236 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI.
+
+Routing is compared bit-exactly against the oracle run on the GPU's own fp32
+router scores; scores, weights and outputs within the stated tolerances.
+Sizes are small enough for the oracle to finish in seconds but span several
+tiles with ragged tails; the full-size workloads are checked on sampled
+tokens."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+moe = pytest.importorskip("aware_expert_routing_gb300")
+import gpu_util as gu  # noqa: E402
+
+TOPK, OEA = 0, 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from aware_expert_routing_gb300 import build as b
+    b.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+    moe.load()
+
+
+def W(name, **kw):
+    base = dict(N=128, k=8, d=512, F=256, B=16, seed=11)
+    base.update(kw)
+    return synth.Workload(name, **base)
+
+
+def run_case(w, B, mode, k0=None, p=1.0, maxP=0, kmax=0, B_valid=-1, L=None, check_e2e=True):
+    L = L if L is not None else synth.make_layer(w, 0, B)
+    D = gu.device_inputs(L, w.bf16)
+    prm = gu.params_for(w, B, mode, k0, p, maxP, kmax, B_valid)
+    r, out, ws, flags = gu.run_layer(w, D, prm)
+    assert flags == 0, f"device flags {flags:#x}"
+    g = gu.to_np(r)
+    bv = B if B_valid < 0 else B_valid
+    lg_ref = oracle.router_logits(L["x"], L["w_router"], L["bias"])
+    if B:
+        tol = (1e-3 if w.bf16 else 1e-5) * np.abs(lg_ref).max()
+        assert np.abs(g["logits"] - lg_ref).max() <= tol
+    ref = gu.check_routing(g, prm, bv)
+    o = oracle.moe_experts(L["x"], L["w_gate"], L["w_up"], L["w_down"], g["expert_idx"],
+                           g["weights"].astype(np.float64))
+    if B:
+        gu.check_output(out, o, w.bf16)
+        if B_valid >= 0:
+            assert (out[B_valid:].float() == 0).all()
+    if check_e2e and B:
+        # The oracle's own scores (fp64 sums rounded to fp32) give the same
+        # routing whenever every token's top-(kmax+1) order is the same.
+        own = oracle.route(lg_ref.astype(np.float32), OEA if mode == OEA else TOPK, prm.k, prm.k0,
+                           prm.p, prm.maxP if 0 < prm.maxP < prm.N else prm.N,
+                           prm.kmax if prm.kmax > 0 else prm.k, bv)
+        depth = (prm.kmax if prm.kmax > 0 else prm.k) + 1
+        same = all(np.array_equal(np.argsort(-g["logits"][i], kind="stable")[:depth],
+                                  np.argsort(-lg_ref[i].astype(np.float32), kind="stable")[:depth])
+                   for i in range(B))
+        if same and not gu.near_tie_tokens(lg_ref, prm.p, prm.k0, bv):
+            assert own["T"] == g["T"] and np.array_equal(own["idx"], g["expert_idx"])
+    return g, out, ref
+
+
+# ---- the tiny fp32 layer (N=16, k=4, d=64, d_ff=128, B=4) -------------------
+@pytest.mark.parametrize("mode,k0,p", [(TOPK, 4, 1.0), (OEA, 2, 0.5)])
+def test_tiny_fp32_layer(mode, k0, p):
+    w = synth.WORKLOADS["tiny_fp32_n16_k4_d64_f128_b4"]
+    run_case(w, w.B, mode, k0, p)
+
+
+# ---- bf16 layers at test sizes ------------------------------------------------
+@pytest.mark.parametrize("mode,k0,p,zipf", [
+    (TOPK, 8, 1.0, False), (OEA, 3, 1.0, False), (OEA, 5, 1.0, False), (OEA, 5, 0.7, True),
+    (TOPK, 8, 1.0, True), (OEA, 1, 1.0, False), (OEA, 8, 1.0, False), (OEA, 4, 0.5, True)])
+def test_bf16_layer_modes(mode, k0, p, zipf):
+    w = W("t_modes", zipf=zipf)
+    run_case(w, w.B, mode, k0, p)
+
+
+@pytest.mark.parametrize("B", [1, 7, 37, 64, 256])
+def test_bf16_ragged_batches(B):
+    w = W("t_ragged", N=64, d=256, F=128, seed=12, zipf=True)
+    run_case(w, B, OEA, 3, 0.7)
+    run_case(w, B, TOPK)
+
+
+@pytest.mark.parametrize("N,k,d,F", [(16, 4, 64, 64), (160, 6, 320, 192), (1024, 8, 128, 64),
+                                     (256, 16, 192, 320), (32, 32, 64, 128)])
+def test_bf16_shapes(N, k, d, F):
+    w = W("t_shapes", N=N, k=k, d=d, F=F, seed=N + d)
+    run_case(w, 29, OEA, max(1, k // 2), 1.0)
+    run_case(w, 29, TOPK)
+
+
+@pytest.mark.parametrize("maxP,kmax", [(6, 8), (12, 8), (128, 11), (10, 10), (3, 5)])
+def test_general_oea_knobs(maxP, kmax):
+    w = W("t_knobs", seed=21)
+    run_case(w, 24, OEA, 3, 0.8, maxP=maxP, kmax=kmax)
+
+
+@pytest.mark.parametrize("mode", [TOPK, OEA])
+def test_padding_tokens(mode):
+    w = W("t_pad", seed=5)
+    g, out, _ = run_case(w, 16, mode, 3, 1.0, B_valid=11)
+    assert (g["expert_idx"][11:] == -1).all() and (g["weights"][11:] == 0).all()
+    g2, _, _ = run_case(w, 11, mode, 3, 1.0, L={**synth.make_layer(w, 0, 16),
+                                                "x": synth.make_layer(w, 0, 16)["x"][:11]})
+    assert g2["T"] == g["T"]
+
+
+def test_hot_experts_many_tokens_per_expert():
+    """Experts with more tokens than one 32-token pass (chunked tiles)."""
+    w = W("t_hot", N=64, d=256, F=192, seed=3)
+    L = synth.make_layer(w, 0, 100)
+    bias = np.zeros(64, np.float32)
+    bias[3], bias[7], bias[40] = 9.0, 8.0, 7.5
+    L["bias"] = bias
+    g, _, _ = run_case(w, 100, TOPK, L=L)
+    assert g["counts"][3] == 100 and g["counts"][7] == 100
+    g, _, _ = run_case(w, 100, OEA, 2, 1.0, L=L)
+    assert g["T"] == 2
+
+
+def test_identical_tokens():
+    w = W("t_same", seed=8)
+    L = synth.make_layer(w, 0, 12)
+    L["x"] = np.repeat(L["x"][:1], 12, axis=0)
+    g, _, _ = run_case(w, 12, OEA, 3, 1.0, L=L)
+    assert g["T"] == 3
+    g, _, _ = run_case(w, 12, TOPK, L=L)
+    assert g["T"] == 8
+
+
+def test_empty_batch():
+    w = W("t_empty")
+    run_case(w, 0, OEA, 3, 1.0)
+    run_case(w, 0, TOPK)
+
+
+def test_all_padding():
+    w = W("t_allpad")
+    g, out, _ = run_case(w, 5, OEA, 3, 1.0, B_valid=0)
+    assert g["T"] == 0 and (out.float() == 0).all()
+
+
+def test_deterministic_and_repeatable():
+    """Same inputs -> same bits, across layer calls and across repeated expert
+    calls on one routing (the in-kernel counters reset themselves)."""
+    w = W("t_det", N=64, d=256, F=128, seed=9, zipf=True)
+    L = synth.make_layer(w, 0, 48)
+    D = gu.device_inputs(L, True)
+    prm = gu.params_for(w, 48, OEA, 4, 0.9)
+    r1, o1, ws, _ = gu.run_layer(w, D, prm)
+    r2, o2, _, _ = gu.run_layer(w, D, prm, ws=ws)
+    assert torch.equal(o1, o2) and torch.equal(r1.expert_idx, r2.expert_idx)
+    assert torch.equal(r1.weights, r2.weights)
+    o3 = torch.empty_like(o1)
+    for _ in range(3):
+        moe.moe_expert_ffn(D["x"], D["w_gate"], D["w_up"], D["w_down"], w.F, prm, r2, o3, ws)
+        assert moe.moe_device_status(ws) == 0
+        assert torch.equal(o1, o3)
+
+
+def test_nonfinite_scores_are_flagged():
+    w = W("t_inf", N=32, d=128, F=64)
+    L = synth.make_layer(w, 0, 4)
+    L["x"][2, 5] = np.inf
+    D = gu.device_inputs(L, True)
+    prm = gu.params_for(w, 4, TOPK)
+    _, _, _, flags = gu.run_layer(w, D, prm)
+    assert flags & moe.FLAG_NONFINITE_SCORE
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_device_generator_matches_host(bf16):
+    n, start, seed, std = 100_003, 12_345, synth.tensor_seed(4, 1, synth.T_GATE), 0.02
+    t = torch.empty(n, dtype=torch.bfloat16 if bf16 else torch.float32, device=gu.DEV)
+    moe.moe_synth_normal(t, seed, float(synth.scale_f32(std)), start)
+    host = synth.normal(seed, (n,), std, bf16, start=start)
+    assert np.array_equal(t.float().cpu().numpy(), host)
+
+
+# ---- full-size workloads, checked on sampled tokens -----------------------------
+def full_size_layer(w: synth.Workload, layer: int, B: int):
+    """Weights generated on the device with the same generator as the host."""
+    bf = torch.bfloat16
+    D = {"x": torch.from_numpy(synth.make_tensor(w, layer, synth.T_X, B)).to(gu.DEV).to(bf).contiguous()}
+    for name, tid in (("w_router", synth.T_ROUTER), ("w_gate", synth.T_GATE), ("w_up", synth.T_UP),
+                      ("w_down", synth.T_DOWN)):
+        t = torch.empty(synth.tensor_shape(w, tid, B), dtype=bf, device=gu.DEV)
+        moe.moe_synth_normal(t, synth.tensor_seed(w.seed, layer, tid), float(synth.scale_f32(synth.tensor_std(w, tid))))
+        D[name] = t
+    b = synth.make_bias(w, layer)
+    D["bias"] = torch.from_numpy(b).to(gu.DEV) if b is not None else None
+    return D
+
+
+@pytest.mark.parametrize("wname,B,runs", [
+    ("qwen3_30b_a3b_uniform_b16", 16, [(TOPK, 8, 1.0), (OEA, 3, 1.0), (OEA, 5, 1.0)]),
+    ("qwen3_30b_a3b_zipf_sweep", 256, [(TOPK, 8, 1.0), (OEA, 5, 0.7)]),
+    ("qwen3_235b_a22b_zipf_b64", 64, [(TOPK, 8, 1.0), (OEA, 5, 0.7)]),
+])
+def test_full_size_sampled(wname, B, runs):
+    w = synth.WORKLOADS[wname]
+    D = full_size_layer(w, 0, B)
+    x = synth.make_tensor(w, 0, synth.T_X, B)
+    wr = synth.make_tensor(w, 0, synth.T_ROUTER)
+    bias = synth.make_bias(w, 0)
+    lg_ref = oracle.router_logits(x, wr, bias)
+    cache = {}
+    for mode, k0, p in runs:
+        prm = gu.params_for(w, B, mode, k0, p)
+        r, out, ws, flags = gu.run_layer(w, D, prm)
+        assert flags == 0
+        g = gu.to_np(r)
+        assert np.abs(g["logits"] - lg_ref).max() <= 1e-3 * np.abs(lg_ref).max()
+        gu.check_routing(g, prm, B)
+        got = out.float().cpu().numpy()
+        for i in sorted({0, B // 2, B - 1}):
+            ref = np.zeros(w.d)
+            for j, e in enumerate(g["expert_idx"][i]):
+                if e < 0:
+                    continue
+                if e not in cache:
+                    cache[e] = synth.make_expert(w, 0, int(e))
+                ref += float(g["weights"][i, j]) * oracle.expert_ffn(x[i], *cache[e])
+            err = np.abs(got[i] - ref).max()
+            assert err <= gu.TOL_BF16 * np.abs(ref).max(), (i, err)
