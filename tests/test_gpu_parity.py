@@ -121,7 +121,7 @@ def test_hot_experts_many_tokens_per_expert():
     w = W("t_hot", N=64, d=256, F=192, seed=3)
     L = synth.make_layer(w, 0, 100)
     bias = np.zeros(64, np.float32)
-    bias[3], bias[7], bias[40] = 9.0, 8.0, 7.5
+    bias[3], bias[7], bias[40] = 30.0, 20.0, 10.0   # gaps far above the score spread
     L["bias"] = bias
     g, _, _ = run_case(w, 100, TOPK, L=L)
     assert g["counts"][3] == 100 and g["counts"][7] == 100
