@@ -175,6 +175,40 @@ moe_status expert_maps(const void* g, const void* u, const void* dn, int N, int 
     return MOE_OK;
 }
 
+// Maps over the workspace buffers read by TMA: the expert-grouped hidden
+// states [pairs][d] and the SwiGLU rows h [pairs][d_ff] (boxes of 8 rows).
+struct WsMapEntry {
+    const void* ws;
+    int pairs, d, F, dev;
+    CUtensorMap maps[2];
+    bool used;
+};
+WsMapEntry g_ws_maps[16];
+int g_ws_next = 0;
+
+moe_status workspace_maps(unsigned char* ws, const WsLayout& L, int pairs, int d, int F, int dev,
+                          CUtensorMap* out) {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (auto& e : g_ws_maps)
+        if (e.used && e.ws == ws && e.pairs == pairs && e.d == d && e.F == F && e.dev == dev) {
+            memcpy(out, e.maps, sizeof e.maps);
+            return MOE_OK;
+        }
+    WsMapEntry& e = g_ws_maps[g_ws_next];
+    g_ws_next = (g_ws_next + 1) % 16;
+    e.used = false;
+    e.ws = ws;
+    e.pairs = pairs;
+    e.d = d;
+    e.F = F;
+    e.dev = dev;
+    if (!encode_2d(&e.maps[0], ws + L.xperm, d, pairs, 8) || !encode_2d(&e.maps[1], ws + L.hbuf, F, pairs, 8))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (workspace)");
+    e.used = true;
+    memcpy(out, e.maps, sizeof e.maps);
+    return MOE_OK;
+}
+
 int num_sms() {
     static int cache[64] = {0};
     int dev = 0;
@@ -288,6 +322,7 @@ moe_status moe_expert_ffn(const void* hidden, const void* w_gate, const void* w_
     a.w = routing->weights;
     a.hbuf = ws + L.hbuf;
     a.ybuf = reinterpret_cast<float*>(ws + L.ybuf);
+    a.xperm = ws + L.xperm;
     a.out = out;
     a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone);
     a.ydone = reinterpret_cast<uint32_t*>(ws + L.ydone);
@@ -307,10 +342,12 @@ moe_status moe_expert_ffn(const void* hidden, const void* w_gate, const void* w_
         if (e != cudaSuccess) return cuda_fail(e, "fp32 expert launch");
         return MOE_OK;
     }
+    if (P.B == 0) return MOE_OK;   // nothing to compute or write
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    CUtensorMap maps[3];
+    CUtensorMap maps[5];
     if ((st = expert_maps(w_gate, w_up, w_down, P.N, d_ff, P.d, dev, maps)) != MOE_OK) return st;
+    if ((st = workspace_maps(ws, L, P.B * P.kslots, P.d, d_ff, dev, maps + 3)) != MOE_OK) return st;
     const int sms = num_sms();
     if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
     e = launch_ffn_bf16(a, maps, sms, s);

@@ -21,13 +21,16 @@ constexpr uint32_t kFlagBadIndex = MOE_FLAG_BAD_INDEX;
 // word and the counters that the expert kernel uses to order its two phases.
 // ---------------------------------------------------------------------------
 struct WsHeader {
-    uint32_t flags;       // MOE_FLAG_* raised by kernels
-    uint32_t ctas_done;   // expert kernel: CTAs finished (last one resets)
-    uint32_t pad[62];
+    uint32_t flags;        // MOE_FLAG_* raised by kernels
+    uint32_t ctas_done;    // expert kernel: CTAs finished (the last one resets the counters)
+    uint32_t gather_done;  // expert kernel: CTAs that finished their share of the gather
+    uint32_t a_done;       // expert kernel: CTAs that finished phase A (h written)
+    uint32_t b_done;       // expert kernel: CTAs that finished phase B (y written)
+    uint32_t pad[59];
 };
 
 struct WsLayout {
-    size_t header, hdone, ydone, pos_of, logits, hbuf, ybuf, total;
+    size_t header, hdone, ydone, pos_of, logits, hbuf, ybuf, xperm, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -44,6 +47,7 @@ inline WsLayout ws_layout(int B, int N, int d, int kslots, int F, int h_elt) {
     L.logits = o; o += align256(sizeof(float) * (size_t)B * N + 4);
     L.hbuf = o;   o += align256((size_t)B * kslots * F * h_elt);
     L.ybuf = o;   o += align256(sizeof(float) * (size_t)B * kslots * d);
+    L.xperm = o;  o += align256((size_t)B * kslots * d * h_elt);
     L.total = o;
     return L;
 }
@@ -87,6 +91,7 @@ struct FfnArgs {
     const float* w;         // [B][kslots] routing weights
     void* hbuf;             // [pairs][F]
     float* ybuf;            // [pairs][d]
+    void* xperm;            // [pairs][d] hidden states grouped by expert
     void* out;              // [B][d]
     uint32_t* hdone;        // [N]
     uint32_t* ydone;        // [d/32]
@@ -100,6 +105,7 @@ struct FfnArgs {
 // Launchers (defined in the .cu files).
 cudaError_t launch_router(const RouterArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+// maps: W_gate, W_up, W_down, gathered hidden states, SwiGLU buffer h.
 cudaError_t launch_ffn_bf16(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s);
 cudaError_t launch_ffn_f32(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_synth(void* dst, int dtype, uint64_t n, uint64_t start, uint64_t seed,
@@ -162,6 +168,18 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
                                             uint64_t* bar, uint64_t policy) {
     asm volatile(
@@ -172,6 +190,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Orders this thread's earlier generic-proxy accesses (and what it has
+// acquired) before its later async-proxy (TMA) accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -179,7 +203,7 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 // Warp-level MMA: D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col) ------
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])

@@ -8,31 +8,40 @@
 // on chip.  Expert form (Qwen3): y = W_down (silu(W_gate x) * (W_up x));
 // combine: out_i = sum_j w_ij y_{e_ij}(x_i) (kept scores, section 2 Q2).
 //
-// Structure (one persistent CTA per SM):
+// Structure (one persistent CTA per SM, 6 warps, cooperative launch):
 //   * Work is a list of tiles.  Phase-A tile (expert a, 16 rows of d_ff,
 //     token chunk c) computes h = silu(W_gate x) * (W_up x) for those rows
-//     and up to 32 tokens and writes h (bf16) to the workspace.  Phase-B
-//     tile (expert a, 32 rows of d, chunk c) computes y = W_down h.  Each
-//     CTA takes an equal, contiguous share of the phase-A tiles and then of
-//     the phase-B tiles, so every CTA streams the same number of bytes.
-//   * Warp 4 is the producer: one lane issues TMA tile loads (128-byte
-//     swizzle, L2 evict-first) into a 12-stage shared-memory ring guarded by
-//     mbarriers.  A stage is 16 KB: 256 K-columns of two 16-row tiles (gate
-//     and up) or of one 32-row tile (down).  The weight stream does not wait
-//     for any other CTA, so it continues across the phase boundary.
-//   * Warps 0-3 are consumers: warp w owns the w-th 64-column block of every
-//     stage and runs warp-level bf16 tensor-core MMAs with the weights as
+//     and up to 16 tokens and writes h (bf16) to the workspace.  Phase-B
+//     tile (expert a, 32 rows of d, chunk c) computes y = W_down h (fp32).
+//     Each CTA takes an equal, contiguous share of the phase-A tiles and
+//     then of the phase-B tiles, so every CTA streams the same bytes.
+//   * Prologue: the CTAs copy the hidden states into an expert-grouped
+//     buffer (row p = the token of pair p) and count themselves done.
+//   * A stage of the 8-deep shared-memory ring holds 256 K-columns of the
+//     weight tile (16 KB: gate+up rows, or 32 down rows) and the matching
+//     columns of the tokens' operand rows (up to 16 rows, 8 KB), all loaded
+//     by TMA with the 128-byte swizzle.  Warp 4 issues the weight loads and
+//     never waits for another CTA, so the weight stream runs on across the
+//     phase boundary.  Weights read once are marked L2 evict-first; an
+//     expert with more than 16 tokens is read once per 16-token pass, the
+//     passes back to back, and its weights use the normal L2 policy so the repeat reads hit L2.  Warp 5 issues the operand loads:
+//     it waits once for the gather and, before the first h row, once for
+//     every CTA to finish phase A.  Both producers arrive on the stage's
+//     full barrier.
+//   * Warps 0-3 are consumers: warp w owns the w-th 64-column block of each
+//     stage and runs warp-level bf16 tensor-core MMAs with the weight rows as
 //     the M side and the tokens as the N side (8 tokens per MMA column
-//     tile), accumulating in fp32.  Tokens' hidden states (phase A) or h
-//     rows (phase B) are loaded straight from global/L2 with 16-byte loads;
-//     the K index inside each 64-column block is permuted identically for
-//     both operands so that every lane reads 32 contiguous bytes.
-//   * At the end of a tile the four warps' partial sums are added in warp
-//     order through shared memory.  Phase A then applies SwiGLU and bumps a
-//     per-expert counter; a phase-B tile first waits (bounded) until all
-//     phase-A tiles of its expert are counted.  Phase B bumps a counter per
-//     32-row output block; the CTA whose tile completes a block performs the
-//     weighted combine of that block for all tokens, in slot order.
+//     tile), accumulating in fp32.  Both operands are read from shared
+//     memory with 16-byte loads; the K index inside each 64-column block is
+//     permuted identically for both operands (k-step s, k-slot pair 2t and
+//     2t+8 map to columns 16t+4s and 16t+4s+2) so every lane reads 32
+//     contiguous bytes and the swizzle keeps the reads conflict free.
+//   * At the end of a tile the four warps' partial sums meet in a
+//     double-buffered shared-memory area and are added in warp order, with
+//     one named barrier per tile; no global fence or atomic per tile.
+//   * After phase B every CTA arrives at a grid-wide counter; once all have
+//     arrived, each CTA combines its slice of the output,
+//     out_i = sum over slots (in slot order) of w_is * y_is.
 //   * The last CTA to finish resets the counters for the next launch.
 // Every result is computed in a fixed order, so runs are bit-reproducible.
 #include "common.cuh"
@@ -41,31 +50,39 @@ namespace moe {
 
 namespace {
 
-constexpr int kCW = 4;                  // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;
-constexpr int kStageBytes = 16384;
-constexpr int kStages = 12;
-constexpr int kChunk = 32;              // tokens per tile pass
+constexpr int kCW = 4;                    // consumer warps
+constexpr int kWarpW = kCW;               // weight producer warp
+constexpr int kWarpO = kCW + 1;           // operand producer warp
+constexpr int kThreads = (kCW + 2) * 32;
+constexpr int kNT = 2;                    // MMA column tiles (8 tokens each) per pass
+constexpr int kChunk = 8 * kNT;           // tokens per tile pass
+constexpr int kWBytes = 16384;            // weight part of a stage
+constexpr int kOBytes = 4 * kNT * 1024;   // operand part: 4 column blocks x kNT boxes of 8 rows
+constexpr int kSlotBytes = kWBytes + kOBytes;
+constexpr int kStages = 8;
+constexpr int kRed = 2 * 4 * kNT * 32;    // partial sums per warp per tile (2 M-tiles)
 constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
 
 struct Smem {
-    float red[kCW][1024];
+    float red[2][kCW][kRed];         // double-buffered per-warp partial sums
     uint64_t full[kStages];
     uint64_t empty[kStages];
     int chunk_off[MOE_MAX_EXPERTS + 1];
+    uint32_t ex_info[MOE_MAX_EXPERTS];  // active index -> id | cnt << 10 | first pair << 19
     int abort_flag;
-    int combine_flag;
     int last_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(Smem);
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kSlotBytes + sizeof(Smem);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Tile {
-    int a, e, rb, c, off, ntok;
+    int a, e, rb, c, off, ntok, nch;
 };
 
-__device__ __forceinline__ Tile decode_tile(long long t, int rbn, const int* chunk_off, int Tn,
-                                            const FfnArgs& A) {
+// Tile t of a phase with rbn row blocks per (expert, chunk); shared memory only.
+__device__ __forceinline__ Tile decode_tile(long long t, int rbn, const Smem& S, int Tn) {
+    const int* chunk_off = S.chunk_off;
     int lo = 0, hi = Tn - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -73,15 +90,21 @@ __device__ __forceinline__ Tile decode_tile(long long t, int rbn, const int* chu
     }
     Tile T;
     T.a = lo;
-    T.e = A.active[lo];
-    const int cnt = A.counts[T.e];
-    T.off = A.offsets[T.e];
-    const int nch = chunk_off[lo + 1] - chunk_off[lo];
+    const uint32_t info = S.ex_info[lo];
+    T.e = info & 1023u;
+    const int cnt = (info >> 10) & 511u;
+    T.off = info >> 19;
+    T.nch = chunk_off[lo + 1] - chunk_off[lo];
     const long long r = t - (long long)chunk_off[lo] * rbn;
-    T.rb = (int)(r / nch);
-    T.c = (int)(r % nch);
+    T.rb = (int)(r / T.nch);
+    T.c = (int)(r % T.nch);
     T.ntok = min(kChunk, cnt - kChunk * T.c);
     return T;
+}
+
+__device__ __forceinline__ void give_up(Smem& S, uint32_t* flags) {
+    *(volatile int*)&S.abort_flag = 1;
+    raise_flag(flags, kFlagTimeout);
 }
 
 // Bounded mbarrier wait; once the CTA has given up, every later wait
@@ -93,10 +116,23 @@ __device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t parity, Smem& S
     while (!*(volatile int*)&S.abort_flag) {
         if (mbar_try_wait(bar, parity)) return;
         if (clock64() - t0 > kWaitCycles) {
-            *(volatile int*)&S.abort_flag = 1;
-            raise_flag(flags, kFlagTimeout);
+            give_up(S, flags);
             return;
         }
+    }
+}
+
+// Bounded wait until *p >= need (acquire, GPU scope).
+__device__ __forceinline__ void wait_counter(const uint32_t* p, uint32_t need, Smem& S, uint32_t* flags) {
+    if (ld_acquire_gpu(p) >= need) return;
+    const long long t0 = clock64();
+    while (!*(volatile int*)&S.abort_flag) {
+        if (ld_acquire_gpu(p) >= need) return;
+        if (clock64() - t0 > kWaitCycles) {
+            give_up(S, flags);
+            return;
+        }
+        __nanosleep(32);
     }
 }
 
@@ -109,39 +145,91 @@ __device__ __forceinline__ void unpack8(uint32_t (&r)[8], uint4 a, uint4 b) {
     r[4] = b.x; r[5] = b.y; r[6] = b.z; r[7] = b.w;
 }
 
-// One 16-row x 64-column weight block of a stage (128-byte swizzled rows):
-// the A fragments of rows g and g+8 for the four k-steps.
-__device__ __forceinline__ void load_a_block(const unsigned char* blk, int g, int t4,
-                                             uint32_t (&r0)[8], uint32_t (&r1)[8]) {
-    const int c0 = ((2 * t4) ^ g) << 4, c1 = ((2 * t4 + 1) ^ g) << 4;
-    unpack8(r0, lds16(blk + g * 128 + c0), lds16(blk + g * 128 + c1));
-    unpack8(r1, lds16(blk + (g + 8) * 128 + c0), lds16(blk + (g + 8) * 128 + c1));
+// Row `row` of a 128-byte-swizzled box: the lane's columns [16*t4, 16*t4+16).
+__device__ __forceinline__ void load_row(const unsigned char* box, int row, int t4, uint32_t (&r)[8]) {
+    const int sw = row & 7;
+    unpack8(r, lds16(box + row * 128 + (((2 * t4) ^ sw) << 4)),
+            lds16(box + row * 128 + (((2 * t4 + 1) ^ sw) << 4)));
 }
 
-__device__ __forceinline__ void mma_block(float (&acc)[4], const uint32_t (&r0)[8], const uint32_t (&r1)[8],
-                                          const uint32_t (&xb)[8]) {
+// Two independent 16-row weight blocks (rows r0/r1 and q0/q1) times the same
+// token block, the four k-steps of a 64-column block, chains interleaved.
+__device__ __forceinline__ void mma_pair(float (&acc0)[4], float (&acc1)[4], const uint32_t (&r0)[8],
+                                         const uint32_t (&r1)[8], const uint32_t (&q0)[8],
+                                         const uint32_t (&q1)[8], const uint32_t (&xb)[8]) {
 #pragma unroll
-    for (int s = 0; s < 4; ++s)
-        mma_bf16_16816(acc, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xb[2 * s], xb[2 * s + 1]);
+    for (int s = 0; s < 4; ++s) {
+        mma_bf16_16816(acc0, r0[2 * s], r1[2 * s], r0[2 * s + 1], r1[2 * s + 1], xb[2 * s], xb[2 * s + 1]);
+        mma_bf16_16816(acc1, q0[2 * s], q1[2 * s], q0[2 * s + 1], q1[2 * s + 1], xb[2 * s], xb[2 * s + 1]);
+    }
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
+struct Ranges {
+    long long a_beg, a_end, b_beg, b_end;
+    int rbA, rbB, SA, SB, Tn, Ctot;
+};
+
+// Consumer side of one tile: wait for each stage, multiply, release it.
+// M-blocks: phase A = (gate rows 0-15, up rows 0-15) at byte offsets 0 and
+// 8192 of the weight part; phase B = (down rows 0-15, rows 16-31) of a
+// 32-row box, 2048 bytes apart.
+template <bool PHASE_A>
+__device__ __forceinline__ void consume_tile(const unsigned char* ring, Smem& S, uint32_t* flags, int nstage,
+                                             int K, int NT, uint32_t& it, float (&acc)[2][kNT][4]) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int j = 0; j < kNT; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.f;
+    for (int s = 0; s < nstage; ++s, ++it) {
+        const int slot = it % kStages;
+        const int kq = min(4, (K - 256 * s) / 64);
+        wait_bar(&S.full[slot], (it / kStages) & 1, S, flags);
+        if (w < kq) {
+            const unsigned char* st = ring + (size_t)slot * kSlotBytes;
+            const unsigned char* op = st + kWBytes + w * kNT * 1024;
+            const unsigned char* b0 = PHASE_A ? st + w * 2048 : st + w * 4096;
+            const unsigned char* b1 = PHASE_A ? st + 8192 + w * 2048 : st + w * 4096;
+            const int r1 = PHASE_A ? 0 : 16;
+            uint32_t a0[8], a1[8], c0[8], c1[8];
+            load_row(b0, g, t4, a0);
+            load_row(b0, g + 8, t4, a1);
+            load_row(b1, r1 + g, t4, c0);
+            load_row(b1, r1 + g + 8, t4, c1);
+#pragma unroll
+            for (int j = 0; j < kNT; ++j)
+                if (j < NT) {
+                    uint32_t X[8];
+                    load_row(op + j * 1024, g, t4, X);
+                    mma_pair(acc[0][j], acc[1][j], a0, a1, c0, c1, X);
+                }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.empty[slot]);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
-                const __grid_constant__ CUtensorMap tm_up, const __grid_constant__ CUtensorMap tm_down) {
+                const __grid_constant__ CUtensorMap tm_up, const __grid_constant__ CUtensorMap tm_down,
+                const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_h) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Smem& S = *reinterpret_cast<Smem*>(ring + (size_t)kStages * kStageBytes);
+    Smem& S = *reinterpret_cast<Smem*>(ring + (size_t)kStages * kSlotBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = A.d, F = A.F;
     uint32_t* flags = &A.hdr->flags;
+    const uint32_t G = gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&S.full[i], 1);
+            mbar_init(&S.full[i], 2);        // weight producer + operand producer
             mbar_init(&S.empty[i], kCW);
         }
         fence_barrier_init();
@@ -152,12 +240,18 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         if (threadIdx.x == 0 && blockIdx.x == 0) raise_flag(flags, kFlagBadIndex);
         Tn = 0;
     }
-    if (warp == 0) {   // chunk offsets of the active experts
+    if (warp == 0) {   // per-expert metadata and chunk offsets of the active experts
         int run = 0;
         if (lane == 0) S.chunk_off[0] = 0;
         for (int a0 = 0; a0 < Tn; a0 += 32) {
             const int a = a0 + lane;
-            const int nch = a < Tn ? (A.counts[A.active[a]] + kChunk - 1) / kChunk : 0;
+            int nch = 0;
+            if (a < Tn) {
+                const int e = A.active[a];
+                const int cnt = A.counts[e];
+                S.ex_info[a] = (uint32_t)e | ((uint32_t)cnt << 10) | ((uint32_t)A.offsets[e] << 19);
+                nch = (cnt + kChunk - 1) / kChunk;
+            }
             int inc = nch;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -168,259 +262,236 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
             run += __shfl_sync(0xffffffffu, inc, 31);
         }
     }
-    if (warp == kCW && lane == 0) {
+    if (warp == kWarpW && lane == 0) {
         prefetch_tensormap(&tm_gate);
         prefetch_tensormap(&tm_up);
         prefetch_tensormap(&tm_down);
     }
+    if (warp == kWarpO && lane == 0) {
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_h);
+    }
     __syncthreads();
 
-    const int Ctot = S.chunk_off[Tn];
-    const int rbA = F / 16, rbB = d / 32;
-    const long long TA = (long long)Ctot * rbA, TB = (long long)Ctot * rbB;
-    const long long G = gridDim.x, b = blockIdx.x;
-    const long long a_beg = TA * b / G, a_end = TA * (b + 1) / G;
-    const long long b_beg = TB * b / G, b_end = TB * (b + 1) / G;
-    const int SA = (d + 255) / 256, SB = (F + 255) / 256;
+    Ranges R;
+    R.Tn = Tn;
+    R.Ctot = S.chunk_off[Tn];
+    R.rbA = F / 16;
+    R.rbB = d / 32;
+    {
+        const long long TA = (long long)R.Ctot * R.rbA, TB = (long long)R.Ctot * R.rbB;
+        const long long b = blockIdx.x;
+        R.a_beg = TA * b / G;
+        R.a_end = TA * (b + 1) / G;
+        R.b_beg = TB * b / G;
+        R.b_end = TB * (b + 1) / G;
+    }
+    R.SA = (d + 255) / 256;
+    R.SB = (F + 255) / 256;
 
-    if (warp == kCW) {
-        // ------------------------------ producer ------------------------------
+    if (warp == kWarpW) {
+        // ---------------------------- weight producer ----------------------------
         if (lane == 0) {
-            const uint64_t pol = l2_evict_first_policy();
+            const uint64_t pol_once = l2_evict_first_policy();
+            const uint64_t pol_keep = l2_evict_normal_policy();
             uint32_t it = 0;
-            for (long long t = a_beg; t < a_end; ++t) {
-                const Tile T = decode_tile(t, rbA, S.chunk_off, Tn, A);
+            for (long long t = R.a_beg; t < R.a_end; ++t) {
+                const Tile T = decode_tile(t, R.rbA, S, Tn);
                 const int row = T.e * F + 16 * T.rb;
-                for (int s = 0; s < SA; ++s, ++it) {
+                const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
+                for (int s = 0; s < R.SA; ++s, ++it) {
                     const int slot = it % kStages;
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
                     const int kq = min(4, (d - 256 * s) / 64);
                     mbar_arrive_expect_tx(&S.full[slot], kq * 2 * 2048);
-                    unsigned char* dst = ring + (size_t)slot * kStageBytes;
+                    unsigned char* dst = ring + (size_t)slot * kSlotBytes;
                     for (int q = 0; q < kq; ++q) {
                         tma_load_2d(dst + q * 2048, &tm_gate, 256 * s + 64 * q, row, &S.full[slot], pol);
                         tma_load_2d(dst + 8192 + q * 2048, &tm_up, 256 * s + 64 * q, row, &S.full[slot], pol);
                     }
                 }
             }
-            for (long long t = b_beg; t < b_end; ++t) {
-                const Tile T = decode_tile(t, rbB, S.chunk_off, Tn, A);
+            for (long long t = R.b_beg; t < R.b_end; ++t) {
+                const Tile T = decode_tile(t, R.rbB, S, Tn);
                 const int row = T.e * d + 32 * T.rb;
-                for (int s = 0; s < SB; ++s, ++it) {
+                const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
+                for (int s = 0; s < R.SB; ++s, ++it) {
                     const int slot = it % kStages;
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
                     const int kq = min(4, (F - 256 * s) / 64);
                     mbar_arrive_expect_tx(&S.full[slot], kq * 4096);
-                    unsigned char* dst = ring + (size_t)slot * kStageBytes;
+                    unsigned char* dst = ring + (size_t)slot * kSlotBytes;
                     for (int q = 0; q < kq; ++q)
                         tma_load_2d(dst + q * 4096, &tm_down, 256 * s + 64 * q, row, &S.full[slot], pol);
                 }
             }
             // Every issued stage is consumed before the consumers reach the
-            // final barrier, so no copy is in flight when the CTA exits.
+            // end, so no copy is in flight when the CTA exits.
+        }
+        __syncwarp();
+    } else if (warp == kWarpO) {
+        // ---------------------------- operand producer ---------------------------
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_last_policy();
+            uint32_t it = 0;
+            if (R.a_end > R.a_beg) {
+                wait_counter(&A.hdr->gather_done, G, S, flags);
+                fence_proxy_async_global();
+            }
+            for (long long t = R.a_beg; t < R.a_end; ++t) {
+                const Tile T = decode_tile(t, R.rbA, S, Tn);
+                const int nt = (T.ntok + 7) >> 3;
+                const int row0 = T.off + kChunk * T.c;
+                for (int s = 0; s < R.SA; ++s, ++it) {
+                    const int slot = it % kStages;
+                    if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
+                    const int kq = min(4, (d - 256 * s) / 64);
+                    mbar_arrive_expect_tx(&S.full[slot], kq * nt * 1024);
+                    unsigned char* dst = ring + (size_t)slot * kSlotBytes + kWBytes;
+                    for (int q = 0; q < kq; ++q)
+                        for (int j = 0; j < nt; ++j)
+                            tma_load_2d(dst + (q * kNT + j) * 1024, &tm_x, 256 * s + 64 * q, row0 + 8 * j,
+                                        &S.full[slot], pol);
+                }
+            }
+            if (R.b_end > R.b_beg) {   // every h row is written once all CTAs finished phase A
+                wait_counter(&A.hdr->a_done, G, S, flags);
+                fence_proxy_async_global();
+            }
+            for (long long t = R.b_beg; t < R.b_end; ++t) {
+                const Tile T = decode_tile(t, R.rbB, S, Tn);
+                const int nt = (T.ntok + 7) >> 3;
+                const int row0 = T.off + kChunk * T.c;
+                for (int s = 0; s < R.SB; ++s, ++it) {
+                    const int slot = it % kStages;
+                    if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
+                    const int kq = min(4, (F - 256 * s) / 64);
+                    mbar_arrive_expect_tx(&S.full[slot], kq * nt * 1024);
+                    unsigned char* dst = ring + (size_t)slot * kSlotBytes + kWBytes;
+                    for (int q = 0; q < kq; ++q)
+                        for (int j = 0; j < nt; ++j)
+                            tma_load_2d(dst + (q * kNT + j) * 1024, &tm_h, 256 * s + 64 * q, row0 + 8 * j,
+                                        &S.full[slot], pol);
+                }
+            }
         }
         __syncwarp();
     } else {
-        // ------------------------------ consumers -----------------------------
-        const int w = warp, g = lane >> 2, t4 = lane & 3, tid = threadIdx.x;
-        const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(A.x);
+        // ------------------------------- consumers -------------------------------
+        const int w = warp, tid = threadIdx.x;
         __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
-        uint32_t it = 0;
+        const int P = A.offsets[A.N];
 
-        // ---- phase A: h = silu(W_gate x) * (W_up x) ----
-        for (long long t = a_beg; t < a_end; ++t) {
-            const Tile T = decode_tile(t, rbA, S.chunk_off, Tn, A);
-            const int NT = (T.ntok + 7) >> 3;
-            const __nv_bfloat16* xr[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int nn = 8 * j + g;
-                xr[j] = nullptr;
-                if (nn < T.ntok) {
-                    const int tok = A.perm[T.off + kChunk * T.c + nn] / A.kslots;
-                    xr[j] = xg + (size_t)tok * d;
-                }
+        // Prologue: this CTA's share of the expert-grouped hidden states.
+        {
+            const long long b = blockIdx.x;
+            const int p0 = (int)((long long)P * b / G), p1 = (int)((long long)P * (b + 1) / G);
+            const int vpr = d / 8;   // 16-byte vectors per row
+            const uint4* xs = static_cast<const uint4*>(A.x);
+            uint4* xp = static_cast<uint4*>(A.xperm);
+            for (long long v = tid; v < (long long)(p1 - p0) * vpr; v += kCW * 32) {
+                const int pr = p0 + (int)(v / vpr), c = (int)(v % vpr);
+                const int tok = A.perm[pr] / A.kslots;
+                xp[(size_t)pr * vpr + c] = __ldg(xs + (size_t)tok * vpr + c);
             }
-            float acc[2][4][4];
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.f;
-
-            for (int s = 0; s < SA; ++s, ++it) {
-                const int slot = it % kStages;
-                const int kq = min(4, (d - 256 * s) / 64);
-                const bool has = w < kq;
-                uint32_t X[4][8];
-                const int col = 256 * s + 64 * w + 16 * t4;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                    if (has && j < NT && xr[j]) {
-                        lo = __ldg(reinterpret_cast<const uint4*>(xr[j] + col));
-                        hi = __ldg(reinterpret_cast<const uint4*>(xr[j] + col + 8));
-                    }
-                    unpack8(X[j], lo, hi);
-                }
-                wait_bar(&S.full[slot], (it / kStages) & 1, S, flags);
-                if (has) {
-                    const unsigned char* st = ring + (size_t)slot * kStageBytes;
-                    uint32_t g0[8], g1[8], u0[8], u1[8];
-                    load_a_block(st + w * 2048, g, t4, g0, g1);
-                    load_a_block(st + 8192 + w * 2048, g, t4, u0, u1);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (j < NT) {
-                            mma_block(acc[0][j], g0, g1, X[j]);
-                            mma_block(acc[1][j], u0, u1, X[j]);
-                        }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.empty[slot]);
-            }
-            // reduce the four warps, SwiGLU, store h
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) S.red[w][(m * 4 + j) * 128 + lane * 4 + q] = acc[m][j][q];
             named_barrier(1, kCW * 32);
-            for (int l = tid; l < 512; l += kCW * 32) {
+            if (tid == 0) {
+                __threadfence();
+                atomicAdd(&A.hdr->gather_done, 1u);
+            }
+        }
+
+        uint32_t it = 0;
+        int buf = 0;
+        float acc[2][kNT][4];
+        // ---- phase A: h = silu(W_gate x) * (W_up x) ----
+        for (long long t = R.a_beg; t < R.a_end; ++t, buf ^= 1) {
+            const Tile T = decode_tile(t, R.rbA, S, Tn);
+            const int NT = (T.ntok + 7) >> 3;
+            consume_tile<true>(ring, S, flags, R.SA, d, NT, it, acc);
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int j = 0; j < kNT; ++j)
+                    if (j < NT)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            S.red[buf][w][(m * kNT + j) * 128 + lane * 4 + q] = acc[m][j][q];
+            named_barrier(1, kCW * 32);
+            // element l = j*128 + lane*4 + q of the gate partials (up at +kNT*128)
+            for (int l = tid; l < NT * 128; l += kCW * 32) {
                 const int j = l >> 7, ln = (l >> 2) & 31, q = l & 3;
                 const int nn = 8 * j + 2 * (ln & 3) + (q & 1);
                 if (nn < T.ntok) {
                     float gs = 0.f, us = 0.f;
 #pragma unroll
                     for (int ww = 0; ww < kCW; ++ww) {
-                        gs += S.red[ww][j * 128 + ln * 4 + q];
-                        us += S.red[ww][(4 + j) * 128 + ln * 4 + q];
+                        gs += S.red[buf][ww][l];
+                        us += S.red[buf][ww][kNT * 128 + l];
                     }
                     const int row = (ln >> 2) + 8 * (q >> 1);
                     const size_t pos = (size_t)T.off + kChunk * T.c + nn;
                     hb[pos * F + 16 * T.rb + row] = __float2bfloat16_rn(silu_f(gs) * us);
                 }
             }
+        }
+        named_barrier(1, kCW * 32);
+        if (tid == 0) {   // this CTA's h rows are written
             __threadfence();
-            named_barrier(1, kCW * 32);
-            if (tid == 0) atomicAdd(&A.hdone[T.a], 1u);
+            atomicAdd(&A.hdr->a_done, 1u);
         }
 
-        // ---- phase B: y = W_down h, combine when an output block is complete ----
-        int ready_a = -1;
-        for (long long t = b_beg; t < b_end; ++t) {
-            const Tile T = decode_tile(t, rbB, S.chunk_off, Tn, A);
+        // ---- phase B: y = W_down h ----
+        for (long long t = R.b_beg; t < R.b_end; ++t, buf ^= 1) {
+            const Tile T = decode_tile(t, R.rbB, S, Tn);
             const int NT = (T.ntok + 7) >> 3;
-            if (T.a != ready_a) {
-                if (tid == 0) {
-                    const uint32_t need = (uint32_t)rbA * (S.chunk_off[T.a + 1] - S.chunk_off[T.a]);
-                    const long long t0 = clock64();
-                    while (ld_acquire_gpu(&A.hdone[T.a]) < need) {
-                        if (*(volatile int*)&S.abort_flag) break;
-                        if (clock64() - t0 > kWaitCycles) {
-                            *(volatile int*)&S.abort_flag = 1;
-                            raise_flag(flags, kFlagTimeout);
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                }
-                named_barrier(1, kCW * 32);
-                ready_a = T.a;
-            }
-            const __nv_bfloat16* hr[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int nn = 8 * j + g;
-                hr[j] = nn < T.ntok ? hb + ((size_t)T.off + kChunk * T.c + nn) * F : nullptr;
-            }
-            float acc[2][4][4];
+            consume_tile<false>(ring, S, flags, R.SB, F, NT, it, acc);
 #pragma unroll
             for (int m = 0; m < 2; ++m)
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < kNT; ++j)
+                    if (j < NT)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.f;
-
-            for (int s = 0; s < SB; ++s, ++it) {
-                const int slot = it % kStages;
-                const int kq = min(4, (F - 256 * s) / 64);
-                const bool has = w < kq;
-                uint32_t X[4][8];
-                const int col = 256 * s + 64 * w + 16 * t4;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-                    if (has && j < NT && hr[j]) {
-                        lo = __ldcg(reinterpret_cast<const uint4*>(hr[j] + col));
-                        hi = __ldcg(reinterpret_cast<const uint4*>(hr[j] + col + 8));
-                    }
-                    unpack8(X[j], lo, hi);
-                }
-                wait_bar(&S.full[slot], (it / kStages) & 1, S, flags);
-                if (has) {
-                    const unsigned char* st = ring + (size_t)slot * kStageBytes + w * 4096;
-                    uint32_t a0[8], a1[8], b0[8], b1[8];
-                    load_a_block(st, g, t4, a0, a1);
-                    load_a_block(st + 2048, g, t4, b0, b1);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (j < NT) {
-                            mma_block(acc[0][j], a0, a1, X[j]);
-                            mma_block(acc[1][j], b0, b1, X[j]);
-                        }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&S.empty[slot]);
-            }
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) S.red[w][(m * 4 + j) * 128 + lane * 4 + q] = acc[m][j][q];
+                        for (int q = 0; q < 4; ++q)
+                            S.red[buf][w][(m * kNT + j) * 128 + lane * 4 + q] = acc[m][j][q];
             named_barrier(1, kCW * 32);
-            for (int l = tid; l < 1024; l += kCW * 32) {
-                const int m = l >> 9, j = (l >> 7) & 3, ln = (l >> 2) & 31, q = l & 3;
+            for (int l = tid; l < 2 * kNT * 128; l += kCW * 32) {
+                const int m = l / (kNT * 128), j = (l >> 7) % kNT, ln = (l >> 2) & 31, q = l & 3;
                 const int nn = 8 * j + 2 * (ln & 3) + (q & 1);
-                if (nn < T.ntok) {
+                if (j < NT && nn < T.ntok) {
                     float ys = 0.f;
 #pragma unroll
-                    for (int ww = 0; ww < kCW; ++ww) ys += S.red[ww][l];
+                    for (int ww = 0; ww < kCW; ++ww) ys += S.red[buf][ww][l];
                     const int row = 16 * m + (ln >> 2) + 8 * (q >> 1);
                     const size_t pos = (size_t)T.off + kChunk * T.c + nn;
                     A.ybuf[pos * d + 32 * T.rb + row] = ys;
                 }
             }
-            __threadfence();
-            named_barrier(1, kCW * 32);
-            if (tid == 0) {
-                const uint32_t old = atomicAdd(&A.ydone[T.rb], 1u);
-                S.combine_flag = (old + 1 == (uint32_t)Ctot);
-                __threadfence();
-            }
-            named_barrier(1, kCW * 32);
-            if (S.combine_flag) {
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(A.out);
-                const int c0 = 32 * T.rb;
-                for (int l = tid; l < A.B * 32; l += kCW * 32) {
-                    const int i = l >> 5, jr = l & 31;
-                    float acc2 = 0.f;
-                    for (int sl = 0; sl < A.kslots; ++sl) {
-                        const int pos = A.pos_of[i * A.kslots + sl];
-                        if (pos >= 0) acc2 += A.w[i * A.kslots + sl] * __ldcg(A.ybuf + (size_t)pos * d + c0 + jr);
-                    }
-                    out[(size_t)i * d + c0 + jr] = __float2bfloat16_rn(acc2);
-                }
-            }
-            named_barrier(1, kCW * 32);
         }
 
-        if (Ctot == 0 && blockIdx.x == 0) {   // nothing routed: the output is zero
+        // ---- combine: after every CTA finished phase B, each combines a slice ----
+        named_barrier(1, kCW * 32);
+        if (tid == 0) {
+            __threadfence();
+            atomicAdd(&A.hdr->b_done, 1u);
+            wait_counter(&A.hdr->b_done, G, S, flags);
+            __threadfence();
+        }
+        named_barrier(1, kCW * 32);
+        {
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(A.out);
-            for (long long l = tid; l < (long long)A.B * d; l += kCW * 32) out[l] = __float2bfloat16_rn(0.f);
+            const long long total = (long long)A.B * d;
+            const long long b = blockIdx.x;
+            const long long o0 = total * b / G, o1 = total * (b + 1) / G;
+            for (long long o = o0 + tid; o < o1; o += kCW * 32) {
+                const int i = (int)(o / d), jc = (int)(o % d);
+                float acc2 = 0.f;
+                for (int sl = 0; sl < A.kslots; ++sl) {
+                    const int pos = A.pos_of[i * A.kslots + sl];
+                    if (pos >= 0) acc2 += A.w[i * A.kslots + sl] * __ldcg(A.ybuf + (size_t)pos * d + jc);
+                }
+                out[o] = __float2bfloat16_rn(acc2);
+            }
         }
     }
 
@@ -429,14 +500,15 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
     if (threadIdx.x == 0) {
         __threadfence();
         const uint32_t old = atomicAdd(&A.hdr->ctas_done, 1u);
-        S.last_flag = (old + 1 == gridDim.x);
+        S.last_flag = (old + 1 == G);
     }
     __syncthreads();
-    if (S.last_flag) {
+    if (S.last_flag && threadIdx.x == 0) {
         __threadfence();
-        for (int i = threadIdx.x; i < A.N; i += kThreads) A.hdone[i] = 0;
-        for (int i = threadIdx.x; i < d / 32; i += kThreads) A.ydone[i] = 0;
-        if (threadIdx.x == 0) A.hdr->ctas_done = 0;
+        A.hdr->gather_done = 0;
+        A.hdr->a_done = 0;
+        A.hdr->b_done = 0;
+        A.hdr->ctas_done = 0;
     }
 }
 
@@ -450,8 +522,18 @@ cudaError_t launch_ffn_bf16(const FfnArgs& a, const CUtensorMap* maps, int num_s
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    ffn_bf16_kernel<<<num_sms, kThreads, kSmemBytes, s>>>(a, maps[0], maps[1], maps[2]);
-    return cudaGetLastError();
+    // Cooperative: all CTAs are resident at once (they meet at grid-wide counters).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ffn_bf16_kernel, a, maps[0], maps[1], maps[2], maps[3], maps[4]);
 }
 
 size_t ffn_bf16_smem_bytes() { return kSmemBytes; }
