@@ -141,14 +141,20 @@ std::mutex g_map_mu;
 MapEntry g_maps[64];
 int g_map_next = 0;
 
-bool encode_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+// A row-major bf16 matrix [rows][cols] (cols a multiple of 64) viewed as 3D
+// {64 columns, rows, cols/64 column blocks}: one box {64, box_rows, 4} moves
+// 256 columns of box_rows rows and lands in shared memory as four
+// consecutive 128-byte-swizzled [box_rows][64] blocks.  One TMA operation
+// per 256 columns keeps the per-operation cost of the TMA unit off the
+// critical path.
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
     auto enc = get_encode();
     if (!enc) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    cuuint64_t dims[3] = {64, rows, cols / 64};
+    cuuint64_t strides[2] = {cols * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, 4};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -167,8 +173,8 @@ moe_status expert_maps(const void* g, const void* u, const void* dn, int N, int 
     g_map_next = (g_map_next + 1) % 64;
     e.key = key;
     e.used = false;
-    if (!encode_2d(&e.maps[0], g, d, (uint64_t)N * F, 16) || !encode_2d(&e.maps[1], u, d, (uint64_t)N * F, 16) ||
-        !encode_2d(&e.maps[2], dn, F, (uint64_t)N * d, 32))
+    if (!encode_3d(&e.maps[0], g, d, (uint64_t)N * F, 16) || !encode_3d(&e.maps[1], u, d, (uint64_t)N * F, 16) ||
+        !encode_3d(&e.maps[2], dn, F, (uint64_t)N * d, 32))
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     e.used = true;
     memcpy(out, e.maps, sizeof e.maps);
@@ -202,7 +208,7 @@ moe_status workspace_maps(unsigned char* ws, const WsLayout& L, int pairs, int d
     e.d = d;
     e.F = F;
     e.dev = dev;
-    if (!encode_2d(&e.maps[0], ws + L.xperm, d, pairs, 8) || !encode_2d(&e.maps[1], ws + L.hbuf, F, pairs, 8))
+    if (!encode_3d(&e.maps[0], ws + L.xperm, d, pairs, 8) || !encode_3d(&e.maps[1], ws + L.hbuf, F, pairs, 8))
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (workspace)");
     e.used = true;
     memcpy(out, e.maps, sizeof e.maps);

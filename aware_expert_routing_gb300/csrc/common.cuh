@@ -105,7 +105,9 @@ struct FfnArgs {
 // Launchers (defined in the .cu files).
 cudaError_t launch_router(const RouterArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
-// maps: W_gate, W_up, W_down, gathered hidden states, SwiGLU buffer h.
+// maps (3D views {64 columns, rows, column blocks of 64}, 128-byte swizzle,
+// boxes of 4 column blocks): W_gate and W_up (16 rows), W_down (32 rows),
+// gathered hidden states and SwiGLU buffer h (8 rows).
 cudaError_t launch_ffn_bf16(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s);
 cudaError_t launch_ffn_f32(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_synth(void* dst, int dtype, uint64_t n, uint64_t start, uint64_t seed,
@@ -186,6 +188,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;"
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+          "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
           "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }

@@ -20,7 +20,9 @@
 //   * A stage of the 8-deep shared-memory ring holds 256 K-columns of the
 //     weight tile (16 KB: gate+up rows, or 32 down rows) and the matching
 //     columns of the tokens' operand rows (up to 16 rows, 8 KB), all loaded
-//     by TMA with the 128-byte swizzle.  Warp 4 issues the weight loads and
+//     by TMA with the 128-byte swizzle through 3D views of the matrices, so
+//     a stage is one or two weight operations plus one per 8 tokens (the
+//     TMA unit's cost per operation, not per byte, limits small boxes).  Warp 4 issues the weight loads and
 //     never waits for another CTA, so the weight stream runs on across the
 //     phase boundary.  Weights read once are marked L2 evict-first; an
 //     expert with more than 16 tokens is read once per 16-token pass, the
@@ -57,7 +59,7 @@ constexpr int kThreads = (kCW + 2) * 32;
 constexpr int kNT = 2;                    // MMA column tiles (8 tokens each) per pass
 constexpr int kChunk = 8 * kNT;           // tokens per tile pass
 constexpr int kWBytes = 16384;            // weight part of a stage
-constexpr int kOBytes = 4 * kNT * 1024;   // operand part: 4 column blocks x kNT boxes of 8 rows
+constexpr int kOBytes = kNT * 4096;       // operand part: kNT boxes of 8 rows x 4 column blocks
 constexpr int kSlotBytes = kWBytes + kOBytes;
 constexpr int kStages = 8;
 constexpr int kRed = 2 * 4 * kNT * 32;    // partial sums per warp per tile (2 M-tiles)
@@ -191,7 +193,7 @@ __device__ __forceinline__ void consume_tile(const unsigned char* ring, Smem& S,
         wait_bar(&S.full[slot], (it / kStages) & 1, S, flags);
         if (w < kq) {
             const unsigned char* st = ring + (size_t)slot * kSlotBytes;
-            const unsigned char* op = st + kWBytes + w * kNT * 1024;
+            const unsigned char* op = st + kWBytes + w * 1024;
             const unsigned char* b0 = PHASE_A ? st + w * 2048 : st + w * 4096;
             const unsigned char* b1 = PHASE_A ? st + 8192 + w * 2048 : st + w * 4096;
             const int r1 = PHASE_A ? 0 : 16;
@@ -204,7 +206,7 @@ __device__ __forceinline__ void consume_tile(const unsigned char* ring, Smem& S,
             for (int j = 0; j < kNT; ++j)
                 if (j < NT) {
                     uint32_t X[8];
-                    load_row(op + j * 1024, g, t4, X);
+                    load_row(op + j * 4096, g, t4, X);
                     mma_pair(acc[0][j], acc[1][j], a0, a1, c0, c1, X);
                 }
         }
@@ -302,13 +304,10 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
                 for (int s = 0; s < R.SA; ++s, ++it) {
                     const int slot = it % kStages;
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    const int kq = min(4, (d - 256 * s) / 64);
-                    mbar_arrive_expect_tx(&S.full[slot], kq * 2 * 2048);
+                    mbar_arrive_expect_tx(&S.full[slot], kWBytes);   // column blocks past d are zero-filled
                     unsigned char* dst = ring + (size_t)slot * kSlotBytes;
-                    for (int q = 0; q < kq; ++q) {
-                        tma_load_2d(dst + q * 2048, &tm_gate, 256 * s + 64 * q, row, &S.full[slot], pol);
-                        tma_load_2d(dst + 8192 + q * 2048, &tm_up, 256 * s + 64 * q, row, &S.full[slot], pol);
-                    }
+                    tma_load_3d(dst, &tm_gate, 0, row, 4 * s, &S.full[slot], pol);
+                    tma_load_3d(dst + 8192, &tm_up, 0, row, 4 * s, &S.full[slot], pol);
                 }
             }
             for (long long t = R.b_beg; t < R.b_end; ++t) {
@@ -318,11 +317,8 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
                 for (int s = 0; s < R.SB; ++s, ++it) {
                     const int slot = it % kStages;
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    const int kq = min(4, (F - 256 * s) / 64);
-                    mbar_arrive_expect_tx(&S.full[slot], kq * 4096);
-                    unsigned char* dst = ring + (size_t)slot * kSlotBytes;
-                    for (int q = 0; q < kq; ++q)
-                        tma_load_2d(dst + q * 4096, &tm_down, 256 * s + 64 * q, row, &S.full[slot], pol);
+                    mbar_arrive_expect_tx(&S.full[slot], kWBytes);
+                    tma_load_3d(ring + (size_t)slot * kSlotBytes, &tm_down, 0, row, 4 * s, &S.full[slot], pol);
                 }
             }
             // Every issued stage is consumed before the consumers reach the
@@ -345,13 +341,10 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
                 for (int s = 0; s < R.SA; ++s, ++it) {
                     const int slot = it % kStages;
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    const int kq = min(4, (d - 256 * s) / 64);
-                    mbar_arrive_expect_tx(&S.full[slot], kq * nt * 1024);
+                    mbar_arrive_expect_tx(&S.full[slot], nt * 4096);
                     unsigned char* dst = ring + (size_t)slot * kSlotBytes + kWBytes;
-                    for (int q = 0; q < kq; ++q)
-                        for (int j = 0; j < nt; ++j)
-                            tma_load_2d(dst + (q * kNT + j) * 1024, &tm_x, 256 * s + 64 * q, row0 + 8 * j,
-                                        &S.full[slot], pol);
+                    for (int j = 0; j < nt; ++j)
+                        tma_load_3d(dst + j * 4096, &tm_x, 0, row0 + 8 * j, 4 * s, &S.full[slot], pol);
                 }
             }
             if (R.b_end > R.b_beg) {   // every h row is written once all CTAs finished phase A
@@ -365,13 +358,10 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
                 for (int s = 0; s < R.SB; ++s, ++it) {
                     const int slot = it % kStages;
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    const int kq = min(4, (F - 256 * s) / 64);
-                    mbar_arrive_expect_tx(&S.full[slot], kq * nt * 1024);
+                    mbar_arrive_expect_tx(&S.full[slot], nt * 4096);
                     unsigned char* dst = ring + (size_t)slot * kSlotBytes + kWBytes;
-                    for (int q = 0; q < kq; ++q)
-                        for (int j = 0; j < nt; ++j)
-                            tma_load_2d(dst + (q * kNT + j) * 1024, &tm_h, 256 * s + 64 * q, row0 + 8 * j,
-                                        &S.full[slot], pol);
+                    for (int j = 0; j < nt; ++j)
+                        tma_load_3d(dst + j * 4096, &tm_h, 0, row0 + 8 * j, 4 * s, &S.full[slot], pol);
                 }
             }
         }
