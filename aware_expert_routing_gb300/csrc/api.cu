@@ -332,6 +332,7 @@ moe_status moe_expert_ffn(const void* hidden, const void* w_gate, const void* w_
     a.out = out;
     a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone);
     a.ydone = reinterpret_cast<uint32_t*>(ws + L.ydone);
+    a.gflag = reinterpret_cast<uint32_t*>(ws + L.gflag);
     a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
     a.w_gate = w_gate;
     a.w_up = w_up;
@@ -354,8 +355,9 @@ moe_status moe_expert_ffn(const void* hidden, const void* w_gate, const void* w_
     CUtensorMap maps[5];
     if ((st = expert_maps(w_gate, w_up, w_down, P.N, d_ff, P.d, dev, maps)) != MOE_OK) return st;
     if ((st = workspace_maps(ws, L, P.B * P.kslots, P.d, d_ff, dev, maps + 3)) != MOE_OK) return st;
-    const int sms = num_sms();
+    int sms = num_sms();
     if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
+    if (sms > kMaxGrid) sms = kMaxGrid;
     e = launch_ffn_bf16(a, maps, sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
     return MOE_OK;

@@ -23,17 +23,19 @@ constexpr uint32_t kFlagBadIndex = MOE_FLAG_BAD_INDEX;
 struct WsHeader {
     uint32_t flags;        // MOE_FLAG_* raised by kernels
     uint32_t ctas_done;    // expert kernel: CTAs finished (the last one resets the counters)
-    uint32_t gather_done;  // expert kernel: CTAs that finished their share of the gather
+    uint32_t unused0;
     uint32_t a_done;       // expert kernel: CTAs that finished phase A (h written)
     uint32_t b_done;       // expert kernel: CTAs that finished phase B (y written)
     uint32_t pad[59];
 };
 
 struct WsLayout {
-    size_t header, hdone, ydone, pos_of, logits, hbuf, ybuf, xperm, total;
+    size_t header, hdone, ydone, gflag, pos_of, logits, hbuf, ybuf, xperm, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr int kMaxGrid = 1024;   // largest grid of the persistent expert kernel
 
 // B, N, d, kslots, F: see moe.h.  elt = bytes per element of the FFN width
 // buffer H (bf16 or fp32).
@@ -43,6 +45,7 @@ inline WsLayout ws_layout(int B, int N, int d, int kslots, int F, int h_elt) {
     L.header = o; o += align256(sizeof(WsHeader));
     L.hdone = o;  o += align256(sizeof(uint32_t) * N);
     L.ydone = o;  o += align256(sizeof(uint32_t) * (d / 32 + 1));
+    L.gflag = o;  o += align256(sizeof(uint32_t) * kMaxGrid);
     L.pos_of = o; o += align256(sizeof(int32_t) * (size_t)B * kslots + 4);
     L.logits = o; o += align256(sizeof(float) * (size_t)B * N + 4);
     L.hbuf = o;   o += align256((size_t)B * kslots * F * h_elt);
@@ -95,6 +98,7 @@ struct FfnArgs {
     void* out;              // [B][d]
     uint32_t* hdone;        // [N]
     uint32_t* ydone;        // [d/32]
+    uint32_t* gflag;        // [grid] CTA finished its share of the gather
     WsHeader* hdr;
     const void* w_gate;     // [N][F][d]   (fp32 path)
     const void* w_up;
@@ -247,6 +251,17 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its memory is visible / allow the next kernel in
+// the stream to be scheduled now (it still waits for us before reading).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Named barrier for a subset of warps.

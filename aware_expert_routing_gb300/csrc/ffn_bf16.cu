@@ -8,7 +8,7 @@
 // on chip.  Expert form (Qwen3): y = W_down (silu(W_gate x) * (W_up x));
 // combine: out_i = sum_j w_ij y_{e_ij}(x_i) (kept scores, section 2 Q2).
 //
-// Structure (one persistent CTA per SM, 6 warps, cooperative launch):
+// Structure (one persistent CTA per SM, 6 warps):
 //   * Work is a list of tiles.  Phase-A tile (expert a, 16 rows of d_ff,
 //     token chunk c) computes h = silu(W_gate x) * (W_up x) for those rows
 //     and up to 16 tokens and writes h (bf16) to the workspace.  Phase-B
@@ -16,7 +16,9 @@
 //     Each CTA takes an equal, contiguous share of the phase-A tiles and
 //     then of the phase-B tiles, so every CTA streams the same bytes.
 //   * Prologue: the CTAs copy the hidden states into an expert-grouped
-//     buffer (row p = the token of pair p) and count themselves done.
+//     buffer (row p = the token of pair p; CTA b copies rows b, b+G, ...)
+//     and each raises its own flag; a CTA's operand warp waits only for the
+//     flags of the CTAs that copied the rows its tiles read.
 //   * A stage of the 8-deep shared-memory ring holds 256 K-columns of the
 //     weight tile (16 KB: gate+up rows, or 32 down rows) and the matching
 //     columns of the tokens' operand rows (up to 16 rows, 8 KB), all loaded
@@ -42,8 +44,8 @@
 //     double-buffered shared-memory area and are added in warp order, with
 //     one named barrier per tile; no global fence or atomic per tile.
 //   * After phase B every CTA arrives at a grid-wide counter; once all have
-//     arrived, each CTA combines its slice of the output,
-//     out_i = sum over slots (in slot order) of w_is * y_is.
+//     arrived, each CTA combines its slice of the output four columns at a
+//     time, out_i = sum over slots (in slot order) of w_is * y_is.
 //   * The last CTA to finish resets the counters for the next launch.
 // Every result is computed in a fixed order, so runs are bit-reproducible.
 #include "common.cuh"
@@ -83,12 +85,12 @@ struct Tile {
 };
 
 // Tile t of a phase with rbn row blocks per (expert, chunk); shared memory only.
-__device__ __forceinline__ Tile decode_tile(long long t, int rbn, const Smem& S, int Tn) {
+__device__ __forceinline__ Tile decode_tile(int t, int rbn, const Smem& S, int Tn) {
     const int* chunk_off = S.chunk_off;
     int lo = 0, hi = Tn - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((long long)chunk_off[mid] * rbn <= t) lo = mid; else hi = mid - 1;
+        if (chunk_off[mid] * rbn <= t) lo = mid; else hi = mid - 1;
     }
     Tile T;
     T.a = lo;
@@ -97,9 +99,9 @@ __device__ __forceinline__ Tile decode_tile(long long t, int rbn, const Smem& S,
     const int cnt = (info >> 10) & 511u;
     T.off = info >> 19;
     T.nch = chunk_off[lo + 1] - chunk_off[lo];
-    const long long r = t - (long long)chunk_off[lo] * rbn;
-    T.rb = (int)(r / T.nch);
-    T.c = (int)(r % T.nch);
+    const int r = t - chunk_off[lo] * rbn;
+    T.rb = r / T.nch;
+    T.c = r - T.rb * T.nch;
     T.ntok = min(kChunk, cnt - kChunk * T.c);
     return T;
 }
@@ -169,7 +171,7 @@ __device__ __forceinline__ void mma_pair(float (&acc0)[4], float (&acc1)[4], con
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
 struct Ranges {
-    long long a_beg, a_end, b_beg, b_end;
+    int a_beg, a_end, b_beg, b_end;
     int rbA, rbB, SA, SB, Tn, Ctot;
 };
 
@@ -237,6 +239,7 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         fence_barrier_init();
         S.abort_flag = 0;
     }
+    grid_dependency_wait();      // routing comes from the preceding kernel
     int Tn = *A.T;
     if (Tn < 0 || Tn > A.N) {
         if (threadIdx.x == 0 && blockIdx.x == 0) raise_flag(flags, kFlagBadIndex);
@@ -283,10 +286,10 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
     {
         const long long TA = (long long)R.Ctot * R.rbA, TB = (long long)R.Ctot * R.rbB;
         const long long b = blockIdx.x;
-        R.a_beg = TA * b / G;
-        R.a_end = TA * (b + 1) / G;
-        R.b_beg = TB * b / G;
-        R.b_end = TB * (b + 1) / G;
+        R.a_beg = (int)(TA * b / G);
+        R.a_end = (int)(TA * (b + 1) / G);
+        R.b_beg = (int)(TB * b / G);
+        R.b_end = (int)(TB * (b + 1) / G);
     }
     R.SA = (d + 255) / 256;
     R.SB = (F + 255) / 256;
@@ -297,7 +300,7 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
             const uint64_t pol_once = l2_evict_first_policy();
             const uint64_t pol_keep = l2_evict_normal_policy();
             uint32_t it = 0;
-            for (long long t = R.a_beg; t < R.a_end; ++t) {
+            for (int t = R.a_beg; t < R.a_end; ++t) {
                 const Tile T = decode_tile(t, R.rbA, S, Tn);
                 const int row = T.e * F + 16 * T.rb;
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
@@ -310,7 +313,7 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
                     tma_load_3d(dst + 8192, &tm_up, 0, row, 4 * s, &S.full[slot], pol);
                 }
             }
-            for (long long t = R.b_beg; t < R.b_end; ++t) {
+            for (int t = R.b_beg; t < R.b_end; ++t) {
                 const Tile T = decode_tile(t, R.rbB, S, Tn);
                 const int row = T.e * d + 32 * T.rb;
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
@@ -327,14 +330,19 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         __syncwarp();
     } else if (warp == kWarpO) {
         // ---------------------------- operand producer ---------------------------
+        if (R.a_end > R.a_beg) {   // the rows of this CTA's phase-A tiles are gathered
+            const Tile T0 = decode_tile(R.a_beg, R.rbA, S, Tn);
+            const Tile T1 = decode_tile(R.a_end - 1, R.rbA, S, Tn);
+            const int p_lo = T0.off, p_hi = T1.off + (int)((S.ex_info[T1.a] >> 10) & 511u);
+            const int nown = min((int)G, p_hi - p_lo);
+            for (int c = lane; c < nown; c += 32) wait_counter(&A.gflag[(p_lo + c) % G], 1u, S, flags);
+            __syncwarp();
+            fence_proxy_async_global();
+        }
         if (lane == 0) {
             const uint64_t pol = l2_evict_last_policy();
             uint32_t it = 0;
-            if (R.a_end > R.a_beg) {
-                wait_counter(&A.hdr->gather_done, G, S, flags);
-                fence_proxy_async_global();
-            }
-            for (long long t = R.a_beg; t < R.a_end; ++t) {
+            for (int t = R.a_beg; t < R.a_end; ++t) {
                 const Tile T = decode_tile(t, R.rbA, S, Tn);
                 const int nt = (T.ntok + 7) >> 3;
                 const int row0 = T.off + kChunk * T.c;
@@ -351,7 +359,7 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
                 wait_counter(&A.hdr->a_done, G, S, flags);
                 fence_proxy_async_global();
             }
-            for (long long t = R.b_beg; t < R.b_end; ++t) {
+            for (int t = R.b_beg; t < R.b_end; ++t) {
                 const Tile T = decode_tile(t, R.rbB, S, Tn);
                 const int nt = (T.ntok + 7) >> 3;
                 const int row0 = T.off + kChunk * T.c;
@@ -370,24 +378,38 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         // ------------------------------- consumers -------------------------------
         const int w = warp, tid = threadIdx.x;
         __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
-        const int P = A.offsets[A.N];
 
-        // Prologue: this CTA's share of the expert-grouped hidden states.
+        // Prologue: this CTA's rows of the expert-grouped hidden states
+        // (rows b, b+G, ...), eight 16-byte loads in flight per thread.
         {
-            const long long b = blockIdx.x;
-            const int p0 = (int)((long long)P * b / G), p1 = (int)((long long)P * (b + 1) / G);
+            const int P = A.offsets[A.N];
             const int vpr = d / 8;   // 16-byte vectors per row
+            const int nrow = P > (int)blockIdx.x ? (P - 1 - (int)blockIdx.x) / (int)G + 1 : 0;
+            const int nvec = nrow * vpr;
             const uint4* xs = static_cast<const uint4*>(A.x);
             uint4* xp = static_cast<uint4*>(A.xperm);
-            for (long long v = tid; v < (long long)(p1 - p0) * vpr; v += kCW * 32) {
-                const int pr = p0 + (int)(v / vpr), c = (int)(v % vpr);
-                const int tok = A.perm[pr] / A.kslots;
-                xp[(size_t)pr * vpr + c] = __ldg(xs + (size_t)tok * vpr + c);
+            for (int v0 = 0; v0 < nvec; v0 += 8 * kCW * 32) {
+                uint4 val[8];
+                size_t dst[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int v = v0 + u * kCW * 32 + tid;
+                    dst[u] = ~size_t(0);
+                    if (v < nvec) {
+                        const int r = v / vpr, c = v - r * vpr;
+                        const int pr = (int)blockIdx.x + r * (int)G;
+                        val[u] = __ldg(xs + (size_t)(A.perm[pr] / A.kslots) * vpr + c);
+                        dst[u] = (size_t)pr * vpr + c;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (dst[u] != ~size_t(0)) xp[dst[u]] = val[u];
             }
             named_barrier(1, kCW * 32);
             if (tid == 0) {
                 __threadfence();
-                atomicAdd(&A.hdr->gather_done, 1u);
+                atomicExch(&A.gflag[blockIdx.x], 1u);
             }
         }
 
@@ -395,7 +417,7 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         int buf = 0;
         float acc[2][kNT][4];
         // ---- phase A: h = silu(W_gate x) * (W_up x) ----
-        for (long long t = R.a_beg; t < R.a_end; ++t, buf ^= 1) {
+        for (int t = R.a_beg; t < R.a_end; ++t, buf ^= 1) {
             const Tile T = decode_tile(t, R.rbA, S, Tn);
             const int NT = (T.ntok + 7) >> 3;
             consume_tile<true>(ring, S, flags, R.SA, d, NT, it, acc);
@@ -432,7 +454,7 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         }
 
         // ---- phase B: y = W_down h ----
-        for (long long t = R.b_beg; t < R.b_end; ++t, buf ^= 1) {
+        for (int t = R.b_beg; t < R.b_end; ++t, buf ^= 1) {
             const Tile T = decode_tile(t, R.rbB, S, Tn);
             const int NT = (T.ntok + 7) >> 3;
             consume_tile<false>(ring, S, flags, R.SB, F, NT, it, acc);
@@ -469,18 +491,35 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         }
         named_barrier(1, kCW * 32);
         {
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(A.out);
-            const long long total = (long long)A.B * d;
-            const long long b = blockIdx.x;
-            const long long o0 = total * b / G, o1 = total * (b + 1) / G;
+            const int d4 = d / 4;
+            const long long total = (long long)A.B * d4;   // groups of four columns
+            const long long o0 = total * blockIdx.x / G, o1 = total * (blockIdx.x + 1) / G;
+            const float4* y4 = reinterpret_cast<const float4*>(A.ybuf);
+            uint2* out = static_cast<uint2*>(A.out);
             for (long long o = o0 + tid; o < o1; o += kCW * 32) {
-                const int i = (int)(o / d), jc = (int)(o % d);
-                float acc2 = 0.f;
-                for (int sl = 0; sl < A.kslots; ++sl) {
-                    const int pos = A.pos_of[i * A.kslots + sl];
-                    if (pos >= 0) acc2 += A.w[i * A.kslots + sl] * __ldcg(A.ybuf + (size_t)pos * d + jc);
+                const int i = (int)(o / d4), c4 = (int)(o - (long long)i * d4);
+                float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int s0 = 0; s0 < A.kslots; s0 += 8) {
+                    float4 yv[8];
+                    float wv[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int sl = s0 + u;
+                        const int pos = sl < A.kslots ? A.pos_of[i * A.kslots + sl] : -1;
+                        wv[u] = pos >= 0 ? A.w[i * A.kslots + sl] : 0.f;
+                        yv[u] = pos >= 0 ? __ldcg(y4 + (size_t)pos * d4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {   // slot order
+                        acc2.x += wv[u] * yv[u].x;
+                        acc2.y += wv[u] * yv[u].y;
+                        acc2.z += wv[u] * yv[u].z;
+                        acc2.w += wv[u] * yv[u].w;
+                    }
                 }
-                out[o] = __float2bfloat16_rn(acc2);
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc2.x, acc2.y);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(acc2.z, acc2.w);
+                out[o] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
             }
         }
     }
@@ -493,9 +532,11 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         S.last_flag = (old + 1 == G);
     }
     __syncthreads();
-    if (S.last_flag && threadIdx.x == 0) {
+    if (S.last_flag) {
         __threadfence();
-        A.hdr->gather_done = 0;
+        for (int i = threadIdx.x; i < (int)G; i += kThreads) A.gflag[i] = 0;
+    }
+    if (S.last_flag && threadIdx.x == 0) {
         A.hdr->a_done = 0;
         A.hdr->b_done = 0;
         A.hdr->ctas_done = 0;
@@ -512,15 +553,19 @@ cudaError_t launch_ffn_bf16(const FfnArgs& a, const CUtensorMap* maps, int num_s
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    // Cooperative: all CTAs are resident at once (they meet at grid-wide counters).
+    // One CTA per SM (the shared-memory size allows no second one), so the
+    // whole grid becomes resident once the preceding kernel has left its SM;
+    // the grid-wide counters wait only on CTAs that never wait on anything
+    // launched after them.  Programmatic dependent launch lets the CTAs start
+    // their prologue while the routing kernel finishes.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, ffn_bf16_kernel, a, maps[0], maps[1], maps[2], maps[3], maps[4]);

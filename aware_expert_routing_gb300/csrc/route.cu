@@ -12,14 +12,15 @@
 //   section 7     padding tokens select nothing.
 // Ranking: larger score first, equal scores by the lower expert id.
 //
-// One warp handles one token at a time; lane l holds the scores of experts
-// l, l+32, l+64, ... in registers.  The k-th best expert is found by k rounds
-// of a warp-wide (score, id) arg-max.  The batch union S_base is an N-bit
-// mask in shared memory built with __ballot_sync + atomicOr.  Grouping by
-// expert uses per-token N-bit masks: one warp per expert counts its tokens
-// with ballots, a block scan gives the offsets, and a second ballot pass
-// writes each pair's position (tokens ascending within an expert).
-#include <float.h>
+// One warp handles one token at a time; lane l holds experts l, l+32, ...
+// as order-preserving 32-bit keys of their fp32 scores (the map is a
+// bijection, so a key gives back its exact score).  The next-ranked expert is
+// one warp max-reduction of the keys and one min-reduction of the ids that
+// hold the maximum.  The batch union S_base is an N-bit mask in shared
+// memory built with __ballot_sync + atomicOr.  Grouping by expert: every
+// kept (token, expert) sets bit (token mod 32) of word [token / 32][expert];
+// per-expert counts and per-chunk prefix counts then give each pair's
+// position directly (tokens ascending within an expert).
 #include <limits.h>
 
 #include "common.cuh"
@@ -29,46 +30,48 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxChunks = MOE_MAX_TOKENS / 32;
+
+// Order-preserving key of a finite fp32 score (-0 and +0 map to one key);
+// 0 is below every score and marks "not selectable".
+__device__ __forceinline__ uint32_t score_key(float f) {
+    const uint32_t b = __float_as_uint(f + 0.0f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_score(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 
 template <int NPL>
-__device__ __forceinline__ void load_scores(const float* row, int N, int lane, float (&v)[NPL],
-                                            bool& nonfinite) {
+__device__ __forceinline__ void load_keys(const float* row, int N, int lane, uint32_t (&kv)[NPL], bool& nonfinite) {
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
         const int e = lane + 32 * j;
-        float x = e < N ? row[e] : -INFINITY;
-        if (e < N && !isfinite(x)) {
-            nonfinite = true;
-            x = -INFINITY;
+        uint32_t k = 0;
+        if (e < N) {
+            const float x = row[e];
+            if (isfinite(x)) k = score_key(x); else nonfinite = true;
         }
-        v[j] = x;
+        kv[j] = k;
     }
 }
 
-// Warp-wide arg-max over the scores whose bit in `excl` is clear.
-// Returns -inf / INT_MAX when no candidate is left.
+// Best remaining expert: largest key among entries whose bit in `excl` is
+// clear, lowest expert id among equal keys.  Returns key 0 when none is left.
 template <int NPL>
-__device__ __forceinline__ void warp_argmax(const float (&v)[NPL], uint32_t excl, int lane,
-                                            float& bv, int& bid) {
-    float best = -INFINITY;
-    int id = INT_MAX;
+__device__ __forceinline__ uint32_t warp_best(const uint32_t (&kv)[NPL], uint32_t excl, int lane, int& id) {
+    uint32_t lk = 0;
+    int lid = INT_MAX;
 #pragma unroll
     for (int j = 0; j < NPL; ++j)
-        if (!((excl >> j) & 1u) && v[j] > best) {   // ascending j = ascending id
-            best = v[j];
-            id = lane + 32 * j;
+        if (!((excl >> j) & 1u) && kv[j] > lk) {   // ascending j = ascending id
+            lk = kv[j];
+            lid = lane + 32 * j;
         }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ob = __shfl_xor_sync(kFull, best, off);
-        const int oi = __shfl_xor_sync(kFull, id, off);
-        if (ob > best || (ob == best && oi < id)) {
-            best = ob;
-            id = oi;
-        }
-    }
-    bv = best;
-    bid = id;
+    const uint32_t m = __reduce_max_sync(kFull, lk);
+    id = (int)__reduce_min_sync(kFull, lk == m ? (uint32_t)lid : 0xffffffffu);
+    return m;
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -77,28 +80,20 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
-    return x;
-}
-
 struct RouteSmem {
-    uint32_t* sbase;    // [32]      S_base bit mask
-    int* snb;           // [B]       n_i
-    int* sidx;          // [B][kslots]
-    uint32_t* tokmask;  // [B][NW]   experts kept by each token
-    int* scnt;          // [N]
-    int* soff;          // [N]
-    int* sact;          // [N]
-    int* scan;          // [64]
+    uint32_t* sbase;   // [32]          S_base bit mask
+    int* snb;          // [B]           n_i
+    int* sidx;         // [B][kslots]   kept experts
+    uint32_t* bits;    // [chunks][N]   bit (i mod 32) set if token i keeps expert e
+    int* pre;          // [chunks][N]   tokens of earlier chunks that keep e
+    int* scnt;         // [N]
+    int* soff;         // [N]
+    int* scan;         // [64]
 };
 
-// Writes the routing of token i: lane r < cnt holds slot r (myid, myval);
-// `kept` holds the lane's bits of the token's expert mask.
-template <int NPL>
+// Writes the routing of token i: lane r < cnt holds slot r (myid, myval).
 __device__ __forceinline__ void finish_token(const RouteArgs& a, RouteSmem& sm, int i, int lane, int cnt,
-                                             int myid, float myval, uint32_t kept, int NW) {
+                                             int myid, float myval, int N) {
     const float l0 = __shfl_sync(kFull, myval, 0);
     const float ex = lane < cnt ? expf(myval - l0) : 0.f;
     const float z = warp_sum(ex);
@@ -108,12 +103,8 @@ __device__ __forceinline__ void finish_token(const RouteArgs& a, RouteSmem& sm, 
         a.idx[q] = used ? myid : -1;
         a.w[q] = used ? ex / z : 0.f;
         sm.sidx[q] = used ? myid : -1;
-        if (!used) a.pos_of[q] = -1;
-    }
-#pragma unroll
-    for (int j = 0; j < NPL; ++j) {
-        const uint32_t word = __ballot_sync(kFull, (kept >> j) & 1u);
-        if (lane == 0 && j < NW) sm.tokmask[(size_t)i * NW + j] = word;
+        if (used) atomicOr(&sm.bits[(i >> 5) * N + myid], 1u << (i & 31));
+        else a.pos_of[q] = -1;
     }
 }
 
@@ -124,7 +115,7 @@ __global__ void route_kernel(RouteArgs a) {
     const int nwarps = nthreads >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = a.N, B = a.B;
-    const int NW = (N + 31) >> 5;
+    const int nch = (B + 31) >> 5;
 
     RouteSmem sm;
     unsigned char* p = smem_raw;
@@ -133,64 +124,66 @@ __global__ void route_kernel(RouteArgs a) {
     sm.snb = reinterpret_cast<int*>(p); p += MOE_MAX_TOKENS * 4;
     sm.scnt = reinterpret_cast<int*>(p); p += MOE_MAX_EXPERTS * 4;
     sm.soff = reinterpret_cast<int*>(p); p += MOE_MAX_EXPERTS * 4;
-    sm.sact = reinterpret_cast<int*>(p); p += MOE_MAX_EXPERTS * 4;
     sm.sidx = reinterpret_cast<int*>(p); p += (size_t)B * a.kslots * 4;
-    sm.tokmask = reinterpret_cast<uint32_t*>(p);
+    sm.bits = reinterpret_cast<uint32_t*>(p); p += (size_t)nch * N * 4;
+    sm.pre = reinterpret_cast<int*>(p);
 
     if (threadIdx.x < 32) sm.sbase[threadIdx.x] = 0;
+    for (int q = threadIdx.x; q < nch * N; q += nthreads) sm.bits[q] = 0;
+    grid_launch_dependents();    // the expert kernel may start its prologue
+    grid_dependency_wait();      // scores come from the router kernel
     __syncthreads();
 
     bool nonfinite = false;
     const bool oea = a.mode == MOE_MODE_OEA;
+    const bool keep_keys = B <= nwarps;   // one token per warp: keys stay in registers
+    uint32_t kv[NPL];
 
     // ---- plain top-k, or OEA phase 1 (baseline and union) ------------------
     for (int i = warp; i < B; i += nwarps) {
-        float v[NPL];
-        load_scores<NPL>(a.logits + (size_t)i * N, N, lane, v, nonfinite);
+        load_keys<NPL>(a.logits + (size_t)i * N, N, lane, kv, nonfinite);
         if (i >= a.B_valid) {           // padding token: selects nothing
             if (lane == 0) {
                 sm.snb[i] = 0;
                 if (a.n_base) a.n_base[i] = 0;
             }
-            if (!oea) finish_token<NPL>(a, sm, i, lane, 0, -1, 0.f, 0u, NW);
+            if (!oea) finish_token(a, sm, i, lane, 0, -1, 0.f, N);
             continue;
         }
         uint32_t taken = 0;
-        int myid = -1;
-        float myval = -INFINITY;
-        int n = 0;
+        int myid = -1, n = 0;
+        float myval = 0.f;
         if (!oea) {
             for (int r = 0; r < a.k; ++r) {
-                float bv; int bid;
-                warp_argmax<NPL>(v, taken, lane, bv, bid);
-                if (bv == -INFINITY) break;
-                if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-                if (lane == r) { myid = bid; myval = bv; }
+                int id;
+                const uint32_t m = warp_best<NPL>(kv, taken, lane, id);
+                if (m == 0) break;
+                if ((id & 31) == lane) taken |= 1u << (id >> 5);
+                if (lane == r) { myid = id; myval = key_score(m); }
                 n = r + 1;
             }
             if (lane == 0 && a.n_base) a.n_base[i] = n;
-            finish_token<NPL>(a, sm, i, lane, n, myid, myval, taken, NW);
+            finish_token(a, sm, i, lane, n, myid, myval, N);
             continue;
         }
         // Phase 1: softmax over all N scores, prefix in rank order, fp32.
-        float m = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < NPL; ++j) m = fmaxf(m, v[j]);
-        m = warp_max(m);
+        int id0;
+        const uint32_t mk = warp_best<NPL>(kv, 0u, lane, id0);
+        const float m = key_score(mk);
         float zl = 0.f;
 #pragma unroll
         for (int j = 0; j < NPL; ++j)
-            if (lane + 32 * j < N && v[j] != -INFINITY) zl += expf(v[j] - m);
+            if (kv[j]) zl += expf(key_score(kv[j]) - m);
         const float Z = warp_sum(zl);
         float prefix = 0.f;
         for (int r = 0; r < a.k0; ++r) {
-            float bv; int bid;
-            warp_argmax<NPL>(v, taken, lane, bv, bid);
-            if (bv == -INFINITY) break;
-            if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+            int id;
+            const uint32_t bk = warp_best<NPL>(kv, taken, lane, id);
+            if (bk == 0) break;
+            if ((id & 31) == lane) taken |= 1u << (id >> 5);
             n = r + 1;
             if (a.p < 1.f) {
-                prefix += expf(bv - m) / Z;
+                prefix += expf(key_score(bk) - m) / Z;
                 if (prefix >= a.p) break;
             }
         }
@@ -213,58 +206,54 @@ __global__ void route_kernel(RouteArgs a) {
         for (int j = 0; j < NPL; ++j)
             if (!((sm.sbase[j] >> lane) & 1u)) notin |= 1u << j;
         for (int i = warp; i < a.B_valid; i += nwarps) {
-            float v[NPL];
-            bool dummy = false;
-            load_scores<NPL>(a.logits + (size_t)i * N, N, lane, v, dummy);
-            uint32_t taken = 0, kept = 0;
+            if (!keep_keys) {
+                bool dummy = false;
+                load_keys<NPL>(a.logits + (size_t)i * N, N, lane, kv, dummy);
+            }
+            uint32_t taken = 0;
             int cnt = 0, myid = -1;
-            float myval = -INFINITY;
+            float myval = 0.f;
             if (a.maxP >= N) {
                 // the in-union experts in rank order; the first n_i are the baseline
                 for (int r = 0; r < a.kmax; ++r) {
-                    float bv; int bid;
-                    warp_argmax<NPL>(v, taken | notin, lane, bv, bid);
-                    if (bv == -INFINITY) break;
-                    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
-                    if (lane == r) { myid = bid; myval = bv; }
+                    int id;
+                    const uint32_t m = warp_best<NPL>(kv, taken | notin, lane, id);
+                    if (m == 0) break;
+                    if ((id & 31) == lane) taken |= 1u << (id >> 5);
+                    if (lane == r) { myid = id; myval = key_score(m); }
                     cnt = r + 1;
                 }
-                kept = taken;
             } else {
                 // walk the ranked list to depth max(maxP, n_i)
                 const int nb = sm.snb[i];
                 const int depth = a.maxP > nb ? a.maxP : nb;
                 for (int r = 0; r < depth && cnt < a.kmax; ++r) {
-                    float bv; int bid;
-                    warp_argmax<NPL>(v, taken, lane, bv, bid);
-                    if (bv == -INFINITY) break;
-                    const bool mine = (bid & 31) == lane;
-                    if (mine) taken |= 1u << (bid >> 5);
-                    const bool in_union = (sm.sbase[bid >> 5] >> (bid & 31)) & 1u;
+                    int id;
+                    const uint32_t m = warp_best<NPL>(kv, taken, lane, id);
+                    if (m == 0) break;
+                    if ((id & 31) == lane) taken |= 1u << (id >> 5);
+                    const bool in_union = (sm.sbase[id >> 5] >> (id & 31)) & 1u;
                     if (r < nb || in_union) {
-                        if (mine) kept |= 1u << (bid >> 5);
-                        if (lane == cnt) { myid = bid; myval = bv; }
+                        if (lane == cnt) { myid = id; myval = key_score(m); }
                         ++cnt;
                     }
                 }
             }
-            finish_token<NPL>(a, sm, i, lane, cnt, myid, myval, kept, NW);
+            finish_token(a, sm, i, lane, cnt, myid, myval, N);
         }
-        for (int i = a.B_valid + warp; i < B; i += nwarps)
-            finish_token<NPL>(a, sm, i, lane, 0, -1, 0.f, 0u, NW);
+        for (int i = a.B_valid + warp; i < B; i += nwarps) finish_token(a, sm, i, lane, 0, -1, 0.f, N);
     }
     if (__any_sync(kFull, nonfinite) && lane == 0) raise_flag(a.flags, kFlagNonFinite);
     __syncthreads();
 
-    // ---- per-expert counts ---------------------------------------------------
-    for (int e = warp; e < N; e += nwarps) {
+    // ---- per-expert counts and per-chunk prefix counts -------------------------
+    for (int e = threadIdx.x; e < N; e += nthreads) {
         int c = 0;
-        for (int i0 = 0; i0 < B; i0 += 32) {
-            const int i = i0 + lane;
-            const uint32_t bit = i < B ? (sm.tokmask[(size_t)i * NW + (e >> 5)] >> (e & 31)) & 1u : 0u;
-            c += __popc(__ballot_sync(kFull, bit));
+        for (int ch = 0; ch < nch; ++ch) {
+            sm.pre[ch * N + e] = c;
+            c += __popc(sm.bits[ch * N + e]);
         }
-        if (lane == 0) sm.scnt[e] = c;
+        sm.scnt[e] = c;
     }
     __syncthreads();
 
@@ -320,40 +309,42 @@ __global__ void route_kernel(RouteArgs a) {
     __syncthreads();
 
     // ---- positions: pairs grouped by expert, tokens ascending -----------------
-    for (int e = warp; e < N; e += nwarps) {
-        if (sm.scnt[e] == 0) continue;
-        int run = 0;
-        const int off = sm.soff[e];
-        for (int i0 = 0; i0 < B; i0 += 32) {
-            const int i = i0 + lane;
-            const uint32_t bit = i < B ? (sm.tokmask[(size_t)i * NW + (e >> 5)] >> (e & 31)) & 1u : 0u;
-            const uint32_t bal = __ballot_sync(kFull, bit);
-            if (bit) {
-                const int pos = off + run + __popc(bal & lanemask_lt());
-                int slot = -1;
-                for (int j = 0; j < a.kslots; ++j)
-                    if (sm.sidx[(size_t)i * a.kslots + j] == e) slot = j;
-                if (slot < 0) {
-                    raise_flag(a.flags, kFlagBadIndex);
-                } else {
-                    a.perm[pos] = i * a.kslots + slot;
-                    a.pos_of[(size_t)i * a.kslots + slot] = pos;
-                }
-            }
-            run += __popc(bal);
-        }
+    for (int q = threadIdx.x; q < B * a.kslots; q += nthreads) {
+        const int e = sm.sidx[q];
+        if (e < 0) continue;
+        const int i = q / a.kslots;
+        const int ch = i >> 5;
+        const int pos = sm.soff[e] + sm.pre[ch * N + e] + __popc(sm.bits[ch * N + e] & ((1u << (i & 31)) - 1u));
+        a.perm[pos] = q;
+        a.pos_of[q] = pos;
     }
 }
 
 template <int NPL>
 cudaError_t launch_route_t(const RouteArgs& a, cudaStream_t s) {
     const int threads = NPL <= 8 ? 1024 : 512;
-    const size_t smem = 32 * 4 + 64 * 4 + MOE_MAX_TOKENS * 4 + 3 * MOE_MAX_EXPERTS * 4 +
-                        (size_t)a.B * a.kslots * 4 + (size_t)a.B * ((a.N + 31) / 32) * 4;
-    cudaError_t e = cudaFuncSetAttribute(route_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    route_kernel<NPL><<<1, threads, smem, s>>>(a);
-    return cudaGetLastError();
+    const int nch = (a.B + 31) / 32;
+    const size_t smem = 32 * 4 + 64 * 4 + MOE_MAX_TOKENS * 4 + 2 * MOE_MAX_EXPERTS * 4 +
+                        (size_t)a.B * a.kslots * 4 + 2 * (size_t)nch * a.N * 4;
+    static bool attr_set = false;
+    if (!attr_set) {
+        const int max_smem = 32 * 4 + 64 * 4 + MOE_MAX_TOKENS * 4 + 2 * MOE_MAX_EXPERTS * 4 +
+                             MOE_MAX_TOKENS * MOE_MAX_SLOTS * 4 + 2 * kMaxChunks * MOE_MAX_EXPERTS * 4;
+        cudaError_t e = cudaFuncSetAttribute(route_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, route_kernel<NPL>, a);
 }
 
 }  // namespace

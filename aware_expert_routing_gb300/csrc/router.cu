@@ -32,6 +32,8 @@ router_bf16_kernel(RouterArgs a) {
     __shared__ float red[kRouterWarps][4 * 128];
     __shared__ float part[4 * 128];
 
+    grid_dependency_wait();      // hidden states come from the preceding kernel
+    grid_launch_dependents();    // the routing kernel may start its prologue
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int e0 = blockIdx.x * 16;
@@ -86,8 +88,12 @@ router_bf16_kernel(RouterArgs a) {
     cluster_sync();
     if (cluster_ctarank() == 0) {
         for (int l = threadIdx.x; l < 512; l += blockDim.x) {
+            float v[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) v[r] = r < a.ks ? ld_dsmem_f32(&part[l], r) : 0.f;
             float s = 0.f;
-            for (int r = 0; r < a.ks; ++r) s += ld_dsmem_f32(&part[l], r);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) s += v[r];   // rank order
             const int j = l >> 7, ln = (l >> 2) & 31, q2 = l & 3;
             const int row = (ln >> 2) + 8 * (q2 >> 1);
             const int tok = tok0 + 8 * j + 2 * (ln & 3) + (q2 & 1);
@@ -104,6 +110,7 @@ router_bf16_kernel(RouterArgs a) {
 // fp32 path: one thread per score, plain FMA over the hidden dimension.
 __global__ void router_f32_kernel(RouterArgs a) {
     extern __shared__ float xs[];
+    grid_dependency_wait();
     const int i = blockIdx.y;
     const float* x = static_cast<const float*>(a.x) + (size_t)i * a.d;
     for (int c = threadIdx.x; c < a.d; c += blockDim.x) xs[c] = x[c];
@@ -139,13 +146,15 @@ cudaError_t launch_router(const RouterArgs& a_in, int dtype, cudaStream_t s) {
     cfg.blockDim = dim3(kRouterWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = a.ks;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, router_bf16_kernel, a);
 }
 
