@@ -215,6 +215,36 @@ moe_status workspace_maps(unsigned char* ws, const WsLayout& L, int pairs, int d
     return MOE_OK;
 }
 
+// Map over the hidden states [B][d] (8-row boxes), cached by pointer.
+struct HidMapEntry {
+    const void* hidden;
+    int B, d, dev;
+    CUtensorMap map;
+    bool used;
+};
+HidMapEntry g_hid_maps[32];
+int g_hid_next = 0;
+
+moe_status hidden_map(const void* hidden, int B, int d, int dev, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (auto& e : g_hid_maps)
+        if (e.used && e.hidden == hidden && e.B == B && e.d == d && e.dev == dev) {
+            *out = e.map;
+            return MOE_OK;
+        }
+    HidMapEntry& e = g_hid_maps[g_hid_next];
+    g_hid_next = (g_hid_next + 1) % 32;
+    e.used = false;
+    e.hidden = hidden;
+    e.B = B;
+    e.d = d;
+    e.dev = dev;
+    if (!encode_3d(&e.map, hidden, d, B, 8)) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (hidden)");
+    e.used = true;
+    *out = e.map;
+    return MOE_OK;
+}
+
 int num_sms() {
     static int cache[64] = {0};
     int dev = 0;
@@ -325,6 +355,7 @@ moe_status moe_expert_ffn(const void* hidden, const void* w_gate, const void* w_
     a.offsets = routing->offsets;
     a.perm = routing->perm;
     a.pos_of = reinterpret_cast<const int32_t*>(ws + L.pos_of);
+    a.idx = routing->expert_idx;
     a.w = routing->weights;
     a.hbuf = ws + L.hbuf;
     a.ybuf = reinterpret_cast<float*>(ws + L.ybuf);
@@ -352,9 +383,10 @@ moe_status moe_expert_ffn(const void* hidden, const void* w_gate, const void* w_
     if (P.B == 0) return MOE_OK;   // nothing to compute or write
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     if ((st = expert_maps(w_gate, w_up, w_down, P.N, d_ff, P.d, dev, maps)) != MOE_OK) return st;
     if ((st = workspace_maps(ws, L, P.B * P.kslots, P.d, d_ff, dev, maps + 3)) != MOE_OK) return st;
+    if ((st = hidden_map(hidden, P.B, P.d, dev, maps + 5)) != MOE_OK) return st;
     int sms = num_sms();
     if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
     if (sms > kMaxGrid) sms = kMaxGrid;

@@ -91,6 +91,7 @@ struct FfnArgs {
     const int32_t* offsets;
     const int32_t* perm;
     const int32_t* pos_of;
+    const int32_t* idx;     // [B][kslots] routing experts
     const float* w;         // [B][kslots] routing weights
     void* hbuf;             // [pairs][F]
     float* ybuf;            // [pairs][d]
@@ -111,7 +112,7 @@ cudaError_t launch_router(const RouterArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 // maps (3D views {64 columns, rows, column blocks of 64}, 128-byte swizzle,
 // boxes of 4 column blocks): W_gate and W_up (16 rows), W_down (32 rows),
-// gathered hidden states and SwiGLU buffer h (8 rows).
+// gathered hidden states, SwiGLU buffer h and the hidden states (8 rows).
 cudaError_t launch_ffn_bf16(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s);
 cudaError_t launch_ffn_f32(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_synth(void* dst, int dtype, uint64_t n, uint64_t start, uint64_t seed,
@@ -267,6 +268,11 @@ __device__ __forceinline__ void grid_launch_dependents() {
 // Named barrier for a subset of warps.
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Arrive at a named barrier without waiting for it to complete.
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {

@@ -8,17 +8,21 @@
 // on chip.  Expert form (Qwen3): y = W_down (silu(W_gate x) * (W_up x));
 // combine: out_i = sum_j w_ij y_{e_ij}(x_i) (kept scores, section 2 Q2).
 //
-// Structure (one persistent CTA per SM, 6 warps):
+// Structure (one persistent CTA per SM, 7 warps):
 //   * Work is a list of tiles.  Phase-A tile (expert a, 16 rows of d_ff,
 //     token chunk c) computes h = silu(W_gate x) * (W_up x) for those rows
 //     and up to 16 tokens and writes h (bf16) to the workspace.  Phase-B
 //     tile (expert a, 32 rows of d, chunk c) computes y = W_down h (fp32).
 //     Each CTA takes an equal, contiguous share of the phase-A tiles and
 //     then of the phase-B tiles, so every CTA streams the same bytes.
-//   * Prologue: the CTAs copy the hidden states into an expert-grouped
-//     buffer (row p = the token of pair p; CTA b copies rows b, b+G, ...)
-//     and each raises its own flag; a CTA's operand warp waits only for the
-//     flags of the CTAs that copied the rows its tiles read.
+//   * Phase-A operands.  Batches of up to 16 tokens: every expert's tile
+//     multiplies the whole batch (two 8-row boxes straight from the hidden
+//     states, no copy), and the epilogue keeps the columns of the tokens
+//     routed to the expert.  Larger batches: the CTAs first copy the hidden
+//     states into an expert-grouped buffer (row p = the token of pair p; CTA
+//     b copies rows b, b+G, ...), each raises its own flag, and a CTA's
+//     operand warp waits only for the flags of the CTAs that copied the
+//     rows its tiles read.
 //   * A stage of the 8-deep shared-memory ring holds 256 K-columns of the
 //     weight tile (16 KB: gate+up rows, or 32 down rows) and the matching
 //     columns of the tokens' operand rows (up to 16 rows, 8 KB), all loaded
@@ -40,9 +44,11 @@
 //     permuted identically for both operands (k-step s, k-slot pair 2t and
 //     2t+8 map to columns 16t+4s and 16t+4s+2) so every lane reads 32
 //     contiguous bytes and the swizzle keeps the reads conflict free.
-//   * At the end of a tile the four warps' partial sums meet in a
-//     double-buffered shared-memory area and are added in warp order, with
-//     one named barrier per tile; no global fence or atomic per tile.
+//   * At the end of a tile the four consumer warps leave their partial sums
+//     in a double-buffered shared-memory area and signal without waiting;
+//     warp 6, the epilogue warp, adds them in warp order and writes h
+//     (SwiGLU) or y, then frees the buffer.  The consumers only wait when
+//     they are two tiles ahead of it.  No global fence or atomic per tile.
 //   * After phase B every CTA arrives at a grid-wide counter; once all have
 //     arrived, each CTA combines its slice of the output four columns at a
 //     time, out_i = sum over slots (in slot order) of w_is * y_is.
@@ -57,7 +63,12 @@ namespace {
 constexpr int kCW = 4;                    // consumer warps
 constexpr int kWarpW = kCW;               // weight producer warp
 constexpr int kWarpO = kCW + 1;           // operand producer warp
-constexpr int kThreads = (kCW + 2) * 32;
+constexpr int kWarpE = kCW + 2;           // epilogue warp
+constexpr int kThreads = (kCW + 3) * 32;
+// Named barriers: 1 consumers (gather), 2/3 partial sums of buffer 0/1 are
+// ready, 4/5 buffer 0/1 is free again, 6 consumers + epilogue warp.
+constexpr uint32_t kBarGather = 1, kBarFull0 = 2, kBarFree0 = 4, kBarEnd = 6;
+constexpr uint32_t kRedThreads = (kCW + 1) * 32;
 constexpr int kNT = 2;                    // MMA column tiles (8 tokens each) per pass
 constexpr int kChunk = 8 * kNT;           // tokens per tile pass
 constexpr int kWBytes = 16384;            // weight part of a stage
@@ -73,6 +84,8 @@ struct Smem {
     uint64_t empty[kStages];
     int chunk_off[MOE_MAX_EXPERTS + 1];
     uint32_t ex_info[MOE_MAX_EXPERTS];  // active index -> id | cnt << 10 | first pair << 19
+    uint16_t ex_of[MOE_MAX_EXPERTS];    // expert id -> active index (batches of <= 16 tokens)
+    uint32_t tokmask[MOE_MAX_EXPERTS];  // active index -> tokens routed to it (batches of <= 16)
     int abort_flag;
     int last_flag;
 };
@@ -220,7 +233,8 @@ __device__ __forceinline__ void consume_tile(const unsigned char* ring, Smem& S,
 __global__ void __launch_bounds__(kThreads, 1)
 ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
                 const __grid_constant__ CUtensorMap tm_up, const __grid_constant__ CUtensorMap tm_down,
-                const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_h) {
+                const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_h,
+                const __grid_constant__ CUtensorMap tm_hid) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -267,6 +281,11 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
             run += __shfl_sync(0xffffffffu, inc, 31);
         }
     }
+    const bool small_b = A.B <= kChunk;   // phase-A operands: the whole batch from the hidden states
+    if (small_b) {
+        for (int q = threadIdx.x; q < Tn; q += kThreads) S.tokmask[q] = 0;
+        for (int q = threadIdx.x; q < Tn; q += kThreads) S.ex_of[A.active[q]] = (uint16_t)q;
+    }
     if (warp == kWarpW && lane == 0) {
         prefetch_tensormap(&tm_gate);
         prefetch_tensormap(&tm_up);
@@ -274,9 +293,20 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
     }
     if (warp == kWarpO && lane == 0) {
         prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_hid);
         prefetch_tensormap(&tm_h);
     }
     __syncthreads();
+    if (small_b) {   // token masks of the active experts
+        for (int q = threadIdx.x; q < A.B * A.kslots; q += kThreads) {
+            const int pos = A.pos_of[q];
+            if (pos >= 0) {
+                const int e = A.idx[q];
+                atomicOr(&S.tokmask[S.ex_of[e]], 1u << (q / A.kslots));
+            }
+        }
+        __syncthreads();
+    }
 
     Ranges R;
     R.Tn = Tn;
@@ -330,7 +360,7 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         __syncwarp();
     } else if (warp == kWarpO) {
         // ---------------------------- operand producer ---------------------------
-        if (R.a_end > R.a_beg) {   // the rows of this CTA's phase-A tiles are gathered
+        if (!small_b && R.a_end > R.a_beg) {   // the rows of this CTA's phase-A tiles are gathered
             const Tile T0 = decode_tile(R.a_beg, R.rbA, S, Tn);
             const Tile T1 = decode_tile(R.a_end - 1, R.rbA, S, Tn);
             const int p_lo = T0.off, p_hi = T1.off + (int)((S.ex_info[T1.a] >> 10) & 511u);
@@ -344,15 +374,16 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
             uint32_t it = 0;
             for (int t = R.a_beg; t < R.a_end; ++t) {
                 const Tile T = decode_tile(t, R.rbA, S, Tn);
-                const int nt = (T.ntok + 7) >> 3;
-                const int row0 = T.off + kChunk * T.c;
+                const int nt = small_b ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
+                const int row0 = small_b ? 0 : T.off + kChunk * T.c;
+                const CUtensorMap* map = small_b ? &tm_hid : &tm_x;
                 for (int s = 0; s < R.SA; ++s, ++it) {
                     const int slot = it % kStages;
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
                     mbar_arrive_expect_tx(&S.full[slot], nt * 4096);
                     unsigned char* dst = ring + (size_t)slot * kSlotBytes + kWBytes;
                     for (int j = 0; j < nt; ++j)
-                        tma_load_3d(dst + j * 4096, &tm_x, 0, row0 + 8 * j, 4 * s, &S.full[slot], pol);
+                        tma_load_3d(dst + j * 4096, map, 0, row0 + 8 * j, 4 * s, &S.full[slot], pol);
                 }
             }
             if (R.b_end > R.b_beg) {   // every h row is written once all CTAs finished phase A
@@ -374,14 +405,14 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < kCW) {
         // ------------------------------- consumers -------------------------------
         const int w = warp, tid = threadIdx.x;
-        __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
 
-        // Prologue: this CTA's rows of the expert-grouped hidden states
-        // (rows b, b+G, ...), eight 16-byte loads in flight per thread.
-        {
+        // Prologue (batches over 16 tokens): this CTA's rows of the
+        // expert-grouped hidden states (rows b, b+G, ...), eight 16-byte
+        // loads in flight per thread.
+        if (!small_b) {
             const int P = A.offsets[A.N];
             const int vpr = d / 8;   // 16-byte vectors per row
             const int nrow = P > (int)blockIdx.x ? (P - 1 - (int)blockIdx.x) / (int)G + 1 : 0;
@@ -406,121 +437,137 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
                 for (int u = 0; u < 8; ++u)
                     if (dst[u] != ~size_t(0)) xp[dst[u]] = val[u];
             }
-            named_barrier(1, kCW * 32);
+            named_barrier(kBarGather, kCW * 32);
             if (tid == 0) {
                 __threadfence();
                 atomicExch(&A.gflag[blockIdx.x], 1u);
             }
         }
 
+        // Every tile: multiply, leave the partial sums, signal the epilogue warp.
         uint32_t it = 0;
-        int buf = 0;
+        int tt = 0;   // tiles of both phases, in order
         float acc[2][kNT][4];
-        // ---- phase A: h = silu(W_gate x) * (W_up x) ----
-        for (int t = R.a_beg; t < R.a_end; ++t, buf ^= 1) {
-            const Tile T = decode_tile(t, R.rbA, S, Tn);
-            const int NT = (T.ntok + 7) >> 3;
-            consume_tile<true>(ring, S, flags, R.SA, d, NT, it, acc);
+        for (int phase = 0; phase < 2; ++phase) {
+            const int t_beg = phase ? R.b_beg : R.a_beg, t_end = phase ? R.b_end : R.a_end;
+            for (int t = t_beg; t < t_end; ++t, ++tt) {
+                const Tile T = decode_tile(t, phase ? R.rbB : R.rbA, S, Tn);
+                const int NT = (phase == 0 && small_b) ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
+                if (phase == 0) consume_tile<true>(ring, S, flags, R.SA, d, NT, it, acc);
+                else consume_tile<false>(ring, S, flags, R.SB, F, NT, it, acc);
+                const int buf = tt & 1;
+                if (tt >= 2) named_barrier(kBarFree0 + buf, kRedThreads);
 #pragma unroll
-            for (int m = 0; m < 2; ++m)
+                for (int m = 0; m < 2; ++m)
 #pragma unroll
-                for (int j = 0; j < kNT; ++j)
-                    if (j < NT)
+                    for (int j = 0; j < kNT; ++j)
+                        if (j < NT)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            S.red[buf][w][(m * kNT + j) * 128 + lane * 4 + q] = acc[m][j][q];
-            named_barrier(1, kCW * 32);
-            // element l = j*128 + lane*4 + q of the gate partials (up at +kNT*128)
-            for (int l = tid; l < NT * 128; l += kCW * 32) {
-                const int j = l >> 7, ln = (l >> 2) & 31, q = l & 3;
-                const int nn = 8 * j + 2 * (ln & 3) + (q & 1);
-                if (nn < T.ntok) {
-                    float gs = 0.f, us = 0.f;
+                            for (int q = 0; q < 4; ++q)
+                                S.red[buf][w][(m * kNT + j) * 128 + lane * 4 + q] = acc[m][j][q];
+                named_barrier_arrive(kBarFull0 + buf, kRedThreads);
+            }
+        }
+        named_barrier(kBarEnd, kRedThreads);
+    } else {
+        // ------------------------------- epilogue warp ------------------------------
+        __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
+        const int ntiles = (R.a_end - R.a_beg) + (R.b_end - R.b_beg);
+        int tt = 0;
+        for (int phase = 0; phase < 2; ++phase) {
+            const int t_beg = phase ? R.b_beg : R.a_beg, t_end = phase ? R.b_end : R.a_end;
+            for (int t = t_beg; t < t_end; ++t, ++tt) {
+                const Tile T = decode_tile(t, phase ? R.rbB : R.rbA, S, Tn);
+                const int NT = (phase == 0 && small_b) ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
+                const uint32_t tmask = small_b ? S.tokmask[T.a] : 0u;
+                const int buf = tt & 1;
+                named_barrier(kBarFull0 + buf, kRedThreads);
+                const float* red = &S.red[buf][0][0];
+                if (phase == 0) {
+                    // element l = j*128 + lane*4 + q of the gate partials (up at +kNT*128)
+                    for (int l = lane; l < NT * 128; l += 32) {
+                        const int j = l >> 7, ln = (l >> 2) & 31, q = l & 3;
+                        const int nn = 8 * j + 2 * (ln & 3) + (q & 1);
+                        // column nn: the tile's nn-th token, or batch token nn
+                        const bool keep = small_b ? ((tmask >> nn) & 1u) != 0 : nn < T.ntok;
+                        if (keep) {
+                            float gs = 0.f, us = 0.f;
 #pragma unroll
-                    for (int ww = 0; ww < kCW; ++ww) {
-                        gs += S.red[buf][ww][l];
-                        us += S.red[buf][ww][kNT * 128 + l];
+                            for (int ww = 0; ww < kCW; ++ww) {
+                                gs += red[ww * kRed + l];
+                                us += red[ww * kRed + kNT * 128 + l];
+                            }
+                            const int row = (ln >> 2) + 8 * (q >> 1);
+                            const size_t pos = small_b ? (size_t)T.off + __popc(tmask & ((1u << nn) - 1u))
+                                                       : (size_t)T.off + kChunk * T.c + nn;
+                            hb[pos * F + 16 * T.rb + row] = __float2bfloat16_rn(silu_f(gs) * us);
+                        }
                     }
-                    const int row = (ln >> 2) + 8 * (q >> 1);
-                    const size_t pos = (size_t)T.off + kChunk * T.c + nn;
-                    hb[pos * F + 16 * T.rb + row] = __float2bfloat16_rn(silu_f(gs) * us);
+                } else {
+                    for (int l = lane; l < 2 * kNT * 128; l += 32) {
+                        const int m = l / (kNT * 128), j = (l >> 7) % kNT, ln = (l >> 2) & 31, q = l & 3;
+                        const int nn = 8 * j + 2 * (ln & 3) + (q & 1);
+                        if (j < NT && nn < T.ntok) {
+                            float ys = 0.f;
+#pragma unroll
+                            for (int ww = 0; ww < kCW; ++ww) ys += red[ww * kRed + l];
+                            const int row = 16 * m + (ln >> 2) + 8 * (q >> 1);
+                            const size_t pos = (size_t)T.off + kChunk * T.c + nn;
+                            A.ybuf[pos * d + 32 * T.rb + row] = ys;
+                        }
+                    }
                 }
+                if (tt + 2 < ntiles) named_barrier_arrive(kBarFree0 + buf, kRedThreads);
+            }
+            __syncwarp();
+            if (phase == 0 && lane == 0) {   // this CTA's h rows are written
+                __threadfence();
+                atomicAdd(&A.hdr->a_done, 1u);
             }
         }
-        named_barrier(1, kCW * 32);
-        if (tid == 0) {   // this CTA's h rows are written
-            __threadfence();
-            atomicAdd(&A.hdr->a_done, 1u);
-        }
-
-        // ---- phase B: y = W_down h ----
-        for (int t = R.b_beg; t < R.b_end; ++t, buf ^= 1) {
-            const Tile T = decode_tile(t, R.rbB, S, Tn);
-            const int NT = (T.ntok + 7) >> 3;
-            consume_tile<false>(ring, S, flags, R.SB, F, NT, it, acc);
-#pragma unroll
-            for (int m = 0; m < 2; ++m)
-#pragma unroll
-                for (int j = 0; j < kNT; ++j)
-                    if (j < NT)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            S.red[buf][w][(m * kNT + j) * 128 + lane * 4 + q] = acc[m][j][q];
-            named_barrier(1, kCW * 32);
-            for (int l = tid; l < 2 * kNT * 128; l += kCW * 32) {
-                const int m = l / (kNT * 128), j = (l >> 7) % kNT, ln = (l >> 2) & 31, q = l & 3;
-                const int nn = 8 * j + 2 * (ln & 3) + (q & 1);
-                if (j < NT && nn < T.ntok) {
-                    float ys = 0.f;
-#pragma unroll
-                    for (int ww = 0; ww < kCW; ++ww) ys += S.red[buf][ww][l];
-                    const int row = 16 * m + (ln >> 2) + 8 * (q >> 1);
-                    const size_t pos = (size_t)T.off + kChunk * T.c + nn;
-                    A.ybuf[pos * d + 32 * T.rb + row] = ys;
-                }
-            }
-        }
-
-        // ---- combine: after every CTA finished phase B, each combines a slice ----
-        named_barrier(1, kCW * 32);
-        if (tid == 0) {
+        // After phase B every CTA arrives; once all have, the output is combined.
+        if (lane == 0) {
             __threadfence();
             atomicAdd(&A.hdr->b_done, 1u);
             wait_counter(&A.hdr->b_done, G, S, flags);
             __threadfence();
         }
-        named_barrier(1, kCW * 32);
-        {
-            const int d4 = d / 4;
-            const long long total = (long long)A.B * d4;   // groups of four columns
-            const long long o0 = total * blockIdx.x / G, o1 = total * (blockIdx.x + 1) / G;
-            const float4* y4 = reinterpret_cast<const float4*>(A.ybuf);
-            uint2* out = static_cast<uint2*>(A.out);
-            for (long long o = o0 + tid; o < o1; o += kCW * 32) {
-                const int i = (int)(o / d4), c4 = (int)(o - (long long)i * d4);
-                float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int s0 = 0; s0 < A.kslots; s0 += 8) {
-                    float4 yv[8];
-                    float wv[8];
+        __syncwarp();
+        named_barrier(kBarEnd, kRedThreads);
+    }
+
+    // ---- combine: each CTA a slice of the output, four columns at a time ----
+    if (warp < kCW || warp == kWarpE) {
+        const int ctid = warp < kCW ? (int)threadIdx.x : kCW * 32 + lane;
+        const int d4 = d / 4;
+        const long long total = (long long)A.B * d4;
+        const long long o0 = total * blockIdx.x / G, o1 = total * (blockIdx.x + 1) / G;
+        const float4* y4 = reinterpret_cast<const float4*>(A.ybuf);
+        uint2* out = static_cast<uint2*>(A.out);
+        for (long long o = o0 + ctid; o < o1; o += kRedThreads) {
+            const int i = (int)(o / d4), c4 = (int)(o - (long long)i * d4);
+            float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < A.kslots; s0 += 8) {
+                float4 yv[8];
+                float wv[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int sl = s0 + u;
-                        const int pos = sl < A.kslots ? A.pos_of[i * A.kslots + sl] : -1;
-                        wv[u] = pos >= 0 ? A.w[i * A.kslots + sl] : 0.f;
-                        yv[u] = pos >= 0 ? __ldcg(y4 + (size_t)pos * d4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {   // slot order
-                        acc2.x += wv[u] * yv[u].x;
-                        acc2.y += wv[u] * yv[u].y;
-                        acc2.z += wv[u] * yv[u].z;
-                        acc2.w += wv[u] * yv[u].w;
-                    }
+                for (int u = 0; u < 8; ++u) {
+                    const int sl = s0 + u;
+                    const int pos = sl < A.kslots ? A.pos_of[i * A.kslots + sl] : -1;
+                    wv[u] = pos >= 0 ? A.w[i * A.kslots + sl] : 0.f;
+                    yv[u] = pos >= 0 ? __ldcg(y4 + (size_t)pos * d4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc2.x, acc2.y);
-                const __nv_bfloat162 hi = __floats2bfloat162_rn(acc2.z, acc2.w);
-                out[o] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {   // slot order
+                    acc2.x += wv[u] * yv[u].x;
+                    acc2.y += wv[u] * yv[u].y;
+                    acc2.z += wv[u] * yv[u].z;
+                    acc2.w += wv[u] * yv[u].w;
+                }
             }
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc2.x, acc2.y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc2.z, acc2.w);
+            out[o] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
         }
     }
 
@@ -568,7 +615,7 @@ cudaError_t launch_ffn_bf16(const FfnArgs& a, const CUtensorMap* maps, int num_s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_bf16_kernel, a, maps[0], maps[1], maps[2], maps[3], maps[4]);
+    return cudaLaunchKernelEx(&cfg, ffn_bf16_kernel, a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]);
 }
 
 size_t ffn_bf16_smem_bytes() { return kSmemBytes; }
