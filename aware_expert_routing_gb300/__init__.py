@@ -26,8 +26,9 @@ FLAG_NONFINITE_SCORE, FLAG_WAIT_TIMEOUT, FLAG_BAD_INDEX = 0x1, 0x2, 0x4
 MAX_TOKENS, MAX_EXPERTS, MAX_SLOTS = 256, 1024, 32
 
 EXPORTED = ["moe_num_slots", "moe_workspace_bytes", "moe_route", "moe_expert_ffn",
-            "moe_decode_layer", "moe_device_status", "moe_synth_normal",
+            "moe_decode_layer", "moe_decode_layer_static", "moe_device_status", "moe_synth_normal",
             "moe_status_string", "moe_last_error"]
+STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class MoeError(RuntimeError):
@@ -74,6 +75,9 @@ def load(path: str | None = None):
     lib.moe_decode_layer.argtypes = [V, V, V, V, V, V, ctypes.c_int32, P(_Params), P(_Routing), V,
                                      V, ctypes.c_size_t, V]
     lib.moe_decode_layer.restype = ctypes.c_int
+    lib.moe_decode_layer_static.argtypes = [V, V, V, V, V, V, ctypes.c_int32, P(_Params), P(_Routing),
+                                            V, V]
+    lib.moe_decode_layer_static.restype = ctypes.c_int
     lib.moe_device_status.argtypes = [V, V, P(ctypes.c_uint32)]
     lib.moe_device_status.restype = ctypes.c_int
     lib.moe_synth_normal.argtypes = [V, ctypes.c_int32, ctypes.c_uint64, ctypes.c_uint64,
@@ -222,6 +226,24 @@ def moe_decode_layer(hidden, w_router, router_bias, w_gate, w_up, w_down, d_ff: 
                                  ctypes.byref(routing.c()), _ptr(out), _ptr(workspace),
                                  workspace.numel(), _stream(stream))
     _check(st, "moe_decode_layer")
+    return out
+
+
+def moe_decode_layer_static(hidden, w_router, router_bias, w_gate, w_up, w_down, d_ff: int,
+                            params: RouteParams, routing: Routing, out, stream=None):
+    """moe_decode_layer without a workspace, for callers that cannot
+    allocate device memory: the scratch is the library's fixed device array
+    of STATIC_SCRATCH_BYTES (see include/moe.h for its limits)."""
+    dt = params.torch_dtype
+    for t, n in ((hidden, "hidden"), (w_router, "w_router"), (w_gate, "w_gate"), (w_up, "w_up"),
+                 (w_down, "w_down"), (out, "out")):
+        _need(t, dt, n)
+    if router_bias is not None:
+        _need(router_bias, torch.float32, "router_bias")
+    st = load().moe_decode_layer_static(_ptr(hidden), _ptr(w_router), _ptr(router_bias), _ptr(w_gate),
+                                        _ptr(w_up), _ptr(w_down), d_ff, ctypes.byref(params.c()),
+                                        ctypes.byref(routing.c()), _ptr(out), _stream(stream))
+    _check(st, "moe_decode_layer_static")
     return out
 
 

@@ -259,6 +259,11 @@ int num_sms() {
 
 }  // namespace
 
+namespace moe {
+// Records `message` as this thread's last error and returns `status`.
+moe_status report_error(moe_status status, const char* message) { return fail(status, "%s", message); }
+}  // namespace moe
+
 extern "C" {
 
 int32_t moe_num_slots(const moe_route_params* params) {

@@ -195,6 +195,35 @@ moe_status moe_decode_layer(const void *hidden, const void *w_router, const floa
                             size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * moe_decode_layer for callers that cannot allocate device memory.  The
+ * pages have no counterpart: this is a property of the library, not of the
+ * method.  A plugin whose host engine owns all device memory, a runtime
+ * that freezes allocation after start-up, or code without access to its
+ * framework's allocator may have no way to provide a workspace.  This call
+ * takes its scratch from one fixed array in the library's own device memory
+ * (MOE_STATIC_SCRATCH_BYTES, held by every GPU that loads the library until
+ * the process exits) and allocates nothing.  Inputs, routing buffers and
+ * output are the caller's, exactly as for moe_decode_layer.
+ *   - A batch whose workspace (moe_workspace_bytes) exceeds
+ *     MOE_STATIC_SCRATCH_BYTES is rejected with MOE_ERR_WORKSPACE before
+ *     anything is launched.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - All calls on a device share its array, which keeps the last call's
+ *     contents; the counters at its front are cleared on `stream` at every
+ *     call.  Calls that overlap on the GPU (for example on two streams) race
+ *     with each other: serialise them.
+ *   - Device flags are not kept between calls; use moe_decode_layer with a
+ *     workspace and moe_device_status() to read them.
+ */
+#define MOE_STATIC_SCRATCH_BYTES (32u << 20)
+moe_status moe_decode_layer_static(const void *hidden, const void *w_router, const float *router_bias,
+                                   const void *w_gate, const void *w_up, const void *w_down,
+                                   int32_t d_ff, const moe_route_params *params,
+                                   const moe_routing *routing, void *out, moe_stream_t stream);
+
+/*
  * Synchronises `stream`, returns the device flag word (MOE_FLAG_*) that the
  * calls on this workspace raised since the last read, and clears it.
  * Returns MOE_ERR_DEVICE_CHECK if any flag was set.
