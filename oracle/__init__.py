@@ -53,7 +53,7 @@ def _load():
             lib.oracle_expert_ffn.restype = None
             lib.oracle_moe_experts.argtypes = [P, P, P, P, i, i, i, i, P, P, P]
             lib.oracle_moe_experts.restype = None
-            lib.oracle_dequant_int4.argtypes = [P, P, i, i, i, P]
+            lib.oracle_dequant_int4.argtypes = [P, i, i, i, P]
             lib.oracle_dequant_int4.restype = None
             _lib = lib
     return _lib
@@ -134,12 +134,12 @@ def moe_experts(x, w_gate, w_up, w_down, idx, w) -> np.ndarray:
     return out
 
 
-def dequant_int4(packed, scales, rows: int, cols: int, group: int = 128) -> np.ndarray:
-    """INT4 group-wise codes * bf16 scales -> fp32 (DynaExq page, section 3.2)."""
+def dequant_int4(packed, rows: int, cols: int, rb: int) -> np.ndarray:
+    """INT4 group-wise codes times bf16 scales -> fp32, from the packed
+    cold-expert byte format (DynaExq page, section 3.2, INT4 tier)."""
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
-    scales = np.ascontiguousarray(scales, dtype=np.uint16)
     out = np.empty((rows, cols), np.float32)
-    _load().oracle_dequant_int4(_ptr(packed), _ptr(scales), rows, cols, group, _ptr(out))
+    _load().oracle_dequant_int4(_ptr(packed), rows, cols, rb, _ptr(out))
     return out
 
 

@@ -216,3 +216,73 @@ def make_layer(w: Workload, layer: int = 0, B: int | None = None, step: int = 0)
         "w_down": make_tensor(w, layer, T_DOWN),
         "bias": make_bias(w, layer),
     }
+
+
+# ---------------------------------------------------------------------------
+# INT4 cold-expert format (input preparation for the mixed-precision layer)
+# ---------------------------------------------------------------------------
+INT4_GROUP = 128     # scale group along the contraction dimension
+INT4_STAGE = 256     # columns per tile chunk
+INT4_RB_GATE_UP = 16  # rows per chunk of W_gate / W_up
+INT4_RB_DOWN = 32     # rows per chunk of W_down
+
+
+def quantize_int4(w: np.ndarray):
+    """Symmetric group-wise INT4 of a [rows][cols] matrix, groups of 128
+    columns: s = bf16(max|w| / 7) (nearest even), q = clamp(rint(w / s), -7, 7)
+    with rint rounding half to even, q = 0 where s = 0.  Returns (q int8
+    [rows][cols], s fp32 [rows][cols/128] holding bf16 values)."""
+    w = np.asarray(w, np.float32)
+    R, K = w.shape
+    g = w.reshape(R, K // INT4_GROUP, INT4_GROUP).astype(np.float64)
+    s = round_bf16((np.abs(g).max(axis=2) / 7.0).astype(np.float32))
+    sd = s.astype(np.float64)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(sd > 0, np.rint(g / np.where(sd > 0, sd, 1.0)), 0.0)
+    q = np.clip(q, -7, 7).astype(np.int8).reshape(R, K)
+    return q, s
+
+
+def pack_int4_tiles(q: np.ndarray, s: np.ndarray, rb: int) -> np.ndarray:
+    """Tile-contiguous byte image of one quantised matrix.
+
+    The matrix is cut into chunks of `rb` rows x 256 columns, stored in the
+    order (row block, column stage).  A chunk is rb*128 bytes of codes
+    followed by rb*2 bf16 scales (row-major [rb][2]: the two 128-column
+    groups of the chunk).  Codes are stored offset by 8 (q + 8 in 0..15).
+    Within a row, column c = 64*b + 16*t + 8*h + o (block b, segment t, word h,
+    offset o) is the nibble at bit 4*(o//2) + 16*(o%2) of 32-bit word
+    (8*b + 2*t + h), little endian: each 16-bit half of a word holds the
+    codes of two adjacent columns four bits apart.
+    """
+    R, K = q.shape
+    assert R % rb == 0 and K % INT4_STAGE == 0
+    nrb, nks = R // rb, K // INT4_STAGE
+    code = (q.astype(np.int16) + 8).astype(np.uint32).reshape(R, K // 8, 8)   # words of 8 columns
+    shifts = np.array([0, 16, 4, 20, 8, 24, 12, 28], np.uint32)
+    words = (code << shifts[None, None, :]).sum(axis=2, dtype=np.uint64).astype(np.uint32)   # [R][K/8]
+    words = words.reshape(nrb, rb, nks, INT4_STAGE // 8).transpose(0, 2, 1, 3)             # [nrb][nks][rb][32]
+    code_bytes = words.astype("<u4").view(np.uint8).reshape(nrb, nks, rb * 128)
+    sb = to_bf16_bits(s).reshape(nrb, rb, nks, 2).transpose(0, 2, 1, 3)                     # [nrb][nks][rb][2]
+    scale_bytes = np.ascontiguousarray(sb).astype("<u2").view(np.uint8).reshape(nrb, nks, rb * 4)
+    return np.concatenate([code_bytes, scale_bytes], axis=2).reshape(-1)
+
+
+def int4_expert_bytes(d: int, F: int) -> int:
+    """Bytes of one expert's three packed INT4 matrices."""
+    return 2 * (F * d // 2 + F * (d // INT4_GROUP) * 2) + (d * F // 2 + d * (F // INT4_GROUP) * 2)
+
+
+def pack_int4_expert(w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray):
+    """(gate, up, down) packed images of one expert, and its (q, s) pairs."""
+    out, qs = [], []
+    for w, rb in ((w_gate, INT4_RB_GATE_UP), (w_up, INT4_RB_GATE_UP), (w_down, INT4_RB_DOWN)):
+        q, s = quantize_int4(w)
+        qs.append((q, s))
+        out.append(pack_int4_tiles(q, s, rb))
+    return out, qs
+
+
+def trace_seed(w: Workload, layer: int, step: int) -> int:
+    """Seed of the hidden states of one step of the hotness trace."""
+    return tensor_seed(w.seed + 7919, layer, T_X, step)

@@ -95,16 +95,52 @@ def test_router_logits_match_library():
     assert np.allclose(oracle.router_logits(x, wr), ref - b, rtol=1e-13, atol=1e-13)
 
 
+def pack_by_definition(q, s, rb):
+    """The packed format built byte by byte from its definition (a second,
+    independent construction)."""
+    R, K = q.shape
+    out = bytearray()
+    for rbi in range(R // rb):
+        for ks in range(K // 256):
+            codes = bytearray(rb * 128)
+            for rr in range(rb):
+                r = rbi * rb + rr
+                for cl in range(256):
+                    o = cl % 8
+                    bit = 4 * (o // 2) + 16 * (o % 2)
+                    word_off = rr * 128 + (cl // 8) * 4
+                    v = (int(q[r, ks * 256 + cl]) + 8) << bit
+                    for byte in range(4):
+                        codes[word_off + byte] |= (v >> (8 * byte)) & 0xFF
+            scales = bytearray()
+            for rr in range(rb):
+                for g in range(2):
+                    bits = int(synth.to_bf16_bits(np.array([s[rbi * rb + rr, ks * 2 + g]], np.float32))[0])
+                    scales += bytes([bits & 0xFF, bits >> 8])
+            out += codes + scales
+    return np.frombuffer(bytes(out), np.uint8)
+
+
 def test_dequant_int4_codes_and_layout():
-    """Every code -8..7 in both nibble positions, two groups with their own
-    scale: w = q * s (DynaExq page, section 3.2, INT4 tier)."""
-    rows, cols, group = 2, 256, 128
-    q = np.tile(np.arange(-8, 8), cols // 16 * rows).reshape(rows, cols)
-    q[1] = q[1][::-1]
-    nib = (q & 0xF).astype(np.uint8)
-    packed = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
-    s = np.array([[0.5, 2.0], [0.25, 1.5]], np.float32)
-    sbits = synth.to_bf16_bits(s)
-    out = oracle.dequant_int4(packed, sbits, rows, cols, group)
-    want = q * np.repeat(s, group, axis=1)
-    assert np.array_equal(out, want.astype(np.float32))
+    """Every code -7..7 at every nibble position, two groups per chunk with
+    their own scales: w = q * s (DynaExq page, section 3.2, INT4 tier)."""
+    rng = np.random.default_rng(6)
+    rows, cols, rb = 32, 512, 16
+    q = rng.integers(-7, 8, size=(rows, cols)).astype(np.int8)
+    q[0, :15] = np.arange(-7, 8)
+    s = synth.round_bf16(rng.uniform(0.01, 2.0, size=(rows, cols // 128)).astype(np.float32))
+    packed = pack_by_definition(q, s, rb)
+    assert np.array_equal(packed, synth.pack_int4_tiles(q, s, rb))
+    out = oracle.dequant_int4(packed, rows, cols, rb)
+    assert np.array_equal(out, (q * np.repeat(s, 128, axis=1)).astype(np.float32))
+
+
+def test_int4_round_trip_within_half_step():
+    """quantise -> pack -> dequantise reproduces each weight within half a
+    quantisation step, and exactly where the weight is a multiple of it."""
+    w = synth.normal(12, (64, 768), 0.03, True)
+    q, s = synth.quantize_int4(w)
+    out = oracle.dequant_int4(synth.pack_int4_tiles(q, s, 32), 64, 768, 32)
+    step = np.repeat(s, 128, axis=1)
+    assert (np.abs(out - w) <= step / 2 + 1e-12).all()
+    assert (np.abs(q) <= 7).all() and (np.abs(q) == 7).any()

@@ -33,7 +33,9 @@ MUTANTS = {
     "padding_tokens_join_union": ("if (i >= B_valid) {\n                nbase[i] = 0;\n                continue;",
                                   "if (0) {\n                nbase[i] = 0;\n                continue;"),
     "max_depth_ignored": ("const int depth = maxP < N ? maxP : N;", "const int depth = N;"),
-    "int4_nibbles_swapped": ("(c & 1) ? (byte >> 4) : (byte & 0xF)", "(c & 1) ? (byte & 0xF) : (byte >> 4)"),
+    "int4_nibble_pairs_swapped": ("const int bit = 4 * (o / 2) + 16 * (o % 2);",
+                                  "const int bit = 16 * (o / 2 % 2) + 4 * (o % 2) + 8 * (o / 4);"),
+    "int4_scale_group_ignored": ("((size_t)rr * 2 + cl / 128) * 2", "((size_t)rr * 2) * 2"),
 }
 
 
@@ -44,7 +46,7 @@ def pins():
            R.test_padding_tokens_select_nothing,
            FFN.test_swiglu_worked_example, FFN.test_expert_algebra,
            FFN.test_combine_is_weighted_sum_in_slot_order, FFN.test_router_logits_match_library,
-           FFN.test_dequant_int4_codes_and_layout]
+           FFN.test_dequant_int4_codes_and_layout, FFN.test_int4_round_trip_within_half_step]
     out += [lambda s=s: R.test_topk_matches_brute_force_with_ties(s) for s in range(6)]
     for args in [(2, 0.5, 16, 4), (2, 0.7, 6, 4), (2, 0.6, 5, 5)]:
         out += [lambda s=s, a=args: R.test_oea_matches_brute_force(s, *a) for s in range(4)]
