@@ -26,8 +26,8 @@ FLAG_NONFINITE_SCORE, FLAG_WAIT_TIMEOUT, FLAG_BAD_INDEX = 0x1, 0x2, 0x4
 MAX_TOKENS, MAX_EXPERTS, MAX_SLOTS = 256, 1024, 32
 
 EXPORTED = ["moe_num_slots", "moe_workspace_bytes", "moe_route", "moe_expert_ffn",
-            "moe_decode_layer", "moe_decode_layer_static", "moe_device_status", "moe_synth_normal",
-            "moe_status_string", "moe_last_error"]
+            "moe_expert_ffn_mixed", "moe_decode_layer", "moe_decode_layer_static", "moe_device_status",
+            "moe_synth_normal", "moe_status_string", "moe_last_error"]
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -42,6 +42,11 @@ class _Params(ctypes.Structure):
                 ("N", ctypes.c_int32), ("k", ctypes.c_int32), ("mode", ctypes.c_int32),
                 ("k0", ctypes.c_int32), ("p", ctypes.c_float), ("maxP", ctypes.c_int32),
                 ("kmax", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class _Mixed(ctypes.Structure):
+    _fields_ = [("slot", ctypes.c_void_p), ("q_gate", ctypes.c_void_p), ("q_up", ctypes.c_void_p),
+                ("q_down", ctypes.c_void_p), ("n_hot", ctypes.c_int32), ("n_cold", ctypes.c_int32)]
 
 
 class _Routing(ctypes.Structure):
@@ -72,6 +77,9 @@ def load(path: str | None = None):
     lib.moe_expert_ffn.argtypes = [V, V, V, V, ctypes.c_int32, P(_Params), P(_Routing), V, V,
                                    ctypes.c_size_t, V]
     lib.moe_expert_ffn.restype = ctypes.c_int
+    lib.moe_expert_ffn_mixed.argtypes = [V, V, V, V, P(_Mixed), ctypes.c_int32, P(_Params), P(_Routing),
+                                         V, V, ctypes.c_size_t, V]
+    lib.moe_expert_ffn_mixed.restype = ctypes.c_int
     lib.moe_decode_layer.argtypes = [V, V, V, V, V, V, ctypes.c_int32, P(_Params), P(_Routing), V,
                                      V, ctypes.c_size_t, V]
     lib.moe_decode_layer.restype = ctypes.c_int
@@ -210,6 +218,46 @@ def moe_expert_ffn(hidden, w_gate, w_up, w_down, d_ff: int, params: RouteParams,
                                _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "moe_expert_ffn")
     return out
+
+
+class MixedExperts:
+    """Device buffers of moe_mixed_experts: bf16 hot experts plus INT4 cold
+    experts in the packed format of include/moe.h."""
+
+    def __init__(self, slot: torch.Tensor, q_gate, q_up, q_down, n_hot: int, n_cold: int):
+        self.slot, self.q_gate, self.q_up, self.q_down = slot, q_gate, q_up, q_down
+        self.n_hot, self.n_cold = n_hot, n_cold
+
+    def c(self) -> _Mixed:
+        return _Mixed(_ptr(self.slot), _ptr(self.q_gate), _ptr(self.q_up), _ptr(self.q_down),
+                      self.n_hot, self.n_cold)
+
+
+def moe_expert_ffn_mixed(hidden, w_gate, w_up, w_down, mixed: MixedExperts, d_ff: int,
+                         params: RouteParams, routing: Routing, out, workspace: torch.Tensor, stream=None):
+    for t, n in ((hidden, "hidden"), (w_gate, "w_gate"), (w_up, "w_up"), (w_down, "w_down"), (out, "out")):
+        _need(t, torch.bfloat16, n)
+    _need(mixed.slot, torch.int32, "slot")
+    st = load().moe_expert_ffn_mixed(_ptr(hidden), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
+                                     ctypes.byref(mixed.c()), d_ff, ctypes.byref(params.c()),
+                                     ctypes.byref(routing.c()), _ptr(out), _ptr(workspace),
+                                     workspace.numel(), _stream(stream))
+    _check(st, "moe_expert_ffn_mixed")
+    return out
+
+
+def ema_hot_set(counts, n_hot: int, alpha: float = 0.9) -> "np.ndarray":
+    """Hot experts of a routing trace (DynaExq page, section 2.5): per step
+    S <- alpha * S + (1 - alpha) * c, S starting at 0, then the n_hot experts
+    with the largest S (ties to the lower id).  `counts` is [steps][N]
+    (selections per expert per step).  Host-side policy arithmetic."""
+    import numpy as np
+    c = np.asarray(counts, dtype=np.float64)
+    S = np.zeros(c.shape[1])
+    for row in c:
+        S = alpha * S + (1.0 - alpha) * row
+    order = sorted(range(c.shape[1]), key=lambda e: (-S[e], e))
+    return np.array(sorted(order[:n_hot]), dtype=np.int64)
 
 
 def moe_decode_layer(hidden, w_router, router_bias, w_gate, w_up, w_down, d_ff: int,

@@ -264,6 +264,94 @@ namespace moe {
 moe_status report_error(moe_status status, const char* message) { return fail(status, "%s", message); }
 }  // namespace moe
 
+namespace {
+moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w_up, const void* w_down,
+                           const moe_mixed_experts* mixed, int32_t d_ff, const moe_route_params* params,
+                           const moe_routing* routing, void* out, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream) {
+    Params P;
+    moe_status st = resolve(params, P);
+    if (st != MOE_OK) return st;
+    if ((st = check_routing(routing, false, P.B)) != MOE_OK) return st;
+    if (d_ff < 64 || d_ff % 64 != 0 || d_ff > 16384)
+        return fail(MOE_ERR_ARG, "d_ff=%d must be a multiple of 64 in 64..16384", d_ff);
+    const int n_hot = mixed ? mixed->n_hot : P.N;
+    if (mixed) {
+        if (P.dtype != MOE_DTYPE_BF16) return fail(MOE_ERR_ARG, "mixed experts need bf16 activations");
+        if (P.d % 256 != 0 || d_ff % 256 != 0)
+            return fail(MOE_ERR_ARG, "mixed experts need d and d_ff multiples of 256");
+        if (!mixed->slot || !aligned(mixed->slot, 4)) return fail(MOE_ERR_ARG, "mixed->slot is NULL or misaligned");
+        if (mixed->n_hot < 1 || mixed->n_cold < 0) return fail(MOE_ERR_ARG, "need n_hot >= 1 and n_cold >= 0");
+        const void* q[] = {mixed->q_gate, mixed->q_up, mixed->q_down};
+        for (const void* p : q)
+            if ((mixed->n_cold > 0 && !p) || !aligned(p, 16))
+                return fail(MOE_ERR_ARG, "an INT4 image is NULL or not 16-byte aligned");
+    }
+    const void* req[] = {w_gate, w_up, w_down, hidden, out};
+    for (int i = 0; i < 5; ++i) {
+        if (!req[i] && (i < 3 || P.B > 0)) return fail(MOE_ERR_ARG, "a tensor pointer is NULL");
+        if (!aligned(req[i], 16)) return fail(MOE_ERR_ARG, "a tensor pointer is not 16-byte aligned");
+    }
+    const WsLayout L = layout(P, d_ff);
+    if ((st = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return st;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    FfnArgs a{};
+    a.x = hidden;
+    a.T = routing->T;
+    a.active = routing->active;
+    a.counts = routing->counts;
+    a.offsets = routing->offsets;
+    a.perm = routing->perm;
+    a.pos_of = reinterpret_cast<const int32_t*>(ws + L.pos_of);
+    a.idx = routing->expert_idx;
+    a.w = routing->weights;
+    a.hbuf = ws + L.hbuf;
+    a.ybuf = reinterpret_cast<float*>(ws + L.ybuf);
+    a.xperm = ws + L.xperm;
+    a.out = out;
+    a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone);
+    a.ydone = reinterpret_cast<uint32_t*>(ws + L.ydone);
+    a.gflag = reinterpret_cast<uint32_t*>(ws + L.gflag);
+    a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
+    a.w_gate = w_gate;
+    a.w_up = w_up;
+    a.w_down = w_down;
+    a.slot = mixed ? mixed->slot : nullptr;
+    a.q_gate = mixed ? static_cast<const uint8_t*>(mixed->q_gate) : nullptr;
+    a.q_up = mixed ? static_cast<const uint8_t*>(mixed->q_up) : nullptr;
+    a.q_down = mixed ? static_cast<const uint8_t*>(mixed->q_down) : nullptr;
+    a.n_hot = n_hot;
+    a.n_cold = mixed ? mixed->n_cold : 0;
+    a.B = P.B;
+    a.N = P.N;
+    a.d = P.d;
+    a.F = d_ff;
+    a.kslots = P.kslots;
+
+    cudaError_t e;
+    if (P.dtype == MOE_DTYPE_F32) {
+        e = launch_ffn_f32(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 expert launch");
+        return MOE_OK;
+    }
+    if (P.B == 0) return MOE_OK;   // nothing to compute or write
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    CUtensorMap maps[6];
+    if ((st = expert_maps(w_gate, w_up, w_down, n_hot, d_ff, P.d, dev, maps)) != MOE_OK) return st;
+    if ((st = workspace_maps(ws, L, P.B * P.kslots, P.d, d_ff, dev, maps + 3)) != MOE_OK) return st;
+    if ((st = hidden_map(hidden, P.B, P.d, dev, maps + 5)) != MOE_OK) return st;
+    int sms = num_sms();
+    if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
+    if (sms > kMaxGrid) sms = kMaxGrid;
+    e = launch_ffn_bf16(a, maps, sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
+    return MOE_OK;
+}
+}  // namespace
+
 extern "C" {
 
 int32_t moe_num_slots(const moe_route_params* params) {
@@ -336,68 +424,17 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
 moe_status moe_expert_ffn(const void* hidden, const void* w_gate, const void* w_up, const void* w_down,
                           int32_t d_ff, const moe_route_params* params, const moe_routing* routing, void* out,
                           void* workspace, size_t workspace_bytes, moe_stream_t stream) {
-    Params P;
-    moe_status st = resolve(params, P);
-    if (st != MOE_OK) return st;
-    if ((st = check_routing(routing, false, P.B)) != MOE_OK) return st;
-    if (d_ff < 64 || d_ff % 64 != 0 || d_ff > 16384)
-        return fail(MOE_ERR_ARG, "d_ff=%d must be a multiple of 64 in 64..16384", d_ff);
-    const void* req[] = {w_gate, w_up, w_down, hidden, out};
-    for (int i = 0; i < 5; ++i) {
-        if (!req[i] && (i < 3 || P.B > 0)) return fail(MOE_ERR_ARG, "a tensor pointer is NULL");
-        if (!aligned(req[i], 16)) return fail(MOE_ERR_ARG, "a tensor pointer is not 16-byte aligned");
-    }
-    const WsLayout L = layout(P, d_ff);
-    if ((st = check_ws(workspace, workspace_bytes, L.total)) != MOE_OK) return st;
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return expert_ffn_impl(hidden, w_gate, w_up, w_down, nullptr, d_ff, params, routing, out, workspace,
+                           workspace_bytes, stream);
+}
 
-    FfnArgs a{};
-    a.x = hidden;
-    a.T = routing->T;
-    a.active = routing->active;
-    a.counts = routing->counts;
-    a.offsets = routing->offsets;
-    a.perm = routing->perm;
-    a.pos_of = reinterpret_cast<const int32_t*>(ws + L.pos_of);
-    a.idx = routing->expert_idx;
-    a.w = routing->weights;
-    a.hbuf = ws + L.hbuf;
-    a.ybuf = reinterpret_cast<float*>(ws + L.ybuf);
-    a.xperm = ws + L.xperm;
-    a.out = out;
-    a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone);
-    a.ydone = reinterpret_cast<uint32_t*>(ws + L.ydone);
-    a.gflag = reinterpret_cast<uint32_t*>(ws + L.gflag);
-    a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
-    a.w_gate = w_gate;
-    a.w_up = w_up;
-    a.w_down = w_down;
-    a.B = P.B;
-    a.N = P.N;
-    a.d = P.d;
-    a.F = d_ff;
-    a.kslots = P.kslots;
-
-    cudaError_t e;
-    if (P.dtype == MOE_DTYPE_F32) {
-        e = launch_ffn_f32(a, s);
-        if (e != cudaSuccess) return cuda_fail(e, "fp32 expert launch");
-        return MOE_OK;
-    }
-    if (P.B == 0) return MOE_OK;   // nothing to compute or write
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    CUtensorMap maps[6];
-    if ((st = expert_maps(w_gate, w_up, w_down, P.N, d_ff, P.d, dev, maps)) != MOE_OK) return st;
-    if ((st = workspace_maps(ws, L, P.B * P.kslots, P.d, d_ff, dev, maps + 3)) != MOE_OK) return st;
-    if ((st = hidden_map(hidden, P.B, P.d, dev, maps + 5)) != MOE_OK) return st;
-    int sms = num_sms();
-    if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
-    if (sms > kMaxGrid) sms = kMaxGrid;
-    e = launch_ffn_bf16(a, maps, sms, s);
-    if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
-    return MOE_OK;
+moe_status moe_expert_ffn_mixed(const void* hidden, const void* w_gate, const void* w_up, const void* w_down,
+                                const moe_mixed_experts* mixed, int32_t d_ff, const moe_route_params* params,
+                                const moe_routing* routing, void* out, void* workspace, size_t workspace_bytes,
+                                moe_stream_t stream) {
+    if (!mixed) return fail(MOE_ERR_ARG, "mixed is NULL");
+    return expert_ffn_impl(hidden, w_gate, w_up, w_down, mixed, d_ff, params, routing, out, workspace,
+                           workspace_bytes, stream);
 }
 
 moe_status moe_decode_layer(const void* hidden, const void* w_router, const float* router_bias,

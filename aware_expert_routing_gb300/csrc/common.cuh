@@ -104,7 +104,12 @@ struct FfnArgs {
     const void* w_gate;     // [N][F][d]   (fp32 path)
     const void* w_up;
     const void* w_down;     // [N][d][F]
+    const int32_t* slot;    // [N] or null: >= 0 bf16 row block, < 0: -1 - INT4 expert
+    const uint8_t* q_gate;  // INT4 experts, packed (see moe.h)
+    const uint8_t* q_up;
+    const uint8_t* q_down;
     int B, N, d, F, kslots;
+    int n_hot, n_cold;
 };
 
 // Launchers (defined in the .cu files).
@@ -204,6 +209,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         " [%0], [%1, {%2, %3, %4}], [%5], %6;"
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
           "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// 1D bulk copy global -> shared (both addresses 16-byte aligned, bytes a
+// multiple of 16), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 

@@ -53,6 +53,16 @@
 //     arrived, each CTA combines its slice of the output four columns at a
 //     time, out_i = sum over slots (in slot order) of w_is * y_is.
 //   * The last CTA to finish resets the counters for the next launch.
+//   * Mixed precision (DynaExq page, section 3.2: hot experts in high
+//     precision, cold experts INT4).  An INT4 expert's matrices are packed as
+//     chunks of (16 or 32 rows) x 256 columns: 128 bytes of 4-bit codes per
+//     row, then the rows' bf16 scales of the two 128-column groups.  Its
+//     tiles have the same geometry as bf16 tiles; a stage is one 1D bulk
+//     copy per matrix.  The consumer decodes a code pair into bf16 exactly
+//     ((nibbles | 0x4300) is 128 + q + 8; subtracting 136 leaves q),
+//     multiplies the integers on the tensor cores, and scales each row's
+//     fp32 partial sum of the 64-column block (one 128-column group) by the
+//     group scale, so q*s is never rounded.
 // Every result is computed in a fixed order, so runs are bit-reproducible.
 #include "common.cuh"
 
@@ -84,8 +94,8 @@ struct Smem {
     uint64_t empty[kStages];
     int chunk_off[MOE_MAX_EXPERTS + 1];
     uint32_t ex_info[MOE_MAX_EXPERTS];  // active index -> id | cnt << 10 | first pair << 19
-    uint16_t ex_of[MOE_MAX_EXPERTS];    // expert id -> active index (batches of <= 16 tokens)
-    uint32_t tokmask[MOE_MAX_EXPERTS];  // active index -> tokens routed to it (batches of <= 16)
+    uint16_t tokmask[MOE_MAX_EXPERTS];  // active index -> tokens routed to it (batches of <= 16)
+    int ex_slot[MOE_MAX_EXPERTS];       // active index -> bf16 row block (>= 0) or -1 - INT4 expert
     int abort_flag;
     int last_flag;
 };
@@ -94,8 +104,11 @@ constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kSlotBytes + sizeof(Smem)
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Tile {
-    int a, e, rb, c, off, ntok, nch;
+    int a, e, rb, c, off, ntok, nch, slot;
 };
+
+constexpr int kQ4ChunkA = 16 * 128 + 16 * 4;   // INT4 chunk of W_gate / W_up: 16 rows x 256 columns
+constexpr int kQ4ChunkB = 32 * 128 + 32 * 4;   // INT4 chunk of W_down: 32 rows x 256 columns
 
 // Tile t of a phase with rbn row blocks per (expert, chunk); shared memory only.
 __device__ __forceinline__ Tile decode_tile(int t, int rbn, const Smem& S, int Tn) {
@@ -112,6 +125,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int rbn, const Smem& S, int T
     const int cnt = (info >> 10) & 511u;
     T.off = info >> 19;
     T.nch = chunk_off[lo + 1] - chunk_off[lo];
+    T.slot = S.ex_slot[lo];
     const int r = t - chunk_off[lo] * rbn;
     T.rb = r / T.nch;
     T.c = r - T.rb * T.nch;
@@ -183,6 +197,33 @@ __device__ __forceinline__ void mma_pair(float (&acc0)[4], float (&acc1)[4], con
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
+// Eight codes (one packed word) -> four bf16x2 A-fragment words, exact:
+// (w >> 4p) & 0x000f000f | 0x43004300 is the pair (128 + c0, 128 + c1) with
+// c = q + 8; subtracting 136 leaves (q0, q1).
+__device__ __forceinline__ void decode_q4(uint32_t w, uint32_t* r) {
+    const __nv_bfloat162 off = __floats2bfloat162_rn(136.f, 136.f);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint32_t v;
+        asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(v) : "r"(w >> (4 * p)), "r"(0x000f000fu), "r"(0x43004300u));
+        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), off);
+        r[p] = *reinterpret_cast<const uint32_t*>(&q);
+    }
+}
+
+// Row `row` of an INT4 chunk (rows of 128 code bytes): the lane's 16 columns
+// of the 64-column block `blk` as eight A-fragment words.
+__device__ __forceinline__ void load_row_q4(const unsigned char* chunk, int row, int blk, int t4, uint32_t (&r)[8]) {
+    const uint2 w = *reinterpret_cast<const uint2*>(chunk + row * 128 + blk * 32 + t4 * 8);
+    decode_q4(w.x, r);
+    decode_q4(w.y, r + 4);
+}
+
+__device__ __forceinline__ float q4_scale(const unsigned char* chunk, int rows, int row, int blk) {
+    const __nv_bfloat16 s = *reinterpret_cast<const __nv_bfloat16*>(chunk + rows * 128 + (row * 2 + (blk >> 1)) * 2);
+    return __bfloat162float(s);
+}
+
 struct Ranges {
     int a_beg, a_end, b_beg, b_end;
     int rbA, rbB, SA, SB, Tn, Ctot;
@@ -194,7 +235,7 @@ struct Ranges {
 // 32-row box, 2048 bytes apart.
 template <bool PHASE_A>
 __device__ __forceinline__ void consume_tile(const unsigned char* ring, Smem& S, uint32_t* flags, int nstage,
-                                             int K, int NT, uint32_t& it, float (&acc)[2][kNT][4]) {
+                                             int K, int NT, bool q4, uint32_t& it, float (&acc)[2][kNT][4]) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
 #pragma unroll
     for (int m = 0; m < 2; ++m)
@@ -206,7 +247,40 @@ __device__ __forceinline__ void consume_tile(const unsigned char* ring, Smem& S,
         const int slot = it % kStages;
         const int kq = min(4, (K - 256 * s) / 64);
         wait_bar(&S.full[slot], (it / kStages) & 1, S, flags);
-        if (w < kq) {
+        if (w < kq && q4) {
+            // INT4 chunk(s): phase A gate at 0 and up at 8192 (16 rows each);
+            // phase B one 32-row chunk.  Integer products into tmp, then each
+            // row's partial sum is scaled by its group scale.
+            const unsigned char* st = ring + (size_t)slot * kSlotBytes;
+            const unsigned char* op = st + kWBytes + w * 1024;
+            const unsigned char* c0p = st;
+            const unsigned char* c1p = PHASE_A ? st + 8192 : st;
+            const int rows = PHASE_A ? 16 : 32;
+            const int r1 = PHASE_A ? 0 : 16;
+            uint32_t a0[8], a1[8], c0[8], c1[8];
+            load_row_q4(c0p, g, w, t4, a0);
+            load_row_q4(c0p, g + 8, w, t4, a1);
+            load_row_q4(c1p, r1 + g, w, t4, c0);
+            load_row_q4(c1p, r1 + g + 8, w, t4, c1);
+            const float s00 = q4_scale(c0p, rows, g, w), s01 = q4_scale(c0p, rows, g + 8, w);
+            const float s10 = q4_scale(c1p, rows, r1 + g, w), s11 = q4_scale(c1p, rows, r1 + g + 8, w);
+#pragma unroll
+            for (int j = 0; j < kNT; ++j)
+                if (j < NT) {
+                    uint32_t X[8];
+                    load_row(op + j * 4096, g, t4, X);
+                    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_pair(t0, t1, a0, a1, c0, c1, X);
+                    acc[0][j][0] += s00 * t0[0];
+                    acc[0][j][1] += s00 * t0[1];
+                    acc[0][j][2] += s01 * t0[2];
+                    acc[0][j][3] += s01 * t0[3];
+                    acc[1][j][0] += s10 * t1[0];
+                    acc[1][j][1] += s10 * t1[1];
+                    acc[1][j][2] += s11 * t1[2];
+                    acc[1][j][3] += s11 * t1[3];
+                }
+        } else if (w < kq) {
             const unsigned char* st = ring + (size_t)slot * kSlotBytes;
             const unsigned char* op = st + kWBytes + w * 1024;
             const unsigned char* b0 = PHASE_A ? st + w * 2048 : st + w * 4096;
@@ -269,6 +343,12 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
                 const int e = A.active[a];
                 const int cnt = A.counts[e];
                 S.ex_info[a] = (uint32_t)e | ((uint32_t)cnt << 10) | ((uint32_t)A.offsets[e] << 19);
+                int sl = A.slot ? A.slot[e] : e;
+                if (sl >= A.n_hot || -1 - sl >= A.n_cold) {   // out of range: flag it, read expert 0
+                    raise_flag(flags, kFlagBadIndex);
+                    sl = A.n_hot > 0 ? 0 : -1;
+                }
+                S.ex_slot[a] = sl;
                 nch = (cnt + kChunk - 1) / kChunk;
             }
             int inc = nch;
@@ -282,10 +362,6 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         }
     }
     const bool small_b = A.B <= kChunk;   // phase-A operands: the whole batch from the hidden states
-    if (small_b) {
-        for (int q = threadIdx.x; q < Tn; q += kThreads) S.tokmask[q] = 0;
-        for (int q = threadIdx.x; q < Tn; q += kThreads) S.ex_of[A.active[q]] = (uint16_t)q;
-    }
     if (warp == kWarpW && lane == 0) {
         prefetch_tensormap(&tm_gate);
         prefetch_tensormap(&tm_up);
@@ -297,13 +373,13 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         prefetch_tensormap(&tm_h);
     }
     __syncthreads();
-    if (small_b) {   // token masks of the active experts
-        for (int q = threadIdx.x; q < A.B * A.kslots; q += kThreads) {
-            const int pos = A.pos_of[q];
-            if (pos >= 0) {
-                const int e = A.idx[q];
-                atomicOr(&S.tokmask[S.ex_of[e]], 1u << (q / A.kslots));
-            }
+    if (small_b) {   // token masks of the active experts (their pairs are consecutive)
+        for (int a = threadIdx.x; a < Tn; a += kThreads) {
+            const uint32_t info = S.ex_info[a];
+            const int cnt = (info >> 10) & 511u, off = info >> 19;
+            uint32_t m = 0;
+            for (int q = 0; q < cnt; ++q) m |= 1u << (A.perm[off + q] / A.kslots);
+            S.tokmask[a] = (uint16_t)m;
         }
         __syncthreads();
     }
@@ -330,28 +406,45 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
             const uint64_t pol_once = l2_evict_first_policy();
             const uint64_t pol_keep = l2_evict_normal_policy();
             uint32_t it = 0;
+            const size_t q4_mat_a = (size_t)(F / 16) * (d / 256) * kQ4ChunkA;   // bytes of one INT4 W_gate / W_up
+            const size_t q4_mat_b = (size_t)(d / 32) * (F / 256) * kQ4ChunkB;   // bytes of one INT4 W_down
             for (int t = R.a_beg; t < R.a_end; ++t) {
                 const Tile T = decode_tile(t, R.rbA, S, Tn);
-                const int row = T.e * F + 16 * T.rb;
+                const int row = T.slot * F + 16 * T.rb;
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
                 for (int s = 0; s < R.SA; ++s, ++it) {
                     const int slot = it % kStages;
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    mbar_arrive_expect_tx(&S.full[slot], kWBytes);   // column blocks past d are zero-filled
                     unsigned char* dst = ring + (size_t)slot * kSlotBytes;
-                    tma_load_3d(dst, &tm_gate, 0, row, 4 * s, &S.full[slot], pol);
-                    tma_load_3d(dst + 8192, &tm_up, 0, row, 4 * s, &S.full[slot], pol);
+                    if (T.slot >= 0) {
+                        mbar_arrive_expect_tx(&S.full[slot], kWBytes);   // column blocks past d are zero-filled
+                        tma_load_3d(dst, &tm_gate, 0, row, 4 * s, &S.full[slot], pol);
+                        tma_load_3d(dst + 8192, &tm_up, 0, row, 4 * s, &S.full[slot], pol);
+                    } else {
+                        const size_t off = (size_t)(-1 - T.slot) * q4_mat_a +
+                                           ((size_t)T.rb * (d / 256) + s) * kQ4ChunkA;
+                        mbar_arrive_expect_tx(&S.full[slot], 2 * kQ4ChunkA);
+                        bulk_load(dst, A.q_gate + off, kQ4ChunkA, &S.full[slot], pol);
+                        bulk_load(dst + 8192, A.q_up + off, kQ4ChunkA, &S.full[slot], pol);
+                    }
                 }
             }
             for (int t = R.b_beg; t < R.b_end; ++t) {
                 const Tile T = decode_tile(t, R.rbB, S, Tn);
-                const int row = T.e * d + 32 * T.rb;
+                const int row = T.slot * d + 32 * T.rb;
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
                 for (int s = 0; s < R.SB; ++s, ++it) {
                     const int slot = it % kStages;
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    mbar_arrive_expect_tx(&S.full[slot], kWBytes);
-                    tma_load_3d(ring + (size_t)slot * kSlotBytes, &tm_down, 0, row, 4 * s, &S.full[slot], pol);
+                    if (T.slot >= 0) {
+                        mbar_arrive_expect_tx(&S.full[slot], kWBytes);
+                        tma_load_3d(ring + (size_t)slot * kSlotBytes, &tm_down, 0, row, 4 * s, &S.full[slot], pol);
+                    } else {
+                        const size_t off = (size_t)(-1 - T.slot) * q4_mat_b +
+                                           ((size_t)T.rb * (F / 256) + s) * kQ4ChunkB;
+                        mbar_arrive_expect_tx(&S.full[slot], kQ4ChunkB);
+                        bulk_load(ring + (size_t)slot * kSlotBytes, A.q_down + off, kQ4ChunkB, &S.full[slot], pol);
+                    }
                 }
             }
             // Every issued stage is consumed before the consumers reach the
@@ -453,8 +546,8 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
             for (int t = t_beg; t < t_end; ++t, ++tt) {
                 const Tile T = decode_tile(t, phase ? R.rbB : R.rbA, S, Tn);
                 const int NT = (phase == 0 && small_b) ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
-                if (phase == 0) consume_tile<true>(ring, S, flags, R.SA, d, NT, it, acc);
-                else consume_tile<false>(ring, S, flags, R.SB, F, NT, it, acc);
+                if (phase == 0) consume_tile<true>(ring, S, flags, R.SA, d, NT, T.slot < 0, it, acc);
+                else consume_tile<false>(ring, S, flags, R.SB, F, NT, T.slot < 0, it, acc);
                 const int buf = tt & 1;
                 if (tt >= 2) named_barrier(kBarFree0 + buf, kRedThreads);
 #pragma unroll

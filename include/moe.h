@@ -187,6 +187,43 @@ moe_status moe_expert_ffn(const void *hidden, const void *w_gate, const void *w_
                           const moe_routing *routing, void *out, void *workspace,
                           size_t workspace_bytes, moe_stream_t stream);
 
+/*
+ * Mixed-precision experts (DynaExq page, section 3.2: frequently used experts
+ * in high precision, the others in a 4-bit version).  Hot experts keep bf16
+ * weights in w_gate / w_up / w_down (laid out as for moe_expert_ffn, with
+ * n_hot experts); cold experts are INT4 with one bf16 scale per row and
+ * 128-column group of the contraction dimension (d for W_gate / W_up, d_ff
+ * for W_down): w = q * s, q in -7..7.
+ *   slot    [N] int32, device: for expert e, slot[e] >= 0 is its index among
+ *           the bf16 experts, slot[e] < 0 means INT4 expert -1 - slot[e].
+ *           An out-of-range slot raises MOE_FLAG_BAD_INDEX.
+ *   q_gate, q_up  [n_cold] packed images of the [d_ff][d] matrices,
+ *   q_down        [n_cold] packed images of the [d][d_ff] matrices.
+ * Packed image of a matrix [rows][cols] with chunk height rb (16 for W_gate
+ * and W_up, 32 for W_down): chunks of rb rows x 256 columns in row-block-major,
+ * column-stage order; a chunk is rb*128 bytes of codes then rb*2 bf16 scales
+ * ([rb][2]: the chunk's two 128-column groups).  In a chunk row, local
+ * column c is the 4-bit field at bit 4*((c%8)/2) + 16*(c%2) of little-endian
+ * 32-bit word c/8 of the row's 128 bytes, holding q + 8.
+ * Requirements: dtype bf16, d and d_ff multiples of 256, n_hot >= 1,
+ * 16-byte aligned images.  Results as moe_expert_ffn; the INT4 products are
+ * exact integers in fp32 and each row's partial sum over a 64-column block is
+ * multiplied by its group scale.
+ */
+typedef struct {
+    const int32_t *slot;
+    const void *q_gate;
+    const void *q_up;
+    const void *q_down;
+    int32_t n_hot;
+    int32_t n_cold;
+} moe_mixed_experts;
+
+moe_status moe_expert_ffn_mixed(const void *hidden, const void *w_gate, const void *w_up, const void *w_down,
+                                const moe_mixed_experts *mixed, int32_t d_ff, const moe_route_params *params,
+                                const moe_routing *routing, void *out, void *workspace, size_t workspace_bytes,
+                                moe_stream_t stream);
+
 /* moe_route followed by moe_expert_ffn on the same stream. */
 moe_status moe_decode_layer(const void *hidden, const void *w_router, const float *router_bias,
                             const void *w_gate, const void *w_up, const void *w_down,
