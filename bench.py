@@ -48,7 +48,7 @@ METRIC = "MoE decode layer µs & HBM GB/s (T·expert bytes roofline) vs B, OEA v
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "qwen3_30b_a3b_uniform_b16"
 HEADLINE = {"qwen3_30b_a3b_uniform_b16": "oea_k0_3", "qwen3_30b_a3b_zipf_sweep": "oea_k0_5_p0.7",
-            "qwen3_235b_a22b_zipf_b64": "oea_k0_5_p0.7"}
+            "qwen3_235b_a22b_zipf_b64": "oea_k0_5_p0.7", "qwen3_30b_a3b_mixed_int4_b32": "oea_k0_5"}
 N_LAYERS = 8          # default rotation; --layers changes it
 
 
@@ -70,6 +70,16 @@ def layer_bytes(w: synth.Workload, B: int, T: float) -> float:
     return router + expert_kernel_bytes(w, B, T)
 
 
+def mixed_kernel_bytes(w: synth.Workload, B: int, n_hot_active: int, n_cold_active: int) -> float:
+    """Expert-kernel bytes with bf16 hot and INT4 cold experts."""
+    return (n_hot_active * w.expert_bytes + n_cold_active * synth.int4_expert_bytes(w.d, w.F)
+            + 2 * B * w.d * 2)
+
+
+def mixed_layer_bytes(w: synth.Workload, B: int, n_hot_active: int, n_cold_active: int) -> float:
+    return w.N * w.d * 2 + B * w.d * 2 + B * w.N * 4 + mixed_kernel_bytes(w, B, n_hot_active, n_cold_active)
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -87,9 +97,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, run: str):
+def recorded_traffic(workload: str, run: str, algo_bytes_per_launch: float):
     """DRAM bytes per launch of the expert kernel from a committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+    capture of the same workload and run, scaled from the captured launch's
+    algorithmic bytes to this run's mean (traffic grows in proportion to the
+    experts streamed); None if the capture predates the kernel source."""
     p = os.path.join(ROOT, "profiles", "ffn_bf16_traffic.json")
     if not os.path.exists(p):
         return None
@@ -98,7 +110,7 @@ def recorded_traffic(workload: str, run: str):
     e = d.get(f"{workload}/{run}")
     if not e or e.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return e.get("dram_bytes_per_launch")
+    return round(e["dram_bytes"] * algo_bytes_per_launch / e["algorithmic_bytes"])
 
 
 # ---------------------------------------------------------------------------
@@ -237,6 +249,46 @@ def cpu_baseline(w, B, run, budget_s, unit_bytes_fn):
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
+def build_mixed(moe, torch, w: synth.Workload, layer: int, D: dict, dev):
+    """Hot set from a 200-step EMA trace of plain top-k on fresh seeded
+    batches of 32 tokens; hot experts stay bf16 (device pool), cold experts
+    are generated on the device, packed to INT4 on the host and uploaded."""
+    bf = torch.bfloat16
+    prm_t = moe.RouteParams(B=32, d=w.d, N=w.N, k=w.k)
+    rt = moe.Routing(prm_t, dev)
+    wst = moe.alloc_workspace(prm_t, 0, dev)
+    xt = torch.empty(32, w.d, dtype=bf, device=dev)
+    counts = []
+    for step in range(200):
+        moe.moe_synth_normal(xt, synth.trace_seed(w, layer, step), float(synth.scale_f32(1.0)))
+        moe.moe_route(xt, D["w_router"], D["bias"], prm_t, rt, wst)
+        counts.append(rt.counts.cpu().numpy())
+    hot = [int(e) for e in moe.ema_hot_set(np.array(counts), w.hot_n)]
+    cold = [e for e in range(w.N) if e not in hot]
+    slot = np.empty(w.N, np.int32)
+    for i, e in enumerate(hot):
+        slot[e] = i
+    for i, e in enumerate(cold):
+        slot[e] = -1 - i
+    hot_idx = torch.tensor(hot, device=dev)
+    pools = {k: D[k].index_select(0, hot_idx).contiguous() for k in ("w_gate", "w_up", "w_down")}
+    q = {k: [] for k in ("w_gate", "w_up", "w_down")}
+    for e in cold:
+        g, u, dn = (D[k][e].float().cpu().numpy() for k in ("w_gate", "w_up", "w_down"))
+        (pg, pu, pd), _ = synth.pack_int4_expert(g, u, dn)
+        q["w_gate"].append(pg)
+        q["w_up"].append(pu)
+        q["w_down"].append(pd)
+    qt = {k: torch.from_numpy(np.stack(v)).to(dev) for k, v in q.items()}
+    mixed = moe.MixedExperts(torch.from_numpy(slot).to(dev), qt["w_gate"], qt["w_up"], qt["w_down"],
+                             len(hot), len(cold))
+    for k in ("w_gate", "w_up", "w_down"):   # the full bf16 tensors are not needed any more
+        D[k] = None
+    D["hot"] = pools
+    D["mixed"] = mixed
+    D["is_hot"] = np.isin(np.arange(w.N), hot)
+
+
 def build_layers(moe, torch, w: synth.Workload, B: int, dev):
     bf = torch.bfloat16
     layers = []
@@ -253,9 +305,22 @@ def build_layers(moe, torch, w: synth.Workload, B: int, dev):
         D["x"] = x
         b = synth.make_bias(w, l)
         D["bias"] = torch.from_numpy(b).to(dev) if b is not None else None
+        if w.int4_cold:
+            build_mixed(moe, torch, w, l, D, dev)
+            torch.cuda.empty_cache()
         layers.append(D)
     torch.cuda.synchronize(dev)
     return layers
+
+
+def expert_call(moe, w, D, prm, routing, out, ws, stream, x=None):
+    x = D["x"] if x is None else x
+    if "mixed" in D:
+        h = D["hot"]
+        moe.moe_expert_ffn_mixed(x, h["w_gate"], h["w_up"], h["w_down"], D["mixed"], w.F, prm, routing, out, ws,
+                                 stream)
+    else:
+        moe.moe_expert_ffn(x, D["w_gate"], D["w_up"], D["w_down"], w.F, prm, routing, out, ws, stream)
 
 
 def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_for=None):
@@ -266,12 +331,22 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
     ws = moe.alloc_workspace(prm, w.F, dev)
     out = torch.empty((B, w.d), dtype=torch.bfloat16, device=dev)
 
-    # T of each layer (routing is deterministic for fixed inputs)
-    Ts = []
+    # T of each layer (routing is deterministic for fixed inputs), and for
+    # mixed layers the active experts' formats
+    Ts, kbytes, lbytes = [], [], []
     with torch.cuda.stream(stream):
         for D in layers:
             moe.moe_route(D["x"], D["w_router"], D["bias"], prm, routing, ws, stream)
-            Ts.append(int(routing.T.item()))
+            T = int(routing.T.item())
+            Ts.append(T)
+            if "mixed" in D:
+                act = routing.active[:T].cpu().numpy()
+                nh = int(D["is_hot"][act].sum())
+                kbytes.append(mixed_kernel_bytes(w, B, nh, T - nh))
+                lbytes.append(mixed_layer_bytes(w, B, nh, T - nh))
+            else:
+                kbytes.append(expert_kernel_bytes(w, B, T))
+                lbytes.append(layer_bytes(w, B, T))
     flags = moe.moe_device_status(ws, stream)
     if flags:
         raise RuntimeError(f"device flags {flags:#x}")
@@ -281,7 +356,7 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
         moe.moe_route(D["x"], D["w_router"], D["bias"], prm, routing, ws, stream)
         if ev_pre is not None:
             ev_pre.record(stream)
-        moe.moe_expert_ffn(D["x"], D["w_gate"], D["w_up"], D["w_down"], w.F, prm, routing, out, ws, stream)
+        expert_call(moe, w, D, prm, routing, out, ws, stream)
         if ev_post is not None:
             ev_post.record(stream)
 
@@ -315,11 +390,10 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
     total_ms = ev_step[0].elapsed_time(ev_step[steps])
     step_us = [ev_step[i].elapsed_time(ev_step[i + 1]) * 1e3 for i in range(steps)]
     ffn_us = [ev_pre[i].elapsed_time(ev_post[i]) * 1e3 for i in range(steps)]
-    T_steps = [Ts[i % N_LAYERS] for i in range(steps)]
-    layer_b = sum(layer_bytes(w, B, T) for T in T_steps)
-    ffn_b = sum(expert_kernel_bytes(w, B, T) for T in T_steps)
+    layer_b = sum(lbytes[i % N_LAYERS] for i in range(steps))
+    ffn_b = sum(kbytes[i % N_LAYERS] for i in range(steps))
     return {
-        "label": label, "T_mean": float(np.mean(Ts)), "T_per_layer": Ts,
+        "label": label, "T_mean": float(np.mean(Ts)), "T_per_layer": Ts, "layer_bytes": lbytes,
         "total_ms": total_ms, "bytes": layer_b,
         "us_per_layer": total_ms * 1e3 / steps,
         "us_per_layer_p10_p50_p90": [float(np.percentile(step_us, q)) for q in (10, 50, 90)],
@@ -333,7 +407,7 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
     }
 
 
-def run_e2e(moe, torch, w, B, layers, run, steps, warmup, dev, stream, Ts):
+def run_e2e(moe, torch, w, B, layers, run, steps, warmup, dev, stream, lbytes):
     """moe_decode_layer with the hidden states copied in from pinned host
     memory and the output copied back, every step, inside the timed region."""
     label, mode, k0, p = run
@@ -350,8 +424,12 @@ def run_e2e(moe, torch, w, B, layers, run, steps, warmup, dev, stream, Ts):
         D = layers[i % N_LAYERS]
         with torch.cuda.stream(stream):
             x_dev.copy_(x_host[i % N_LAYERS], non_blocking=True)
-            moe.moe_decode_layer(x_dev, D["w_router"], D["bias"], D["w_gate"], D["w_up"], D["w_down"], w.F,
-                                 prm, routing, out, ws, stream)
+            if "mixed" in D:
+                moe.moe_route(x_dev, D["w_router"], D["bias"], prm, routing, ws, stream)
+                expert_call(moe, w, D, prm, routing, out, ws, stream, x=x_dev)
+            else:
+                moe.moe_decode_layer(x_dev, D["w_router"], D["bias"], D["w_gate"], D["w_up"], D["w_down"],
+                                     w.F, prm, routing, out, ws, stream)
             out_host.copy_(out, non_blocking=True)
 
     for i in range(warmup):
@@ -369,7 +447,7 @@ def run_e2e(moe, torch, w, B, layers, run, steps, warmup, dev, stream, Ts):
     flags = moe.moe_device_status(ws, stream)
     if flags:
         raise RuntimeError(f"device flags {flags:#x}")
-    b = sum(layer_bytes(w, B, Ts[i % N_LAYERS]) for i in range(steps))
+    b = sum(lbytes[i % N_LAYERS] for i in range(steps))
     return {"value": b / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": B * w.d * 2,
             "d2h_bytes_per_step": B * w.d * 2, "us_per_layer": ms * 1e3 / steps, "_bytes": b, "_ms": ms}
 
@@ -434,13 +512,16 @@ def main_ours(args):
     smi = gpu_smi_id(torch, dev)
 
     results = {}
+    if args.only_run:
+        runs = {args.only_run: runs[args.only_run]}
+        head = runs[args.only_run]
     for label, run in runs.items():
         res = run_mode(moe, torch, w, B, layers, run, args.steps, args.warmup, dev, stream,
                        clocks_for=smi if label == head[0] else None)
         res.pop("objs")
         results[label] = res
     hr = results[head[0]]
-    e2e = run_e2e(moe, torch, w, B, layers, head, args.steps, args.warmup, dev, stream, hr["T_per_layer"])
+    e2e = run_e2e(moe, torch, w, B, layers, head, args.steps, args.warmup, dev, stream, hr["layer_bytes"])
 
     # whole job: bytes of all ranks / slowest rank
     t_max = reduce_max(torch, dev, hr["total_ms"])
@@ -455,13 +536,16 @@ def main_ours(args):
     peaks = measured_peaks()
     ach = hr["ffn_gbs"]
     roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": recorded_traffic(w.name, head[0]),
+            "frac": round(ach / peaks["hbm_gbs"], 4),
+            "traffic": recorded_traffic(w.name, head[0], hr["ffn_bytes_per_launch"]),
             "kernel": "ffn_bf16_kernel", "peak_source": peaks["source"],
             "algorithmic_bytes_per_launch": round(hr["ffn_bytes_per_launch"]),
             "mean_launch_us": round(hr["ffn_us_mean"], 2)}
     base = None
     if not args.no_cpu_baseline:
-        base = cpu_baseline(w, B, head, args.cpu_budget, lambda T: layer_bytes(w, B, T))
+        mean_b = float(np.mean(hr["layer_bytes"]))
+        base = cpu_baseline(w, B, head, args.cpu_budget,
+                            (lambda T: mean_b) if w.int4_cold else (lambda T: layer_bytes(w, B, T)))
     modes = {}
     for label, r in results.items():
         modes[label] = {"T": round(r["T_mean"], 2), "us_per_layer": round(r["us_per_layer"], 2),
@@ -556,6 +640,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep-out", default="")
     ap.add_argument("--layers", type=int, default=8, help="distinct layers rotated through")
+    ap.add_argument("--only-run", default="", help="time only this routing run (profiling)")
     args = ap.parse_args()
     global N_LAYERS
     N_LAYERS = args.layers
