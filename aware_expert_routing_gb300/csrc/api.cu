@@ -306,6 +306,7 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     a.perm = routing->perm;
     a.pos_of = reinterpret_cast<const int32_t*>(ws + L.pos_of);
     a.idx = routing->expert_idx;
+    a.exinfo = reinterpret_cast<const uint32_t*>(ws + L.exinfo);
     a.w = routing->weights;
     a.hbuf = ws + L.hbuf;
     a.ybuf = reinterpret_cast<float*>(ws + L.ybuf);
@@ -415,6 +416,7 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
     a.perm = routing->perm;
     a.pos_of = reinterpret_cast<int32_t*>(ws + L.pos_of);
     a.n_base = routing->n_base;
+    a.exinfo = reinterpret_cast<uint32_t*>(ws + L.exinfo);
     a.flags = &reinterpret_cast<WsHeader*>(ws + L.header)->flags;
     e = launch_route(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");

@@ -30,7 +30,7 @@ struct WsHeader {
 };
 
 struct WsLayout {
-    size_t header, hdone, ydone, gflag, pos_of, logits, hbuf, ybuf, xperm, total;
+    size_t header, hdone, ydone, gflag, exinfo, pos_of, logits, hbuf, ybuf, xperm, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -46,6 +46,7 @@ inline WsLayout ws_layout(int B, int N, int d, int kslots, int F, int h_elt) {
     L.hdone = o;  o += align256(sizeof(uint32_t) * N);
     L.ydone = o;  o += align256(sizeof(uint32_t) * (d / 32 + 1));
     L.gflag = o;  o += align256(sizeof(uint32_t) * kMaxGrid);
+    L.exinfo = o; o += align256(sizeof(uint32_t) * 2 * N);   // per active expert: info, token mask
     L.pos_of = o; o += align256(sizeof(int32_t) * (size_t)B * kslots + 4);
     L.logits = o; o += align256(sizeof(float) * (size_t)B * N + 4);
     L.hbuf = o;   o += align256((size_t)B * kslots * F * h_elt);
@@ -80,6 +81,7 @@ struct RouteArgs {
     int32_t* perm;          // [B*kslots]
     int32_t* pos_of;        // [B*kslots]
     int32_t* n_base;        // [B] or null
+    uint32_t* exinfo;       // [2][N]: active expert a -> id | cnt << 10 | first pair << 19; tokens (B <= 32)
     uint32_t* flags;
 };
 
@@ -91,6 +93,7 @@ struct FfnArgs {
     const int32_t* offsets;
     const int32_t* perm;
     const int32_t* pos_of;
+    const uint32_t* exinfo; // [2][N] written by the routing kernel
     const int32_t* idx;     // [B][kslots] routing experts
     const float* w;         // [B][kslots] routing weights
     void* hbuf;             // [pairs][F]

@@ -340,9 +340,11 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
             const int a = a0 + lane;
             int nch = 0;
             if (a < Tn) {
-                const int e = A.active[a];
-                const int cnt = A.counts[e];
-                S.ex_info[a] = (uint32_t)e | ((uint32_t)cnt << 10) | ((uint32_t)A.offsets[e] << 19);
+                const uint32_t info = A.exinfo[a];   // written by the routing kernel
+                const int e = info & 1023u;
+                const int cnt = (info >> 10) & 511u;
+                S.ex_info[a] = info;
+                S.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
                 int sl = A.slot ? A.slot[e] : e;
                 if (sl >= A.n_hot || -1 - sl >= A.n_cold) {   // out of range: flag it, read expert 0
                     raise_flag(flags, kFlagBadIndex);
@@ -373,16 +375,6 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         prefetch_tensormap(&tm_h);
     }
     __syncthreads();
-    if (small_b) {   // token masks of the active experts (their pairs are consecutive)
-        for (int a = threadIdx.x; a < Tn; a += kThreads) {
-            const uint32_t info = S.ex_info[a];
-            const int cnt = (info >> 10) & 511u, off = info >> 19;
-            uint32_t m = 0;
-            for (int q = 0; q < cnt; ++q) m |= 1u << (A.perm[off + q] / A.kslots);
-            S.tokmask[a] = (uint16_t)m;
-        }
-        __syncthreads();
-    }
 
     Ranges R;
     R.Tn = Tn;

@@ -19,8 +19,9 @@
 // hold the maximum.  The batch union S_base is an N-bit mask in shared
 // memory built with __ballot_sync + atomicOr.  Grouping by expert: every
 // kept (token, expert) sets bit (token mod 32) of word [token / 32][expert];
-// per-expert counts and per-chunk prefix counts then give each pair's
-// position directly (tokens ascending within an expert).
+// one warp turns those words into per-expert counts, offsets and per-chunk
+// prefix counts, which give each pair's position directly (tokens ascending
+// within an expert).
 #include <limits.h>
 
 #include "common.cuh"
@@ -86,9 +87,7 @@ struct RouteSmem {
     int* sidx;         // [B][kslots]   kept experts
     uint32_t* bits;    // [chunks][N]   bit (i mod 32) set if token i keeps expert e
     int* pre;          // [chunks][N]   tokens of earlier chunks that keep e
-    int* scnt;         // [N]
-    int* soff;         // [N]
-    int* scan;         // [64]
+    int* soff;         // [N]           first pair of expert e
 };
 
 // Writes the routing of token i: lane r < cnt holds slot r (myid, myval).
@@ -120,9 +119,7 @@ __global__ void route_kernel(RouteArgs a) {
     RouteSmem sm;
     unsigned char* p = smem_raw;
     sm.sbase = reinterpret_cast<uint32_t*>(p); p += 32 * 4;
-    sm.scan = reinterpret_cast<int*>(p); p += 64 * 4;
     sm.snb = reinterpret_cast<int*>(p); p += MOE_MAX_TOKENS * 4;
-    sm.scnt = reinterpret_cast<int*>(p); p += MOE_MAX_EXPERTS * 4;
     sm.soff = reinterpret_cast<int*>(p); p += MOE_MAX_EXPERTS * 4;
     sm.sidx = reinterpret_cast<int*>(p); p += (size_t)B * a.kslots * 4;
     sm.bits = reinterpret_cast<uint32_t*>(p); p += (size_t)nch * N * 4;
@@ -246,65 +243,47 @@ __global__ void route_kernel(RouteArgs a) {
     if (__any_sync(kFull, nonfinite) && lane == 0) raise_flag(a.flags, kFlagNonFinite);
     __syncthreads();
 
-    // ---- per-expert counts and per-chunk prefix counts -------------------------
-    for (int e = threadIdx.x; e < N; e += nthreads) {
-        int c = 0;
-        for (int ch = 0; ch < nch; ++ch) {
-            sm.pre[ch * N + e] = c;
-            c += __popc(sm.bits[ch * N + e]);
-        }
-        sm.scnt[e] = c;
-    }
-    __syncthreads();
-
-    // ---- block exclusive scan of counts and of (count > 0) -------------------
-    {
-        const int per = (N + nthreads - 1) / nthreads;
-        const int e0 = threadIdx.x * per;
-        int s1 = 0, s2 = 0;
-        for (int q = 0; q < per; ++q) {
-            const int e = e0 + q;
-            if (e < N) { s1 += sm.scnt[e]; s2 += sm.scnt[e] > 0; }
-        }
-        int i1 = s1, i2 = s2;   // warp inclusive scans
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int u1 = __shfl_up_sync(kFull, i1, off), u2 = __shfl_up_sync(kFull, i2, off);
-            if (lane >= off) { i1 += u1; i2 += u2; }
-        }
-        if (lane == 31) { sm.scan[warp] = i1; sm.scan[32 + warp] = i2; }
-        __syncthreads();
-        if (warp == 0) {
-            int t1 = lane < nwarps ? sm.scan[lane] : 0, t2 = lane < nwarps ? sm.scan[32 + lane] : 0;
+    // ---- counts, offsets, active list and per-expert info (one warp) ---------
+    if (warp == 0) {   // 32 consecutive experts per round, running totals in registers
+        int base1 = 0, base2 = 0;
+        for (int eb = 0; eb < N; eb += 32) {
+            const int e = eb + lane;
+            int c = 0;
+            if (e < N)
+                for (int ch = 0; ch < nch; ++ch) {
+                    sm.pre[ch * N + e] = c;
+                    c += __popc(sm.bits[ch * N + e]);
+                }
+            const int act = c > 0;
+            int i1 = c, i2 = act;   // inclusive scans across the warp
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const int u1 = __shfl_up_sync(kFull, t1, off), u2 = __shfl_up_sync(kFull, t2, off);
-                if (lane >= off) { t1 += u1; t2 += u2; }
+                const int u1 = __shfl_up_sync(kFull, i1, off), u2 = __shfl_up_sync(kFull, i2, off);
+                if (lane >= off) { i1 += u1; i2 += u2; }
             }
-            __syncwarp();
-            if (lane < nwarps) { sm.scan[lane] = t1; sm.scan[32 + lane] = t2; }
-        }
-        __syncthreads();
-        int ex1 = (warp ? sm.scan[warp - 1] : 0) + i1 - s1;
-        int ex2 = (warp ? sm.scan[32 + warp - 1] : 0) + i2 - s2;
-        for (int q = 0; q < per; ++q) {
-            const int e = e0 + q;
+            const int ex1 = base1 + i1 - c, ex2 = base2 + i2 - act;
             if (e < N) {
-                const int c = sm.scnt[e];
                 sm.soff[e] = ex1;
                 a.counts[e] = c;
                 a.offsets[e] = ex1;
-                if (c > 0) a.active[ex2] = e;
-                ex1 += c;
-                ex2 += c > 0;
+                if (act) {
+                    a.active[ex2] = e;
+                    a.exinfo[ex2] = (uint32_t)e | ((uint32_t)c << 10) | ((uint32_t)ex1 << 19);
+                    a.exinfo[N + ex2] = B <= 32 ? sm.bits[e] : 0u;
+                }
             }
+            base1 += __shfl_sync(kFull, i1, 31);
+            base2 += __shfl_sync(kFull, i2, 31);
         }
-        const int total = sm.scan[nwarps - 1], T = sm.scan[32 + nwarps - 1];
-        if (threadIdx.x == 0) {
-            a.offsets[N] = total;
-            *a.T = T;
+        if (lane == 0) {
+            a.offsets[N] = base1;
+            *a.T = base2;
         }
-        for (int q = T + threadIdx.x; q < N; q += nthreads) a.active[q] = -1;
+        for (int q = base2 + lane; q < N; q += 32) {
+            a.active[q] = -1;
+            a.exinfo[q] = 0;
+            a.exinfo[N + q] = 0;
+        }
     }
     __syncthreads();
 
@@ -324,11 +303,11 @@ template <int NPL>
 cudaError_t launch_route_t(const RouteArgs& a, cudaStream_t s) {
     const int threads = NPL <= 8 ? 1024 : 512;
     const int nch = (a.B + 31) / 32;
-    const size_t smem = 32 * 4 + 64 * 4 + MOE_MAX_TOKENS * 4 + 2 * MOE_MAX_EXPERTS * 4 +
+    const size_t smem = 32 * 4 + MOE_MAX_TOKENS * 4 + MOE_MAX_EXPERTS * 4 +
                         (size_t)a.B * a.kslots * 4 + 2 * (size_t)nch * a.N * 4;
     static bool attr_set = false;
     if (!attr_set) {
-        const int max_smem = 32 * 4 + 64 * 4 + MOE_MAX_TOKENS * 4 + 2 * MOE_MAX_EXPERTS * 4 +
+        const int max_smem = 32 * 4 + MOE_MAX_TOKENS * 4 + MOE_MAX_EXPERTS * 4 +
                              MOE_MAX_TOKENS * MOE_MAX_SLOTS * 4 + 2 * kMaxChunks * MOE_MAX_EXPERTS * 4;
         cudaError_t e = cudaFuncSetAttribute(route_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e != cudaSuccess) return e;

@@ -5,9 +5,10 @@
 //
 // bf16 path.  One CTA computes a 16-expert x 32-token tile over a slice of
 // the hidden dimension with warp-level tensor-core MMAs; the KS CTAs that
-// share a tile form a thread-block cluster and CTA rank 0 adds their
-// partial tiles through distributed shared memory in rank order, so the
-// result is deterministic and no global atomics or second launch are needed.
+// share a tile form a thread-block cluster; each rank adds one slice of the
+// tile over all ranks' partial tiles through distributed shared memory, in
+// rank order, so the result is deterministic and no global atomics or
+// second launch are needed.
 //
 // Operand loads.  Both operands come straight from global memory with
 // 16-byte loads.  Within a 64-column block, lane (g = lane/4, t = lane%4)
@@ -86,8 +87,11 @@ router_bf16_kernel(RouterArgs a) {
         part[l] = s;
     }
     cluster_sync();
-    if (cluster_ctarank() == 0) {
-        for (int l = threadIdx.x; l < 512; l += blockDim.x) {
+    {   // each cluster rank adds up and stores its slice of the tile
+        const int rank = (int)cluster_ctarank();
+        const int per = (512 + a.ks - 1) / a.ks;
+        const int lend = min(512, (rank + 1) * per);
+        for (int l = rank * per + (int)threadIdx.x; l < lend; l += blockDim.x) {
             float v[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) v[r] = r < a.ks ? ld_dsmem_f32(&part[l], r) : 0.f;
@@ -104,7 +108,7 @@ router_bf16_kernel(RouterArgs a) {
             }
         }
     }
-    cluster_sync();   // keep every CTA's shared memory alive until rank 0 read it
+    cluster_sync();   // keep every CTA's shared memory alive until all ranks have read it
 }
 
 // fp32 path: one thread per score, plain FMA over the hidden dimension.

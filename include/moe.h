@@ -168,8 +168,11 @@ moe_status moe_route(const void *hidden, const void *w_router, const float *rout
 
 /*
  * Expert FFN + weighted combine (steps 4-5) for a batch routed by
- * moe_route() with the same params.  Reads only activated experts, each
- * expert's three matrices once from HBM.
+ * moe_route() with the same params and the same workspace: besides the
+ * routing outputs it reads the per-pair positions and per-expert records
+ * that moe_route left in the workspace, so no other call may use that
+ * workspace in between.  Reads only activated experts, each expert's three
+ * matrices once from HBM.
  *   hidden  [B][d]        dtype  the hidden states given to moe_route.
  *   w_gate  [N][d_ff][d]  dtype  expert gate projections.
  *   w_up    [N][d_ff][d]  dtype  expert up projections.
