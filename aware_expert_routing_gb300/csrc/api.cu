@@ -313,7 +313,6 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     a.xperm = ws + L.xperm;
     a.out = out;
     a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone);
-    a.ydone = reinterpret_cast<uint32_t*>(ws + L.ydone);
     a.gflag = reinterpret_cast<uint32_t*>(ws + L.gflag);
     a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
     a.w_gate = w_gate;

@@ -23,14 +23,14 @@ constexpr uint32_t kFlagBadIndex = MOE_FLAG_BAD_INDEX;
 struct WsHeader {
     uint32_t flags;        // MOE_FLAG_* raised by kernels
     uint32_t ctas_done;    // expert kernel: CTAs finished (the last one resets the counters)
+    uint32_t next_tile;    // expert kernel: tiles claimed beyond each CTA's first
     uint32_t unused0;
-    uint32_t a_done;       // expert kernel: CTAs that finished phase A (h written)
-    uint32_t b_done;       // expert kernel: CTAs that finished phase B (y written)
+    uint32_t b_done;       // expert kernel: CTAs that finished all their tiles (y written)
     uint32_t pad[59];
 };
 
 struct WsLayout {
-    size_t header, hdone, ydone, gflag, exinfo, pos_of, logits, hbuf, ybuf, xperm, total;
+    size_t header, hdone, gflag, exinfo, pos_of, logits, hbuf, ybuf, xperm, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -43,8 +43,7 @@ inline WsLayout ws_layout(int B, int N, int d, int kslots, int F, int h_elt) {
     WsLayout L;
     size_t o = 0;
     L.header = o; o += align256(sizeof(WsHeader));
-    L.hdone = o;  o += align256(sizeof(uint32_t) * N);
-    L.ydone = o;  o += align256(sizeof(uint32_t) * (d / 32 + 1));
+    L.hdone = o;  o += align256(sizeof(uint32_t) * (N + (size_t)B * kslots / 16 + 1));   // per token chunk
     L.gflag = o;  o += align256(sizeof(uint32_t) * kMaxGrid);
     L.exinfo = o; o += align256(sizeof(uint32_t) * 2 * N);   // per active expert: info, token mask
     L.pos_of = o; o += align256(sizeof(int32_t) * (size_t)B * kslots + 4);
@@ -100,8 +99,7 @@ struct FfnArgs {
     float* ybuf;            // [pairs][d]
     void* xperm;            // [pairs][d] hidden states grouped by expert
     void* out;              // [B][d]
-    uint32_t* hdone;        // [N]
-    uint32_t* ydone;        // [d/32]
+    uint32_t* hdone;        // [token chunks] phase-A tiles of the chunk whose h rows are written
     uint32_t* gflag;        // [grid] CTA finished its share of the gather
     WsHeader* hdr;
     const void* w_gate;     // [N][F][d]   (fp32 path)

@@ -12,30 +12,38 @@
 //   * Work is a list of tiles.  Phase-A tile (expert a, 16 rows of d_ff,
 //     token chunk c) computes h = silu(W_gate x) * (W_up x) for those rows
 //     and up to 16 tokens and writes h (bf16) to the workspace.  Phase-B
-//     tile (expert a, 32 rows of d, chunk c) computes y = W_down h (fp32).
-//     Each CTA takes an equal, contiguous share of the phase-A tiles and
-//     then of the phase-B tiles, so every CTA streams the same bytes.
+//     tile (expert a, 64 rows of d, chunk c) computes y = W_down h (fp32).
+//     The list holds every phase-A tile, then every phase-B tile, each in
+//     active-expert order.  CTA b starts with tile b and claims each next
+//     tile from one grid-wide counter, so the tiles are taken in list order
+//     and all CTAs finish within about one tile of each other.  The weight
+//     warp claims the tiles and posts them to a 16-entry shared-memory
+//     queue that the other warps read; the epilogue warp frees the entries.
+//   * A phase-B tile needs the h rows of its token chunk: the epilogue
+//     warp counts each finished phase-A tile on the chunk's counter, and
+//     the operand warp waits for that count before it loads h.  All
+//     phase-A tiles precede all phase-B tiles in the list and wait on
+//     nothing later, so these waits always end.
 //   * Phase-A operands.  Batches of up to 16 tokens: every expert's tile
 //     multiplies the whole batch (two 8-row boxes straight from the hidden
 //     states, no copy), and the epilogue keeps the columns of the tokens
 //     routed to the expert.  Larger batches: the CTAs first copy the hidden
 //     states into an expert-grouped buffer (row p = the token of pair p; CTA
-//     b copies rows b, b+G, ...), each raises its own flag, and a CTA's
-//     operand warp waits only for the flags of the CTAs that copied the
-//     rows its tiles read.
-//   * A stage of the 8-deep shared-memory ring holds 256 K-columns of the
-//     weight tile (16 KB: gate+up rows, or 32 down rows) and the matching
+//     b copies rows b, b+G, ...) and each raises its own flag; the operand
+//     warp waits for all flags before its first phase-A tile.
+//   * A stage of the 7-deep shared-memory ring holds 256 K-columns of the
+//     weight tile (16 KB: 16 gate + 16 up rows, or 32 down rows) and the matching
 //     columns of the tokens' operand rows (up to 16 rows, 8 KB), all loaded
 //     by TMA with the 128-byte swizzle through 3D views of the matrices, so
 //     a stage is one or two weight operations plus one per 8 tokens (the
-//     TMA unit's cost per operation, not per byte, limits small boxes).  Warp 4 issues the weight loads and
-//     never waits for another CTA, so the weight stream runs on across the
-//     phase boundary.  Weights read once are marked L2 evict-first; an
-//     expert with more than 16 tokens is read once per 16-token pass, the
-//     passes back to back, and its weights use the normal L2 policy so the repeat reads hit L2.  Warp 5 issues the operand loads:
-//     it waits once for the gather and, before the first h row, once for
-//     every CTA to finish phase A.  Both producers arrive on the stage's
-//     full barrier.
+//     TMA unit's cost per operation, not per byte, limits small boxes).
+//     Warp 4 issues the weight loads and never waits for another CTA.
+//     Weights read once are marked L2 evict-first; an expert with more than
+//     16 tokens is read once per 16-token pass, the passes are neighbours in
+//     the list (so they run at about the same time on different SMs), and
+//     its weights use the normal L2 policy so the repeat reads hit L2.
+//     Warp 5 issues the operand loads.  Both producers arrive on the
+//     stage's full barrier.
 //   * Warps 0-3 are consumers: warp w owns the w-th 64-column block of each
 //     stage and runs warp-level bf16 tensor-core MMAs with the weight rows as
 //     the M side and the tokens as the N side (8 tokens per MMA column
@@ -48,10 +56,11 @@
 //     in a double-buffered shared-memory area and signal without waiting;
 //     warp 6, the epilogue warp, adds them in warp order and writes h
 //     (SwiGLU) or y, then frees the buffer.  The consumers only wait when
-//     they are two tiles ahead of it.  No global fence or atomic per tile.
-//   * After phase B every CTA arrives at a grid-wide counter; once all have
-//     arrived, each CTA combines its slice of the output four columns at a
-//     time, out_i = sum over slots (in slot order) of w_is * y_is.
+//     they are two tiles ahead of it.
+//   * After its last tile every CTA arrives at a grid-wide counter; once
+//     all have arrived, each CTA combines its slice of the output four
+//     columns at a time, out_i = sum over slots (in slot order) of
+//     w_is * y_is.
 //   * The last CTA to finish resets the counters for the next launch.
 //   * Mixed precision (DynaExq page, section 3.2: hot experts in high
 //     precision, cold experts INT4).  An INT4 expert's matrices are packed as
@@ -84,14 +93,19 @@ constexpr int kChunk = 8 * kNT;           // tokens per tile pass
 constexpr int kWBytes = 16384;            // weight part of a stage
 constexpr int kOBytes = kNT * 4096;       // operand part: kNT boxes of 8 rows x 4 column blocks
 constexpr int kSlotBytes = kWBytes + kOBytes;
-constexpr int kStages = 8;
-constexpr int kRed = 2 * 4 * kNT * 32;    // partial sums per warp per tile (2 M-tiles)
+constexpr int kStages = 7;
+constexpr int kQ = 16;                    // tile queue entries
+constexpr int kRed = 4 * 4 * kNT * 32;    // partial sums per warp per tile (up to 4 M-tiles)
 constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
 
 struct Smem {
     float red[2][kCW][kRed];         // double-buffered per-warp partial sums
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t tq_full[kQ];            // tile queue: entry posted by the weight producer
+    uint64_t tq_empty[kQ];           // entry released by the epilogue warp
+    int tq[kQ];                      // tile index, or -1 once the list is exhausted
+    int red_tile[2];                 // tile whose partial sums are in red[b], or -1 (no more tiles)
     int chunk_off[MOE_MAX_EXPERTS + 1];
     uint32_t ex_info[MOE_MAX_EXPERTS];  // active index -> id | cnt << 10 | first pair << 19
     uint16_t tokmask[MOE_MAX_EXPERTS];  // active index -> tokens routed to it (batches of <= 16)
@@ -224,28 +238,27 @@ __device__ __forceinline__ float q4_scale(const unsigned char* chunk, int rows, 
     return __bfloat162float(s);
 }
 
-struct Ranges {
-    int a_beg, a_end, b_beg, b_end;
-    int rbA, rbB, SA, SB, Tn, Ctot;
-};
-
 // Consumer side of one tile: wait for each stage, multiply, release it.
 // M-blocks: phase A = (gate rows 0-15, up rows 0-15) at byte offsets 0 and
-// 8192 of the weight part; phase B = (down rows 0-15, rows 16-31) of a
-// 32-row box, 2048 bytes apart.
+// 8192 of the weight part (acc[0], acc[1]); phase B: stage s holds rows
+// 32 * (s & 1) .. + 31 of the tile's 64 down rows for the K block s >> 1,
+// as one 32-row box whose row halves are 2048 bytes apart (acc[2 (s & 1)],
+// acc[2 (s & 1) + 1]).
 template <bool PHASE_A>
 __device__ __forceinline__ void consume_tile(const unsigned char* ring, Smem& S, uint32_t* flags, int nstage,
-                                             int K, int NT, bool q4, uint32_t& it, float (&acc)[2][kNT][4]) {
+                                             int K, int NT, bool q4, uint32_t& it, float (&acc)[4][kNT][4]) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
+    for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int j = 0; j < kNT; ++j)
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[m][j][q] = 0.f;
     for (int s = 0; s < nstage; ++s, ++it) {
         const int slot = it % kStages;
-        const int kq = min(4, (K - 256 * s) / 64);
+        const int kb = PHASE_A ? s : s >> 1;       // K block of 256 columns
+        const bool hi = !PHASE_A && (s & 1);       // phase B: rows 32-63 of the tile
+        const int kq = min(4, (K - 256 * kb) / 64);
         wait_bar(&S.full[slot], (it / kStages) & 1, S, flags);
         if (w < kq && q4) {
             // INT4 chunk(s): phase A gate at 0 and up at 8192 (16 rows each);
@@ -271,14 +284,16 @@ __device__ __forceinline__ void consume_tile(const unsigned char* ring, Smem& S,
                     load_row(op + j * 4096, g, t4, X);
                     float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
                     mma_pair(t0, t1, a0, a1, c0, c1, X);
-                    acc[0][j][0] += s00 * t0[0];
-                    acc[0][j][1] += s00 * t0[1];
-                    acc[0][j][2] += s01 * t0[2];
-                    acc[0][j][3] += s01 * t0[3];
-                    acc[1][j][0] += s10 * t1[0];
-                    acc[1][j][1] += s10 * t1[1];
-                    acc[1][j][2] += s11 * t1[2];
-                    acc[1][j][3] += s11 * t1[3];
+                    float (&u0)[4] = hi ? acc[2][j] : acc[0][j];
+                    float (&u1)[4] = hi ? acc[3][j] : acc[1][j];
+                    u0[0] += s00 * t0[0];
+                    u0[1] += s00 * t0[1];
+                    u0[2] += s01 * t0[2];
+                    u0[3] += s01 * t0[3];
+                    u1[0] += s10 * t1[0];
+                    u1[1] += s10 * t1[1];
+                    u1[2] += s11 * t1[2];
+                    u1[3] += s11 * t1[3];
                 }
         } else if (w < kq) {
             const unsigned char* st = ring + (size_t)slot * kSlotBytes;
@@ -296,7 +311,8 @@ __device__ __forceinline__ void consume_tile(const unsigned char* ring, Smem& S,
                 if (j < NT) {
                     uint32_t X[8];
                     load_row(op + j * 4096, g, t4, X);
-                    mma_pair(acc[0][j], acc[1][j], a0, a1, c0, c1, X);
+                    if (hi) mma_pair(acc[2][j], acc[3][j], a0, a1, c0, c1, X);
+                    else mma_pair(acc[0][j], acc[1][j], a0, a1, c0, c1, X);
                 }
         }
         __syncwarp();
@@ -323,6 +339,10 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&S.full[i], 2);        // weight producer + operand producer
             mbar_init(&S.empty[i], kCW);
+        }
+        for (int i = 0; i < kQ; ++i) {
+            mbar_init(&S.tq_full[i], 1);
+            mbar_init(&S.tq_empty[i], 1);
         }
         fence_barrier_init();
         S.abort_flag = 0;
@@ -376,66 +396,74 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
     }
     __syncthreads();
 
-    Ranges R;
-    R.Tn = Tn;
-    R.Ctot = S.chunk_off[Tn];
-    R.rbA = F / 16;
-    R.rbB = d / 32;
-    {
-        const long long TA = (long long)R.Ctot * R.rbA, TB = (long long)R.Ctot * R.rbB;
-        const long long b = blockIdx.x;
-        R.a_beg = (int)(TA * b / G);
-        R.a_end = (int)(TA * (b + 1) / G);
-        R.b_beg = (int)(TB * b / G);
-        R.b_end = (int)(TB * (b + 1) / G);
-    }
-    R.SA = (d + 255) / 256;
-    R.SB = (F + 255) / 256;
+    // Tiles: phase A (expert, 16 rows of d_ff, chunk) first, then phase B
+    // (expert, 64 rows of d, chunk), both in active-expert order.
+    const int rbA = F / 16, rbB = d / 64;
+    const int SA = (d + 255) / 256, SB = (F + 255) / 256;
+    const int TA = S.chunk_off[Tn] * rbA;
+    const int Ttot = TA + S.chunk_off[Tn] * rbB;
 
     if (warp == kWarpW) {
         // ---------------------------- weight producer ----------------------------
+        // Claims the CTA's tiles (its first tile is its block index, the
+        // others come from one grid-wide counter, so the tiles are taken in
+        // list order and every CTA runs until the list is exhausted), posts
+        // each to the tile queue and streams its weights.
         if (lane == 0) {
             const uint64_t pol_once = l2_evict_first_policy();
             const uint64_t pol_keep = l2_evict_normal_policy();
             uint32_t it = 0;
             const size_t q4_mat_a = (size_t)(F / 16) * (d / 256) * kQ4ChunkA;   // bytes of one INT4 W_gate / W_up
             const size_t q4_mat_b = (size_t)(d / 32) * (F / 256) * kQ4ChunkB;   // bytes of one INT4 W_down
-            for (int t = R.a_beg; t < R.a_end; ++t) {
-                const Tile T = decode_tile(t, R.rbA, S, Tn);
-                const int row = T.slot * F + 16 * T.rb;
-                const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
-                for (int s = 0; s < R.SA; ++s, ++it) {
-                    const int slot = it % kStages;
-                    if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    unsigned char* dst = ring + (size_t)slot * kSlotBytes;
-                    if (T.slot >= 0) {
-                        mbar_arrive_expect_tx(&S.full[slot], kWBytes);   // column blocks past d are zero-filled
-                        tma_load_3d(dst, &tm_gate, 0, row, 4 * s, &S.full[slot], pol);
-                        tma_load_3d(dst + 8192, &tm_up, 0, row, 4 * s, &S.full[slot], pol);
-                    } else {
-                        const size_t off = (size_t)(-1 - T.slot) * q4_mat_a +
-                                           ((size_t)T.rb * (d / 256) + s) * kQ4ChunkA;
-                        mbar_arrive_expect_tx(&S.full[slot], 2 * kQ4ChunkA);
-                        bulk_load(dst, A.q_gate + off, kQ4ChunkA, &S.full[slot], pol);
-                        bulk_load(dst + 8192, A.q_up + off, kQ4ChunkA, &S.full[slot], pol);
+            // claims run two tiles ahead so that the atomic's latency is hidden
+            int next0 = (int)blockIdx.x;
+            int next1 = next0 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
+            for (int n = 0;; ++n) {
+                const int q = n % kQ;
+                if (n >= kQ) wait_bar(&S.tq_empty[q], ((n / kQ) - 1) & 1, S, flags);
+                const int tile = next0 < Ttot ? next0 : -1;
+                S.tq[q] = tile;
+                mbar_arrive(&S.tq_full[q]);
+                if (tile < 0) break;
+                next0 = next1;
+                next1 = next1 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
+                if (tile < TA) {
+                    const Tile T = decode_tile(tile, rbA, S, Tn);
+                    const int row = T.slot * F + 16 * T.rb;
+                    const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
+                    for (int s = 0; s < SA; ++s, ++it) {
+                        const int slot = it % kStages;
+                        if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
+                        unsigned char* dst = ring + (size_t)slot * kSlotBytes;
+                        if (T.slot >= 0) {
+                            mbar_arrive_expect_tx(&S.full[slot], kWBytes);   // column blocks past d are zero-filled
+                            tma_load_3d(dst, &tm_gate, 0, row, 4 * s, &S.full[slot], pol);
+                            tma_load_3d(dst + 8192, &tm_up, 0, row, 4 * s, &S.full[slot], pol);
+                        } else {
+                            const size_t off = (size_t)(-1 - T.slot) * q4_mat_a +
+                                               ((size_t)T.rb * (d / 256) + s) * kQ4ChunkA;
+                            mbar_arrive_expect_tx(&S.full[slot], 2 * kQ4ChunkA);
+                            bulk_load(dst, A.q_gate + off, kQ4ChunkA, &S.full[slot], pol);
+                            bulk_load(dst + 8192, A.q_up + off, kQ4ChunkA, &S.full[slot], pol);
+                        }
                     }
-                }
-            }
-            for (int t = R.b_beg; t < R.b_end; ++t) {
-                const Tile T = decode_tile(t, R.rbB, S, Tn);
-                const int row = T.slot * d + 32 * T.rb;
-                const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
-                for (int s = 0; s < R.SB; ++s, ++it) {
-                    const int slot = it % kStages;
-                    if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    if (T.slot >= 0) {
-                        mbar_arrive_expect_tx(&S.full[slot], kWBytes);
-                        tma_load_3d(ring + (size_t)slot * kSlotBytes, &tm_down, 0, row, 4 * s, &S.full[slot], pol);
-                    } else {
-                        const size_t off = (size_t)(-1 - T.slot) * q4_mat_b +
-                                           ((size_t)T.rb * (F / 256) + s) * kQ4ChunkB;
-                        mbar_arrive_expect_tx(&S.full[slot], kQ4ChunkB);
-                        bulk_load(ring + (size_t)slot * kSlotBytes, A.q_down + off, kQ4ChunkB, &S.full[slot], pol);
+                } else {
+                    const Tile T = decode_tile(tile - TA, rbB, S, Tn);
+                    const int row = T.slot * d + 64 * T.rb;
+                    const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;
+                    for (int s = 0; s < 2 * SB; ++s, ++it) {   // K block s >> 1, row half s & 1
+                        const int slot = it % kStages;
+                        if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
+                        if (T.slot >= 0) {
+                            mbar_arrive_expect_tx(&S.full[slot], kWBytes);
+                            tma_load_3d(ring + (size_t)slot * kSlotBytes, &tm_down, 0, row + 32 * (s & 1), 4 * (s >> 1),
+                                        &S.full[slot], pol);
+                        } else {
+                            const size_t off = (size_t)(-1 - T.slot) * q4_mat_b +
+                                               ((size_t)(2 * T.rb + (s & 1)) * (F / 256) + (s >> 1)) * kQ4ChunkB;
+                            mbar_arrive_expect_tx(&S.full[slot], kQ4ChunkB);
+                            bulk_load(ring + (size_t)slot * kSlotBytes, A.q_down + off, kQ4ChunkB, &S.full[slot], pol);
+                        }
                     }
                 }
             }
@@ -445,51 +473,43 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
         __syncwarp();
     } else if (warp == kWarpO) {
         // ---------------------------- operand producer ---------------------------
-        if (!small_b && R.a_end > R.a_beg) {   // the rows of this CTA's phase-A tiles are gathered
-            const Tile T0 = decode_tile(R.a_beg, R.rbA, S, Tn);
-            const Tile T1 = decode_tile(R.a_end - 1, R.rbA, S, Tn);
-            const int p_lo = T0.off, p_hi = T1.off + (int)((S.ex_info[T1.a] >> 10) & 511u);
-            const int nown = min((int)G, p_hi - p_lo);
-            for (int c = lane; c < nown; c += 32) wait_counter(&A.gflag[(p_lo + c) % G], 1u, S, flags);
-            __syncwarp();
-            fence_proxy_async_global();
-        }
-        if (lane == 0) {
-            const uint64_t pol = l2_evict_last_policy();
-            uint32_t it = 0;
-            for (int t = R.a_beg; t < R.a_end; ++t) {
-                const Tile T = decode_tile(t, R.rbA, S, Tn);
-                const int nt = small_b ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
-                const int row0 = small_b ? 0 : T.off + kChunk * T.c;
-                const CUtensorMap* map = small_b ? &tm_hid : &tm_x;
-                for (int s = 0; s < R.SA; ++s, ++it) {
-                    const int slot = it % kStages;
-                    if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    mbar_arrive_expect_tx(&S.full[slot], nt * 4096);
-                    unsigned char* dst = ring + (size_t)slot * kSlotBytes + kWBytes;
-                    for (int j = 0; j < nt; ++j)
-                        tma_load_3d(dst + j * 4096, map, 0, row0 + 8 * j, 4 * s, &S.full[slot], pol);
-                }
-            }
-            if (R.b_end > R.b_beg) {   // every h row is written once all CTAs finished phase A
-                wait_counter(&A.hdr->a_done, G, S, flags);
+        const uint64_t pol = l2_evict_last_policy();
+        uint32_t it = 0;
+        bool gathered = small_b;
+        for (int n = 0;; ++n) {
+            const int q = n % kQ;
+            wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
+            const int tile = S.tq[q];
+            if (tile < 0) break;
+            const bool ph_a = tile < TA;
+            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn);
+            if (ph_a && !gathered) {   // every CTA has copied its rows of the grouped hidden states
+                for (int c = lane; c < (int)G; c += 32) wait_counter(&A.gflag[c], 1u, S, flags);
+                __syncwarp();
                 fence_proxy_async_global();
+                gathered = true;
             }
-            for (int t = R.b_beg; t < R.b_end; ++t) {
-                const Tile T = decode_tile(t, R.rbB, S, Tn);
-                const int nt = (T.ntok + 7) >> 3;
-                const int row0 = T.off + kChunk * T.c;
-                for (int s = 0; s < R.SB; ++s, ++it) {
+            if (lane == 0) {
+                if (!ph_a) {   // every phase-A tile of this token chunk has written its h rows
+                    wait_counter(&A.hdone[S.chunk_off[T.a] + T.c], (uint32_t)rbA, S, flags);
+                    fence_proxy_async_global();
+                }
+                const int nt = (ph_a && small_b) ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
+                const int row0 = (ph_a && small_b) ? 0 : T.off + kChunk * T.c;
+                const CUtensorMap* map = ph_a ? (small_b ? &tm_hid : &tm_x) : &tm_h;
+                const int ns = ph_a ? SA : 2 * SB;
+                for (int s = 0; s < ns; ++s, ++it) {
                     const int slot = it % kStages;
+                    const int kb = ph_a ? s : s >> 1;   // phase B: both row halves use the same h columns
                     if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
                     mbar_arrive_expect_tx(&S.full[slot], nt * 4096);
                     unsigned char* dst = ring + (size_t)slot * kSlotBytes + kWBytes;
                     for (int j = 0; j < nt; ++j)
-                        tma_load_3d(dst + j * 4096, &tm_h, 0, row0 + 8 * j, 4 * s, &S.full[slot], pol);
+                        tma_load_3d(dst + j * 4096, map, 0, row0 + 8 * j, 4 * kb, &S.full[slot], pol);
                 }
             }
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp < kCW) {
         // ------------------------------- consumers -------------------------------
         const int w = warp, tid = threadIdx.x;
@@ -529,88 +549,102 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
             }
         }
 
-        // Every tile: multiply, leave the partial sums, signal the epilogue warp.
+        // Every tile: multiply, leave the partial sums and the tile index,
+        // signal the epilogue warp; after the last tile hand over -1.  The
+        // epilogue warp follows this sequence, so both sides always agree
+        // on the number of hand-offs.
         uint32_t it = 0;
-        int tt = 0;   // tiles of both phases, in order
-        float acc[2][kNT][4];
-        for (int phase = 0; phase < 2; ++phase) {
-            const int t_beg = phase ? R.b_beg : R.a_beg, t_end = phase ? R.b_end : R.a_end;
-            for (int t = t_beg; t < t_end; ++t, ++tt) {
-                const Tile T = decode_tile(t, phase ? R.rbB : R.rbA, S, Tn);
-                const int NT = (phase == 0 && small_b) ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
-                if (phase == 0) consume_tile<true>(ring, S, flags, R.SA, d, NT, T.slot < 0, it, acc);
-                else consume_tile<false>(ring, S, flags, R.SB, F, NT, T.slot < 0, it, acc);
-                const int buf = tt & 1;
-                if (tt >= 2) named_barrier(kBarFree0 + buf, kRedThreads);
-#pragma unroll
-                for (int m = 0; m < 2; ++m)
-#pragma unroll
-                    for (int j = 0; j < kNT; ++j)
-                        if (j < NT)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                S.red[buf][w][(m * kNT + j) * 128 + lane * 4 + q] = acc[m][j][q];
+        float acc[4][kNT][4];
+        int n = 0;
+        for (;; ++n) {
+            const int q = n % kQ;
+            wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
+            const int tile = S.tq[q];
+            const int buf = n & 1;
+            if (tile < 0) {
+                if (n >= 2) named_barrier(kBarFree0 + buf, kRedThreads);
+                if (tid == 0) S.red_tile[buf] = -1;
                 named_barrier_arrive(kBarFull0 + buf, kRedThreads);
+                break;
             }
+            const bool ph_a = tile < TA;
+            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn);
+            const int NT = (ph_a && small_b) ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
+            if (ph_a) consume_tile<true>(ring, S, flags, SA, d, NT, T.slot < 0, it, acc);
+            else consume_tile<false>(ring, S, flags, 2 * SB, F, NT, T.slot < 0, it, acc);
+            if (n >= 2) named_barrier(kBarFree0 + buf, kRedThreads);
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int j = 0; j < kNT; ++j)
+                    if (j < NT && (m < 2 || !ph_a))
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq)
+                            S.red[buf][w][(m * kNT + j) * 128 + lane * 4 + qq] = acc[m][j][qq];
+            if (tid == 0) S.red_tile[buf] = tile;
+            named_barrier_arrive(kBarFull0 + buf, kRedThreads);
         }
+        // the epilogue warp frees the buffer of the last tile once more
+        if (n >= 1) named_barrier(kBarFree0 + ((n + 1) & 1), kRedThreads);
         named_barrier(kBarEnd, kRedThreads);
     } else {
         // ------------------------------- epilogue warp ------------------------------
         __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
-        const int ntiles = (R.a_end - R.a_beg) + (R.b_end - R.b_beg);
-        int tt = 0;
-        for (int phase = 0; phase < 2; ++phase) {
-            const int t_beg = phase ? R.b_beg : R.a_beg, t_end = phase ? R.b_end : R.a_end;
-            for (int t = t_beg; t < t_end; ++t, ++tt) {
-                const Tile T = decode_tile(t, phase ? R.rbB : R.rbA, S, Tn);
-                const int NT = (phase == 0 && small_b) ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
-                const uint32_t tmask = small_b ? S.tokmask[T.a] : 0u;
-                const int buf = tt & 1;
-                named_barrier(kBarFull0 + buf, kRedThreads);
-                const float* red = &S.red[buf][0][0];
-                if (phase == 0) {
-                    // element l = j*128 + lane*4 + q of the gate partials (up at +kNT*128)
-                    for (int l = lane; l < NT * 128; l += 32) {
-                        const int j = l >> 7, ln = (l >> 2) & 31, q = l & 3;
-                        const int nn = 8 * j + 2 * (ln & 3) + (q & 1);
-                        // column nn: the tile's nn-th token, or batch token nn
-                        const bool keep = small_b ? ((tmask >> nn) & 1u) != 0 : nn < T.ntok;
-                        if (keep) {
-                            float gs = 0.f, us = 0.f;
+        for (int n = 0;; ++n) {
+            const int buf = n & 1;
+            named_barrier(kBarFull0 + buf, kRedThreads);
+            const int tile = S.red_tile[buf];
+            if (tile < 0) break;
+            const bool ph_a = tile < TA;
+            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn);
+            const int NT = (ph_a && small_b) ? (A.B + 7) >> 3 : (T.ntok + 7) >> 3;
+            const uint32_t tmask = small_b ? S.tokmask[T.a] : 0u;
+            const float* red = &S.red[buf][0][0];
+            if (ph_a) {
+                // element l = j*128 + lane*4 + q of the gate partials (up at +kNT*128)
+                for (int l = lane; l < NT * 128; l += 32) {
+                    const int j = l >> 7, ln = (l >> 2) & 31, qq = l & 3;
+                    const int nn = 8 * j + 2 * (ln & 3) + (qq & 1);
+                    // column nn: the tile's nn-th token, or batch token nn
+                    const bool keep = small_b ? ((tmask >> nn) & 1u) != 0 : nn < T.ntok;
+                    if (keep) {
+                        float gs = 0.f, us = 0.f;
 #pragma unroll
-                            for (int ww = 0; ww < kCW; ++ww) {
-                                gs += red[ww * kRed + l];
-                                us += red[ww * kRed + kNT * 128 + l];
-                            }
-                            const int row = (ln >> 2) + 8 * (q >> 1);
-                            const size_t pos = small_b ? (size_t)T.off + __popc(tmask & ((1u << nn) - 1u))
-                                                       : (size_t)T.off + kChunk * T.c + nn;
-                            hb[pos * F + 16 * T.rb + row] = __float2bfloat16_rn(silu_f(gs) * us);
+                        for (int ww = 0; ww < kCW; ++ww) {   // warp order
+                            gs += red[ww * kRed + l];
+                            us += red[ww * kRed + kNT * 128 + l];
                         }
-                    }
-                } else {
-                    for (int l = lane; l < 2 * kNT * 128; l += 32) {
-                        const int m = l / (kNT * 128), j = (l >> 7) % kNT, ln = (l >> 2) & 31, q = l & 3;
-                        const int nn = 8 * j + 2 * (ln & 3) + (q & 1);
-                        if (j < NT && nn < T.ntok) {
-                            float ys = 0.f;
-#pragma unroll
-                            for (int ww = 0; ww < kCW; ++ww) ys += red[ww * kRed + l];
-                            const int row = 16 * m + (ln >> 2) + 8 * (q >> 1);
-                            const size_t pos = (size_t)T.off + kChunk * T.c + nn;
-                            A.ybuf[pos * d + 32 * T.rb + row] = ys;
-                        }
+                        const int row = (ln >> 2) + 8 * (qq >> 1);
+                        const size_t pos = small_b ? (size_t)T.off + __popc(tmask & ((1u << nn) - 1u))
+                                                   : (size_t)T.off + kChunk * T.c + nn;
+                        hb[pos * F + 16 * T.rb + row] = __float2bfloat16_rn(silu_f(gs) * us);
                     }
                 }
-                if (tt + 2 < ntiles) named_barrier_arrive(kBarFree0 + buf, kRedThreads);
+            } else {
+                for (int l = lane; l < 4 * kNT * 128; l += 32) {
+                    const int m = l / (kNT * 128), j = (l >> 7) % kNT, ln = (l >> 2) & 31, qq = l & 3;
+                    const int nn = 8 * j + 2 * (ln & 3) + (qq & 1);
+                    if (j < NT && nn < T.ntok) {
+                        float ys = 0.f;
+#pragma unroll
+                        for (int ww = 0; ww < kCW; ++ww) ys += red[ww * kRed + l];
+                        const int row = 16 * m + (ln >> 2) + 8 * (qq >> 1);
+                        const size_t pos = (size_t)T.off + kChunk * T.c + nn;
+                        A.ybuf[pos * d + 64 * T.rb + row] = ys;
+                    }
+                }
             }
+            named_barrier_arrive(kBarFree0 + buf, kRedThreads);
             __syncwarp();
-            if (phase == 0 && lane == 0) {   // this CTA's h rows are written
-                __threadfence();
-                atomicAdd(&A.hdr->a_done, 1u);
+            if (lane == 0) {
+                if (ph_a) {   // these h rows are written
+                    __threadfence();
+                    atomicAdd(&A.hdone[S.chunk_off[T.a] + T.c], 1u);
+                }
+                mbar_arrive(&S.tq_empty[n % kQ]);   // tile n came from queue entry n
             }
         }
-        // After phase B every CTA arrives; once all have, the output is combined.
+        // Every CTA arrives after its last tile; once all have, the output is combined.
         if (lane == 0) {
             __threadfence();
             atomicAdd(&A.hdr->b_done, 1u);
@@ -667,9 +701,10 @@ ffn_bf16_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gate,
     if (S.last_flag) {
         __threadfence();
         for (int i = threadIdx.x; i < (int)G; i += kThreads) A.gflag[i] = 0;
+        for (int i = threadIdx.x; i < S.chunk_off[Tn]; i += kThreads) A.hdone[i] = 0;
     }
     if (S.last_flag && threadIdx.x == 0) {
-        A.hdr->a_done = 0;
+        A.hdr->next_tile = 0;
         A.hdr->b_done = 0;
         A.hdr->ctas_done = 0;
     }
