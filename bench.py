@@ -13,7 +13,9 @@ value     = algorithmic bytes / device time for the headline routing run
             activated experts, read once) + the router weights
             N*d*2 + activations (x read twice, scores, output).
 roofline  = the expert kernel alone: its algorithmic bytes per launch over
-            its mean launch time (CUDA events on the launching stream),
+            its mean launch time (CUDA events on the launching stream,
+            recorded around every launch in a second timed pass of the same
+            steps; the headline pass has events only at its two ends),
             against the measured HBM copy bandwidth.
 e2e       = the same metric through moe_decode_layer with host buffers: the
             step's hidden states are copied from pinned host memory and the
@@ -323,7 +325,7 @@ def expert_call(moe, w, D, prm, routing, out, ws, stream, x=None):
         moe.moe_expert_ffn(x, D["w_gate"], D["w_up"], D["w_down"], w.F, prm, routing, out, ws, stream)
 
 
-def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_for=None):
+def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_for=None, detail_steps=2000):
     label, mode, k0, p = run
     prm = moe.RouteParams(B=B, d=w.d, N=w.N, k=w.k, mode=moe.MODE_OEA if mode == "oea" else moe.MODE_TOPK,
                           k0=k0, p=p)
@@ -363,19 +365,21 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize(dev)
-    ev_step = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    ev_pre = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ev_post = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+
+    # Timed region 1 (the headline): K steps back to back, one event pair
+    # around all of them, so consecutive kernels overlap their launch and
+    # prologue as they do in use.
     clocks = Clocks(clocks_for) if clocks_for else None
     if clocks:
         time.sleep(0.5)          # nvidia-smi start-up
     barrier(torch)
     torch.cuda.synchronize(dev)
     t_start = datetime.datetime.now()
-    ev_step[0].record(stream)
+    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_a.record(stream)
     for i in range(steps):
-        step(i, ev_pre[i], ev_post[i])
-        ev_step[i + 1].record(stream)
+        step(i)
+    ev_b.record(stream)
     torch.cuda.synchronize(dev)
     t_end = datetime.datetime.now()
     barrier(torch)
@@ -384,24 +388,43 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
         time.sleep(0.2)
         clocks.window(t_start, t_end)
         clk = clocks.stop()
+    total_ms = ev_a.elapsed_time(ev_b)
+
+    # Timed region 2: the same steps with an event at every step boundary
+    # and around every expert-kernel launch (per-step percentiles and the
+    # expert kernel's launch duration for the roofline).  An event between
+    # two kernels keeps the second from starting early, so these steps run
+    # slower than region 1's.
+    n2 = min(steps, detail_steps)
+    ev_step = [torch.cuda.Event(enable_timing=True) for _ in range(n2 + 1)]
+    ev_pre = [torch.cuda.Event(enable_timing=True) for _ in range(n2)]
+    ev_post = [torch.cuda.Event(enable_timing=True) for _ in range(n2)]
+    barrier(torch)
+    torch.cuda.synchronize(dev)
+    ev_step[0].record(stream)
+    for i in range(n2):
+        step(i, ev_pre[i], ev_post[i])
+        ev_step[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(torch)
     flags = moe.moe_device_status(ws, stream)
     if flags:
         raise RuntimeError(f"device flags {flags:#x}")
-    total_ms = ev_step[0].elapsed_time(ev_step[steps])
-    step_us = [ev_step[i].elapsed_time(ev_step[i + 1]) * 1e3 for i in range(steps)]
-    ffn_us = [ev_pre[i].elapsed_time(ev_post[i]) * 1e3 for i in range(steps)]
+    step_us = [ev_step[i].elapsed_time(ev_step[i + 1]) * 1e3 for i in range(n2)]
+    ffn_us = [ev_pre[i].elapsed_time(ev_post[i]) * 1e3 for i in range(n2)]
     layer_b = sum(lbytes[i % N_LAYERS] for i in range(steps))
-    ffn_b = sum(kbytes[i % N_LAYERS] for i in range(steps))
+    ffn_b = sum(kbytes[i % N_LAYERS] for i in range(n2))
     return {
         "label": label, "T_mean": float(np.mean(Ts)), "T_per_layer": Ts, "layer_bytes": lbytes,
         "total_ms": total_ms, "bytes": layer_b,
         "us_per_layer": total_ms * 1e3 / steps,
         "us_per_layer_p10_p50_p90": [float(np.percentile(step_us, q)) for q in (10, 50, 90)],
+        "us_per_layer_with_kernel_events": float(np.mean(step_us)),
         "gbs": layer_b / (total_ms * 1e-3) / 1e9,
         "tokens_per_s": B * steps / (total_ms * 1e-3),
         "ffn_us_mean": float(np.mean(ffn_us)),
         "ffn_gbs": ffn_b / (sum(ffn_us) * 1e-6) / 1e9,
-        "ffn_bytes_per_launch": ffn_b / steps,
+        "ffn_bytes_per_launch": ffn_b / n2,
         "clocks": clk, "launches": 3 * steps,
         "objs": (prm, routing, ws, out),
     }
@@ -552,6 +575,7 @@ def main_ours(args):
                         "us_p10_p50_p90": [round(v, 2) for v in r["us_per_layer_p10_p50_p90"]],
                         "gbs": round(r["gbs"], 1), "tokens_per_s": round(r["tokens_per_s"]),
                         "frac_of_measured_hbm": round(r["gbs"] / peaks["hbm_gbs"], 4),
+                        "us_per_layer_with_kernel_events": round(r["us_per_layer_with_kernel_events"], 2),
                         "ffn_us": round(r["ffn_us_mean"], 2), "ffn_gbs": round(r["ffn_gbs"], 1)}
     if "topk" in results:
         for label, r in results.items():
