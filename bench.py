@@ -589,8 +589,8 @@ def main_ours(args):
         "data": "synthetic: seeded SplitMix64/Irwin-Hall weights and hidden states, random init",
         "config": {"workload": w.name, "B": B, "N": w.N, "k": w.k, "d": w.d, "d_ff": w.F,
                    "routing": head[0], "layers_rotated": N_LAYERS, "runs": sorted(runs),
-                   "l2": "inputs larger than L2: 8-layer rotation, %.2f GB of expert weights per layer"
-                         % (w.N * w.expert_bytes / 1e9),
+                   "l2": "inputs larger than L2: %d-layer rotation, %.2f GB of expert weights per layer"
+                         % (N_LAYERS, w.N * w.expert_bytes / 1e9),
                    "parallelism": f"replicas x{world}"},
         "modes": modes, "roofline": roof, "cpu_baseline": base, "e2e": e2e,
         "clocks": hr["clocks"], "gpu_launches": hr["launches"],
