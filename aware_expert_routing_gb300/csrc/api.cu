@@ -147,12 +147,13 @@ int g_map_next = 0;
 // consecutive 128-byte-swizzled [box_rows][64] blocks.  One TMA operation
 // per 256 columns keeps the per-operation cost of the TMA unit off the
 // critical path.
-bool encode_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+               uint32_t box_blocks = 4) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[3] = {64, rows, cols / 64};
     cuuint64_t strides[2] = {cols * 2, 128};
-    cuuint32_t box[3] = {64, box_rows, 4};
+    cuuint32_t box[3] = {64, box_rows, box_blocks};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -242,6 +243,112 @@ moe_status hidden_map(const void* hidden, int B, int d, int dev, CUtensorMap* ou
     if (!encode_3d(&e.map, hidden, d, B, 8)) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (hidden)");
     e.used = true;
     *out = e.map;
+    return MOE_OK;
+}
+
+// ---- tensor maps of the tcgen05 expert kernel (boxes one 64-column block wide)
+// W_gate and W_up ([rows][cols] each) interleaved 8 rows at a time through
+// one 5D view {64 columns, 8 rows, 2 matrices, rows/8 row groups, cols/64
+// column blocks}: one box {64, 8, 2, 8, 1} lands as 8 x {8 rows of the lower
+// matrix, the same 8 rows of the other} = 128 rows x 64 columns.  The matrix
+// stride is the distance between the two arrays, lower address first
+// (*swap: W_up is the lower one).  Fails if the arrays coincide or lie 2^40
+// bytes or more apart (the tensor-map stride limit).
+bool encode_gate_up_5d(CUtensorMap* m, const void* g, const void* u, uint64_t cols, uint64_t rows, bool* swap) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const uintptr_t pg = reinterpret_cast<uintptr_t>(g), pu = reinterpret_cast<uintptr_t>(u);
+    *swap = pu < pg;
+    const uintptr_t lo = *swap ? pu : pg, hi = *swap ? pg : pu;
+    const uint64_t delta = hi - lo;
+    if (delta == 0 || delta % 16 != 0 || delta >= (1ull << 40) || rows % 8 != 0) return false;
+    cuuint64_t dims[5] = {64, 8, 2, rows / 8, cols / 64};
+    cuuint64_t strides[4] = {cols * 2, delta, 8 * cols * 2, 128};
+    cuuint32_t box[5] = {64, 8, 2, 8, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, reinterpret_cast<void*>(lo), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct TcMapEntry {
+    MapKey key;
+    CUtensorMap maps[4];   // gate/up 5D (or W_gate 8-row boxes), W_up 8-row boxes, W_down 128-row boxes
+    bool fused, swap, used;
+};
+TcMapEntry g_tc_maps[64];
+int g_tc_next = 0;
+
+moe_status tc_expert_maps(const void* g, const void* u, const void* dn, int N, int F, int d, int dev,
+                          CUtensorMap* out, bool* fused, bool* swap) {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    MapKey key{g, u, dn, N, F, d, dev};
+    for (auto& e : g_tc_maps)
+        if (e.used && e.key == key) {
+            memcpy(out, e.maps, sizeof e.maps);
+            *fused = e.fused;
+            *swap = e.swap;
+            return MOE_OK;
+        }
+    TcMapEntry& e = g_tc_maps[g_tc_next];
+    g_tc_next = (g_tc_next + 1) % 64;
+    e.key = key;
+    e.used = false;
+    e.swap = false;
+    e.fused = encode_gate_up_5d(&e.maps[0], g, u, d, (uint64_t)N * F, &e.swap);
+    if (!e.fused) {   // two maps, 8-row boxes (used when W_gate and W_up cannot share one map)
+        e.swap = false;
+        if (!encode_3d(&e.maps[0], g, d, (uint64_t)N * F, 8, 1))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_gate)");
+    }
+    if (!encode_3d(&e.maps[1], u, d, (uint64_t)N * F, 8, 1) || !encode_3d(&e.maps[2], dn, F, (uint64_t)N * d, 128, 1))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_up / W_down)");
+    e.maps[3] = e.maps[0];
+    e.used = true;
+    memcpy(out, e.maps, sizeof e.maps);
+    *fused = e.fused;
+    *swap = e.swap;
+    return MOE_OK;
+}
+
+// Workspace maps of the tcgen05 kernel: expert-grouped hidden states and h
+// (16-row boxes), and the hidden states themselves (16-row boxes: the whole
+// batch of up to 16 tokens; rows past B read as zeros).
+struct TcOpEntry {
+    const void* ws;
+    const void* hidden;
+    int pairs, B, d, F, dev;
+    CUtensorMap maps[3];
+    bool used;
+};
+TcOpEntry g_tc_ops[32];
+int g_tc_ops_next = 0;
+
+moe_status tc_operand_maps(unsigned char* ws, const WsLayout& L, const void* hidden, int pairs, int B, int d, int F,
+                           int dev, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (auto& e : g_tc_ops)
+        if (e.used && e.ws == ws && e.hidden == hidden && e.pairs == pairs && e.B == B && e.d == d && e.F == F &&
+            e.dev == dev) {
+            memcpy(out, e.maps, sizeof e.maps);
+            return MOE_OK;
+        }
+    TcOpEntry& e = g_tc_ops[g_tc_ops_next];
+    g_tc_ops_next = (g_tc_ops_next + 1) % 32;
+    e.used = false;
+    e.ws = ws;
+    e.hidden = hidden;
+    e.pairs = pairs;
+    e.B = B;
+    e.d = d;
+    e.F = F;
+    e.dev = dev;
+    if (!encode_3d(&e.maps[0], ws + L.xperm, d, pairs, 16, 1) || !encode_3d(&e.maps[1], ws + L.hbuf, F, pairs, 16, 1) ||
+        !encode_3d(&e.maps[2], hidden, d, B, 16, 1))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (operands)");
+    e.used = true;
+    memcpy(out, e.maps, sizeof e.maps);
     return MOE_OK;
 }
 
@@ -339,13 +446,29 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     if (P.B == 0) return MOE_OK;   // nothing to compute or write
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int sms = num_sms();
+    if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
+    if (sms > kMaxGrid) sms = kMaxGrid;
+    if (!mixed) {   // bf16 experts: the tcgen05 kernel
+        CUtensorMap maps[7];
+        bool fused = false, swap = false;
+        CUtensorMap wm[4];
+        if ((st = tc_expert_maps(w_gate, w_up, w_down, P.N, d_ff, P.d, dev, wm, &fused, &swap)) != MOE_OK) return st;
+        maps[0] = wm[0];                       // gate/up 5D, or W_gate
+        maps[1] = wm[0];                       // W_gate (8-row boxes; read when not fused)
+        maps[2] = wm[1];                       // W_up
+        maps[3] = wm[2];                       // W_down
+        if ((st = tc_operand_maps(ws, L, hidden, P.B * P.kslots, P.B, P.d, d_ff, dev, maps + 4)) != MOE_OK) return st;
+        a.gu_fused = fused ? 1 : 0;
+        a.gu_swap = swap ? 1 : 0;
+        e = launch_ffn_tc(a, maps, sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
+        return MOE_OK;
+    }
     CUtensorMap maps[6];
     if ((st = expert_maps(w_gate, w_up, w_down, n_hot, d_ff, P.d, dev, maps)) != MOE_OK) return st;
     if ((st = workspace_maps(ws, L, P.B * P.kslots, P.d, d_ff, dev, maps + 3)) != MOE_OK) return st;
     if ((st = hidden_map(hidden, P.B, P.d, dev, maps + 5)) != MOE_OK) return st;
-    int sms = num_sms();
-    if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
-    if (sms > kMaxGrid) sms = kMaxGrid;
     e = launch_ffn_bf16(a, maps, sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
     return MOE_OK;

@@ -1,0 +1,553 @@
+// ffn_tc.cu -- grouped SwiGLU expert FFN + weighted combine on the
+// 5th-generation tensor cores (tcgen05), bf16 weights.
+//
+// Page "Opportunistic Expert Activation (OEA)": at decode the MoE layer is
+// memory bound and its latency is set by fetching every activated expert's
+// weights from HBM (section 2 Q1, section 4 check 4).  This kernel streams
+// each activated expert's gate, up and down matrices from HBM once and does
+// the arithmetic of all the tokens routed to it while the tile is on chip.
+// Expert form (Qwen3): y = W_down (silu(W_gate x) * (W_up x)); combine:
+// out_i = sum_j w_ij y_{e_ij}(x_i) (kept scores, section 2 Q2).
+//
+// Structure (one persistent CTA per SM, 7 warps):
+//   * Work is a list of tiles.  Phase-A tile (expert a, 64 rows of d_ff,
+//     token chunk c): the 64 W_gate rows and the 64 W_up rows of the same
+//     d_ff indices, interleaved 8 rows at a time (rows 16g..16g+7 = gate
+//     rows 8g..8g+7, rows 16g+8..16g+15 = the up rows), form the 128-row A
+//     operand of a tcgen05 MMA with M = 128; the chunk's 16 token rows are
+//     the N = 16 operand; K = d.  Phase-B tile (expert a, 128 rows of d,
+//     chunk c): W_down rows times the chunk's h rows, K = d_ff.  The list
+//     holds every phase-A tile, then every phase-B tile, each in active-
+//     expert order; CTA b starts with tile b and claims each next tile (two
+//     ahead) from one grid-wide counter, so all CTAs finish within about
+//     one tile of each other.
+//   * Warp 4 claims the tiles, posts them to a 16-entry shared-memory queue
+//     and streams the weights: one TMA operation per 16 KB stage (128 rows x
+//     64 columns, 128-byte swizzle; the gate/up interleave comes from one 5D
+//     tensor map over both matrices).  Warp 5 streams the 16 token rows of
+//     each stage (2 KB): the whole batch of up to 16 tokens straight from
+//     the hidden states, or rows of the expert-grouped copy of the hidden
+//     states, or (phase B) rows of h once every phase-A tile of the chunk
+//     has written them (a per-chunk counter).  Ring: 10 stages of 18 KB.
+//   * Warp 6, lane 0, issues the MMAs: four K=16 steps per stage straight
+//     from the swizzled shared memory (no register staging), fp32
+//     accumulators in tensor memory, four 16-column accumulator buffers.
+//     tcgen05.commit frees each stage when its MMAs have completed and marks
+//     a tile's accumulator full.
+//   * Warps 0-3 (tensor-memory lanes 32w..32w+31, one D row per thread)
+//     read a finished accumulator with tcgen05.ld and free it; phase A:
+//     the lane holding gate row r takes the matching up row from the lane
+//     8 above (shuffle), applies SwiGLU and stores h (bf16) for the tile's
+//     tokens; phase B: stores y (fp32).  After a phase-A tile the four warps
+//     meet at a shared-memory barrier and one thread releases the chunk's
+//     counter.
+//   * All phase-A tiles precede all phase-B tiles in the list and wait on
+//     nothing later, so every wait ends.  After its last tile every CTA
+//     arrives at one grid-wide counter; once all have, each CTA combines a
+//     slice of the output (float4, slot order).  The last CTA resets the
+//     counters for the next launch.
+// Every wait is bounded; a wait that gives up raises MOE_FLAG_WAIT_TIMEOUT
+// and the CTA runs to its end without waiting again.
+#include "common.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kEpiWarps = 4;             // warps 0-3: epilogue
+constexpr int kWarpW = 4;                // weight producer
+constexpr int kWarpO = 5;                // operand producer
+constexpr int kWarpM = 6;                // MMA issuer, owner of the tensor memory
+constexpr int kThreads = 7 * 32;
+constexpr int kM = 128;                  // weight rows per tile (MMA M)
+constexpr int kN = 16;                   // token columns per tile (MMA N)
+constexpr int kWBytes = kM * 128;        // 128 rows x 64 bf16
+constexpr int kOBytes = kN * 128;        // 16 token rows x 64 bf16
+constexpr int kSlotBytes = kWBytes + kOBytes;
+constexpr int kStages = 10;
+constexpr int kQ = 16;                   // tile queue entries
+constexpr int kAcc = 4;                  // accumulator buffers
+constexpr uint32_t kTmemCols = 64;       // kAcc x kN fp32 columns
+constexpr uint32_t kBarEpi = 1;          // named barrier of the four epilogue warps
+constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
+constexpr uint32_t kIdesc = umma_idesc_bf16(kM, kN);
+static_assert(kSlotBytes % 1024 == 0, "stages must stay 1024-byte aligned for the 128-byte swizzle");
+
+struct Smem {
+    uint64_t full[kStages];              // both producers (+ transaction bytes)
+    uint64_t empty[kStages];             // tcgen05.commit after the stage's MMAs
+    uint64_t acc_full[kAcc];             // tcgen05.commit after a tile's last MMA
+    uint64_t acc_empty[kAcc];            // the four epilogue warps
+    uint64_t tq_full[kQ];                // tile queue entry posted by the weight warp
+    uint64_t tq_empty[kQ];               // entry released by the four epilogue warps
+    uint64_t mma_done;                   // every MMA issued has completed
+    uint64_t h_written;                  // the four epilogue warps stored a phase-A tile's h rows
+    int tq[kQ];                          // tile index, or -1 once the list is exhausted
+    int chunk_off[MOE_MAX_EXPERTS + 1];
+    uint32_t ex_info[MOE_MAX_EXPERTS];   // active index -> id | cnt << 10 | first pair << 19
+    uint16_t tokmask[MOE_MAX_EXPERTS];   // active index -> tokens routed to it (batches of <= 16)
+    uint32_t tmem_base;
+    int abort_flag;
+    int last_flag;
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kSlotBytes + sizeof(Smem);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+struct Tile {
+    int a, e, rb, c, off, ntok, nch;
+};
+
+// Tile t of a phase with rbn row blocks per (expert, chunk); shared memory only.
+__device__ __forceinline__ Tile decode_tile(int t, int rbn, const Smem& S, int Tn) {
+    int lo = 0, hi = Tn - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (S.chunk_off[mid] * rbn <= t) lo = mid; else hi = mid - 1;
+    }
+    Tile T;
+    T.a = lo;
+    const uint32_t info = S.ex_info[lo];
+    T.e = info & 1023u;
+    const int cnt = (info >> 10) & 511u;
+    T.off = info >> 19;
+    T.nch = S.chunk_off[lo + 1] - S.chunk_off[lo];
+    const int r = t - S.chunk_off[lo] * rbn;
+    T.rb = r / T.nch;
+    T.c = r - T.rb * T.nch;
+    T.ntok = min(kN, cnt - kN * T.c);
+    return T;
+}
+
+__device__ __forceinline__ void give_up(Smem& S, uint32_t* flags) {
+    *(volatile int*)&S.abort_flag = 1;
+    raise_flag(flags, kFlagTimeout);
+}
+
+// Bounded mbarrier wait; once the CTA has given up every later wait returns
+// at once, so the control flow (and every barrier) still completes.
+__device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t parity, Smem& S, uint32_t* flags) {
+    if (mbar_try_wait(bar, parity)) return;
+    const long long t0 = clock64();
+    while (!*(volatile int*)&S.abort_flag) {
+        if (mbar_try_wait(bar, parity)) return;
+        if (clock64() - t0 > kWaitCycles) {
+            give_up(S, flags);
+            return;
+        }
+    }
+}
+
+// Bounded wait until *p >= need (acquire, GPU scope).
+__device__ __forceinline__ void wait_counter(const uint32_t* p, uint32_t need, Smem& S, uint32_t* flags) {
+    if (ld_acquire_gpu(p) >= need) return;
+    const long long t0 = clock64();
+    while (!*(volatile int*)&S.abort_flag) {
+        if (ld_acquire_gpu(p) >= need) return;
+        if (clock64() - t0 > kWaitCycles) {
+            give_up(S, flags);
+            return;
+        }
+        __nanosleep(32);
+    }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const __grid_constant__ CUtensorMap tm_gate,
+              const __grid_constant__ CUtensorMap tm_up, const __grid_constant__ CUtensorMap tm_down,
+              const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_h,
+              const __grid_constant__ CUtensorMap tm_hid) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* ring = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Smem& S = *reinterpret_cast<Smem*>(ring + (size_t)kStages * kSlotBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = A.d, F = A.F;
+    uint32_t* flags = &A.hdr->flags;
+    const uint32_t G = gridDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&S.full[i], 2);          // weight producer + operand producer
+            mbar_init(&S.empty[i], 1);         // tcgen05.commit
+        }
+        for (int i = 0; i < kAcc; ++i) {
+            mbar_init(&S.acc_full[i], 1);
+            mbar_init(&S.acc_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < kQ; ++i) {
+            mbar_init(&S.tq_full[i], 1);
+            mbar_init(&S.tq_empty[i], kEpiWarps);
+        }
+        mbar_init(&S.mma_done, 1);
+        mbar_init(&S.h_written, kEpiWarps);
+        fence_barrier_init();
+        S.abort_flag = 0;
+    }
+    if (warp == kWarpM) tmem_alloc(&S.tmem_base, kTmemCols);
+    grid_dependency_wait();      // routing comes from the preceding kernel
+    int Tn = *A.T;
+    if (Tn < 0 || Tn > A.N) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) raise_flag(flags, kFlagBadIndex);
+        Tn = 0;
+    }
+    if (warp == 0) {   // per-expert records and chunk offsets of the active experts
+        int run = 0;
+        if (lane == 0) S.chunk_off[0] = 0;
+        for (int a0 = 0; a0 < Tn; a0 += 32) {
+            const int a = a0 + lane;
+            int nch = 0;
+            if (a < Tn) {
+                const uint32_t info = A.exinfo[a];   // written by the routing kernel
+                S.ex_info[a] = info;
+                S.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
+                nch = ((int)((info >> 10) & 511u) + kN - 1) / kN;
+            }
+            int inc = nch;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += u;
+            }
+            if (a < Tn) S.chunk_off[a + 1] = run + inc;
+            run += __shfl_sync(0xffffffffu, inc, 31);
+        }
+    }
+    if (warp == kWarpW && lane == 0) {
+        prefetch_tensormap(A.gu_fused ? &tm_gu : &tm_gate);
+        if (!A.gu_fused) prefetch_tensormap(&tm_up);
+        prefetch_tensormap(&tm_down);
+    }
+    if (warp == kWarpO && lane == 0) {
+        prefetch_tensormap(&tm_x);
+        prefetch_tensormap(&tm_hid);
+        prefetch_tensormap(&tm_h);
+    }
+    tmem_fence_before_sync();
+    __syncthreads();
+    tmem_fence_after_sync();
+    const uint32_t tmem = S.tmem_base;
+
+    // Tiles: phase A (expert, 64 rows of d_ff, chunk) first, then phase B
+    // (expert, 128 rows of d, chunk), both in active-expert order.
+    const int rbA = F / 64, rbB = (d + kM - 1) / kM;
+    const int SA = d / 64, SB = F / 64;             // stages per tile (K blocks of 64)
+    const int TA = S.chunk_off[Tn] * rbA;
+    const int Ttot = TA + S.chunk_off[Tn] * rbB;
+    const bool small_b = A.B <= kN;                 // phase-A operand: the whole batch
+
+    if (warp == kWarpW) {
+        // ---------------------------- weight producer ----------------------------
+        if (lane == 0) {
+            const uint64_t pol_once = l2_evict_first_policy();
+            const uint64_t pol_keep = l2_evict_normal_policy();
+            uint32_t it = 0;
+            // claims run two tiles ahead so that the atomic's latency is hidden
+            int next0 = (int)blockIdx.x;
+            int next1 = next0 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
+            for (int n = 0;; ++n) {
+                const int q = n % kQ;
+                if (n >= kQ) wait_bar(&S.tq_empty[q], ((n / kQ) - 1) & 1, S, flags);
+                const int tile = next0 < Ttot ? next0 : -1;
+                S.tq[q] = tile;
+                mbar_arrive(&S.tq_full[q]);
+                if (tile < 0) break;
+                next0 = next1;
+                next1 = next1 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
+                const bool ph_a = tile < TA;
+                const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn);
+                const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;   // chunked experts are re-read from L2
+                const int row0 = ph_a ? T.e * F + 64 * T.rb : T.e * d + kM * T.rb;
+                const int ns = ph_a ? SA : SB;
+                for (int s = 0; s < ns; ++s, ++it) {
+                    const int slot = it % kStages;
+                    if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
+                    unsigned char* dst = ring + (size_t)slot * kSlotBytes;
+                    mbar_arrive_expect_tx(&S.full[slot], kWBytes);
+                    if (!ph_a) {
+                        // 128 W_down rows (rows past the expert's d are computed and dropped)
+                        tma_load_3d(dst, &tm_down, 0, row0, s, &S.full[slot], pol);
+                    } else if (A.gu_fused) {
+                        // 8 row groups x {8 rows of the lower matrix, 8 rows of the other}
+                        tma_load_5d(dst, &tm_gu, 0, 0, 0, row0 / 8, s, &S.full[slot], pol);
+                    } else {
+#pragma unroll 1
+                        for (int g = 0; g < 8; ++g) {
+                            tma_load_3d(dst + (2 * g) * 1024, &tm_gate, 0, row0 + 8 * g, s, &S.full[slot], pol);
+                            tma_load_3d(dst + (2 * g + 1) * 1024, &tm_up, 0, row0 + 8 * g, s, &S.full[slot], pol);
+                        }
+                    }
+                }
+            }
+            // Every issued stage is consumed before the MMA warp finishes,
+            // so no copy is in flight when the CTA exits.
+        }
+        __syncwarp();
+    } else if (warp == kWarpO) {
+        // ---------------------------- operand producer ---------------------------
+        const uint64_t pol = l2_evict_last_policy();
+        uint32_t it = 0;
+        bool gathered = small_b;
+        for (int n = 0;; ++n) {
+            const int q = n % kQ;
+            wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
+            const int tile = S.tq[q];
+            if (tile < 0) break;
+            const bool ph_a = tile < TA;
+            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn);
+            if (ph_a && !gathered) {   // every CTA has copied its rows of the grouped hidden states
+                for (int c = lane; c < (int)G; c += 32) wait_counter(&A.gflag[c], 1u, S, flags);
+                __syncwarp();
+                fence_proxy_async_global();
+                gathered = true;
+            }
+            if (lane == 0) {
+                if (!ph_a) {   // every phase-A tile of this token chunk has written its h rows
+                    wait_counter(&A.hdone[S.chunk_off[T.a] + T.c], (uint32_t)rbA, S, flags);
+                    fence_proxy_async_global();
+                }
+                const CUtensorMap* map = ph_a ? (small_b ? &tm_hid : &tm_x) : &tm_h;
+                const int row = (ph_a && small_b) ? 0 : T.off + kN * T.c;
+                const int ns = ph_a ? SA : SB;
+                for (int s = 0; s < ns; ++s, ++it) {
+                    const int slot = it % kStages;
+                    if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
+                    mbar_arrive_expect_tx(&S.full[slot], kOBytes);   // rows past the end read as zeros
+                    tma_load_3d(ring + (size_t)slot * kSlotBytes + kWBytes, map, 0, row, s, &S.full[slot], pol);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == kWarpM) {
+        // ------------------------------ MMA issuer -------------------------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int n = 0;; ++n) {
+                const int q = n % kQ;
+                wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
+                const int tile = S.tq[q];
+                if (tile < 0) break;
+                const int ns = tile < TA ? SA : SB;
+                const int b = n % kAcc;
+                if (n >= kAcc) {   // the epilogue has read this accumulator's previous tile
+                    wait_bar(&S.acc_empty[b], ((n / kAcc) - 1) & 1, S, flags);
+                    tmem_fence_after_sync();
+                }
+                const uint32_t dt = tmem + (uint32_t)(b * kN);
+                for (int s = 0; s < ns; ++s, ++it) {
+                    const int slot = it % kStages;
+                    wait_bar(&S.full[slot], (it / kStages) & 1, S, flags);
+                    tmem_fence_after_sync();
+                    const uint32_t a0 = smem_u32(ring + (size_t)slot * kSlotBytes);
+                    const uint32_t b0 = a0 + kWBytes;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)   // K = 16 per step: 32 bytes along the swizzled row
+                        umma_bf16(dt, umma_sdesc_sw128(a0 + 32 * k), umma_sdesc_sw128(b0 + 32 * k), kIdesc,
+                                  (s | k) ? 1u : 0u);
+                    umma_commit(&S.empty[slot]);   // the stage is free once these MMAs are done
+                }
+                umma_commit(&S.acc_full[b]);
+            }
+            umma_commit(&S.mma_done);
+            wait_bar(&S.mma_done, 0, S, flags);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------- epilogue --------------------------------
+        const int tid = threadIdx.x;   // 0..127
+
+        // Prologue (batches over 16 tokens): this CTA's rows of the
+        // expert-grouped hidden states (rows b, b+G, ...), eight 16-byte
+        // loads in flight per thread.
+        if (!small_b) {
+            const int P = A.offsets[A.N];
+            const int vpr = d / 8;   // 16-byte vectors per row
+            const int nrow = P > (int)blockIdx.x ? (P - 1 - (int)blockIdx.x) / (int)G + 1 : 0;
+            const int nvec = nrow * vpr;
+            const uint4* xs = static_cast<const uint4*>(A.x);
+            uint4* xp = static_cast<uint4*>(A.xperm);
+            for (int v0 = 0; v0 < nvec; v0 += 8 * kEpiWarps * 32) {
+                uint4 val[8];
+                size_t dst[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int v = v0 + u * kEpiWarps * 32 + tid;
+                    dst[u] = ~size_t(0);
+                    if (v < nvec) {
+                        const int r = v / vpr, c = v - r * vpr;
+                        const int pr = (int)blockIdx.x + r * (int)G;
+                        val[u] = __ldg(xs + (size_t)(A.perm[pr] / A.kslots) * vpr + c);
+                        dst[u] = (size_t)pr * vpr + c;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (dst[u] != ~size_t(0)) xp[dst[u]] = val[u];
+            }
+            named_barrier(kBarEpi, kEpiWarps * 32);
+            if (tid == 0) {
+                __threadfence();
+                atomicExch(&A.gflag[blockIdx.x], 1u);
+            }
+        }
+
+        __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
+        const int i = 32 * warp + lane;                    // this thread's D row (tensor-memory lane)
+        const uint32_t lane_addr = (uint32_t)(32 * warp) << 16;
+        uint32_t na = 0;   // phase-A tiles so far (parity of h_written)
+        for (int n = 0;; ++n) {
+            const int q = n % kQ;
+            wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
+            const int tile = S.tq[q];
+            if (tile < 0) break;
+            const bool ph_a = tile < TA;
+            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn);
+            const int b = n % kAcc;
+            wait_bar(&S.acc_full[b], (n / kAcc) & 1, S, flags);
+            tmem_fence_after_sync();
+            float v[16];
+            tmem_ld16(tmem + lane_addr + (uint32_t)(b * kN), v);
+            tmem_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+            if (ph_a) {
+                // D row i = (2g + m) * 8 + r holds gate (m = 0) or up (m = 1) row
+                // 8g + r of the tile, or the reverse when the map starts at W_up;
+                // the partner row is 8 lanes away in the same warp.
+                const int m = (i >> 3) & 1;
+                const int frow = 64 * T.rb + 8 * (i >> 4) + (i & 7);
+                const uint32_t tmask = small_b ? S.tokmask[T.a] : 0u;
+#pragma unroll
+                for (int j = 0; j < kN; ++j) {
+                    const float other = __shfl_down_sync(0xffffffffu, v[j], 8);
+                    const float gs = A.gu_swap ? other : v[j];
+                    const float us = A.gu_swap ? v[j] : other;
+                    // column j: batch token j (small batches) or the chunk's j-th pair
+                    const bool keep = small_b ? ((tmask >> j) & 1u) != 0 : j < T.ntok;
+                    if (m == 0 && keep) {
+                        const size_t pos = small_b ? (size_t)T.off + __popc(tmask & ((1u << j) - 1u))
+                                                   : (size_t)T.off + kN * T.c + j;
+                        hb[pos * F + frow] = __float2bfloat16_rn(silu_f(gs) * us);
+                    }
+                }
+                // All four warps wait for the barrier's phase, so no warp can
+                // arrive for the next phase-A tile before this one completes.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.h_written);
+                wait_bar(&S.h_written, na & 1, S, flags);
+                if (tid == 0) {   // all four warps have stored: release the chunk's counter
+                    __threadfence();
+                    atomicAdd(&A.hdone[S.chunk_off[T.a] + T.c], 1u);
+                }
+                ++na;
+            } else {
+                const int row = kM * T.rb + i;
+                if (row < d) {
+#pragma unroll
+                    for (int j = 0; j < kN; ++j)
+                        if (j < T.ntok) A.ybuf[((size_t)T.off + kN * T.c + j) * d + row] = v[j];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.tq_empty[q]);
+        }
+    }
+
+    // ---- every CTA arrives after its last tile; then the combine ----
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(&A.hdr->b_done, 1u);
+        wait_counter(&A.hdr->b_done, G, S, flags);
+        __threadfence();
+    }
+    __syncthreads();
+    {
+        const int d4 = d / 4;
+        const long long total = (long long)A.B * d4;
+        const long long o0 = total * blockIdx.x / G, o1 = total * (blockIdx.x + 1) / G;
+        const float4* y4 = reinterpret_cast<const float4*>(A.ybuf);
+        uint2* out = static_cast<uint2*>(A.out);
+        for (long long o = o0 + threadIdx.x; o < o1; o += kThreads) {
+            const int i = (int)(o / d4), c4 = (int)(o - (long long)i * d4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < A.kslots; s0 += 8) {
+                float4 yv[8];
+                float wv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int sl = s0 + u;
+                    const int pos = sl < A.kslots ? A.pos_of[i * A.kslots + sl] : -1;
+                    wv[u] = pos >= 0 ? A.w[i * A.kslots + sl] : 0.f;
+                    yv[u] = pos >= 0 ? __ldcg(y4 + (size_t)pos * d4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {   // slot order
+                    acc.x += wv[u] * yv[u].x;
+                    acc.y += wv[u] * yv[u].y;
+                    acc.z += wv[u] * yv[u].z;
+                    acc.w += wv[u] * yv[u].w;
+                }
+            }
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+            out[o] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+        }
+    }
+
+    // ---- release the tensor memory; the last CTA resets the counters ----
+    tmem_fence_before_sync();
+    __syncthreads();
+    if (warp == kWarpM) {
+        tmem_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t old = atomicAdd(&A.hdr->ctas_done, 1u);
+        S.last_flag = (old + 1 == G);
+    }
+    __syncthreads();
+    if (S.last_flag) {
+        __threadfence();
+        for (int k = threadIdx.x; k < (int)G; k += kThreads) A.gflag[k] = 0;
+        for (int k = threadIdx.x; k < S.chunk_off[Tn]; k += kThreads) A.hdone[k] = 0;
+    }
+    if (S.last_flag && threadIdx.x == 0) {
+        A.hdr->next_tile = 0;
+        A.hdr->b_done = 0;
+        A.hdr->ctas_done = 0;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(ffn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    // One CTA per SM (the shared-memory size allows no second one, so the
+    // tensor memory is never contended); programmatic dependent launch lets
+    // the CTAs allocate and prefetch while the routing kernel finishes.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ffn_tc_kernel, a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                              maps[6]);
+}
+
+}  // namespace moe

@@ -116,6 +116,37 @@ def test_padding_tokens(mode):
     assert g2["T"] == g["T"]
 
 
+@pytest.mark.parametrize("layout", ["up_above_gate", "up_below_gate", "gate_is_up"])
+@pytest.mark.parametrize("B", [16, 37])
+def test_gate_up_layouts(layout, B):
+    """W_gate and W_up are read through one tensor map spanning both arrays
+    when possible (lower address first), through two maps otherwise; every
+    arrangement gives the oracle's result."""
+    w = W("t_gu", N=32, d=256, F=192, seed=17)
+    L = synth.make_layer(w, 0, B)
+    if layout == "gate_is_up":
+        L["w_up"] = L["w_gate"]
+    D = gu.device_inputs(L, w.bf16)
+    both = torch.empty((2,) + tuple(D["w_gate"].shape), dtype=D["w_gate"].dtype, device=gu.DEV)
+    if layout == "up_above_gate":
+        both[0], both[1] = D["w_gate"], D["w_up"]
+        D["w_gate"], D["w_up"] = both[0], both[1]
+    elif layout == "up_below_gate":
+        both[0], both[1] = D["w_up"], D["w_gate"]
+        D["w_gate"], D["w_up"] = both[1], both[0]
+    else:
+        D["w_up"] = D["w_gate"]
+    for mode, k0 in ((TOPK, 8), (OEA, 3)):
+        prm = gu.params_for(w, B, mode, k0, 1.0)
+        r, out, ws, flags = gu.run_layer(w, D, prm)
+        assert flags == 0, f"device flags {flags:#x}"
+        g = gu.to_np(r)
+        gu.check_routing(g, prm, B)
+        o = oracle.moe_experts(L["x"], L["w_gate"], L["w_up"], L["w_down"], g["expert_idx"],
+                               g["weights"].astype(np.float64))
+        gu.check_output(out, o, w.bf16)
+
+
 def test_hot_experts_many_tokens_per_expert():
     """Experts with more tokens than one 32-token pass (chunked tiles)."""
     w = W("t_hot", N=64, d=256, F=192, seed=3)
