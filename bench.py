@@ -91,26 +91,33 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
+def expert_kernel(w: synth.Workload) -> tuple:
+    """(kernel name, source file) of the expert kernel that runs the workload:
+    the tcgen05 kernel for bf16 experts, the warp-MMA kernel for the mixed
+    bf16/INT4 experts."""
+    return ("ffn_bf16_kernel", "ffn_bf16.cu") if w.int4_cold else ("ffn_tc_kernel", "ffn_tc.cu")
+
+
+def kernel_source_hash(source: str = "ffn_tc.cu") -> str:
     h = hashlib.sha256()
-    for f in ("ffn_bf16.cu", "common.cuh"):
+    for f in (source, "common.cuh"):
         with open(os.path.join(ROOT, "aware_expert_routing_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, run: str, algo_bytes_per_launch: float):
+def recorded_traffic(workload: str, run: str, algo_bytes_per_launch: float, source: str = "ffn_tc.cu"):
     """DRAM bytes per launch of the expert kernel from a committed ncu
     capture of the same workload and run, scaled from the captured launch's
     algorithmic bytes to this run's mean (traffic grows in proportion to the
     experts streamed); None if the capture predates the kernel source."""
-    p = os.path.join(ROOT, "profiles", "ffn_bf16_traffic.json")
+    p = os.path.join(ROOT, "profiles", "expert_kernel_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(f"{workload}/{run}")
-    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+    if not e or e.get("kernel_source_hash") != kernel_source_hash(source):
         return None
     return round(e["dram_bytes"] * algo_bytes_per_launch / e["algorithmic_bytes"])
 
@@ -560,8 +567,8 @@ def main_ours(args):
     ach = hr["ffn_gbs"]
     roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(ach / peaks["hbm_gbs"], 4),
-            "traffic": recorded_traffic(w.name, head[0], hr["ffn_bytes_per_launch"]),
-            "kernel": "ffn_bf16_kernel", "peak_source": peaks["source"],
+            "traffic": recorded_traffic(w.name, head[0], hr["ffn_bytes_per_launch"], expert_kernel(w)[1]),
+            "kernel": expert_kernel(w)[0], "peak_source": peaks["source"],
             "algorithmic_bytes_per_launch": round(hr["ffn_bytes_per_launch"]),
             "mean_launch_us": round(hr["ffn_us_mean"], 2)}
     base = None
