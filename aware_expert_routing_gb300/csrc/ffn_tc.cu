@@ -14,8 +14,11 @@
 //     token chunk c): the 64 W_gate rows and the 64 W_up rows of the same
 //     d_ff indices, interleaved 8 rows at a time (rows 16g..16g+7 = gate
 //     rows 8g..8g+7, rows 16g+8..16g+15 = the up rows), form the 128-row A
-//     operand of a tcgen05 MMA with M = 128; the chunk's 16 token rows are
-//     the N = 16 operand; K = d.  Phase-B tile (expert a, 128 rows of d,
+//     operand of a tcgen05 MMA with M = 128; the chunk's token rows are the
+//     N operand (N = the chunk's tokens rounded up to 16; a chunk holds the
+//     whole batch of up to 16 tokens, else up to nmax = the largest expert's
+//     token count rounded up to 16, at most 128, so most experts' weights
+//     are streamed once); K = d.  Phase-B tile (expert a, 128 rows of d,
 //     chunk c): W_down rows times the chunk's h rows, K = d_ff.  The list
 //     holds every phase-A tile, then every phase-B tile, each in active-
 //     expert order; CTA b starts with tile b and claims each next tile (two
@@ -25,13 +28,15 @@
 //     and streams the weights: one TMA operation per 16 KB stage (128 rows x
 //     64 columns, 128-byte swizzle; the gate/up interleave comes from one 5D
 //     tensor map over both matrices).  Warp 5 streams the 16 token rows of
-//     each stage (2 KB): the whole batch of up to 16 tokens straight from
-//     the hidden states, or rows of the expert-grouped copy of the hidden
-//     states, or (phase B) rows of h once every phase-A tile of the chunk
-//     has written them (a per-chunk counter).  Ring: 10 stages of 18 KB.
+//     each stage (16-row boxes): the whole batch of up to 16 tokens straight
+//     from the hidden states, or rows of the expert-grouped copy of the
+//     hidden states, or (phase B) rows of h once every phase-A tile of the
+//     chunk has written them (a per-chunk counter).  Ring: 180 KB of stages
+//     of 16 KB + nmax x 128 bytes (10 stages at nmax = 16, 5 at 128).
 //   * Warp 6, lane 0, issues the MMAs: four K=16 steps per stage straight
 //     from the swizzled shared memory (no register staging), fp32
-//     accumulators in tensor memory, four 16-column accumulator buffers.
+//     accumulators in tensor memory, four accumulator buffers (16 columns
+//     each for batches of up to 16 tokens, else 128).
 //     tcgen05.commit frees each stage when its MMAs have completed and marks
 //     a tile's accumulator full.
 //   * Warps 0-3 (tensor-memory lanes 32w..32w+31, one D row per thread)
@@ -60,22 +65,21 @@ constexpr int kWarpO = 5;                // operand producer
 constexpr int kWarpM = 6;                // MMA issuer, owner of the tensor memory
 constexpr int kThreads = 7 * 32;
 constexpr int kM = 128;                  // weight rows per tile (MMA M)
-constexpr int kN = 16;                   // token columns per tile (MMA N)
+constexpr int kNMax = 128;               // most token columns per tile (MMA N)
 constexpr int kWBytes = kM * 128;        // 128 rows x 64 bf16
-constexpr int kOBytes = kN * 128;        // 16 token rows x 64 bf16
-constexpr int kSlotBytes = kWBytes + kOBytes;
-constexpr int kStages = 10;
+constexpr int kRingBytes = 10 * (kWBytes + 16 * 128);   // 10 stages with 16 token rows
+constexpr int kMaxStages = 10;
 constexpr int kQ = 16;                   // tile queue entries
 constexpr int kAcc = 4;                  // accumulator buffers
-constexpr uint32_t kTmemCols = 64;       // kAcc x kN fp32 columns
+constexpr uint32_t kTmemCols = kAcc * kNMax;   // fp32 columns (batches over 16 tokens)
+constexpr uint32_t kTmemColsSmall = kAcc * 16;  // batches of up to 16 tokens
 constexpr uint32_t kBarEpi = 1;          // named barrier of the four epilogue warps
 constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
-constexpr uint32_t kIdesc = umma_idesc_bf16(kM, kN);
-static_assert(kSlotBytes % 1024 == 0, "stages must stay 1024-byte aligned for the 128-byte swizzle");
+static_assert(kTmemCols <= 512, "tensor memory has 512 columns");
 
 struct Smem {
-    uint64_t full[kStages];              // both producers (+ transaction bytes)
-    uint64_t empty[kStages];             // tcgen05.commit after the stage's MMAs
+    uint64_t full[kMaxStages];           // both producers (+ transaction bytes)
+    uint64_t empty[kMaxStages];          // tcgen05.commit after the stage's MMAs
     uint64_t acc_full[kAcc];             // tcgen05.commit after a tile's last MMA
     uint64_t acc_empty[kAcc];            // the four epilogue warps
     uint64_t tq_full[kQ];                // tile queue entry posted by the weight warp
@@ -87,11 +91,12 @@ struct Smem {
     uint32_t ex_info[MOE_MAX_EXPERTS];   // active index -> id | cnt << 10 | first pair << 19
     uint16_t tokmask[MOE_MAX_EXPERTS];   // active index -> tokens routed to it (batches of <= 16)
     uint32_t tmem_base;
+    int nmax;                            // tokens per chunk for this launch (multiple of 16)
     int abort_flag;
     int last_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kSlotBytes + sizeof(Smem);
+constexpr size_t kSmemBytes = 1024 + (size_t)kRingBytes + sizeof(Smem);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Tile {
@@ -99,7 +104,7 @@ struct Tile {
 };
 
 // Tile t of a phase with rbn row blocks per (expert, chunk); shared memory only.
-__device__ __forceinline__ Tile decode_tile(int t, int rbn, const Smem& S, int Tn) {
+__device__ __forceinline__ Tile decode_tile(int t, int rbn, const Smem& S, int Tn, int nmax) {
     int lo = 0, hi = Tn - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -115,7 +120,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int rbn, const Smem& S, int T
     const int r = t - S.chunk_off[lo] * rbn;
     T.rb = r / T.nch;
     T.c = r - T.rb * T.nch;
-    T.ntok = min(kN, cnt - kN * T.c);
+    T.ntok = min(nmax, cnt - nmax * T.c);
     return T;
 }
 
@@ -154,6 +159,22 @@ __device__ __forceinline__ void wait_counter(const uint32_t* p, uint32_t need, S
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
+// Position in the stage ring (the stage count is set per launch): slot,
+// phase parity, and whether the ring has wrapped once (a producer then
+// waits for the slot to be freed).
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0;
+    bool wrapped = false;
+    __device__ __forceinline__ void next(int nst) {
+        if (++slot == nst) {
+            slot = 0;
+            phase ^= 1u;
+            wrapped = true;
+        }
+    }
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
 ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const __grid_constant__ CUtensorMap tm_gate,
               const __grid_constant__ CUtensorMap tm_up, const __grid_constant__ CUtensorMap tm_down,
@@ -162,7 +183,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Smem& S = *reinterpret_cast<Smem*>(ring + (size_t)kStages * kSlotBytes);
+    Smem& S = *reinterpret_cast<Smem*>(ring + (size_t)kRingBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = A.d, F = A.F;
@@ -170,7 +191,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     const uint32_t G = gridDim.x;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&S.full[i], 2);          // weight producer + operand producer
             mbar_init(&S.empty[i], 1);         // tcgen05.commit
         }
@@ -187,25 +208,36 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         fence_barrier_init();
         S.abort_flag = 0;
     }
-    if (warp == kWarpM) tmem_alloc(&S.tmem_base, kTmemCols);
+    // accumulator buffers: kAcc x nmax columns, nmax = 16 for batches of up to 16
+    const uint32_t tmem_cols = A.B <= 16 ? kTmemColsSmall : kTmemCols;
+    const int acc_stride = A.B <= 16 ? 16 : kNMax;
+    if (warp == kWarpM) tmem_alloc(&S.tmem_base, tmem_cols);
     grid_dependency_wait();      // routing comes from the preceding kernel
     int Tn = *A.T;
     if (Tn < 0 || Tn > A.N) {
         if (threadIdx.x == 0 && blockIdx.x == 0) raise_flag(flags, kFlagBadIndex);
         Tn = 0;
     }
-    if (warp == 0) {   // per-expert records and chunk offsets of the active experts
+    if (warp == 0) {   // per-expert records, chunk width and chunk offsets of the active experts
+        int maxcnt = 0;
+        for (int a = lane; a < Tn; a += 32) {
+            const uint32_t info = A.exinfo[a];   // written by the routing kernel
+            S.ex_info[a] = info;
+            S.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
+            maxcnt = max(maxcnt, (int)((info >> 10) & 511u));
+        }
+        maxcnt = __reduce_max_sync(0xffffffffu, maxcnt);
+        // a chunk holds up to nmax tokens: the whole batch for batches of up to
+        // 16, else the largest expert's tokens rounded up to 16, at most 128
+        const int nmax = A.B <= 16 ? 16 : min(kNMax, max(16, (maxcnt + 15) & ~15));
+        if (lane == 0) S.nmax = nmax;
+        __syncwarp();
         int run = 0;
         if (lane == 0) S.chunk_off[0] = 0;
         for (int a0 = 0; a0 < Tn; a0 += 32) {
             const int a = a0 + lane;
             int nch = 0;
-            if (a < Tn) {
-                const uint32_t info = A.exinfo[a];   // written by the routing kernel
-                S.ex_info[a] = info;
-                S.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
-                nch = ((int)((info >> 10) & 511u) + kN - 1) / kN;
-            }
+            if (a < Tn) nch = ((int)((S.ex_info[a] >> 10) & 511u) + nmax - 1) / nmax;
             int inc = nch;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -237,14 +269,17 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     const int SA = d / 64, SB = F / 64;             // stages per tile (K blocks of 64)
     const int TA = S.chunk_off[Tn] * rbA;
     const int Ttot = TA + S.chunk_off[Tn] * rbB;
-    const bool small_b = A.B <= kN;                 // phase-A operand: the whole batch
+    const bool small_b = A.B <= 16;                 // phase-A operand: the whole batch
+    const int nmax = S.nmax;
+    const int slot_bytes = kWBytes + nmax * 128;    // 16 KB of weights + nmax token rows
+    const int nst = min(kMaxStages, kRingBytes / slot_bytes);
 
     if (warp == kWarpW) {
         // ---------------------------- weight producer ----------------------------
         if (lane == 0) {
             const uint64_t pol_once = l2_evict_first_policy();
             const uint64_t pol_keep = l2_evict_normal_policy();
-            uint32_t it = 0;
+            RingPos rp;
             // claims run two tiles ahead so that the atomic's latency is hidden
             int next0 = (int)blockIdx.x;
             int next1 = next0 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
@@ -258,14 +293,14 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 next0 = next1;
                 next1 = next1 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
                 const bool ph_a = tile < TA;
-                const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn);
+                const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn, nmax);
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;   // chunked experts are re-read from L2
                 const int row0 = ph_a ? T.e * F + 64 * T.rb : T.e * d + kM * T.rb;
                 const int ns = ph_a ? SA : SB;
-                for (int s = 0; s < ns; ++s, ++it) {
-                    const int slot = it % kStages;
-                    if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    unsigned char* dst = ring + (size_t)slot * kSlotBytes;
+                for (int s = 0; s < ns; ++s, rp.next(nst)) {
+                    const int slot = rp.slot;
+                    if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
+                    unsigned char* dst = ring + (size_t)slot * slot_bytes;
                     mbar_arrive_expect_tx(&S.full[slot], kWBytes);
                     if (!ph_a) {
                         // 128 W_down rows (rows past the expert's d are computed and dropped)
@@ -289,7 +324,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     } else if (warp == kWarpO) {
         // ---------------------------- operand producer ---------------------------
         const uint64_t pol = l2_evict_last_policy();
-        uint32_t it = 0;
+        RingPos rp;
         bool gathered = small_b;
         for (int n = 0;; ++n) {
             const int q = n % kQ;
@@ -297,7 +332,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const int tile = S.tq[q];
             if (tile < 0) break;
             const bool ph_a = tile < TA;
-            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn);
+            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn, nmax);
             if (ph_a && !gathered) {   // every CTA has copied its rows of the grouped hidden states
                 for (int c = lane; c < (int)G; c += 32) wait_counter(&A.gflag[c], 1u, S, flags);
                 __syncwarp();
@@ -310,13 +345,16 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     fence_proxy_async_global();
                 }
                 const CUtensorMap* map = ph_a ? (small_b ? &tm_hid : &tm_x) : &tm_h;
-                const int row = (ph_a && small_b) ? 0 : T.off + kN * T.c;
+                const int row = (ph_a && small_b) ? 0 : T.off + nmax * T.c;
+                const int nb = (ph_a && small_b) ? 1 : (T.ntok + 15) >> 4;   // 16-row boxes = MMA N / 16
                 const int ns = ph_a ? SA : SB;
-                for (int s = 0; s < ns; ++s, ++it) {
-                    const int slot = it % kStages;
-                    if (it >= kStages) wait_bar(&S.empty[slot], ((it / kStages) - 1) & 1, S, flags);
-                    mbar_arrive_expect_tx(&S.full[slot], kOBytes);   // rows past the end read as zeros
-                    tma_load_3d(ring + (size_t)slot * kSlotBytes + kWBytes, map, 0, row, s, &S.full[slot], pol);
+                for (int s = 0; s < ns; ++s, rp.next(nst)) {
+                    const int slot = rp.slot;
+                    if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
+                    mbar_arrive_expect_tx(&S.full[slot], nb * 2048);   // rows past the end read as zeros
+                    unsigned char* dst = ring + (size_t)slot * slot_bytes + kWBytes;
+                    for (int j = 0; j < nb; ++j)
+                        tma_load_3d(dst + j * 2048, map, 0, row + 16 * j, s, &S.full[slot], pol);
                 }
             }
             __syncwarp();
@@ -324,28 +362,35 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     } else if (warp == kWarpM) {
         // ------------------------------ MMA issuer -------------------------------
         if (lane == 0) {
-            uint32_t it = 0;
+            RingPos rp;
             for (int n = 0;; ++n) {
                 const int q = n % kQ;
                 wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
                 const int tile = S.tq[q];
                 if (tile < 0) break;
-                const int ns = tile < TA ? SA : SB;
+                const bool ph_a = tile < TA;
+                int ntile = 16;   // MMA N: batches of up to 16 always use 16 columns
+                if (!small_b) {
+                    const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn, nmax);
+                    ntile = (ph_a && small_b) ? 16 : (T.ntok + 15) & ~15;
+                }
+                const uint32_t idesc = umma_idesc_bf16(kM, ntile);
+                const int ns = ph_a ? SA : SB;
                 const int b = n % kAcc;
                 if (n >= kAcc) {   // the epilogue has read this accumulator's previous tile
                     wait_bar(&S.acc_empty[b], ((n / kAcc) - 1) & 1, S, flags);
                     tmem_fence_after_sync();
                 }
-                const uint32_t dt = tmem + (uint32_t)(b * kN);
-                for (int s = 0; s < ns; ++s, ++it) {
-                    const int slot = it % kStages;
-                    wait_bar(&S.full[slot], (it / kStages) & 1, S, flags);
+                const uint32_t dt = tmem + (uint32_t)(b * acc_stride);
+                for (int s = 0; s < ns; ++s, rp.next(nst)) {
+                    const int slot = rp.slot;
+                    wait_bar(&S.full[slot], rp.phase, S, flags);
                     tmem_fence_after_sync();
-                    const uint32_t a0 = smem_u32(ring + (size_t)slot * kSlotBytes);
+                    const uint32_t a0 = smem_u32(ring + (size_t)slot * slot_bytes);
                     const uint32_t b0 = a0 + kWBytes;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)   // K = 16 per step: 32 bytes along the swizzled row
-                        umma_bf16(dt, umma_sdesc_sw128(a0 + 32 * k), umma_sdesc_sw128(b0 + 32 * k), kIdesc,
+                        umma_bf16(dt, umma_sdesc_sw128(a0 + 32 * k), umma_sdesc_sw128(b0 + 32 * k), idesc,
                                   (s | k) ? 1u : 0u);
                     umma_commit(&S.empty[slot]);   // the stage is free once these MMAs are done
                 }
@@ -404,15 +449,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const int tile = S.tq[q];
             if (tile < 0) break;
             const bool ph_a = tile < TA;
-            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn);
+            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn, nmax);
             const int b = n % kAcc;
+            const int ngroups = (ph_a && small_b) ? 1 : (T.ntok + 15) >> 4;   // 16-column groups of D
             wait_bar(&S.acc_full[b], (n / kAcc) & 1, S, flags);
             tmem_fence_after_sync();
-            float v[16];
-            tmem_ld16(tmem + lane_addr + (uint32_t)(b * kN), v);
-            tmem_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&S.acc_empty[b]);
             if (ph_a) {
                 // D row i = (2g + m) * 8 + r holds gate (m = 0) or up (m = 1) row
                 // 8g + r of the tile, or the reverse when the map starts at W_up;
@@ -420,22 +461,32 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 const int m = (i >> 3) & 1;
                 const int frow = 64 * T.rb + 8 * (i >> 4) + (i & 7);
                 const uint32_t tmask = small_b ? S.tokmask[T.a] : 0u;
+                for (int cg = 0; cg < ngroups; ++cg) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_addr + (uint32_t)(b * acc_stride + 16 * cg), v);
+                    if (cg == ngroups - 1) {   // the accumulator is in registers: free it
+                        tmem_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+                    }
 #pragma unroll
-                for (int j = 0; j < kN; ++j) {
-                    const float other = __shfl_down_sync(0xffffffffu, v[j], 8);
-                    const float gs = A.gu_swap ? other : v[j];
-                    const float us = A.gu_swap ? v[j] : other;
-                    // column j: batch token j (small batches) or the chunk's j-th pair
-                    const bool keep = small_b ? ((tmask >> j) & 1u) != 0 : j < T.ntok;
-                    if (m == 0 && keep) {
-                        const size_t pos = small_b ? (size_t)T.off + __popc(tmask & ((1u << j) - 1u))
-                                                   : (size_t)T.off + kN * T.c + j;
-                        hb[pos * F + frow] = __float2bfloat16_rn(silu_f(gs) * us);
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = 16 * cg + jj;
+                        const float other = __shfl_down_sync(0xffffffffu, v[jj], 8);
+                        const float gs = A.gu_swap ? other : v[jj];
+                        const float us = A.gu_swap ? v[jj] : other;
+                        // column j: batch token j (small batches) or the chunk's j-th pair
+                        const bool keep = small_b ? ((tmask >> j) & 1u) != 0 : j < T.ntok;
+                        if (m == 0 && keep) {
+                            const size_t pos = small_b ? (size_t)T.off + __popc(tmask & ((1u << j) - 1u))
+                                                       : (size_t)T.off + nmax * T.c + j;
+                            hb[pos * F + frow] = __float2bfloat16_rn(silu_f(gs) * us);
+                        }
                     }
                 }
+                __syncwarp();
                 // All four warps wait for the barrier's phase, so no warp can
                 // arrive for the next phase-A tile before this one completes.
-                __syncwarp();
                 if (lane == 0) mbar_arrive(&S.h_written);
                 wait_bar(&S.h_written, na & 1, S, flags);
                 if (tid == 0) {   // all four warps have stored: release the chunk's counter
@@ -445,10 +496,21 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 ++na;
             } else {
                 const int row = kM * T.rb + i;
-                if (row < d) {
+                for (int cg = 0; cg < ngroups; ++cg) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_addr + (uint32_t)(b * acc_stride + 16 * cg), v);
+                    if (cg == ngroups - 1) {
+                        tmem_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+                    }
+                    if (row < d) {
 #pragma unroll
-                    for (int j = 0; j < kN; ++j)
-                        if (j < T.ntok) A.ybuf[((size_t)T.off + kN * T.c + j) * d + row] = v[j];
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int j = 16 * cg + jj;
+                            if (j < T.ntok) A.ybuf[((size_t)T.off + nmax * T.c + j) * d + row] = v[jj];
+                        }
+                    }
                 }
             }
             __syncwarp();
@@ -503,7 +565,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     __syncthreads();
     if (warp == kWarpM) {
         tmem_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, tmem_cols);
     }
     if (threadIdx.x == 0) {
         __threadfence();
