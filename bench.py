@@ -605,6 +605,8 @@ def main_ours(args):
     print(json.dumps(line), flush=True)
     if args.sweep_out:
         sweep(moe, torch, w, dev, stream, args)
+    if args.linearity_out:
+        linearity(moe, torch, w, dev, stream, args)
 
 
 def sweep(moe, torch, w, dev, stream, args):
@@ -624,6 +626,65 @@ def sweep(moe, torch, w, dev, stream, args):
         torch.cuda.empty_cache()
     with open(args.sweep_out, "w") as f:
         json.dump(rows, f, indent=1)
+
+
+def linear_fit(X: np.ndarray, y: np.ndarray) -> dict:
+    """Least squares y = X beta; coefficients and R^2."""
+    beta, *_ = np.linalg.lstsq(X, y, rcond=None)
+    pred = X @ beta
+    ss_res = float(np.sum((y - pred) ** 2))
+    ss_tot = float(np.sum((y - y.mean()) ** 2))
+    return {"coef": [float(b) for b in beta], "r2": 1.0 - ss_res / ss_tot if ss_tot > 0 else 1.0}
+
+
+def linearity(moe, torch, w, dev, stream, args):
+    """Latency against T (distinct activated experts) and sum(cnt_e) (token-
+    expert pairs), the OEA page's cost model (section 4: latency grows with
+    the number of activated experts).  T is forced by a router bias of +20 on
+    T experts drawn with a seeded generator (every token's top-k then lies
+    among them) with top-min(k, T) routing, so sum(cnt_e) = B min(k, T);
+    B in {1, 4, 16, 64} varies sum(cnt_e) independently of T.  Fits
+    us = a sum(cnt_e) + b T + c for the whole layer and the expert kernel;
+    b is the cost of one more activated expert, 3 d d_ff 2 / b its
+    streaming rate.  32 distinct layers rotate (1.2 GB of experts each at
+    the 30B shapes), so even T = 1 streams 300 MB per rotation, above the
+    126 MB L2."""
+    import dataclasses
+    global N_LAYERS
+    saved, N_LAYERS = N_LAYERS, 32
+    rows = []
+    steps = max(100, args.steps // 20)
+    for B in (1, 4, 16, 64):
+        base = build_layers(moe, torch, w, B, dev)
+        for Tt in (1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128):
+            if Tt > w.N:
+                continue
+            k = min(w.k, Tt)
+            wk = dataclasses.replace(w, k=k)
+            bias = np.zeros(w.N, np.float32)
+            bias[np.random.default_rng(1000 + Tt).choice(w.N, Tt, replace=False)] = 20.0
+            bias_d = torch.from_numpy(bias).to(dev)
+            layers = [dict(D, bias=bias_d) for D in base]
+            r = run_mode(moe, torch, wk, B, layers, ("topk", "topk", k, 1.0), steps, args.warmup, dev, stream,
+                         detail_steps=steps)
+            r.pop("objs")
+            rows.append({"B": B, "k": k, "T_forced": Tt, "T": r["T_mean"], "sum_cnt": B * k,
+                         "us_per_layer": r["us_per_layer"], "ffn_us": r["ffn_us_mean"]})
+            log(json.dumps(rows[-1]))
+        del base
+        torch.cuda.empty_cache()
+    N_LAYERS = saved
+    X = np.array([[r["sum_cnt"], r["T"], 1.0] for r in rows])
+    out = {"workload": w.name, "model": "us = a * sum_cnt + b * T + c", "layers_rotated": 32, "rows": rows}
+    for key, col in (("fit_layer", "us_per_layer"), ("fit_expert_kernel", "ffn_us")):
+        f = linear_fit(X, np.array([r[col] for r in rows]))
+        a, b, c = f["coef"]
+        out[key] = {"a_us_per_pair": a, "b_us_per_expert": b, "c_us": c, "r2": f["r2"],
+                    "expert_bytes": w.expert_bytes,
+                    "streaming_gbs_per_added_expert": w.expert_bytes / (b * 1e-6) / 1e9 if b > 0 else None}
+    with open(args.linearity_out, "w") as f:
+        json.dump(out, f, indent=1)
+    log(json.dumps({k: v for k, v in out.items() if k.startswith("fit")}))
 
 
 # ---------------------------------------------------------------------------
@@ -670,6 +731,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep-out", default="")
+    ap.add_argument("--linearity-out", default="", help="latency-vs-T sweep and fit, written to this file")
     ap.add_argument("--layers", type=int, default=8, help="distinct layers rotated through")
     ap.add_argument("--only-run", default="", help="time only this routing run (profiling)")
     args = ap.parse_args()

@@ -1,0 +1,22 @@
+"""The latency-vs-T fit of bench.py (CPU): exact data gives the planted
+coefficients and R^2 = 1; noise lowers R^2."""
+import os
+import sys
+
+import numpy as np
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def test_linear_fit_recovers_plane():
+    rng = np.random.default_rng(3)
+    sum_cnt = rng.integers(1, 512, 40).astype(float)
+    T = rng.integers(1, 128, 40).astype(float)
+    y = 0.05 * sum_cnt + 1.4 * T + 9.0
+    X = np.stack([sum_cnt, T, np.ones_like(T)], axis=1)
+    f = bench.linear_fit(X, y)
+    assert np.allclose(f["coef"], [0.05, 1.4, 9.0], rtol=1e-9, atol=1e-9)
+    assert abs(f["r2"] - 1.0) < 1e-12
+    g = bench.linear_fit(X, y + rng.normal(0, 5.0, 40))
+    assert 0.5 < g["r2"] < 1.0

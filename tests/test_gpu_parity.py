@@ -238,6 +238,10 @@ def full_size_layer(w: synth.Workload, layer: int, B: int):
     ("qwen3_30b_a3b_uniform_b16", 16, [(TOPK, 8, 1.0), (OEA, 3, 1.0), (OEA, 5, 1.0)]),
     ("qwen3_30b_a3b_zipf_sweep", 256, [(TOPK, 8, 1.0), (OEA, 5, 0.7)]),
     ("qwen3_235b_a22b_zipf_b64", 64, [(TOPK, 8, 1.0), (OEA, 5, 0.7)]),
+    # few activated experts: the expert kernel splits K across CTAs
+    ("qwen3_30b_a3b_zipf_sweep", 1, [(TOPK, 8, 1.0), (OEA, 5, 0.7)]),
+    ("qwen3_30b_a3b_zipf_sweep", 4, [(TOPK, 8, 1.0), (OEA, 5, 0.7)]),
+    ("qwen3_235b_a22b_zipf_b64", 16, [(OEA, 5, 0.7)]),
 ])
 def test_full_size_sampled(wname, B, runs):
     w = synth.WORKLOADS[wname]
