@@ -11,10 +11,6 @@
 
 #include "common.cuh"
 
-namespace moe {
-size_t ffn_bf16_smem_bytes();
-}
-
 using namespace moe;
 
 namespace {
@@ -131,15 +127,7 @@ struct MapKey {
     }
 };
 
-struct MapEntry {
-    MapKey key;
-    CUtensorMap maps[3];
-    bool used;
-};
-
 std::mutex g_map_mu;
-MapEntry g_maps[64];
-int g_map_next = 0;
 
 // A row-major bf16 matrix [rows][cols] (cols a multiple of 64) viewed as 3D
 // {64 columns, rows, cols/64 column blocks}: one box {64, box_rows, 4} moves
@@ -159,91 +147,6 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
-}
-
-moe_status expert_maps(const void* g, const void* u, const void* dn, int N, int F, int d, int dev,
-                       CUtensorMap* out) {
-    std::lock_guard<std::mutex> lk(g_map_mu);
-    MapKey key{g, u, dn, N, F, d, dev};
-    for (auto& e : g_maps)
-        if (e.used && e.key == key) {
-            memcpy(out, e.maps, sizeof e.maps);
-            return MOE_OK;
-        }
-    MapEntry& e = g_maps[g_map_next];
-    g_map_next = (g_map_next + 1) % 64;
-    e.key = key;
-    e.used = false;
-    if (!encode_3d(&e.maps[0], g, d, (uint64_t)N * F, 16) || !encode_3d(&e.maps[1], u, d, (uint64_t)N * F, 16) ||
-        !encode_3d(&e.maps[2], dn, F, (uint64_t)N * d, 32))
-        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    e.used = true;
-    memcpy(out, e.maps, sizeof e.maps);
-    return MOE_OK;
-}
-
-// Maps over the workspace buffers read by TMA: the expert-grouped hidden
-// states [pairs][d] and the SwiGLU rows h [pairs][d_ff] (boxes of 8 rows).
-struct WsMapEntry {
-    const void* ws;
-    int pairs, d, F, dev;
-    CUtensorMap maps[2];
-    bool used;
-};
-WsMapEntry g_ws_maps[16];
-int g_ws_next = 0;
-
-moe_status workspace_maps(unsigned char* ws, const WsLayout& L, int pairs, int d, int F, int dev,
-                          CUtensorMap* out) {
-    std::lock_guard<std::mutex> lk(g_map_mu);
-    for (auto& e : g_ws_maps)
-        if (e.used && e.ws == ws && e.pairs == pairs && e.d == d && e.F == F && e.dev == dev) {
-            memcpy(out, e.maps, sizeof e.maps);
-            return MOE_OK;
-        }
-    WsMapEntry& e = g_ws_maps[g_ws_next];
-    g_ws_next = (g_ws_next + 1) % 16;
-    e.used = false;
-    e.ws = ws;
-    e.pairs = pairs;
-    e.d = d;
-    e.F = F;
-    e.dev = dev;
-    if (!encode_3d(&e.maps[0], ws + L.xperm, d, pairs, 8) || !encode_3d(&e.maps[1], ws + L.hbuf, F, pairs, 8))
-        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (workspace)");
-    e.used = true;
-    memcpy(out, e.maps, sizeof e.maps);
-    return MOE_OK;
-}
-
-// Map over the hidden states [B][d] (8-row boxes), cached by pointer.
-struct HidMapEntry {
-    const void* hidden;
-    int B, d, dev;
-    CUtensorMap map;
-    bool used;
-};
-HidMapEntry g_hid_maps[32];
-int g_hid_next = 0;
-
-moe_status hidden_map(const void* hidden, int B, int d, int dev, CUtensorMap* out) {
-    std::lock_guard<std::mutex> lk(g_map_mu);
-    for (auto& e : g_hid_maps)
-        if (e.used && e.hidden == hidden && e.B == B && e.d == d && e.dev == dev) {
-            *out = e.map;
-            return MOE_OK;
-        }
-    HidMapEntry& e = g_hid_maps[g_hid_next];
-    g_hid_next = (g_hid_next + 1) % 32;
-    e.used = false;
-    e.hidden = hidden;
-    e.B = B;
-    e.d = d;
-    e.dev = dev;
-    if (!encode_3d(&e.map, hidden, d, B, 8)) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (hidden)");
-    e.used = true;
-    *out = e.map;
-    return MOE_OK;
 }
 
 // ---- tensor maps of the tcgen05 expert kernel (boxes one 64-column block wide)
@@ -385,8 +288,8 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     const int n_hot = mixed ? mixed->n_hot : P.N;
     if (mixed) {
         if (P.dtype != MOE_DTYPE_BF16) return fail(MOE_ERR_ARG, "mixed experts need bf16 activations");
-        if (P.d % 256 != 0 || d_ff % 256 != 0)
-            return fail(MOE_ERR_ARG, "mixed experts need d and d_ff multiples of 256");
+        if (P.d % 128 != 0 || d_ff % 128 != 0)
+            return fail(MOE_ERR_ARG, "mixed experts need d and d_ff multiples of 128");
         if (!mixed->slot || !aligned(mixed->slot, 4)) return fail(MOE_ERR_ARG, "mixed->slot is NULL or misaligned");
         if (mixed->n_hot < 1 || mixed->n_cold < 0) return fail(MOE_ERR_ARG, "need n_hot >= 1 and n_cold >= 0");
         const void* q[] = {mixed->q_gate, mixed->q_up, mixed->q_down};
@@ -449,11 +352,11 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     int sms = num_sms();
     if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
     if (sms > kMaxGrid) sms = kMaxGrid;
-    if (!mixed) {   // bf16 experts: the tcgen05 kernel
+    {   // the tcgen05 expert kernel (bf16 experts, and INT4 experts through its converter warps)
         CUtensorMap maps[7];
         bool fused = false, swap = false;
         CUtensorMap wm[4];
-        if ((st = tc_expert_maps(w_gate, w_up, w_down, P.N, d_ff, P.d, dev, wm, &fused, &swap)) != MOE_OK) return st;
+        if ((st = tc_expert_maps(w_gate, w_up, w_down, n_hot, d_ff, P.d, dev, wm, &fused, &swap)) != MOE_OK) return st;
         maps[0] = wm[0];                       // gate/up 5D, or W_gate
         maps[1] = wm[0];                       // W_gate (8-row boxes; read when not fused)
         maps[2] = wm[1];                       // W_up
@@ -465,13 +368,7 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
         if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
         return MOE_OK;
     }
-    CUtensorMap maps[6];
-    if ((st = expert_maps(w_gate, w_up, w_down, n_hot, d_ff, P.d, dev, maps)) != MOE_OK) return st;
-    if ((st = workspace_maps(ws, L, P.B * P.kslots, P.d, d_ff, dev, maps + 3)) != MOE_OK) return st;
-    if ((st = hidden_map(hidden, P.B, P.d, dev, maps + 5)) != MOE_OK) return st;
-    e = launch_ffn_bf16(a, maps, sms, s);
-    if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
-    return MOE_OK;
+
 }
 }  // namespace
 

@@ -105,7 +105,7 @@ struct FfnArgs {
     const void* w_gate;     // [N][F][d]   (fp32 path)
     const void* w_up;
     const void* w_down;     // [N][d][F]
-    const int32_t* slot;    // [N] or null: >= 0 bf16 row block, < 0: -1 - INT4 expert
+    const int32_t* slot;    // [N] or null: >= 0 bf16 expert, < 0: -1 - INT4 expert
     const uint8_t* q_gate;  // INT4 experts, packed (see moe.h)
     const uint8_t* q_up;
     const uint8_t* q_down;
@@ -118,10 +118,6 @@ struct FfnArgs {
 // Launchers (defined in the .cu files).
 cudaError_t launch_router(const RouterArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
-// maps (3D views {64 columns, rows, column blocks of 64}, 128-byte swizzle,
-// boxes of 4 column blocks): W_gate and W_up (16 rows), W_down (32 rows),
-// gathered hidden states, SwiGLU buffer h and the hidden states (8 rows).
-cudaError_t launch_ffn_bf16(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s);
 // tcgen05 expert kernel (bf16 weights).  maps: W_gate/W_up interleaved 8
 // rows at a time (5D, gu_fused) or W_gate and W_up alone (8-row boxes),
 // W_down (128-row boxes), gathered hidden states, h and the hidden states

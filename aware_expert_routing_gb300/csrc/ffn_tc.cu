@@ -9,7 +9,7 @@
 // Expert form (Qwen3): y = W_down (silu(W_gate x) * (W_up x)); combine:
 // out_i = sum_j w_ij y_{e_ij}(x_i) (kept scores, section 2 Q2).
 //
-// Structure (one persistent CTA per SM, 7 warps):
+// Structure (one persistent CTA per SM, 15 warps):
 //   * Work is a list of tiles.  Phase-A tile (expert a, 64 rows of d_ff,
 //     token chunk c): the 64 W_gate rows and the 64 W_up rows of the same
 //     d_ff indices, interleaved 8 rows at a time (rows 16g..16g+7 = gate
@@ -39,6 +39,12 @@
 //     each for batches of up to 16 tokens, else 128).
 //     tcgen05.commit frees each stage when its MMAs have completed and marks
 //     a tile's accumulator full.
+//   * INT4 experts (DynaExq page, section 3.2): warp 4 bulk-copies the
+//     packed chunks of a stage into a 4-slot raw ring; warps 7-14 decode
+//     them (exact integer codes, times the row's group scale, rounded once
+//     to bf16) into the stage's 128-byte-swizzled A operand, fence it for
+//     the tensor core's async proxy and arrive on the stage's barrier in
+//     place of warp 4.
 //   * Warps 0-3 (tensor-memory lanes 32w..32w+31, one D row per thread)
 //     read a finished accumulator with tcgen05.ld and free it; phase A:
 //     the lane holding gate row r takes the matching up row from the lane
@@ -63,12 +69,19 @@ constexpr int kEpiWarps = 4;             // warps 0-3: epilogue
 constexpr int kWarpW = 4;                // weight producer
 constexpr int kWarpO = 5;                // operand producer
 constexpr int kWarpM = 6;                // MMA issuer, owner of the tensor memory
-constexpr int kThreads = 7 * 32;
+constexpr int kWarpC = 7;                // warps 7-14: INT4 converters
+constexpr int kConvWarps = 8;
+constexpr int kThreads = (kWarpC + kConvWarps) * 32;
 constexpr int kM = 128;                  // weight rows per tile (MMA M)
 constexpr int kNMax = 128;               // most token columns per tile (MMA N)
 constexpr int kWBytes = kM * 128;        // 128 rows x 64 bf16
 constexpr int kRingBytes = 10 * (kWBytes + 16 * 128);   // 10 stages with 16 token rows
 constexpr int kMaxStages = 10;
+constexpr int kRaw = 4;                  // packed INT4 chunks in flight
+constexpr int kQ4A = 64 * 32 + 64 * 2;   // INT4 chunk of W_gate / W_up: 64 rows x 64 columns + scales
+constexpr int kQ4B = 128 * 32 + 128 * 2; // INT4 chunk of W_down: 128 rows x 64 columns + scales
+constexpr int kRawBytes = 2 * kQ4A;      // a phase-A stage needs a W_gate and a W_up chunk
+static_assert(kRawBytes == kQ4B, "one raw slot fits either stage");
 constexpr int kQ = 16;                   // tile queue entries
 constexpr int kAcc = 4;                  // accumulator buffers
 constexpr uint32_t kTmemCols = kAcc * kNMax;   // fp32 columns (batches over 16 tokens)
@@ -86,17 +99,22 @@ struct Smem {
     uint64_t tq_empty[kQ];               // entry released by the four epilogue warps
     uint64_t mma_done;                   // every MMA issued has completed
     uint64_t h_written;                  // the four epilogue warps stored a phase-A tile's h rows
+    uint64_t raw_full[kRaw];             // packed INT4 chunks landed (bulk copies)
+    uint64_t raw_empty[kRaw];            // the four converter warps have read them
+    uint64_t conv_bar;                   // the four converter warps meet (bounded wait)
+    uint32_t raw_info[kRaw];             // target ring slot | phase A << 8, or ~0u (no more chunks)
     int tq[kQ];                          // tile index, or -1 once the list is exhausted
     int chunk_off[MOE_MAX_EXPERTS + 1];
     uint32_t ex_info[MOE_MAX_EXPERTS];   // active index -> id | cnt << 10 | first pair << 19
     uint16_t tokmask[MOE_MAX_EXPERTS];   // active index -> tokens routed to it (batches of <= 16)
+    int ex_slot[MOE_MAX_EXPERTS];        // active index -> bf16 expert (>= 0) or -1 - INT4 expert
     uint32_t tmem_base;
     int nmax;                            // tokens per chunk for this launch (multiple of 16)
     int abort_flag;
     int last_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kRingBytes + sizeof(Smem);
+constexpr size_t kSmemBytes = 1024 + (size_t)kRingBytes + (size_t)kRaw * kRawBytes + sizeof(Smem);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct Tile {
@@ -159,6 +177,38 @@ __device__ __forceinline__ void wait_counter(const uint32_t* p, uint32_t need, S
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
+// Eight INT4 codes (one packed word, column 2p in the low and 2p+1 in the
+// high half of nibble pair p) -> eight bf16 weights q*s, columns in order.
+// (w >> 4p) & 0x000f000f | 0x43004300 is the bf16 pair (128 + c, 128 + c')
+// with c = q + 8; subtracting 136 leaves q exactly; the product with the
+// group scale is rounded once to bf16.
+__device__ __forceinline__ uint4 decode_q4_row8(uint32_t w, __nv_bfloat162 s2) {
+    const __nv_bfloat162 off = __floats2bfloat162_rn(136.f, 136.f);
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint32_t v;
+        asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(v) : "r"(w >> (4 * p)), "r"(0x000f000fu), "r"(0x43004300u));
+        const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v), off);
+        const __nv_bfloat162 x = __hmul2(q, s2);
+        o[p] = *reinterpret_cast<const uint32_t*>(&x);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The four converter warps meet; every warp calls this the same number of
+// times, and the wait is bounded.
+__device__ __forceinline__ void conv_sync(Smem& S, uint32_t& nsync, uint32_t* flags, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.conv_bar);
+    wait_bar(&S.conv_bar, nsync & 1, S, flags);
+    ++nsync;
+}
+
 // Position in the stage ring (the stage count is set per launch): slot,
 // phase parity, and whether the ring has wrapped once (a producer then
 // waits for the slot to be freed).
@@ -183,7 +233,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Smem& S = *reinterpret_cast<Smem*>(ring + (size_t)kRingBytes);
+    unsigned char* raw = ring + (size_t)kRingBytes;   // kRaw packed INT4 slots
+    Smem& S = *reinterpret_cast<Smem*>(raw + (size_t)kRaw * kRawBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = A.d, F = A.F;
@@ -205,6 +256,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         }
         mbar_init(&S.mma_done, 1);
         mbar_init(&S.h_written, kEpiWarps);
+        for (int i = 0; i < kRaw; ++i) {
+            mbar_init(&S.raw_full[i], 1);
+            mbar_init(&S.raw_empty[i], kConvWarps);
+        }
+        mbar_init(&S.conv_bar, kConvWarps);
         fence_barrier_init();
         S.abort_flag = 0;
     }
@@ -225,6 +281,13 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             S.ex_info[a] = info;
             S.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
             maxcnt = max(maxcnt, (int)((info >> 10) & 511u));
+            const int e = info & 1023u;
+            int sl = A.slot ? A.slot[e] : e;
+            if (sl >= A.n_hot || -1 - sl >= A.n_cold) {   // out of range: flag it, read expert 0
+                raise_flag(flags, kFlagBadIndex);
+                sl = A.n_hot > 0 ? 0 : -1;
+            }
+            S.ex_slot[a] = sl;
         }
         maxcnt = __reduce_max_sync(0xffffffffu, maxcnt);
         // a chunk holds up to nmax tokens: the whole batch for batches of up to
@@ -279,7 +342,9 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         if (lane == 0) {
             const uint64_t pol_once = l2_evict_first_policy();
             const uint64_t pol_keep = l2_evict_normal_policy();
-            RingPos rp;
+            RingPos rp, rq;   // stage ring, packed INT4 ring
+            const size_t q4_mat_a = (size_t)(F / 64) * (d / 64) * kQ4A;    // bytes of one INT4 W_gate / W_up
+            const size_t q4_mat_b = (size_t)(d / kM) * (F / 64) * kQ4B;    // bytes of one INT4 W_down
             // claims run two tiles ahead so that the atomic's latency is hidden
             int next0 = (int)blockIdx.x;
             int next1 = next0 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
@@ -295,12 +360,34 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 const bool ph_a = tile < TA;
                 const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn, nmax);
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;   // chunked experts are re-read from L2
-                const int row0 = ph_a ? T.e * F + 64 * T.rb : T.e * d + kM * T.rb;
+                const int sl = S.ex_slot[T.a];                          // bf16 expert, or -1 - INT4 expert
+                const int row0 = ph_a ? sl * F + 64 * T.rb : sl * d + kM * T.rb;
                 const int ns = ph_a ? SA : SB;
                 for (int s = 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
                     unsigned char* dst = ring + (size_t)slot * slot_bytes;
+                    if (sl < 0) {
+                        // INT4 expert: the packed chunk(s) go to a raw slot; the converter
+                        // warps write the bf16 stage and arrive on its barrier.
+                        const int r = rq.slot;
+                        if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
+                        S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u);
+                        unsigned char* rdst = raw + (size_t)r * kRawBytes;
+                        const int c = -1 - sl;
+                        if (ph_a) {
+                            const size_t off = (size_t)c * q4_mat_a + ((size_t)T.rb * (d / 64) + s) * kQ4A;
+                            mbar_arrive_expect_tx(&S.raw_full[r], 2 * kQ4A);
+                            bulk_load(rdst, A.q_gate + off, kQ4A, &S.raw_full[r], pol);
+                            bulk_load(rdst + kQ4A, A.q_up + off, kQ4A, &S.raw_full[r], pol);
+                        } else {
+                            const size_t off = (size_t)c * q4_mat_b + ((size_t)T.rb * (F / 64) + s) * kQ4B;
+                            mbar_arrive_expect_tx(&S.raw_full[r], kQ4B);
+                            bulk_load(rdst, A.q_down + off, kQ4B, &S.raw_full[r], pol);
+                        }
+                        rq.next(kRaw);
+                        continue;
+                    }
                     mbar_arrive_expect_tx(&S.full[slot], kWBytes);
                     if (!ph_a) {
                         // 128 W_down rows (rows past the expert's d are computed and dropped)
@@ -316,6 +403,12 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                         }
                     }
                 }
+            }
+            {   // no more INT4 chunks: the converter warps stop
+                const int r = rq.slot;
+                if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
+                S.raw_info[r] = ~0u;
+                mbar_arrive(&S.raw_full[r]);
             }
             // Every issued stage is consumed before the MMA warp finishes,
             // so no copy is in flight when the CTA exits.
@@ -400,6 +493,44 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             wait_bar(&S.mma_done, 0, S, flags);
         }
         __syncwarp();
+    } else if (warp >= kWarpC) {
+        // ----------------------------- INT4 converters ----------------------------
+        // Each packed stage becomes the 128 x 64 bf16 A operand of one ring
+        // stage, 128-byte swizzled like a TMA box: output row i, 16-byte unit u
+        // (8 columns) at i*128 + ((u ^ (i & 7)) << 4).  Phase A: row i =
+        // (2g + m)*8 + r is row 8g + r of W_gate (m = 0) or W_up (m = 1).
+        const int ct = threadIdx.x - kWarpC * 32;   // 0..kConvWarps*32-1
+        RingPos rq;
+        uint32_t nsync = 0;
+        for (;;) {
+            if (A.n_cold == 0) break;                  // no INT4 experts in this launch
+            const int r = rq.slot;
+            wait_bar(&S.raw_full[r], rq.phase, S, flags);
+            const uint32_t info = S.raw_info[r];
+            if (info == ~0u) break;
+            const int slot = (int)(info & 255u);
+            const bool ph_a = (info >> 8) & 1u;
+            const unsigned char* src = raw + (size_t)r * kRawBytes;
+            unsigned char* dstA = ring + (size_t)slot * slot_bytes;
+#pragma unroll
+            for (int it = 0; it < 1024 / (kConvWarps * 32); ++it) {   // 128 rows x 8 units
+                const int k = it * (kConvWarps * 32) + ct;
+                const int i = k >> 3, u = k & 7;
+                const unsigned char* ch = ph_a ? src + ((i >> 3) & 1) * kQ4A : src;
+                const int srow = ph_a ? 8 * (i >> 4) + (i & 7) : i;
+                const int rows = ph_a ? 64 : kM;
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(ch + srow * 32 + u * 4);
+                const __nv_bfloat16 sc = *reinterpret_cast<const __nv_bfloat16*>(ch + rows * 32 + srow * 2);
+                *reinterpret_cast<uint4*>(dstA + i * 128 + ((u ^ (i & 7)) << 4)) =
+                    decode_q4_row8(w, __bfloat162bfloat162(sc));
+            }
+            fence_proxy_async_shared();   // the tensor core reads the stage through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.raw_empty[r]);   // this warp has read the packed chunk
+            conv_sync(S, nsync, flags, lane);              // all four warps have written their rows
+            if (ct == 0) mbar_arrive(&S.full[slot]);       // in place of the weight warp
+            rq.next(kRaw);
+        }
     } else {
         // ------------------------------- epilogue --------------------------------
         const int tid = threadIdx.x;   // 0..127
@@ -461,6 +592,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 const int m = (i >> 3) & 1;
                 const int frow = 64 * T.rb + 8 * (i >> 4) + (i & 7);
                 const uint32_t tmask = small_b ? S.tokmask[T.a] : 0u;
+                const bool swap = A.gu_swap && S.ex_slot[T.a] >= 0;   // INT4 stages hold the gate rows first
                 for (int cg = 0; cg < ngroups; ++cg) {
                     float v[16];
                     tmem_ld16(tmem + lane_addr + (uint32_t)(b * acc_stride + 16 * cg), v);
@@ -473,8 +605,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     for (int jj = 0; jj < 16; ++jj) {
                         const int j = 16 * cg + jj;
                         const float other = __shfl_down_sync(0xffffffffu, v[jj], 8);
-                        const float gs = A.gu_swap ? other : v[jj];
-                        const float us = A.gu_swap ? v[jj] : other;
+                        const float gs = swap ? other : v[jj];
+                        const float us = swap ? v[jj] : other;
                         // column j: batch token j (small batches) or the chunk's j-th pair
                         const bool keep = small_b ? ((tmask >> j) & 1u) != 0 : j < T.ntok;
                         if (m == 0 && keep) {

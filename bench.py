@@ -92,10 +92,9 @@ def measured_peaks() -> dict:
 
 
 def expert_kernel(w: synth.Workload) -> tuple:
-    """(kernel name, source file) of the expert kernel that runs the workload:
-    the tcgen05 kernel for bf16 experts, the warp-MMA kernel for the mixed
-    bf16/INT4 experts."""
-    return ("ffn_bf16_kernel", "ffn_bf16.cu") if w.int4_cold else ("ffn_tc_kernel", "ffn_tc.cu")
+    """(kernel name, source file) of the expert kernel that runs the workload
+    (the tcgen05 kernel for bf16 and mixed bf16/INT4 experts)."""
+    return ("ffn_tc_kernel", "ffn_tc.cu")
 
 
 def kernel_source_hash(source: str = "ffn_tc.cu") -> str:

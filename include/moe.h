@@ -202,16 +202,17 @@ moe_status moe_expert_ffn(const void *hidden, const void *w_gate, const void *w_
  *           An out-of-range slot raises MOE_FLAG_BAD_INDEX.
  *   q_gate, q_up  [n_cold] packed images of the [d_ff][d] matrices,
  *   q_down        [n_cold] packed images of the [d][d_ff] matrices.
- * Packed image of a matrix [rows][cols] with chunk height rb (16 for W_gate
- * and W_up, 32 for W_down): chunks of rb rows x 256 columns in row-block-major,
- * column-stage order; a chunk is rb*128 bytes of codes then rb*2 bf16 scales
- * ([rb][2]: the chunk's two 128-column groups).  In a chunk row, local
- * column c is the 4-bit field at bit 4*((c%8)/2) + 16*(c%2) of little-endian
- * 32-bit word c/8 of the row's 128 bytes, holding q + 8.
- * Requirements: dtype bf16, d and d_ff multiples of 256, n_hot >= 1,
- * 16-byte aligned images.  Results as moe_expert_ffn; the INT4 products are
- * exact integers in fp32 and each row's partial sum over a 64-column block is
- * multiplied by its group scale.
+ * Packed image of a matrix [rows][cols] with chunk height rb (64 for W_gate
+ * and W_up, 128 for W_down): chunks of rb rows x 64 columns in row-block-
+ * major, column-block order; a chunk is rb*32 bytes of codes then rb bf16
+ * scales (one per row: the scale of the 128-column group holding the
+ * chunk's columns).  In a chunk row, local column c is the 4-bit field at
+ * bit 4*((c%8)/2) + 16*(c%2) of little-endian 32-bit word c/8 of the row's
+ * 32 bytes, holding q + 8.
+ * Requirements: dtype bf16, d and d_ff multiples of 128, n_hot >= 1,
+ * 16-byte aligned images.  Results as moe_expert_ffn; each INT4 weight is
+ * decoded to q exactly and multiplied by its group scale with one rounding
+ * to bf16 before the tensor-core products (fp32 accumulation).
  */
 typedef struct {
     const int32_t *slot;

@@ -36,7 +36,7 @@ def build_mixed(w, L, hot, active=None):
     for i, e in enumerate(cold):
         slot[e] = -1 - i
     eff = {k: L[k].copy() for k in ("w_gate", "w_up", "w_down")}
-    na, nd = F * d // 2 + F * (d // 128) * 2, d * F // 2 + d * (F // 128) * 2
+    na, nd = F * d // 2 + F * (d // 64) * 2, d * F // 2 + d * (F // 64) * 2   # codes + a scale per 64-column chunk
     qg = np.zeros((len(cold), na), np.uint8)
     qu = np.zeros((len(cold), na), np.uint8)
     qd = np.zeros((len(cold), nd), np.uint8)
@@ -45,9 +45,9 @@ def build_mixed(w, L, hot, active=None):
             continue
         (pg, pu, pd), _ = synth.pack_int4_expert(L["w_gate"][e], L["w_up"][e], L["w_down"][e])
         qg[i], qu[i], qd[i] = pg, pu, pd
-        eff["w_gate"][e] = oracle.dequant_int4(pg, F, d, 16)
-        eff["w_up"][e] = oracle.dequant_int4(pu, F, d, 16)
-        eff["w_down"][e] = oracle.dequant_int4(pd, d, F, 32)
+        eff["w_gate"][e] = oracle.dequant_int4(pg, F, d, synth.INT4_RB_GATE_UP)
+        eff["w_up"][e] = oracle.dequant_int4(pu, F, d, synth.INT4_RB_GATE_UP)
+        eff["w_down"][e] = oracle.dequant_int4(pd, d, F, synth.INT4_RB_DOWN)
     bf = torch.bfloat16
     dev = gu.DEV
     hot_w = {k: torch.from_numpy(L[k][hot]).to(dev).to(bf).contiguous() for k in ("w_gate", "w_up", "w_down")}
@@ -155,7 +155,7 @@ def test_full_size_mixed_sampled():
     idx0 = r0.expert_idx.cpu().numpy()
     sample = (0, 13, B - 1)
     used = {int(e) for i in sample for e in idx0[i] if e >= 0}
-    na, nd = F * d // 2 + F * (d // 128) * 2, d * F // 2 + d * (F // 128) * 2
+    na, nd = F * d // 2 + F * (d // 64) * 2, d * F // 2 + d * (F // 64) * 2   # codes + a scale per 64-column chunk
     qg = np.zeros((len(cold), na), np.uint8)
     qu = np.zeros((len(cold), na), np.uint8)
     qd = np.zeros((len(cold), nd), np.uint8)
@@ -168,8 +168,8 @@ def test_full_size_mixed_sampled():
             (pg, pu, pd), _ = synth.pack_int4_expert(g, u, dn)
             i = cold.index(e)
             qg[i], qu[i], qd[i] = pg, pu, pd
-            eff[e] = (oracle.dequant_int4(pg, F, d, 16), oracle.dequant_int4(pu, F, d, 16),
-                      oracle.dequant_int4(pd, d, F, 32))
+            eff[e] = (oracle.dequant_int4(pg, F, d, synth.INT4_RB_GATE_UP), oracle.dequant_int4(pu, F, d, synth.INT4_RB_GATE_UP),
+                      oracle.dequant_int4(pd, d, F, synth.INT4_RB_DOWN))
     mixed = moe.MixedExperts(torch.from_numpy(slot).to(dev), torch.from_numpy(qg).to(dev),
                              torch.from_numpy(qu).to(dev), torch.from_numpy(qd).to(dev), len(hot), len(cold))
     r, out = run_mixed(w, L, D, hot_w, mixed, prm)

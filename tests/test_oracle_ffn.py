@@ -97,33 +97,35 @@ def test_router_logits_match_library():
 
 def pack_by_definition(q, s, rb):
     """The packed format built byte by byte from its definition (a second,
-    independent construction)."""
+    independent construction): chunks of rb rows x 64 columns, codes then
+    one bf16 scale per row."""
     R, K = q.shape
     out = bytearray()
     for rbi in range(R // rb):
-        for ks in range(K // 256):
-            codes = bytearray(rb * 128)
+        for kb in range(K // 64):
+            codes = bytearray(rb * 32)
             for rr in range(rb):
                 r = rbi * rb + rr
-                for cl in range(256):
+                for cl in range(64):
                     o = cl % 8
                     bit = 4 * (o // 2) + 16 * (o % 2)
-                    word_off = rr * 128 + (cl // 8) * 4
-                    v = (int(q[r, ks * 256 + cl]) + 8) << bit
+                    word_off = rr * 32 + (cl // 8) * 4
+                    v = (int(q[r, kb * 64 + cl]) + 8) << bit
                     for byte in range(4):
                         codes[word_off + byte] |= (v >> (8 * byte)) & 0xFF
             scales = bytearray()
             for rr in range(rb):
-                for g in range(2):
-                    bits = int(synth.to_bf16_bits(np.array([s[rbi * rb + rr, ks * 2 + g]], np.float32))[0])
-                    scales += bytes([bits & 0xFF, bits >> 8])
+                group = (kb * 64) // 128
+                bits = int(synth.to_bf16_bits(np.array([s[rbi * rb + rr, group]], np.float32))[0])
+                scales += bytes([bits & 0xFF, bits >> 8])
             out += codes + scales
     return np.frombuffer(bytes(out), np.uint8)
 
 
 def test_dequant_int4_codes_and_layout():
-    """Every code -7..7 at every nibble position, two groups per chunk with
-    their own scales: w = q * s (DynaExq page, section 3.2, INT4 tier)."""
+    """Every code -7..7 at every nibble position, four 128-column groups per
+    row with their own scales, several row and column chunks: w = q * s
+    (DynaExq page, section 3.2, INT4 tier)."""
     rng = np.random.default_rng(6)
     rows, cols, rb = 32, 512, 16
     q = rng.integers(-7, 8, size=(rows, cols)).astype(np.int8)

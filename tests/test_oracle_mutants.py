@@ -35,7 +35,8 @@ MUTANTS = {
     "max_depth_ignored": ("const int depth = maxP < N ? maxP : N;", "const int depth = N;"),
     "int4_nibble_pairs_swapped": ("const int bit = 4 * (o / 2) + 16 * (o % 2);",
                                   "const int bit = 16 * (o / 2 % 2) + 4 * (o % 2) + 8 * (o / 4);"),
-    "int4_scale_group_ignored": ("((size_t)rr * 2 + cl / 128) * 2", "((size_t)rr * 2) * 2"),
+    "int4_scale_row_ignored": ("(size_t)rb * 32 + (size_t)rr * 2;", "(size_t)rb * 32;"),
+    "int4_chunk_order_swapped": ("((size_t)rbi * nkb + kb) * chunk", "((size_t)kb * (rows / rb) + rbi) * chunk"),
 }
 
 
