@@ -268,11 +268,40 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     const uint32_t tmem_cols = A.B <= 16 ? kTmemColsSmall : kTmemCols;
     const int acc_stride = A.B <= 16 ? 16 : kNMax;
     if (warp == kWarpM) tmem_alloc(&S.tmem_base, tmem_cols);
+    __syncthreads();             // barriers initialised (this overlaps the routing kernel)
     grid_dependency_wait();      // routing comes from the preceding kernel
     int Tn = *A.T;
     if (Tn < 0 || Tn > A.N) {
         if (threadIdx.x == 0 && blockIdx.x == 0) raise_flag(flags, kFlagBadIndex);
         Tn = 0;
+    }
+    // Batches of up to 16 tokens: the CTA's first tile is phase-A tile
+    // blockIdx.x of a one-chunk-per-expert list, so the weight warp starts
+    // its stages now, while warp 0 builds the per-expert records.
+    int fast_stages = 0;
+    if (warp == kWarpW && lane == 0 && A.B <= 16) {
+        const int rbA0 = F / 64, t0 = (int)blockIdx.x;
+        if (t0 < Tn * rbA0) {
+            const int e = (int)(A.exinfo[t0 / rbA0] & 1023u);
+            const int sl = A.slot ? A.slot[e] : e;
+            if (sl >= 0 && sl < A.n_hot) {
+                const uint64_t pol = l2_evict_first_policy();
+                const int row0 = sl * F + 64 * (t0 % rbA0);
+                fast_stages = min(d / 64, min(kMaxStages, kRingBytes / (kWBytes + 16 * 128)));
+                for (int s = 0; s < fast_stages; ++s) {
+                    unsigned char* dst = ring + (size_t)s * (kWBytes + 16 * 128);
+                    mbar_arrive_expect_tx(&S.full[s], kWBytes);
+                    if (A.gu_fused) {
+                        tma_load_5d(dst, &tm_gu, 0, 0, 0, row0 / 8, s, &S.full[s], pol);
+                    } else {
+                        for (int g = 0; g < 8; ++g) {
+                            tma_load_3d(dst + (2 * g) * 1024, &tm_gate, 0, row0 + 8 * g, s, &S.full[s], pol);
+                            tma_load_3d(dst + (2 * g + 1) * 1024, &tm_up, 0, row0 + 8 * g, s, &S.full[s], pol);
+                        }
+                    }
+                }
+            }
+        }
     }
     if (warp == 0) {   // per-expert records, chunk width and chunk offsets of the active experts
         int maxcnt = 0;
@@ -348,6 +377,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             // claims run two tiles ahead so that the atomic's latency is hidden
             int next0 = (int)blockIdx.x;
             int next1 = next0 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
+            for (int s = 0; s < fast_stages; ++s) rp.next(nst);   // stages issued before the prologue
             for (int n = 0;; ++n) {
                 const int q = n % kQ;
                 if (n >= kQ) wait_bar(&S.tq_empty[q], ((n / kQ) - 1) & 1, S, flags);
@@ -363,7 +393,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 const int sl = S.ex_slot[T.a];                          // bf16 expert, or -1 - INT4 expert
                 const int row0 = ph_a ? sl * F + 64 * T.rb : sl * d + kM * T.rb;
                 const int ns = ph_a ? SA : SB;
-                for (int s = 0; s < ns; ++s, rp.next(nst)) {
+                for (int s = n == 0 ? fast_stages : 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
                     unsigned char* dst = ring + (size_t)slot * slot_bytes;
@@ -651,6 +681,21 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     }
 
     // ---- every CTA arrives after its last tile; then the combine ----
+    // This thread's first output of the combine: its slots' pair positions
+    // and weights (routing results) are loaded before the grid barrier.
+    const int d4 = d / 4;
+    const long long ctotal = (long long)A.B * d4;
+    const long long co0 = ctotal * blockIdx.x / G, co1 = ctotal * (blockIdx.x + 1) / G;
+    int pf_pos[8];
+    float pf_w[8];
+    if (co0 + (long long)threadIdx.x < co1) {
+        const int i0 = (int)((co0 + threadIdx.x) / d4);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            pf_pos[u] = u < A.kslots ? A.pos_of[i0 * A.kslots + u] : -1;
+            pf_w[u] = pf_pos[u] >= 0 ? A.w[i0 * A.kslots + u] : 0.f;
+        }
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
@@ -660,12 +705,10 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     }
     __syncthreads();
     {
-        const int d4 = d / 4;
-        const long long total = (long long)A.B * d4;
-        const long long o0 = total * blockIdx.x / G, o1 = total * (blockIdx.x + 1) / G;
         const float4* y4 = reinterpret_cast<const float4*>(A.ybuf);
         uint2* out = static_cast<uint2*>(A.out);
-        for (long long o = o0 + threadIdx.x; o < o1; o += kThreads) {
+        bool first = true;
+        for (long long o = co0 + threadIdx.x; o < co1; o += kThreads, first = false) {
             const int i = (int)(o / d4), c4 = (int)(o - (long long)i * d4);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int s0 = 0; s0 < A.kslots; s0 += 8) {
@@ -674,8 +717,14 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int sl = s0 + u;
-                    const int pos = sl < A.kslots ? A.pos_of[i * A.kslots + sl] : -1;
-                    wv[u] = pos >= 0 ? A.w[i * A.kslots + sl] : 0.f;
+                    int pos;
+                    if (first && s0 == 0) {
+                        pos = pf_pos[u];
+                        wv[u] = pf_w[u];
+                    } else {
+                        pos = sl < A.kslots ? A.pos_of[i * A.kslots + sl] : -1;
+                        wv[u] = pos >= 0 ? A.w[i * A.kslots + sl] : 0.f;
+                    }
                     yv[u] = pos >= 0 ? __ldcg(y4 + (size_t)pos * d4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
