@@ -19,9 +19,9 @@
 // hold the maximum.  The batch union S_base is an N-bit mask in shared
 // memory built with __ballot_sync + atomicOr.  Grouping by expert: every
 // kept (token, expert) sets bit (token mod 32) of word [token / 32][expert];
-// one warp turns those words into per-expert counts, offsets and per-chunk
-// prefix counts, which give each pair's position directly (tokens ascending
-// within an expert).
+// the warps, 32 experts each, turn those words into per-expert counts,
+// offsets and per-chunk prefix counts, which give each pair's position
+// directly (tokens ascending within an expert).
 #include <limits.h>
 
 #include "common.cuh"
@@ -88,6 +88,7 @@ struct RouteSmem {
     uint32_t* bits;    // [chunks][N]   bit (i mod 32) set if token i keeps expert e
     int* pre;          // [chunks][N]   tokens of earlier chunks that keep e
     int* soff;         // [N]           first pair of expert e
+    uint32_t* btot;    // [32]          packed totals of 32-expert blocks
 };
 
 // Writes the routing of token i: lane r < cnt holds slot r (myid, myval).
@@ -119,6 +120,7 @@ __global__ void route_kernel(RouteArgs a) {
     RouteSmem sm;
     unsigned char* p = smem_raw;
     sm.sbase = reinterpret_cast<uint32_t*>(p); p += 32 * 4;
+    sm.btot = reinterpret_cast<uint32_t*>(p); p += 32 * 4;
     sm.snb = reinterpret_cast<int*>(p); p += MOE_MAX_TOKENS * 4;
     sm.soff = reinterpret_cast<int*>(p); p += MOE_MAX_EXPERTS * 4;
     sm.sidx = reinterpret_cast<int*>(p); p += (size_t)B * a.kslots * 4;
@@ -133,8 +135,12 @@ __global__ void route_kernel(RouteArgs a) {
 
     bool nonfinite = false;
     const bool oea = a.mode == MOE_MODE_OEA;
-    const bool keep_keys = B <= nwarps;   // one token per warp: keys stay in registers
+    const bool keep_keys = B <= nwarps;   // one token per warp: keys and picks stay in registers
     uint32_t kv[NPL];
+    // Phase-1 picks of this warp's token (used by phase 2 when keep_keys).
+    uint32_t taken1 = 0;
+    int n1 = 0, myid1 = -1;
+    float myval1 = 0.f;
 
     // ---- plain top-k, or OEA phase 1 (baseline and union) ------------------
     for (int i = warp; i < B; i += nwarps) {
@@ -163,23 +169,28 @@ __global__ void route_kernel(RouteArgs a) {
             finish_token(a, sm, i, lane, n, myid, myval, N);
             continue;
         }
-        // Phase 1: softmax over all N scores, prefix in rank order, fp32.
-        int id0;
-        const uint32_t mk = warp_best<NPL>(kv, 0u, lane, id0);
-        const float m = key_score(mk);
-        float zl = 0.f;
+        // Phase 1: top-n_i in rank order; with top-p on, the softmax over all
+        // N scores (fp32) gives the prefix mass that stops the selection.
+        const bool top_p = a.p < 1.f;
+        float m = 0.f, Z = 1.f;
+        if (top_p) {
+            int id0;
+            m = key_score(warp_best<NPL>(kv, 0u, lane, id0));
+            float zl = 0.f;
 #pragma unroll
-        for (int j = 0; j < NPL; ++j)
-            if (kv[j]) zl += expf(key_score(kv[j]) - m);
-        const float Z = warp_sum(zl);
+            for (int j = 0; j < NPL; ++j)
+                if (kv[j]) zl += expf(key_score(kv[j]) - m);
+            Z = warp_sum(zl);
+        }
         float prefix = 0.f;
         for (int r = 0; r < a.k0; ++r) {
             int id;
             const uint32_t bk = warp_best<NPL>(kv, taken, lane, id);
             if (bk == 0) break;
             if ((id & 31) == lane) taken |= 1u << (id >> 5);
+            if (lane == r) { myid = id; myval = key_score(bk); }
             n = r + 1;
-            if (a.p < 1.f) {
+            if (top_p) {
                 prefix += expf(key_score(bk) - m) / Z;
                 if (prefix >= a.p) break;
             }
@@ -193,26 +204,32 @@ __global__ void route_kernel(RouteArgs a) {
             sm.snb[i] = n;
             if (a.n_base) a.n_base[i] = n;
         }
+        taken1 = taken; n1 = n; myid1 = myid; myval1 = myval;
     }
     __syncthreads();
 
     // ---- OEA phase 2: piggyback inside S_base -------------------------------
+    // The baseline (the token's top-n_i) lies inside S_base and heads both the
+    // in-union list and the walked list, so with the phase-1 picks still in
+    // registers the selection resumes at rank n_i.
     if (oea) {
         uint32_t notin = 0;
 #pragma unroll
         for (int j = 0; j < NPL; ++j)
             if (!((sm.sbase[j] >> lane) & 1u)) notin |= 1u << j;
         for (int i = warp; i < a.B_valid; i += nwarps) {
-            if (!keep_keys) {
+            uint32_t taken = 0;
+            int cnt = 0, myid = -1, r0 = 0;
+            float myval = 0.f;
+            if (keep_keys) {
+                taken = taken1; cnt = n1; r0 = n1; myid = myid1; myval = myval1;
+            } else {
                 bool dummy = false;
                 load_keys<NPL>(a.logits + (size_t)i * N, N, lane, kv, dummy);
             }
-            uint32_t taken = 0;
-            int cnt = 0, myid = -1;
-            float myval = 0.f;
             if (a.maxP >= N) {
                 // the in-union experts in rank order; the first n_i are the baseline
-                for (int r = 0; r < a.kmax; ++r) {
+                for (int r = r0; r < a.kmax; ++r) {
                     int id;
                     const uint32_t m = warp_best<NPL>(kv, taken | notin, lane, id);
                     if (m == 0) break;
@@ -224,7 +241,7 @@ __global__ void route_kernel(RouteArgs a) {
                 // walk the ranked list to depth max(maxP, n_i)
                 const int nb = sm.snb[i];
                 const int depth = a.maxP > nb ? a.maxP : nb;
-                for (int r = 0; r < depth && cnt < a.kmax; ++r) {
+                for (int r = r0; r < depth && cnt < a.kmax; ++r) {
                     int id;
                     const uint32_t m = warp_best<NPL>(kv, taken, lane, id);
                     if (m == 0) break;
@@ -243,25 +260,55 @@ __global__ void route_kernel(RouteArgs a) {
     if (__any_sync(kFull, nonfinite) && lane == 0) raise_flag(a.flags, kFlagNonFinite);
     __syncthreads();
 
-    // ---- counts, offsets, active list and per-expert info (one warp) ---------
-    if (warp == 0) {   // 32 consecutive experts per round, running totals in registers
-        int base1 = 0, base2 = 0;
-        for (int eb = 0; eb < N; eb += 32) {
-            const int e = eb + lane;
+    // ---- counts, offsets, active list and per-expert info ---------------------
+    // Warp w scans expert blocks w, w + nwarps, ... (32 experts each) with one
+    // packed inclusive scan of (count | active << 26); the block totals meet in
+    // shared memory and each warp then adds the totals of the blocks before
+    // its own.  A block's count is at most B * kslots < 2^26 and its active
+    // count at most 32, so the packed sum never carries across fields.
+    constexpr int kBlkPerWarp = NPL <= 16 ? 1 : 2;   // 32 (or 16) warps cover N / 32 blocks
+    const int nblk = (N + 31) >> 5;
+    int cnt_r[kBlkPerWarp];
+    uint32_t inc_r[kBlkPerWarp];
+#pragma unroll
+    for (int u = 0; u < kBlkPerWarp; ++u) {
+        const int b = warp + u * nwarps;
+        cnt_r[u] = 0;
+        inc_r[u] = 0;
+        if (b < nblk) {
+            const int e = (b << 5) + lane;
             int c = 0;
             if (e < N)
                 for (int ch = 0; ch < nch; ++ch) {
                     sm.pre[ch * N + e] = c;
                     c += __popc(sm.bits[ch * N + e]);
                 }
-            const int act = c > 0;
-            int i1 = c, i2 = act;   // inclusive scans across the warp
+            uint32_t v = (uint32_t)c | ((uint32_t)(c > 0) << 26);
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                const int u1 = __shfl_up_sync(kFull, i1, off), u2 = __shfl_up_sync(kFull, i2, off);
-                if (lane >= off) { i1 += u1; i2 += u2; }
+                const uint32_t t = __shfl_up_sync(kFull, v, off);
+                if (lane >= off) v += t;
             }
-            const int ex1 = base1 + i1 - c, ex2 = base2 + i2 - act;
+            cnt_r[u] = c;
+            inc_r[u] = v;
+            if (lane == 31) sm.btot[b] = v;
+        }
+    }
+    __syncthreads();
+    {
+        // totals of all blocks (for T and offsets[N]) and of the blocks before each of ours
+        const uint32_t tv = lane < nblk ? sm.btot[lane] : 0u;
+        const int tc = (int)(tv & ((1u << 26) - 1)), ta = (int)(tv >> 26);
+#pragma unroll
+        for (int u = 0; u < kBlkPerWarp; ++u) {
+            const int b = warp + u * nwarps;
+            if (b >= nblk) break;
+            const int e = (b << 5) + lane;
+            const int base1 = __reduce_add_sync(kFull, lane < b ? tc : 0);
+            const int base2 = __reduce_add_sync(kFull, lane < b ? ta : 0);
+            const int c = cnt_r[u], act = c > 0;
+            const int ex1 = base1 + (int)(inc_r[u] & ((1u << 26) - 1)) - c;
+            const int ex2 = base2 + (int)(inc_r[u] >> 26) - act;
             if (e < N) {
                 sm.soff[e] = ex1;
                 a.counts[e] = c;
@@ -272,14 +319,14 @@ __global__ void route_kernel(RouteArgs a) {
                     a.exinfo[N + ex2] = B <= 32 ? sm.bits[e] : 0u;
                 }
             }
-            base1 += __shfl_sync(kFull, i1, 31);
-            base2 += __shfl_sync(kFull, i2, 31);
         }
-        if (lane == 0) {
-            a.offsets[N] = base1;
-            *a.T = base2;
+        const int total = __reduce_add_sync(kFull, tc);
+        const int T = __reduce_add_sync(kFull, ta);
+        if (threadIdx.x == 0) {
+            a.offsets[N] = total;
+            *a.T = T;
         }
-        for (int q = base2 + lane; q < N; q += 32) {
+        for (int q = T + threadIdx.x; q < N; q += nthreads) {
             a.active[q] = -1;
             a.exinfo[q] = 0;
             a.exinfo[N + q] = 0;
@@ -303,11 +350,11 @@ template <int NPL>
 cudaError_t launch_route_t(const RouteArgs& a, cudaStream_t s) {
     const int threads = NPL <= 8 ? 1024 : 512;
     const int nch = (a.B + 31) / 32;
-    const size_t smem = 32 * 4 + MOE_MAX_TOKENS * 4 + MOE_MAX_EXPERTS * 4 +
+    const size_t smem = 2 * 32 * 4 + MOE_MAX_TOKENS * 4 + MOE_MAX_EXPERTS * 4 +
                         (size_t)a.B * a.kslots * 4 + 2 * (size_t)nch * a.N * 4;
     static bool attr_set = false;
     if (!attr_set) {
-        const int max_smem = 32 * 4 + MOE_MAX_TOKENS * 4 + MOE_MAX_EXPERTS * 4 +
+        const int max_smem = 2 * 32 * 4 + MOE_MAX_TOKENS * 4 + MOE_MAX_EXPERTS * 4 +
                              MOE_MAX_TOKENS * MOE_MAX_SLOTS * 4 + 2 * kMaxChunks * MOE_MAX_EXPERTS * 4;
         cudaError_t e = cudaFuncSetAttribute(route_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e != cudaSuccess) return e;

@@ -106,6 +106,17 @@ def test_general_oea_knobs(maxP, kmax):
     run_case(w, 24, OEA, 3, 0.8, maxP=maxP, kmax=kmax)
 
 
+@pytest.mark.parametrize("N", [32, 256, 512, 1024])
+@pytest.mark.parametrize("B", [12, 48])
+@pytest.mark.parametrize("maxP,p", [(0, 1.0), (0, 0.6), (7, 1.0), (5, 0.8)])
+def test_route_branches(N, B, maxP, p):
+    # Every expert-count class of the routing kernel, with one token per warp
+    # (picks kept in registers across the phases) and with more tokens than
+    # warps (keys reloaded), both phase-2 forms and top-p on and off.
+    w = W("t_branches", N=N, k=8, d=128, F=64, seed=N + B + maxP, zipf=True)
+    run_case(w, B, OEA, 3, p, maxP=maxP, kmax=10, B_valid=B - 3)
+
+
 @pytest.mark.parametrize("mode", [TOPK, OEA])
 def test_padding_tokens(mode):
     w = W("t_pad", seed=5)
