@@ -149,15 +149,17 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
     return r == CUDA_SUCCESS;
 }
 
-// ---- tensor maps of the tcgen05 expert kernel (boxes one 64-column block wide)
+// ---- tensor maps of the tcgen05 expert kernel
 // W_gate and W_up ([rows][cols] each) interleaved 8 rows at a time through
 // one 5D view {64 columns, 8 rows, 2 matrices, rows/8 row groups, cols/64
-// column blocks}: one box {64, 8, 2, 8, 1} lands as 8 x {8 rows of the lower
-// matrix, the same 8 rows of the other} = 128 rows x 64 columns.  The matrix
+// column blocks}: one box {64, 8, 2, 8, kb} lands as kb consecutive blocks of
+// 8 x {8 rows of the lower matrix, the same 8 rows of the other} = 128 rows
+// x 64 columns.  The matrix
 // stride is the distance between the two arrays, lower address first
 // (*swap: W_up is the lower one).  Fails if the arrays coincide or lie 2^40
 // bytes or more apart (the tensor-map stride limit).
-bool encode_gate_up_5d(CUtensorMap* m, const void* g, const void* u, uint64_t cols, uint64_t rows, bool* swap) {
+bool encode_gate_up_5d(CUtensorMap* m, const void* g, const void* u, uint64_t cols, uint64_t rows, bool* swap,
+                       uint32_t box_blocks = 1) {
     auto enc = get_encode();
     if (!enc) return false;
     const uintptr_t pg = reinterpret_cast<uintptr_t>(g), pu = reinterpret_cast<uintptr_t>(u);
@@ -167,7 +169,7 @@ bool encode_gate_up_5d(CUtensorMap* m, const void* g, const void* u, uint64_t co
     if (delta == 0 || delta % 16 != 0 || delta >= (1ull << 40) || rows % 8 != 0) return false;
     cuuint64_t dims[5] = {64, 8, 2, rows / 8, cols / 64};
     cuuint64_t strides[4] = {cols * 2, delta, 8 * cols * 2, 128};
-    cuuint32_t box[5] = {64, 8, 2, 8, 1};
+    cuuint32_t box[5] = {64, 8, 2, 8, box_blocks};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, reinterpret_cast<void*>(lo), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -175,9 +177,19 @@ bool encode_gate_up_5d(CUtensorMap* m, const void* g, const void* u, uint64_t co
     return r == CUDA_SUCCESS;
 }
 
+// Blocks of 64 columns per stage for batches of up to 16 tokens: the most
+// of 4, 2, 1 that divides both d / 64 and d_ff / 64.
+int small_batch_blocks(int d, int F) {
+    for (int kb = 4; kb > 1; kb >>= 1)
+        if ((d / 64) % kb == 0 && (F / 64) % kb == 0) return kb;
+    return 1;
+}
+
 struct TcMapEntry {
     MapKey key;
-    CUtensorMap maps[4];   // gate/up 5D (or W_gate 8-row boxes), W_up 8-row boxes, W_down 128-row boxes
+    // gate/up 5D (or W_gate 8-row boxes), W_up 8-row boxes, W_down 128-row boxes
+    // (one block wide); gate/up 5D and W_down kb blocks wide
+    CUtensorMap maps[5];
     bool fused, swap, used;
 };
 TcMapEntry g_tc_maps[64];
@@ -207,7 +219,13 @@ moe_status tc_expert_maps(const void* g, const void* u, const void* dn, int N, i
     }
     if (!encode_3d(&e.maps[1], u, d, (uint64_t)N * F, 8, 1) || !encode_3d(&e.maps[2], dn, F, (uint64_t)N * d, 128, 1))
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_up / W_down)");
+    const uint32_t kb = (uint32_t)small_batch_blocks(d, F);
     e.maps[3] = e.maps[0];
+    bool swap4 = false;
+    if (e.fused && !encode_gate_up_5d(&e.maps[3], g, u, d, (uint64_t)N * F, &swap4, kb))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_gate / W_up, wide boxes)");
+    if (!encode_3d(&e.maps[4], dn, F, (uint64_t)N * d, 128, kb))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_down, wide boxes)");
     e.used = true;
     memcpy(out, e.maps, sizeof e.maps);
     *fused = e.fused;
@@ -217,12 +235,13 @@ moe_status tc_expert_maps(const void* g, const void* u, const void* dn, int N, i
 
 // Workspace maps of the tcgen05 kernel: expert-grouped hidden states and h
 // (16-row boxes), and the hidden states themselves (16-row boxes: the whole
-// batch of up to 16 tokens; rows past B read as zeros).
+// batch of up to 16 tokens; rows past B read as zeros); then the hidden
+// states and h with boxes kb blocks wide (batches of up to 16 tokens).
 struct TcOpEntry {
     const void* ws;
     const void* hidden;
     int pairs, B, d, F, dev;
-    CUtensorMap maps[3];
+    CUtensorMap maps[5];
     bool used;
 };
 TcOpEntry g_tc_ops[32];
@@ -247,8 +266,10 @@ moe_status tc_operand_maps(unsigned char* ws, const WsLayout& L, const void* hid
     e.d = d;
     e.F = F;
     e.dev = dev;
+    const uint32_t kb = (uint32_t)small_batch_blocks(d, F);
     if (!encode_3d(&e.maps[0], ws + L.xperm, d, pairs, 16, 1) || !encode_3d(&e.maps[1], ws + L.hbuf, F, pairs, 16, 1) ||
-        !encode_3d(&e.maps[2], hidden, d, B, 16, 1))
+        !encode_3d(&e.maps[2], hidden, d, B, 16, 1) || !encode_3d(&e.maps[3], hidden, d, B, 16, kb) ||
+        !encode_3d(&e.maps[4], ws + L.hbuf, F, pairs, 16, kb))
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (operands)");
     e.used = true;
     memcpy(out, e.maps, sizeof e.maps);
@@ -323,6 +344,8 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     a.xperm = ws + L.xperm;
     a.out = out;
     a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone);
+    a.nused = reinterpret_cast<const int32_t*>(ws + L.nused);
+    a.ycnt = reinterpret_cast<uint32_t*>(ws + L.ycnt);
     a.gflag = reinterpret_cast<uint32_t*>(ws + L.gflag);
     a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
     a.w_gate = w_gate;
@@ -353,17 +376,25 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
     if (sms > kMaxGrid) sms = kMaxGrid;
     {   // the tcgen05 expert kernel (bf16 experts, and INT4 experts through its converter warps)
-        CUtensorMap maps[7];
+        CUtensorMap maps[11];
         bool fused = false, swap = false;
-        CUtensorMap wm[4];
+        CUtensorMap wm[5], om[5];
         if ((st = tc_expert_maps(w_gate, w_up, w_down, n_hot, d_ff, P.d, dev, wm, &fused, &swap)) != MOE_OK) return st;
+        if ((st = tc_operand_maps(ws, L, hidden, P.B * P.kslots, P.B, P.d, d_ff, dev, om)) != MOE_OK) return st;
         maps[0] = wm[0];                       // gate/up 5D, or W_gate
         maps[1] = wm[0];                       // W_gate (8-row boxes; read when not fused)
         maps[2] = wm[1];                       // W_up
         maps[3] = wm[2];                       // W_down
-        if ((st = tc_operand_maps(ws, L, hidden, P.B * P.kslots, P.B, P.d, d_ff, dev, maps + 4)) != MOE_OK) return st;
+        maps[4] = om[0];                       // grouped hidden states
+        maps[5] = om[1];                       // h
+        maps[6] = om[2];                       // hidden states
+        maps[7] = wm[3];                       // gate/up 5D, kb blocks wide
+        maps[8] = wm[4];                       // W_down, kb blocks wide
+        maps[9] = om[3];                       // hidden states, kb blocks wide
+        maps[10] = om[4];                      // h, kb blocks wide
         a.gu_fused = fused ? 1 : 0;
         a.gu_swap = swap ? 1 : 0;
+        a.kbs = small_batch_blocks(P.d, d_ff);
         e = launch_ffn_tc(a, maps, sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
         return MOE_OK;
@@ -436,6 +467,9 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
     a.pos_of = reinterpret_cast<int32_t*>(ws + L.pos_of);
     a.n_base = routing->n_base;
     a.exinfo = reinterpret_cast<uint32_t*>(ws + L.exinfo);
+    a.nused = reinterpret_cast<int32_t*>(ws + L.nused);
+    a.ycnt = reinterpret_cast<uint32_t*>(ws + L.ycnt);
+    a.rbd = (P.d + 127) / 128;
     a.flags = &reinterpret_cast<WsHeader*>(ws + L.header)->flags;
     e = launch_route(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");

@@ -30,7 +30,7 @@ struct WsHeader {
 };
 
 struct WsLayout {
-    size_t header, hdone, gflag, exinfo, pos_of, logits, hbuf, ybuf, xperm, total;
+    size_t header, hdone, gflag, exinfo, pos_of, nused, ycnt, logits, hbuf, ybuf, xperm, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -47,6 +47,8 @@ inline WsLayout ws_layout(int B, int N, int d, int kslots, int F, int h_elt) {
     L.gflag = o;  o += align256(sizeof(uint32_t) * kMaxGrid);
     L.exinfo = o; o += align256(sizeof(uint32_t) * 2 * N);   // per active expert: info, token mask
     L.pos_of = o; o += align256(sizeof(int32_t) * (size_t)B * kslots + 4);
+    L.nused = o;  o += align256(sizeof(int32_t) * (size_t)B + 4);                  // kept slots per token
+    L.ycnt = o;   o += align256(sizeof(uint32_t) * (size_t)B * ((d + 127) / 128) + 4);   // per (token, 128 rows of d)
     L.logits = o; o += align256(sizeof(float) * (size_t)B * N + 4);
     L.hbuf = o;   o += align256((size_t)B * kslots * F * h_elt);
     L.ybuf = o;   o += align256(sizeof(float) * (size_t)B * kslots * d);
@@ -81,6 +83,9 @@ struct RouteArgs {
     int32_t* pos_of;        // [B*kslots]
     int32_t* n_base;        // [B] or null
     uint32_t* exinfo;       // [2][N]: active expert a -> id | cnt << 10 | first pair << 19; tokens (B <= 32)
+    int32_t* nused;         // [B] kept slots of each token
+    uint32_t* ycnt;         // [B][rbd] set to nused: the expert kernel counts each row block's y slices down
+    int rbd;                // row blocks of 128 in d
     uint32_t* flags;
 };
 
@@ -100,6 +105,8 @@ struct FfnArgs {
     void* xperm;            // [pairs][d] hidden states grouped by expert
     void* out;              // [B][d]
     uint32_t* hdone;        // [token chunks] phase-A tiles of the chunk whose h rows are written
+    const int32_t* nused;   // [B] kept slots of each token (routing kernel)
+    uint32_t* ycnt;         // [B][ceil(d / 128)] y slices still missing; the last writer combines
     uint32_t* gflag;        // [grid] CTA finished its share of the gather
     WsHeader* hdr;
     const void* w_gate;     // [N][F][d]   (fp32 path)
@@ -113,15 +120,19 @@ struct FfnArgs {
     int n_hot, n_cold;
     int gu_fused;           // tcgen05 kernel: W_gate and W_up through one interleaving 5D map
     int gu_swap;            // that map starts at W_up (the lower address): up rows come first
+    int kbs;                // tcgen05 kernel: 64-column blocks per stage for batches of up to 16 tokens
+    int smem_bytes;         // tcgen05 kernel: dynamic shared memory of the launch (set by the launcher)
 };
 
 // Launchers (defined in the .cu files).
 cudaError_t launch_router(const RouterArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
-// tcgen05 expert kernel (bf16 weights).  maps: W_gate/W_up interleaved 8
-// rows at a time (5D, gu_fused) or W_gate and W_up alone (8-row boxes),
-// W_down (128-row boxes), gathered hidden states, h and the hidden states
-// (16-row boxes); all boxes 64 columns wide.
+// tcgen05 expert kernel (bf16 weights).  maps[0..6]: W_gate/W_up
+// interleaved 8 rows at a time (5D, gu_fused) or W_gate and W_up alone
+// (8-row boxes), W_down (128-row boxes), gathered hidden states, h and the
+// hidden states (16-row boxes), all one 64-column block wide; maps[7..10]:
+// the 5D gate/up map, W_down, the hidden states and h with boxes kbs blocks
+// wide (batches of up to 16 tokens).
 cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s);
 cudaError_t launch_ffn_f32(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_synth(void* dst, int dtype, uint64_t n, uint64_t start, uint64_t seed,
@@ -359,6 +370,19 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 // Programmatic dependent launch: wait until the preceding kernel in the
 // stream has completed and its memory is visible / allow the next kernel in
 // the stream to be scheduled now (it still waits for us before reading).
+// Atomic add at GPU scope with release semantics (earlier writes this
+// thread has made or observed are visible before it) and no result.
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Atomic add at GPU scope with acquire and release semantics; returns the old value.
+__device__ __forceinline__ uint32_t atom_acq_rel_gpu_add(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }

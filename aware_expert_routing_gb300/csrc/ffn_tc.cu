@@ -9,7 +9,7 @@
 // Expert form (Qwen3): y = W_down (silu(W_gate x) * (W_up x)); combine:
 // out_i = sum_j w_ij y_{e_ij}(x_i) (kept scores, section 2 Q2).
 //
-// Structure (one persistent CTA per SM, 15 warps):
+// Structure (one persistent CTA per SM, 16 warps):
 //   * Work is a list of tiles.  Phase-A tile (expert a, 64 rows of d_ff,
 //     token chunk c): the 64 W_gate rows and the 64 W_up rows of the same
 //     d_ff indices, interleaved 8 rows at a time (rows 16g..16g+7 = gate
@@ -21,18 +21,24 @@
 //     are streamed once); K = d.  Phase-B tile (expert a, 128 rows of d,
 //     chunk c): W_down rows times the chunk's h rows, K = d_ff.  The list
 //     holds every phase-A tile, then every phase-B tile, each in active-
-//     expert order; CTA b starts with tile b and claims each next tile (two
+//     expert order; CTA b starts with tile b and claims each next tile (one
 //     ahead) from one grid-wide counter, so all CTAs finish within about
 //     one tile of each other.
 //   * Warp 4 claims the tiles, posts them to a 16-entry shared-memory queue
-//     and streams the weights: one TMA operation per 16 KB stage (128 rows x
-//     64 columns, 128-byte swizzle; the gate/up interleave comes from one 5D
-//     tensor map over both matrices).  Warp 5 streams the 16 token rows of
-//     each stage (16-row boxes): the whole batch of up to 16 tokens straight
-//     from the hidden states, or rows of the expert-grouped copy of the
-//     hidden states, or (phase B) rows of h once every phase-A tile of the
-//     chunk has written them (a per-chunk counter).  Ring: 180 KB of stages
-//     of 16 KB + nmax x 128 bytes (10 stages at nmax = 16, 5 at 128).
+//     and streams the weights: one TMA operation per stage of KB blocks of
+//     128 rows x 64 columns (128-byte swizzle; the gate/up interleave comes
+//     from one 5D tensor map over both matrices).  A TMA unit's rate per SM
+//     grows with the bytes of each operation, so batches of up to 16 tokens
+//     use KB = 4 (64 KB per operation) where d and d_ff allow it, larger
+//     batches KB = 1.  Warp 5 streams the token rows of each stage (16-row
+//     boxes): the whole batch of up to 16 tokens straight from the hidden
+//     states, or rows of the expert-grouped copy of the hidden states, or
+//     (phase B) rows of h once every phase-A tile of the chunk has written
+//     them (a per-chunk counter).  The stage ring takes the shared memory
+//     that the barriers and per-expert tables leave (3 stages of 72 KB at
+//     KB = 4, up to 12 of 18 KB at KB = 1 and nmax = 16).  For batches of up
+//     to 16 tokens warp 4 also loads the first tile's first stages (token
+//     rows, then weights) right after the routing kernel ends.
 //   * Warp 6, lane 0, issues the MMAs: four K=16 steps per stage straight
 //     from the swizzled shared memory (no register staging), fp32
 //     accumulators in tensor memory, four accumulator buffers (16 columns
@@ -51,12 +57,18 @@
 //     8 above (shuffle), applies SwiGLU and stores h (bf16) for the tile's
 //     tokens; phase B: stores y (fp32).  After a phase-A tile the four warps
 //     meet at a shared-memory barrier and one thread releases the chunk's
-//     counter.
+//     counter.  A finished phase-B tile goes to warp 15 through a small
+//     queue; it counts each of the tile's tokens down on the token's
+//     counter for the tile's 128 rows of d (set to the token's kept slots
+//     by the routing kernel), with release semantics, so the epilogue
+//     warps never wait for their stores to drain.
+//   * After its role every warp takes (token, 128 rows) combine items: it
+//     waits until the item's counter is zero, sums the kept weights times
+//     the y rows in slot order, writes the output rows and restores the
+//     counter for the next launch.
 //   * All phase-A tiles precede all phase-B tiles in the list and wait on
-//     nothing later, so every wait ends.  After its last tile every CTA
-//     arrives at one grid-wide counter; once all have, each CTA combines a
-//     slice of the output (float4, slot order).  The last CTA resets the
-//     counters for the next launch.
+//     nothing later, so every wait ends.  The last CTA to finish resets the
+//     tile and chunk counters for the next launch.
 // Every wait is bounded; a wait that gives up raises MOE_FLAG_WAIT_TIMEOUT
 // and the CTA runs to its end without waiting again.
 #include "common.cuh"
@@ -71,17 +83,18 @@ constexpr int kWarpO = 5;                // operand producer
 constexpr int kWarpM = 6;                // MMA issuer, owner of the tensor memory
 constexpr int kWarpC = 7;                // warps 7-14: INT4 converters
 constexpr int kConvWarps = 8;
-constexpr int kThreads = (kWarpC + kConvWarps) * 32;
+constexpr int kWarpN = kWarpC + kConvWarps;   // warp 15: counts finished y slices down
+constexpr int kThreads = (kWarpN + 1) * 32;
+constexpr int kNQ = 8;                   // phase-B tiles handed to warp 15
 constexpr int kM = 128;                  // weight rows per tile (MMA M)
 constexpr int kNMax = 128;               // most token columns per tile (MMA N)
-constexpr int kWBytes = kM * 128;        // 128 rows x 64 bf16
-constexpr int kRingBytes = 10 * (kWBytes + 16 * 128);   // 10 stages with 16 token rows
-constexpr int kMaxStages = 10;
+constexpr int kWBytes = kM * 128;        // one K block: 128 rows x 64 bf16
+constexpr int kMaxStages = 12;
 constexpr int kRaw = 4;                  // packed INT4 chunks in flight
 constexpr int kQ4A = 64 * 32 + 64 * 2;   // INT4 chunk of W_gate / W_up: 64 rows x 64 columns + scales
 constexpr int kQ4B = 128 * 32 + 128 * 2; // INT4 chunk of W_down: 128 rows x 64 columns + scales
 constexpr int kRawBytes = 2 * kQ4A;      // a phase-A stage needs a W_gate and a W_up chunk
-static_assert(kRawBytes == kQ4B, "one raw slot fits either stage");
+static_assert(kRawBytes == kQ4B, "one raw slot fits either K block");
 constexpr int kQ = 16;                   // tile queue entries
 constexpr int kAcc = 4;                  // accumulator buffers
 constexpr uint32_t kTmemCols = kAcc * kNMax;   // fp32 columns (batches over 16 tokens)
@@ -98,44 +111,59 @@ struct Smem {
     uint64_t tq_full[kQ];                // tile queue entry posted by the weight warp
     uint64_t tq_empty[kQ];               // entry released by the four epilogue warps
     uint64_t mma_done;                   // every MMA issued has completed
-    uint64_t h_written;                  // the four epilogue warps stored a phase-A tile's h rows
+    uint64_t epi_bar;                    // the four epilogue warps meet (bounded wait)
+    uint64_t nt_full[kNQ];               // the four epilogue warps stored a phase-B tile's y rows
+    uint64_t nt_empty[kNQ];              // warp 15 has counted them down
+    int4 nt_info[kNQ];                   // first pair, pairs (-1: no more tiles), row block
     uint64_t raw_full[kRaw];             // packed INT4 chunks landed (bulk copies)
     uint64_t raw_empty[kRaw];            // the four converter warps have read them
     uint64_t conv_bar;                   // the four converter warps meet (bounded wait)
-    uint32_t raw_info[kRaw];             // target ring slot | phase A << 8, or ~0u (no more chunks)
+    uint32_t raw_info[kRaw];             // ring slot | phase A << 8 | K block << 9 | last << 13, or ~0u
     int tq[kQ];                          // tile index, or -1 once the list is exhausted
-    int chunk_off[MOE_MAX_EXPERTS + 1];
-    uint32_t ex_info[MOE_MAX_EXPERTS];   // active index -> id | cnt << 10 | first pair << 19
-    uint16_t tokmask[MOE_MAX_EXPERTS];   // active index -> tokens routed to it (batches of <= 16)
-    int ex_slot[MOE_MAX_EXPERTS];        // active index -> bf16 expert (>= 0) or -1 - INT4 expert
+    int fast_ops;                        // stages of the first tile whose token rows warp 4 has loaded
     uint32_t tmem_base;
     int nmax;                            // tokens per chunk for this launch (multiple of 16)
     int abort_flag;
     int last_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kRingBytes + (size_t)kRaw * kRawBytes + sizeof(Smem);
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// Per-expert tables in shared memory, after Smem, sized by N at launch.
+struct Tabs {
+    int* chunk_off;       // [N + 1] first token chunk of each active expert
+    uint32_t* ex_info;    // [N] active index -> id | cnt << 10 | first pair << 19
+    int* ex_slot;         // [N] active index -> bf16 expert (>= 0) or -1 - INT4 expert
+    uint16_t* tokmask;    // [N] active index -> tokens routed to it (batches of <= 16)
+};
+
+__host__ __device__ constexpr size_t tabs_bytes(int N) {
+    return (((size_t)(N + 1) * 4 + (size_t)N * 4 + (size_t)N * 4 + (size_t)N * 2) + 15) & ~size_t(15);
+}
+
+// Stage ring bytes left in `total` bytes of dynamic shared memory (whole KB).
+__host__ __device__ constexpr size_t ring_bytes_for(size_t total, int N, bool int4) {
+    return (total - 1024 - ((sizeof(Smem) + 15) & ~size_t(15)) - tabs_bytes(N) -
+            (int4 ? (size_t)kRaw * kRawBytes : 0)) & ~size_t(1023);
+}
 
 struct Tile {
     int a, e, rb, c, off, ntok, nch;
 };
 
 // Tile t of a phase with rbn row blocks per (expert, chunk); shared memory only.
-__device__ __forceinline__ Tile decode_tile(int t, int rbn, const Smem& S, int Tn, int nmax) {
+__device__ __forceinline__ Tile decode_tile(int t, int rbn, const Tabs& X, int Tn, int nmax) {
     int lo = 0, hi = Tn - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (S.chunk_off[mid] * rbn <= t) lo = mid; else hi = mid - 1;
+        if (X.chunk_off[mid] * rbn <= t) lo = mid; else hi = mid - 1;
     }
     Tile T;
     T.a = lo;
-    const uint32_t info = S.ex_info[lo];
+    const uint32_t info = X.ex_info[lo];
     T.e = info & 1023u;
     const int cnt = (info >> 10) & 511u;
     T.off = info >> 19;
-    T.nch = S.chunk_off[lo + 1] - S.chunk_off[lo];
-    const int r = t - S.chunk_off[lo] * rbn;
+    T.nch = X.chunk_off[lo + 1] - X.chunk_off[lo];
+    const int r = t - X.chunk_off[lo] * rbn;
     T.rb = r / T.nch;
     T.c = r - T.rb * T.nch;
     T.ntok = min(nmax, cnt - nmax * T.c);
@@ -175,6 +203,23 @@ __device__ __forceinline__ void wait_counter(const uint32_t* p, uint32_t need, S
     }
 }
 
+// Bounded wait until *p == 0 (acquire, GPU scope), polling with a backoff
+// of up to 128 ns so that waiting warps load the memory system little.
+__device__ __forceinline__ void wait_zero(const uint32_t* p, Smem& S, uint32_t* flags) {
+    if (ld_acquire_gpu(p) == 0u) return;
+    const long long t0 = clock64();
+    uint32_t ns = 32;
+    while (!*(volatile int*)&S.abort_flag) {
+        if (ld_acquire_gpu(p) == 0u) return;
+        if (clock64() - t0 > kWaitCycles) {
+            give_up(S, flags);
+            return;
+        }
+        __nanosleep(ns);
+        if (ns < 128) ns <<= 1;
+    }
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
 
 // Eight INT4 codes (one packed word, column 2p in the low and 2p+1 in the
@@ -209,6 +254,15 @@ __device__ __forceinline__ void conv_sync(Smem& S, uint32_t& nsync, uint32_t* fl
     ++nsync;
 }
 
+// The four epilogue warps meet (bounded wait); every warp calls this the
+// same number of times.
+__device__ __forceinline__ void epi_meet(Smem& S, uint32_t& nm, uint32_t* flags, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.epi_bar);
+    wait_bar(&S.epi_bar, nm & 1, S, flags);
+    ++nm;
+}
+
 // Position in the stage ring (the stage count is set per launch): slot,
 // phase parity, and whether the ring has wrapped once (a producer then
 // waits for the slot to be freed).
@@ -229,17 +283,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const __grid_constant__ CUtensorMap tm_gate,
               const __grid_constant__ CUtensorMap tm_up, const __grid_constant__ CUtensorMap tm_down,
               const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_h,
-              const __grid_constant__ CUtensorMap tm_hid) {
+              const __grid_constant__ CUtensorMap tm_hid, const __grid_constant__ CUtensorMap tm_gu4,
+              const __grid_constant__ CUtensorMap tm_down4, const __grid_constant__ CUtensorMap tm_hid4,
+              const __grid_constant__ CUtensorMap tm_h4) {
     extern __shared__ unsigned char smem_raw[];
+    // [stage ring][kRaw packed INT4 slots, with INT4 experts][Smem][tables]
+    const bool has_q4 = A.n_cold > 0;
+    const int ring_bytes = (int)ring_bytes_for((size_t)A.smem_bytes, A.N, has_q4);
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char* raw = ring + (size_t)kRingBytes;   // kRaw packed INT4 slots
-    Smem& S = *reinterpret_cast<Smem*>(raw + (size_t)kRaw * kRawBytes);
+    unsigned char* raw = ring + ring_bytes;
+    Smem& S = *reinterpret_cast<Smem*>(raw + (has_q4 ? kRaw * kRawBytes : 0));
+    Tabs X;
+    X.chunk_off = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(&S) + ((sizeof(Smem) + 15) & ~size_t(15)));
+    X.ex_info = reinterpret_cast<uint32_t*>(X.chunk_off + A.N + 1);
+    X.ex_slot = reinterpret_cast<int*>(X.ex_info + A.N);
+    X.tokmask = reinterpret_cast<uint16_t*>(X.ex_slot + A.N);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = A.d, F = A.F;
     uint32_t* flags = &A.hdr->flags;
     const uint32_t G = gridDim.x;
+    // K blocks (64 columns) per stage: batches of up to 16 tokens move
+    // A.kbs blocks per TMA operation, since the TMA unit's rate per SM grows
+    // with the size of each operation; larger batches one block.
+    const bool small_b = A.B <= 16;                 // phase-A operand: the whole batch
+    const int KB = (small_b && A.gu_fused) ? A.kbs : 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kMaxStages; ++i) {
@@ -255,7 +324,12 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             mbar_init(&S.tq_empty[i], kEpiWarps);
         }
         mbar_init(&S.mma_done, 1);
-        mbar_init(&S.h_written, kEpiWarps);
+        mbar_init(&S.epi_bar, kEpiWarps);
+        for (int i = 0; i < kNQ; ++i) {
+            mbar_init(&S.nt_full[i], kEpiWarps);
+            mbar_init(&S.nt_empty[i], 1);
+            S.nt_info[i] = make_int4(0, 0, 0, 0);
+        }
         for (int i = 0; i < kRaw; ++i) {
             mbar_init(&S.raw_full[i], 1);
             mbar_init(&S.raw_empty[i], kConvWarps);
@@ -263,10 +337,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         mbar_init(&S.conv_bar, kConvWarps);
         fence_barrier_init();
         S.abort_flag = 0;
+        S.fast_ops = 0;
     }
     // accumulator buffers: kAcc x nmax columns, nmax = 16 for batches of up to 16
-    const uint32_t tmem_cols = A.B <= 16 ? kTmemColsSmall : kTmemCols;
-    const int acc_stride = A.B <= 16 ? 16 : kNMax;
+    const uint32_t tmem_cols = small_b ? kTmemColsSmall : kTmemCols;
+    const int acc_stride = small_b ? 16 : kNMax;
     if (warp == kWarpM) tmem_alloc(&S.tmem_base, tmem_cols);
     __syncthreads();             // barriers initialised (this overlaps the routing kernel)
     grid_dependency_wait();      // routing comes from the preceding kernel
@@ -277,9 +352,10 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     }
     // Batches of up to 16 tokens: the CTA's first tile is phase-A tile
     // blockIdx.x of a one-chunk-per-expert list, so the weight warp starts
-    // its stages now, while warp 0 builds the per-expert records.
+    // its stages now (each stage's token rows first, then its weights), while
+    // warp 0 builds the per-expert records.
     int fast_stages = 0;
-    if (warp == kWarpW && lane == 0 && A.B <= 16) {
+    if (warp == kWarpW && lane == 0 && small_b) {
         const int rbA0 = F / 64, t0 = (int)blockIdx.x;
         if (t0 < Tn * rbA0) {
             const int e = (int)(A.exinfo[t0 / rbA0] & 1023u);
@@ -287,12 +363,16 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             if (sl >= 0 && sl < A.n_hot) {
                 const uint64_t pol = l2_evict_first_policy();
                 const int row0 = sl * F + 64 * (t0 % rbA0);
-                fast_stages = min(d / 64, min(kMaxStages, kRingBytes / (kWBytes + 16 * 128)));
+                const int sb = KB * (kWBytes + 16 * 128);   // the slot size of this launch (nmax = 16)
+                fast_stages = min(d / 64 / KB, min(kMaxStages, ring_bytes / sb));
+                const uint64_t pol_x = l2_evict_last_policy();
                 for (int s = 0; s < fast_stages; ++s) {
-                    unsigned char* dst = ring + (size_t)s * (kWBytes + 16 * 128);
-                    mbar_arrive_expect_tx(&S.full[s], kWBytes);
+                    unsigned char* dst = ring + (size_t)s * sb;
+                    mbar_arrive_expect_tx(&S.full[s], KB * 2048);   // rows past B read as zeros
+                    tma_load_3d(dst + KB * kWBytes, KB > 1 ? &tm_hid4 : &tm_hid, 0, 0, s * KB, &S.full[s], pol_x);
+                    mbar_arrive_expect_tx(&S.full[s], KB * kWBytes);
                     if (A.gu_fused) {
-                        tma_load_5d(dst, &tm_gu, 0, 0, 0, row0 / 8, s, &S.full[s], pol);
+                        tma_load_5d(dst, KB > 1 ? &tm_gu4 : &tm_gu, 0, 0, 0, row0 / 8, s * KB, &S.full[s], pol);
                     } else {
                         for (int g = 0; g < 8; ++g) {
                             tma_load_3d(dst + (2 * g) * 1024, &tm_gate, 0, row0 + 8 * g, s, &S.full[s], pol);
@@ -300,6 +380,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                         }
                     }
                 }
+                S.fast_ops = fast_stages;   // read by the operand warp after the barrier below
             }
         }
     }
@@ -307,8 +388,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         int maxcnt = 0;
         for (int a = lane; a < Tn; a += 32) {
             const uint32_t info = A.exinfo[a];   // written by the routing kernel
-            S.ex_info[a] = info;
-            S.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
+            X.ex_info[a] = info;
+            X.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
             maxcnt = max(maxcnt, (int)((info >> 10) & 511u));
             const int e = info & 1023u;
             int sl = A.slot ? A.slot[e] : e;
@@ -316,39 +397,43 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 raise_flag(flags, kFlagBadIndex);
                 sl = A.n_hot > 0 ? 0 : -1;
             }
-            S.ex_slot[a] = sl;
+            X.ex_slot[a] = sl;
         }
         maxcnt = __reduce_max_sync(0xffffffffu, maxcnt);
         // a chunk holds up to nmax tokens: the whole batch for batches of up to
         // 16, else the largest expert's tokens rounded up to 16, at most 128
-        const int nmax = A.B <= 16 ? 16 : min(kNMax, max(16, (maxcnt + 15) & ~15));
+        const int nmax = small_b ? 16 : min(kNMax, max(16, (maxcnt + 15) & ~15));
         if (lane == 0) S.nmax = nmax;
         __syncwarp();
         int run = 0;
-        if (lane == 0) S.chunk_off[0] = 0;
+        if (lane == 0) X.chunk_off[0] = 0;
         for (int a0 = 0; a0 < Tn; a0 += 32) {
             const int a = a0 + lane;
             int nch = 0;
-            if (a < Tn) nch = ((int)((S.ex_info[a] >> 10) & 511u) + nmax - 1) / nmax;
+            if (a < Tn) nch = ((int)((X.ex_info[a] >> 10) & 511u) + nmax - 1) / nmax;
             int inc = nch;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const int u = __shfl_up_sync(0xffffffffu, inc, off);
                 if (lane >= off) inc += u;
             }
-            if (a < Tn) S.chunk_off[a + 1] = run + inc;
+            if (a < Tn) X.chunk_off[a + 1] = run + inc;
             run += __shfl_sync(0xffffffffu, inc, 31);
         }
     }
     if (warp == kWarpW && lane == 0) {
-        prefetch_tensormap(A.gu_fused ? &tm_gu : &tm_gate);
+        prefetch_tensormap(A.gu_fused ? (KB > 1 ? &tm_gu4 : &tm_gu) : &tm_gate);
         if (!A.gu_fused) prefetch_tensormap(&tm_up);
-        prefetch_tensormap(&tm_down);
+        prefetch_tensormap(KB > 1 ? &tm_down4 : &tm_down);
     }
     if (warp == kWarpO && lane == 0) {
-        prefetch_tensormap(&tm_x);
-        prefetch_tensormap(&tm_hid);
-        prefetch_tensormap(&tm_h);
+        if (small_b) {
+            prefetch_tensormap(KB > 1 ? &tm_hid4 : &tm_hid);
+            prefetch_tensormap(KB > 1 ? &tm_h4 : &tm_h);
+        } else {
+            prefetch_tensormap(&tm_x);
+            prefetch_tensormap(&tm_h);
+        }
     }
     tmem_fence_before_sync();
     __syncthreads();
@@ -358,13 +443,14 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // Tiles: phase A (expert, 64 rows of d_ff, chunk) first, then phase B
     // (expert, 128 rows of d, chunk), both in active-expert order.
     const int rbA = F / 64, rbB = (d + kM - 1) / kM;
-    const int SA = d / 64, SB = F / 64;             // stages per tile (K blocks of 64)
-    const int TA = S.chunk_off[Tn] * rbA;
-    const int Ttot = TA + S.chunk_off[Tn] * rbB;
-    const bool small_b = A.B <= 16;                 // phase-A operand: the whole batch
+    const int SA = d / 64 / KB, SB = F / 64 / KB;   // stages per tile (KB blocks of 64 columns)
+    const int TA = X.chunk_off[Tn] * rbA;
+    const int Ttot = TA + X.chunk_off[Tn] * rbB;
     const int nmax = S.nmax;
-    const int slot_bytes = kWBytes + nmax * 128;    // 16 KB of weights + nmax token rows
-    const int nst = min(kMaxStages, kRingBytes / slot_bytes);
+    // a slot: KB weight blocks of 16 KB, then KB operand blocks of nmax rows
+    const int slot_bytes = KB * (kWBytes + nmax * 128);
+    const int obytes = nmax * 128;                  // one operand block
+    const int nst = min(kMaxStages, ring_bytes / slot_bytes);
 
     if (warp == kWarpW) {
         // ---------------------------- weight producer ----------------------------
@@ -374,9 +460,9 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             RingPos rp, rq;   // stage ring, packed INT4 ring
             const size_t q4_mat_a = (size_t)(F / 64) * (d / 64) * kQ4A;    // bytes of one INT4 W_gate / W_up
             const size_t q4_mat_b = (size_t)(d / kM) * (F / 64) * kQ4B;    // bytes of one INT4 W_down
-            // claims run two tiles ahead so that the atomic's latency is hidden
+            // CTA b starts with tile b; the next tile is claimed when this
+            // one is posted, so the atomic's latency hides behind its stages
             int next0 = (int)blockIdx.x;
-            int next1 = next0 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
             for (int s = 0; s < fast_stages; ++s) rp.next(nst);   // stages issued before the prologue
             for (int n = 0;; ++n) {
                 const int q = n % kQ;
@@ -385,12 +471,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 S.tq[q] = tile;
                 mbar_arrive(&S.tq_full[q]);
                 if (tile < 0) break;
-                next0 = next1;
-                next1 = next1 < Ttot ? (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u) : Ttot;
+                next0 = (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u);
                 const bool ph_a = tile < TA;
-                const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn, nmax);
+                const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;   // chunked experts are re-read from L2
-                const int sl = S.ex_slot[T.a];                          // bf16 expert, or -1 - INT4 expert
+                const int sl = X.ex_slot[T.a];                          // bf16 expert, or -1 - INT4 expert
                 const int row0 = ph_a ? sl * F + 64 * T.rb : sl * d + kM * T.rb;
                 const int ns = ph_a ? SA : SB;
                 for (int s = n == 0 ? fast_stages : 0; s < ns; ++s, rp.next(nst)) {
@@ -398,34 +483,40 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
                     unsigned char* dst = ring + (size_t)slot * slot_bytes;
                     if (sl < 0) {
-                        // INT4 expert: the packed chunk(s) go to a raw slot; the converter
-                        // warps write the bf16 stage and arrive on its barrier.
-                        const int r = rq.slot;
-                        if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
-                        S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u);
-                        unsigned char* rdst = raw + (size_t)r * kRawBytes;
+                        // INT4 expert: the packed chunks of the stage's K blocks go to
+                        // raw slots; the converter warps write the bf16 blocks and
+                        // arrive on the stage's barrier after its last one.
                         const int c = -1 - sl;
-                        if (ph_a) {
-                            const size_t off = (size_t)c * q4_mat_a + ((size_t)T.rb * (d / 64) + s) * kQ4A;
-                            mbar_arrive_expect_tx(&S.raw_full[r], 2 * kQ4A);
-                            bulk_load(rdst, A.q_gate + off, kQ4A, &S.raw_full[r], pol);
-                            bulk_load(rdst + kQ4A, A.q_up + off, kQ4A, &S.raw_full[r], pol);
-                        } else {
-                            const size_t off = (size_t)c * q4_mat_b + ((size_t)T.rb * (F / 64) + s) * kQ4B;
-                            mbar_arrive_expect_tx(&S.raw_full[r], kQ4B);
-                            bulk_load(rdst, A.q_down + off, kQ4B, &S.raw_full[r], pol);
+#pragma unroll 1
+                        for (int kb = 0; kb < KB; ++kb) {
+                            const int r = rq.slot;
+                            if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
+                            S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u) | ((uint32_t)kb << 9) |
+                                            (kb == KB - 1 ? (1u << 13) : 0u);
+                            unsigned char* rdst = raw + (size_t)r * kRawBytes;
+                            const int kblk = s * KB + kb;
+                            if (ph_a) {
+                                const size_t off = (size_t)c * q4_mat_a + ((size_t)T.rb * (d / 64) + kblk) * kQ4A;
+                                mbar_arrive_expect_tx(&S.raw_full[r], 2 * kQ4A);
+                                bulk_load(rdst, A.q_gate + off, kQ4A, &S.raw_full[r], pol);
+                                bulk_load(rdst + kQ4A, A.q_up + off, kQ4A, &S.raw_full[r], pol);
+                            } else {
+                                const size_t off = (size_t)c * q4_mat_b + ((size_t)T.rb * (F / 64) + kblk) * kQ4B;
+                                mbar_arrive_expect_tx(&S.raw_full[r], kQ4B);
+                                bulk_load(rdst, A.q_down + off, kQ4B, &S.raw_full[r], pol);
+                            }
+                            rq.next(kRaw);
                         }
-                        rq.next(kRaw);
                         continue;
                     }
-                    mbar_arrive_expect_tx(&S.full[slot], kWBytes);
+                    mbar_arrive_expect_tx(&S.full[slot], KB * kWBytes);
                     if (!ph_a) {
                         // 128 W_down rows (rows past the expert's d are computed and dropped)
-                        tma_load_3d(dst, &tm_down, 0, row0, s, &S.full[slot], pol);
+                        tma_load_3d(dst, KB > 1 ? &tm_down4 : &tm_down, 0, row0, s * KB, &S.full[slot], pol);
                     } else if (A.gu_fused) {
                         // 8 row groups x {8 rows of the lower matrix, 8 rows of the other}
-                        tma_load_5d(dst, &tm_gu, 0, 0, 0, row0 / 8, s, &S.full[slot], pol);
-                    } else {
+                        tma_load_5d(dst, KB > 1 ? &tm_gu4 : &tm_gu, 0, 0, 0, row0 / 8, s * KB, &S.full[slot], pol);
+                    } else {   // KB = 1
 #pragma unroll 1
                         for (int g = 0; g < 8; ++g) {
                             tma_load_3d(dst + (2 * g) * 1024, &tm_gate, 0, row0 + 8 * g, s, &S.full[slot], pol);
@@ -448,6 +539,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         // ---------------------------- operand producer ---------------------------
         const uint64_t pol = l2_evict_last_policy();
         RingPos rp;
+        const int fast_ops = S.fast_ops;   // stages of the first tile already loaded by warp 4
+        for (int s = 0; s < fast_ops; ++s) rp.next(nst);
         bool gathered = small_b;
         for (int n = 0;; ++n) {
             const int q = n % kQ;
@@ -455,7 +548,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const int tile = S.tq[q];
             if (tile < 0) break;
             const bool ph_a = tile < TA;
-            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn, nmax);
+            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
             if (ph_a && !gathered) {   // every CTA has copied its rows of the grouped hidden states
                 for (int c = lane; c < (int)G; c += 32) wait_counter(&A.gflag[c], 1u, S, flags);
                 __syncwarp();
@@ -464,20 +557,23 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             }
             if (lane == 0) {
                 if (!ph_a) {   // every phase-A tile of this token chunk has written its h rows
-                    wait_counter(&A.hdone[S.chunk_off[T.a] + T.c], (uint32_t)rbA, S, flags);
+                    wait_counter(&A.hdone[X.chunk_off[T.a] + T.c], (uint32_t)rbA, S, flags);
                     fence_proxy_async_global();
                 }
-                const CUtensorMap* map = ph_a ? (small_b ? &tm_hid : &tm_x) : &tm_h;
+                // KB > 1 only for batches of up to 16 tokens: one 16-row box of KB
+                // blocks, which lands as KB consecutive [16 rows][64] operand blocks
+                const CUtensorMap* map = ph_a ? (small_b ? (KB > 1 ? &tm_hid4 : &tm_hid) : &tm_x)
+                                              : (KB > 1 ? &tm_h4 : &tm_h);
                 const int row = (ph_a && small_b) ? 0 : T.off + nmax * T.c;
                 const int nb = (ph_a && small_b) ? 1 : (T.ntok + 15) >> 4;   // 16-row boxes = MMA N / 16
                 const int ns = ph_a ? SA : SB;
-                for (int s = 0; s < ns; ++s, rp.next(nst)) {
+                for (int s = n == 0 ? fast_ops : 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
-                    mbar_arrive_expect_tx(&S.full[slot], nb * 2048);   // rows past the end read as zeros
-                    unsigned char* dst = ring + (size_t)slot * slot_bytes + kWBytes;
+                    mbar_arrive_expect_tx(&S.full[slot], nb * 2048 * KB);   // rows past the end read as zeros
+                    unsigned char* dst = ring + (size_t)slot * slot_bytes + KB * kWBytes;
                     for (int j = 0; j < nb; ++j)
-                        tma_load_3d(dst + j * 2048, map, 0, row + 16 * j, s, &S.full[slot], pol);
+                        tma_load_3d(dst + j * 2048, map, 0, row + 16 * j, s * KB, &S.full[slot], pol);
                 }
             }
             __syncwarp();
@@ -494,8 +590,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 const bool ph_a = tile < TA;
                 int ntile = 16;   // MMA N: batches of up to 16 always use 16 columns
                 if (!small_b) {
-                    const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn, nmax);
-                    ntile = (ph_a && small_b) ? 16 : (T.ntok + 15) & ~15;
+                    const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
+                    ntile = (T.ntok + 15) & ~15;
                 }
                 const uint32_t idesc = umma_idesc_bf16(kM, ntile);
                 const int ns = ph_a ? SA : SB;
@@ -510,11 +606,14 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     wait_bar(&S.full[slot], rp.phase, S, flags);
                     tmem_fence_after_sync();
                     const uint32_t a0 = smem_u32(ring + (size_t)slot * slot_bytes);
-                    const uint32_t b0 = a0 + kWBytes;
+                    const uint32_t b0 = a0 + KB * kWBytes;
+#pragma unroll 1
+                    for (int kb = 0; kb < KB; ++kb) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)   // K = 16 per step: 32 bytes along the swizzled row
-                        umma_bf16(dt, umma_sdesc_sw128(a0 + 32 * k), umma_sdesc_sw128(b0 + 32 * k), idesc,
-                                  (s | k) ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k)   // K = 16 per step: 32 bytes along the swizzled row
+                            umma_bf16(dt, umma_sdesc_sw128(a0 + kb * kWBytes + 32 * k),
+                                      umma_sdesc_sw128(b0 + kb * obytes + 32 * k), idesc, (s | kb | k) ? 1u : 0u);
+                    }
                     umma_commit(&S.empty[slot]);   // the stage is free once these MMAs are done
                 }
                 umma_commit(&S.acc_full[b]);
@@ -523,6 +622,24 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             wait_bar(&S.mma_done, 0, S, flags);
         }
         __syncwarp();
+    } else if (warp == kWarpN) {
+        // ----------------------------- count-down warp ----------------------------
+        // Each finished phase-B tile's tokens count down their counters for
+        // the tile's 128 rows of d.  The release (after the acquire of the
+        // epilogue warps' barrier) makes their y stores visible first.
+        for (uint32_t p = 0;; ++p) {
+            const int slot = (int)(p % kNQ);
+            wait_bar(&S.nt_full[slot], (p / kNQ) & 1, S, flags);
+            if (*(volatile int*)&S.abort_flag) break;
+            const int4 inf = S.nt_info[slot];
+            if (inf.y < 0) break;
+            for (int j = lane; j < inf.y; j += 32) {
+                const int tok = A.perm[inf.x + j] / A.kslots;
+                red_release_gpu_add(&A.ycnt[(size_t)tok * rbB + inf.z], 0xffffffffu);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.nt_empty[slot]);
+        }
     } else if (warp >= kWarpC) {
         // ----------------------------- INT4 converters ----------------------------
         // Each packed stage becomes the 128 x 64 bf16 A operand of one ring
@@ -540,8 +657,10 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             if (info == ~0u) break;
             const int slot = (int)(info & 255u);
             const bool ph_a = (info >> 8) & 1u;
+            const int kb = (int)((info >> 9) & 15u);
+            const bool last = (info >> 13) & 1u;
             const unsigned char* src = raw + (size_t)r * kRawBytes;
-            unsigned char* dstA = ring + (size_t)slot * slot_bytes;
+            unsigned char* dstA = ring + (size_t)slot * slot_bytes + kb * kWBytes;
 #pragma unroll
             for (int it = 0; it < 1024 / (kConvWarps * 32); ++it) {   // 128 rows x 8 units
                 const int k = it * (kConvWarps * 32) + ct;
@@ -557,8 +676,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             fence_proxy_async_shared();   // the tensor core reads the stage through the async proxy
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.raw_empty[r]);   // this warp has read the packed chunk
-            conv_sync(S, nsync, flags, lane);              // all four warps have written their rows
-            if (ct == 0) mbar_arrive(&S.full[slot]);       // in place of the weight warp
+            conv_sync(S, nsync, flags, lane);              // all the converter warps have written their rows
+            if (ct == 0 && last) mbar_arrive(&S.full[slot]);   // in place of the weight warp
             rq.next(kRaw);
         }
     } else {
@@ -603,14 +722,24 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
         const int i = 32 * warp + lane;                    // this thread's D row (tensor-memory lane)
         const uint32_t lane_addr = (uint32_t)(32 * warp) << 16;
-        uint32_t na = 0;   // phase-A tiles so far (parity of h_written)
+        uint32_t nm = 0;   // meetings of the four warps so far (parity of epi_bar)
+        uint32_t np = 0;   // phase-B tiles handed to warp 15
+        // hands a finished phase-B tile (or the end, ntok = -1) to warp 15
+        auto hand_over = [&](int pair0, int ntok, int rb) {
+            const int slot = (int)(np % kNQ);
+            if (np >= kNQ) wait_bar(&S.nt_empty[slot], ((np / kNQ) - 1) & 1, S, flags);
+            if (tid == 0) S.nt_info[slot] = make_int4(pair0, ntok, rb, 0);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.nt_full[slot]);
+            ++np;
+        };
         for (int n = 0;; ++n) {
             const int q = n % kQ;
             wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
             const int tile = S.tq[q];
             if (tile < 0) break;
             const bool ph_a = tile < TA;
-            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, S, Tn, nmax);
+            const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
             const int b = n % kAcc;
             const int ngroups = (ph_a && small_b) ? 1 : (T.ntok + 15) >> 4;   // 16-column groups of D
             wait_bar(&S.acc_full[b], (n / kAcc) & 1, S, flags);
@@ -621,8 +750,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 // the partner row is 8 lanes away in the same warp.
                 const int m = (i >> 3) & 1;
                 const int frow = 64 * T.rb + 8 * (i >> 4) + (i & 7);
-                const uint32_t tmask = small_b ? S.tokmask[T.a] : 0u;
-                const bool swap = A.gu_swap && S.ex_slot[T.a] >= 0;   // INT4 stages hold the gate rows first
+                const uint32_t tmask = small_b ? X.tokmask[T.a] : 0u;
+                const bool swap = A.gu_swap && X.ex_slot[T.a] >= 0;   // INT4 stages hold the gate rows first
                 for (int cg = 0; cg < ngroups; ++cg) {
                     float v[16];
                     tmem_ld16(tmem + lane_addr + (uint32_t)(b * acc_stride + 16 * cg), v);
@@ -646,16 +775,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                         }
                     }
                 }
-                __syncwarp();
-                // All four warps wait for the barrier's phase, so no warp can
-                // arrive for the next phase-A tile before this one completes.
-                if (lane == 0) mbar_arrive(&S.h_written);
-                wait_bar(&S.h_written, na & 1, S, flags);
-                if (tid == 0) {   // all four warps have stored: release the chunk's counter
-                    __threadfence();
-                    atomicAdd(&A.hdone[S.chunk_off[T.a] + T.c], 1u);
-                }
-                ++na;
+                // All four warps wait for each meeting's phase, so no warp can
+                // arrive for the next meeting before this one completes.
+                epi_meet(S, nm, flags, lane);
+                if (tid == 0)   // all four warps have stored: release the chunk's counter
+                    red_release_gpu_add(&A.hdone[X.chunk_off[T.a] + T.c], 1u);
             } else {
                 const int row = kM * T.rb + i;
                 for (int cg = 0; cg < ngroups; ++cg) {
@@ -674,70 +798,76 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                         }
                     }
                 }
+                // the tile's y rows are stored: warp 15 counts its tokens down
+                hand_over(T.off + nmax * T.c, T.ntok, T.rb);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.tq_empty[q]);
         }
+        hand_over(0, -1, 0);   // no more tiles
     }
 
-    // ---- every CTA arrives after its last tile; then the combine ----
-    // This thread's first output of the combine: its slots' pair positions
-    // and weights (routing results) are loaded before the grid barrier.
-    const int d4 = d / 4;
-    const long long ctotal = (long long)A.B * d4;
-    const long long co0 = ctotal * blockIdx.x / G, co1 = ctotal * (blockIdx.x + 1) / G;
-    int pf_pos[8];
-    float pf_w[8];
-    if (co0 + (long long)threadIdx.x < co1) {
-        const int i0 = (int)((co0 + threadIdx.x) / d4);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            pf_pos[u] = u < A.kslots ? A.pos_of[i0 * A.kslots + u] : -1;
-            pf_w[u] = pf_pos[u] >= 0 ? A.w[i0 * A.kslots + u] : 0.f;
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(&A.hdr->b_done, 1u);
-        wait_counter(&A.hdr->b_done, G, S, flags);
-        __threadfence();
-    }
-    __syncthreads();
+    // ---- combine: one warp per (token, 128 rows of d) ----
+    // Item it goes to CTA it mod G; the idle INT4 converter warps take the
+    // first items of a CTA, the epilogue warps the last.  The warp waits
+    // until every y slice of its rows is stored (the counter is zero,
+    // acquire), sums the kept weights times the y rows in slot order, and
+    // sets the counter back to the token's kept slots for the next launch.
+    // Tokens that keep no expert find zero at once and get rows of zeros.
     {
+        // converters 0-7, producers and MMA 8-10, count-down warp 11, epilogue 12-15
+        const int widx = warp == kWarpN ? kConvWarps + 3
+                       : warp >= kWarpC ? warp - kWarpC
+                       : warp >= kWarpW ? kConvWarps + warp - kWarpW : kConvWarps + 4 + warp;
+        const int nitems = A.B * rbB;
+        const int ks = A.kslots;
         const float4* y4 = reinterpret_cast<const float4*>(A.ybuf);
-        uint2* out = static_cast<uint2*>(A.out);
-        bool first = true;
-        for (long long o = co0 + threadIdx.x; o < co1; o += kThreads, first = false) {
-            const int i = (int)(o / d4), c4 = (int)(o - (long long)i * d4);
+        uint2* out2 = static_cast<uint2*>(A.out);
+        for (int it = (int)blockIdx.x + (int)G * widx; it < nitems; it += (int)G * (kThreads / 32)) {
+            const int tok = it / rbB, r0 = (it - tok * rbB) * kM + 4 * lane;
+            uint32_t* c = &A.ycnt[it];
+            // the first eight slots' positions and weights (routing results) before the wait
+            int pos0[8];
+            float wv0[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                pos0[u] = u < ks ? A.pos_of[tok * ks + u] : -1;
+                wv0[u] = u < ks ? A.w[tok * ks + u] : 0.f;
+            }
+            if (lane == 0) wait_zero(c, S, flags);
+            __syncwarp();
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s0 = 0; s0 < A.kslots; s0 += 8) {
-                float4 yv[8];
+            for (int s0 = 0; s0 < ks; s0 += 8) {
+                int pos[8];
                 float wv[8];
+                float4 yv[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int sl = s0 + u;
-                    int pos;
-                    if (first && s0 == 0) {
-                        pos = pf_pos[u];
-                        wv[u] = pf_w[u];
-                    } else {
-                        pos = sl < A.kslots ? A.pos_of[i * A.kslots + sl] : -1;
-                        wv[u] = pos >= 0 ? A.w[i * A.kslots + sl] : 0.f;
-                    }
-                    yv[u] = pos >= 0 ? __ldcg(y4 + (size_t)pos * d4 + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    pos[u] = s0 == 0 ? pos0[u] : sl < ks ? A.pos_of[tok * ks + sl] : -1;
+                    wv[u] = s0 == 0 ? wv0[u] : sl < ks ? A.w[tok * ks + sl] : 0.f;
                 }
 #pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    yv[u] = (pos[u] >= 0 && r0 < d) ? __ldcg(y4 + ((size_t)pos[u] * d + r0) / 4)
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
                 for (int u = 0; u < 8; ++u) {   // slot order
-                    acc.x += wv[u] * yv[u].x;
-                    acc.y += wv[u] * yv[u].y;
-                    acc.z += wv[u] * yv[u].z;
-                    acc.w += wv[u] * yv[u].w;
+                    const float wu = pos[u] >= 0 ? wv[u] : 0.f;
+                    acc.x += wu * yv[u].x;
+                    acc.y += wu * yv[u].y;
+                    acc.z += wu * yv[u].z;
+                    acc.w += wu * yv[u].w;
                 }
             }
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-            out[o] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+            if (r0 < d) {
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                out2[((size_t)tok * d + r0) / 4] =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+            }
+            __syncwarp();
+            if (lane == 0) *c = (uint32_t)A.nused[tok];
         }
     }
 
@@ -757,32 +887,46 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     if (S.last_flag) {
         __threadfence();
         for (int k = threadIdx.x; k < (int)G; k += kThreads) A.gflag[k] = 0;
-        for (int k = threadIdx.x; k < S.chunk_off[Tn]; k += kThreads) A.hdone[k] = 0;
+        for (int k = threadIdx.x; k < X.chunk_off[Tn]; k += kThreads) A.hdone[k] = 0;
     }
     if (S.last_flag && threadIdx.x == 0) {
         A.hdr->next_tile = 0;
-        A.hdr->b_done = 0;
         A.hdr->ctas_done = 0;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(ffn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
+cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_sms, cudaStream_t s) {
+    // All the shared memory a CTA may have: the stage ring takes what the
+    // barriers, the per-expert tables and the INT4 slots leave.
+    static int smem_optin[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!smem_optin[dev]) {
+        int v = 0;
+        if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+        if ((e = cudaFuncSetAttribute(ffn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, v)) != cudaSuccess)
+            return e;
+        smem_optin[dev] = v;
     }
+    FfnArgs a = a_in;
+    a.smem_bytes = smem_optin[dev];
+    // the ring must hold two stages of the largest slot this launch can use
+    const int kb = (a.B <= 16 && a.gu_fused) ? a.kbs : 1;
+    const size_t slot = a.B <= 16 ? (size_t)kb * (kWBytes + 16 * 128) : (size_t)kWBytes + kNMax * 128;
+    if ((size_t)a.smem_bytes < 4096 + tabs_bytes(a.N) + (size_t)kRaw * kRawBytes ||
+        ring_bytes_for((size_t)a.smem_bytes, a.N, a.n_cold > 0) < 2 * slot)
+        return cudaErrorInvalidConfiguration;
     // One CTA per SM (the shared-memory size allows no second one, so the
     // tensor memory is never contended); programmatic dependent launch lets
     // the CTAs allocate and prefetch while the routing kernel finishes.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = (size_t)a.smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -790,7 +934,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap* maps, int num_sms
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, ffn_tc_kernel, a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                              maps[6]);
+                              maps[6], maps[7], maps[8], maps[9], maps[10]);
 }
 
 }  // namespace moe

@@ -10,6 +10,8 @@
 //   sections 4-5  maxP (rank depth of phase 2) and k^max (experts per token).
 //   section 4     per-expert loads cnt_e, T = number of experts with cnt_e > 0.
 //   section 7     padding tokens select nothing.
+// Each token's kept-slot count also seeds one counter per 128 rows of d,
+// which the expert kernel counts down as the token's y slices are written.
 // Ranking: larger score first, equal scores by the lower expert id.
 //
 // One warp handles one token at a time; lane l holds experts l, l+32, ...
@@ -97,6 +99,8 @@ __device__ __forceinline__ void finish_token(const RouteArgs& a, RouteSmem& sm, 
     const float l0 = __shfl_sync(kFull, myval, 0);
     const float ex = lane < cnt ? expf(myval - l0) : 0.f;
     const float z = warp_sum(ex);
+    if (lane == 0) a.nused[i] = cnt;
+    for (int r = lane; r < a.rbd; r += 32) a.ycnt[(size_t)i * a.rbd + r] = (uint32_t)cnt;
     if (lane < a.kslots) {
         const size_t q = (size_t)i * a.kslots + lane;
         const bool used = lane < cnt;

@@ -169,9 +169,11 @@ moe_status moe_route(const void *hidden, const void *w_router, const float *rout
 /*
  * Expert FFN + weighted combine (steps 4-5) for a batch routed by
  * moe_route() with the same params and the same workspace: besides the
- * routing outputs it reads the per-pair positions and per-expert records
- * that moe_route left in the workspace, so no other call may use that
- * workspace in between.  Reads only activated experts, each expert's three
+ * routing outputs it reads the per-pair positions, per-expert records and
+ * per-(token, 128 rows of d) combine counters that moe_route left in the
+ * workspace, so no other call may use that workspace in between.  A
+ * completed call leaves them as it found them, so it may be repeated on the
+ * same routing.  Reads only activated experts, each expert's three
  * matrices once from HBM.
  *   hidden  [B][d]        dtype  the hidden states given to moe_route.
  *   w_gate  [N][d_ff][d]  dtype  expert gate projections.

@@ -87,6 +87,24 @@ def test_mixed_layer_parity(mode, k0, p, B):
     assert np.abs(ref - ref_bf16).max() > 1e-3 * np.abs(ref_bf16).max()
 
 
+@pytest.mark.parametrize("d,F,B", [(512, 256, 8), (384, 128, 16), (512, 256, 1), (256, 384, 5)])
+def test_mixed_small_batches(d, F, B):
+    # Batches of up to 16 tokens: INT4 stages of 4, 2 or 1 column blocks,
+    # each block converted from its own packed chunk.
+    w = synth.Workload("t_mixed_small", N=32, k=4, d=d, F=F, B=B, seed=d + F + B, zipf=True)
+    L = synth.make_layer(w, 0, B)
+    hot = [1, 2, 5, 8, 13, 21, 30]
+    hot_w, mixed, eff = build_mixed(w, L, hot)
+    D = gu.device_inputs(L, True)
+    prm = gu.params_for(w, B, OEA, 3, 1.0)
+    r, out = run_mixed(w, L, D, hot_w, mixed, prm)
+    g = gu.to_np(r)
+    gu.check_routing(g, prm, B)
+    ref = oracle.moe_experts(L["x"], eff["w_gate"], eff["w_up"], eff["w_down"], g["expert_idx"],
+                             g["weights"].astype(np.float64))
+    gu.check_output(out, ref, True)
+
+
 def test_bad_slot_is_flagged():
     w = synth.Workload("t_mixed_bad", N=16, k=2, d=256, F=256, B=8, seed=3)
     L = synth.make_layer(w, 0, 8)

@@ -100,6 +100,18 @@ def test_bf16_shapes(N, k, d, F):
     run_case(w, 29, TOPK)
 
 
+@pytest.mark.parametrize("N,k,d,F", [(32, 4, 320, 192), (64, 8, 384, 128), (128, 8, 512, 256),
+                                     (16, 4, 256, 768)])
+@pytest.mark.parametrize("B", [1, 6, 16])
+def test_small_batch_stage_widths(N, k, d, F, B):
+    # Batches of up to 16 tokens stream 1, 2 or 4 column blocks per stage
+    # (the most that divides both d / 64 and d_ff / 64): every width, a
+    # single token, a partial and a full batch.
+    w = W("t_widths", N=N, k=k, d=d, F=F, seed=d + F + B)
+    run_case(w, B, OEA, max(1, k // 2), 1.0)
+    run_case(w, B, TOPK)
+
+
 @pytest.mark.parametrize("maxP,kmax", [(6, 8), (12, 8), (128, 11), (10, 10), (3, 5)])
 def test_general_oea_knobs(maxP, kmax):
     w = W("t_knobs", seed=21)
