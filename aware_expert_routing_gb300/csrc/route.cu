@@ -1,5 +1,5 @@
 // route.cu -- per-token expert selection (plain top-k or OEA) and grouping of
-// the (token, slot) pairs by expert, in one CTA.
+// the (token, slot) pairs by expert, in one thread-block cluster.
 //
 // Page "Opportunistic Expert Activation (OEA)":
 //   section 2 Q2  phase 1: n_i = min(k0, t_i), t_i the adaptive top-p count;
@@ -14,16 +14,20 @@
 // which the expert kernel counts down as the token's y slices are written.
 // Ranking: larger score first, equal scores by the lower expert id.
 //
-// One warp handles one token at a time; lane l holds experts l, l+32, ...
-// as order-preserving 32-bit keys of their fp32 scores (the map is a
-// bijection, so a key gives back its exact score).  The next-ranked expert is
-// one warp max-reduction of the keys and one min-reduction of the ids that
-// hold the maximum.  The batch union S_base is an N-bit mask in shared
-// memory built with __ballot_sync + atomicOr.  Grouping by expert: every
-// kept (token, expert) sets bit (token mod 32) of word [token / 32][expert];
-// the warps, 32 experts each, turn those words into per-expert counts,
-// offsets and per-chunk prefix counts, which give each pair's position
-// directly (tokens ascending within an expert).
+// CTA r of the cluster (one CTA per 32 tokens, up to 8) handles tokens
+// 32r..32r+31, one warp per token (two with 512 threads).  Lane l holds
+// experts l, l+32, ... as order-preserving 32-bit keys of their fp32 scores
+// (the map is a bijection, so a key gives back its exact score).  The
+// next-ranked expert is one warp max-reduction of the keys and one
+// min-reduction of the ids that hold the maximum.  Each CTA builds the union
+// of its tokens' baselines as an N-bit mask in shared memory (__ballot_sync +
+// atomicOr); after a cluster barrier every CTA ORs the masks of all CTAs
+// (distributed shared memory) into S_base.  Grouping by expert: every kept
+// (token, expert) sets bit (token mod 32) of the CTA's word [expert]; after a
+// second cluster barrier every CTA reads all CTAs' words, and its warps, 32
+// experts each, turn them into per-expert counts, offsets and the pairs of
+// earlier CTAs, which give each pair's position directly (tokens ascending
+// within an expert).  CTA 0 writes the per-expert arrays.
 #include <limits.h>
 
 #include "common.cuh"
@@ -33,7 +37,8 @@ namespace moe {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kMaxChunks = MOE_MAX_TOKENS / 32;
+constexpr int kMaxCtas = MOE_MAX_TOKENS / 32;   // cluster size for the largest batch
+static_assert(kMaxCtas <= 8, "a portable cluster holds at most 8 CTAs");
 
 // Order-preserving key of a finite fp32 score (-0 and +0 map to one key);
 // 0 is below every score and marks "not selectable".
@@ -83,19 +88,28 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+__device__ __forceinline__ uint32_t ld_dsmem_u32(const uint32_t* local, uint32_t rank) {
+    uint32_t raddr, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(raddr) : "memory");
+    return v;
+}
+
 struct RouteSmem {
-    uint32_t* sbase;   // [32]          S_base bit mask
-    int* snb;          // [B]           n_i
-    int* sidx;         // [B][kslots]   kept experts
-    uint32_t* bits;    // [chunks][N]   bit (i mod 32) set if token i keeps expert e
-    int* pre;          // [chunks][N]   tokens of earlier chunks that keep e
-    int* soff;         // [N]           first pair of expert e
+    uint32_t* sbase;   // [32]          union of this CTA's tokens' baselines
+    uint32_t* sball;   // [32]          S_base: union over the cluster
     uint32_t* btot;    // [32]          packed totals of 32-expert blocks
+    int* snb;          // [32]          n_i of this CTA's tokens
+    int* soff;         // [N]           first pair of expert e
+    int* pre;          // [N]           pairs of expert e of earlier CTAs' tokens
+    uint32_t* bits;    // [N]           bit il set if this CTA's token il keeps expert e
+    int* sidx;         // [32][kslots]  kept experts of this CTA's tokens
 };
 
-// Writes the routing of token i: lane r < cnt holds slot r (myid, myval).
-__device__ __forceinline__ void finish_token(const RouteArgs& a, RouteSmem& sm, int i, int lane, int cnt,
-                                             int myid, float myval, int N) {
+// Writes the routing of token i (this CTA's token il): lane r < cnt holds
+// slot r (myid, myval).
+__device__ __forceinline__ void finish_token(const RouteArgs& a, RouteSmem& sm, int i, int il, int lane, int cnt,
+                                             int myid, float myval) {
     const float l0 = __shfl_sync(kFull, myval, 0);
     const float ex = lane < cnt ? expf(myval - l0) : 0.f;
     const float z = warp_sum(ex);
@@ -106,8 +120,8 @@ __device__ __forceinline__ void finish_token(const RouteArgs& a, RouteSmem& sm, 
         const bool used = lane < cnt;
         a.idx[q] = used ? myid : -1;
         a.w[q] = used ? ex / z : 0.f;
-        sm.sidx[q] = used ? myid : -1;
-        if (used) atomicOr(&sm.bits[(i >> 5) * N + myid], 1u << (i & 31));
+        sm.sidx[il * a.kslots + lane] = used ? myid : -1;
+        if (used) atomicOr(&sm.bits[myid], 1u << il);
         else a.pos_of[q] = -1;
     }
 }
@@ -119,27 +133,32 @@ __global__ void route_kernel(RouteArgs a) {
     const int nwarps = nthreads >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = a.N, B = a.B;
-    const int nch = (B + 31) >> 5;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t ncta = gridDim.x;                 // the whole grid is one cluster
+    const int tb = 32 * (int)rank;                   // this CTA's tokens: [tb, te)
+    const int te = min(B, tb + 32);
+    const int bv = min(te, max(tb, a.B_valid));      // valid tokens of this CTA: [tb, bv)
 
     RouteSmem sm;
     unsigned char* p = smem_raw;
     sm.sbase = reinterpret_cast<uint32_t*>(p); p += 32 * 4;
+    sm.sball = reinterpret_cast<uint32_t*>(p); p += 32 * 4;
     sm.btot = reinterpret_cast<uint32_t*>(p); p += 32 * 4;
-    sm.snb = reinterpret_cast<int*>(p); p += MOE_MAX_TOKENS * 4;
-    sm.soff = reinterpret_cast<int*>(p); p += MOE_MAX_EXPERTS * 4;
-    sm.sidx = reinterpret_cast<int*>(p); p += (size_t)B * a.kslots * 4;
-    sm.bits = reinterpret_cast<uint32_t*>(p); p += (size_t)nch * N * 4;
-    sm.pre = reinterpret_cast<int*>(p);
+    sm.snb = reinterpret_cast<int*>(p); p += 32 * 4;
+    sm.soff = reinterpret_cast<int*>(p); p += (size_t)N * 4;
+    sm.pre = reinterpret_cast<int*>(p); p += (size_t)N * 4;
+    sm.bits = reinterpret_cast<uint32_t*>(p); p += (size_t)N * 4;
+    sm.sidx = reinterpret_cast<int*>(p);
 
     if (threadIdx.x < 32) sm.sbase[threadIdx.x] = 0;
-    for (int q = threadIdx.x; q < nch * N; q += nthreads) sm.bits[q] = 0;
+    for (int q = threadIdx.x; q < N; q += nthreads) sm.bits[q] = 0;
     grid_launch_dependents();    // the expert kernel may start its prologue
     grid_dependency_wait();      // scores come from the router kernel
     __syncthreads();
 
     bool nonfinite = false;
     const bool oea = a.mode == MOE_MODE_OEA;
-    const bool keep_keys = B <= nwarps;   // one token per warp: keys and picks stay in registers
+    const bool keep_keys = te - tb <= nwarps;   // one token per warp: keys and picks stay in registers
     uint32_t kv[NPL];
     // Phase-1 picks of this warp's token (used by phase 2 when keep_keys).
     uint32_t taken1 = 0;
@@ -147,14 +166,15 @@ __global__ void route_kernel(RouteArgs a) {
     float myval1 = 0.f;
 
     // ---- plain top-k, or OEA phase 1 (baseline and union) ------------------
-    for (int i = warp; i < B; i += nwarps) {
+    for (int i = tb + warp; i < te; i += nwarps) {
+        const int il = i - tb;
         load_keys<NPL>(a.logits + (size_t)i * N, N, lane, kv, nonfinite);
         if (i >= a.B_valid) {           // padding token: selects nothing
             if (lane == 0) {
-                sm.snb[i] = 0;
+                sm.snb[il] = 0;
                 if (a.n_base) a.n_base[i] = 0;
             }
-            if (!oea) finish_token(a, sm, i, lane, 0, -1, 0.f, N);
+            if (!oea) finish_token(a, sm, i, il, lane, 0, -1, 0.f);
             continue;
         }
         uint32_t taken = 0;
@@ -170,7 +190,7 @@ __global__ void route_kernel(RouteArgs a) {
                 n = r + 1;
             }
             if (lane == 0 && a.n_base) a.n_base[i] = n;
-            finish_token(a, sm, i, lane, n, myid, myval, N);
+            finish_token(a, sm, i, il, lane, n, myid, myval);
             continue;
         }
         // Phase 1: top-n_i in rank order; with top-p on, the softmax over all
@@ -205,23 +225,35 @@ __global__ void route_kernel(RouteArgs a) {
             if (lane == 0 && word) atomicOr(&sm.sbase[j], word);
         }
         if (lane == 0) {
-            sm.snb[i] = n;
+            sm.snb[il] = n;
             if (a.n_base) a.n_base[i] = n;
         }
         taken1 = taken; n1 = n; myid1 = myid; myval1 = myval;
     }
-    __syncthreads();
 
     // ---- OEA phase 2: piggyback inside S_base -------------------------------
     // The baseline (the token's top-n_i) lies inside S_base and heads both the
     // in-union list and the walked list, so with the phase-1 picks still in
     // registers the selection resumes at rank n_i.
     if (oea) {
+        const uint32_t* sb = sm.sbase;   // S_base
+        if (ncta > 1) {
+            cluster_sync();   // every CTA's union is complete
+            if (threadIdx.x < 32) {
+                uint32_t w = 0;
+                for (uint32_t r = 0; r < ncta; ++r)
+                    w |= r == rank ? sm.sbase[threadIdx.x] : ld_dsmem_u32(&sm.sbase[threadIdx.x], r);
+                sm.sball[threadIdx.x] = w;
+            }
+            sb = sm.sball;
+        }
+        __syncthreads();
         uint32_t notin = 0;
 #pragma unroll
         for (int j = 0; j < NPL; ++j)
-            if (!((sm.sbase[j] >> lane) & 1u)) notin |= 1u << j;
-        for (int i = warp; i < a.B_valid; i += nwarps) {
+            if (!((sb[j] >> lane) & 1u)) notin |= 1u << j;
+        for (int i = tb + warp; i < bv; i += nwarps) {
+            const int il = i - tb;
             uint32_t taken = 0;
             int cnt = 0, myid = -1, r0 = 0;
             float myval = 0.f;
@@ -243,33 +275,35 @@ __global__ void route_kernel(RouteArgs a) {
                 }
             } else {
                 // walk the ranked list to depth max(maxP, n_i)
-                const int nb = sm.snb[i];
+                const int nb = sm.snb[il];
                 const int depth = a.maxP > nb ? a.maxP : nb;
                 for (int r = r0; r < depth && cnt < a.kmax; ++r) {
                     int id;
                     const uint32_t m = warp_best<NPL>(kv, taken, lane, id);
                     if (m == 0) break;
                     if ((id & 31) == lane) taken |= 1u << (id >> 5);
-                    const bool in_union = (sm.sbase[id >> 5] >> (id & 31)) & 1u;
+                    const bool in_union = (sb[id >> 5] >> (id & 31)) & 1u;
                     if (r < nb || in_union) {
                         if (lane == cnt) { myid = id; myval = key_score(m); }
                         ++cnt;
                     }
                 }
             }
-            finish_token(a, sm, i, lane, cnt, myid, myval, N);
+            finish_token(a, sm, i, il, lane, cnt, myid, myval);
         }
-        for (int i = a.B_valid + warp; i < B; i += nwarps) finish_token(a, sm, i, lane, 0, -1, 0.f, N);
+        for (int i = bv + warp; i < te; i += nwarps) finish_token(a, sm, i, i - tb, lane, 0, -1, 0.f);
     }
     if (__any_sync(kFull, nonfinite) && lane == 0) raise_flag(a.flags, kFlagNonFinite);
-    __syncthreads();
+    if (ncta > 1) cluster_sync(); else __syncthreads();   // every CTA's (token, expert) words are complete
 
     // ---- counts, offsets, active list and per-expert info ---------------------
-    // Warp w scans expert blocks w, w + nwarps, ... (32 experts each) with one
-    // packed inclusive scan of (count | active << 26); the block totals meet in
-    // shared memory and each warp then adds the totals of the blocks before
-    // its own.  A block's count is at most B * kslots < 2^26 and its active
-    // count at most 32, so the packed sum never carries across fields.
+    // Warp w scans expert blocks w, w + nwarps, ... (32 experts each): per
+    // expert the pairs of every CTA (its words, read across the cluster) and
+    // of the CTAs before this one, then one packed inclusive scan of
+    // (count | active << 26) across the block; the block totals meet in
+    // shared memory and each warp adds the totals of the blocks before its
+    // own.  A block's count is at most B * kslots < 2^26 and its active count
+    // at most 32, so the packed sum never carries across fields.
     constexpr int kBlkPerWarp = NPL <= 16 ? 1 : 2;   // 32 (or 16) warps cover N / 32 blocks
     const int nblk = (N + 31) >> 5;
     int cnt_r[kBlkPerWarp];
@@ -282,11 +316,17 @@ __global__ void route_kernel(RouteArgs a) {
         if (b < nblk) {
             const int e = (b << 5) + lane;
             int c = 0;
-            if (e < N)
-                for (int ch = 0; ch < nch; ++ch) {
-                    sm.pre[ch * N + e] = c;
-                    c += __popc(sm.bits[ch * N + e]);
+            if (e < N) {
+                uint32_t w[kMaxCtas];
+#pragma unroll
+                for (int r = 0; r < kMaxCtas; ++r)
+                    w[r] = r < (int)ncta ? (r == (int)rank ? sm.bits[e] : ld_dsmem_u32(&sm.bits[e], r)) : 0u;
+#pragma unroll
+                for (int r = 0; r < kMaxCtas; ++r) {
+                    if (r == (int)rank) sm.pre[e] = c;
+                    c += __popc(w[r]);
                 }
+            }
             uint32_t v = (uint32_t)c | ((uint32_t)(c > 0) << 26);
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -303,6 +343,7 @@ __global__ void route_kernel(RouteArgs a) {
         // totals of all blocks (for T and offsets[N]) and of the blocks before each of ours
         const uint32_t tv = lane < nblk ? sm.btot[lane] : 0u;
         const int tc = (int)(tv & ((1u << 26) - 1)), ta = (int)(tv >> 26);
+        const bool writer = rank == 0;
 #pragma unroll
         for (int u = 0; u < kBlkPerWarp; ++u) {
             const int b = warp + u * nwarps;
@@ -315,65 +356,66 @@ __global__ void route_kernel(RouteArgs a) {
             const int ex2 = base2 + (int)(inc_r[u] >> 26) - act;
             if (e < N) {
                 sm.soff[e] = ex1;
-                a.counts[e] = c;
-                a.offsets[e] = ex1;
-                if (act) {
-                    a.active[ex2] = e;
-                    a.exinfo[ex2] = (uint32_t)e | ((uint32_t)c << 10) | ((uint32_t)ex1 << 19);
-                    a.exinfo[N + ex2] = B <= 32 ? sm.bits[e] : 0u;
+                if (writer) {
+                    a.counts[e] = c;
+                    a.offsets[e] = ex1;
+                    if (act) {
+                        a.active[ex2] = e;
+                        a.exinfo[ex2] = (uint32_t)e | ((uint32_t)c << 10) | ((uint32_t)ex1 << 19);
+                        a.exinfo[N + ex2] = B <= 32 ? sm.bits[e] : 0u;   // one CTA: its words are all tokens'
+                    }
                 }
             }
         }
         const int total = __reduce_add_sync(kFull, tc);
         const int T = __reduce_add_sync(kFull, ta);
-        if (threadIdx.x == 0) {
-            a.offsets[N] = total;
-            *a.T = T;
-        }
-        for (int q = T + threadIdx.x; q < N; q += nthreads) {
-            a.active[q] = -1;
-            a.exinfo[q] = 0;
-            a.exinfo[N + q] = 0;
+        if (writer) {
+            if (threadIdx.x == 0) {
+                a.offsets[N] = total;
+                *a.T = T;
+            }
+            for (int q = T + threadIdx.x; q < N; q += nthreads) {
+                a.active[q] = -1;
+                a.exinfo[q] = 0;
+                a.exinfo[N + q] = 0;
+            }
         }
     }
     __syncthreads();
 
     // ---- positions: pairs grouped by expert, tokens ascending -----------------
-    for (int q = threadIdx.x; q < B * a.kslots; q += nthreads) {
+    for (int q = threadIdx.x; q < (te - tb) * a.kslots; q += nthreads) {
         const int e = sm.sidx[q];
         if (e < 0) continue;
-        const int i = q / a.kslots;
-        const int ch = i >> 5;
-        const int pos = sm.soff[e] + sm.pre[ch * N + e] + __popc(sm.bits[ch * N + e] & ((1u << (i & 31)) - 1u));
-        a.perm[pos] = q;
-        a.pos_of[q] = pos;
+        const int il = q / a.kslots;
+        const int pos = sm.soff[e] + sm.pre[e] + __popc(sm.bits[e] & ((1u << il) - 1u));
+        const int qg = tb * a.kslots + q;
+        a.perm[pos] = qg;
+        a.pos_of[qg] = pos;
     }
+    if (ncta > 1) cluster_sync();   // no CTA leaves while another may still read its words
 }
 
 template <int NPL>
 cudaError_t launch_route_t(const RouteArgs& a, cudaStream_t s) {
     const int threads = NPL <= 8 ? 1024 : 512;
-    const int nch = (a.B + 31) / 32;
-    const size_t smem = 2 * 32 * 4 + MOE_MAX_TOKENS * 4 + MOE_MAX_EXPERTS * 4 +
-                        (size_t)a.B * a.kslots * 4 + 2 * (size_t)nch * a.N * 4;
-    static bool attr_set = false;
-    if (!attr_set) {
-        const int max_smem = 2 * 32 * 4 + MOE_MAX_TOKENS * 4 + MOE_MAX_EXPERTS * 4 +
-                             MOE_MAX_TOKENS * MOE_MAX_SLOTS * 4 + 2 * kMaxChunks * MOE_MAX_EXPERTS * 4;
-        cudaError_t e = cudaFuncSetAttribute(route_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    const int ncta = a.B > 0 ? (a.B + 31) / 32 : 1;
+    const size_t smem = 4 * 32 * 4 + 3 * (size_t)a.N * 4 + 32 * (size_t)a.kslots * 4;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1);
+    cfg.gridDim = dim3(ncta);
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // batches of up to 32 tokens: one CTA, launched without a cluster
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = ncta;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = ncta > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, route_kernel<NPL>, a);
 }
 

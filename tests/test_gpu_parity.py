@@ -100,6 +100,16 @@ def test_bf16_shapes(N, k, d, F):
     run_case(w, 29, TOPK)
 
 
+@pytest.mark.parametrize("N", [128, 1024])
+@pytest.mark.parametrize("maxP,p", [(0, 1.0), (5, 0.8)])
+def test_route_full_cluster(N, maxP, p):
+    # The largest batch: eight CTAs of 32 tokens (one or two per warp),
+    # S_base and the per-expert counts gathered across all of them.
+    w = W("t_cluster", N=N, k=8, d=128, F=64, seed=N + maxP, zipf=True)
+    run_case(w, 256, OEA, 3, p, maxP=maxP, kmax=10, B_valid=250)
+    run_case(w, 256, TOPK)
+
+
 @pytest.mark.parametrize("N,k,d,F", [(32, 4, 320, 192), (64, 8, 384, 128), (128, 8, 512, 256),
                                      (16, 4, 256, 768)])
 @pytest.mark.parametrize("B", [1, 6, 16])
