@@ -346,7 +346,6 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone);
     a.nused = reinterpret_cast<const int32_t*>(ws + L.nused);
     a.ycnt = reinterpret_cast<uint32_t*>(ws + L.ycnt);
-    a.gflag = reinterpret_cast<uint32_t*>(ws + L.gflag);
     a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
     a.w_gate = w_gate;
     a.w_up = w_up;

@@ -25,12 +25,12 @@ struct WsHeader {
     uint32_t ctas_done;    // expert kernel: CTAs finished (the last one resets the counters)
     uint32_t next_tile;    // expert kernel: tiles claimed beyond each CTA's first
     uint32_t unused0;
-    uint32_t b_done;       // expert kernel: CTAs that finished all their tiles (y written)
+    uint32_t gathered;     // expert kernel: CTAs that copied their rows of the grouped hidden states
     uint32_t pad[59];
 };
 
 struct WsLayout {
-    size_t header, hdone, gflag, exinfo, pos_of, nused, ycnt, logits, hbuf, ybuf, xperm, total;
+    size_t header, hdone, exinfo, pos_of, nused, ycnt, logits, hbuf, ybuf, xperm, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -44,7 +44,6 @@ inline WsLayout ws_layout(int B, int N, int d, int kslots, int F, int h_elt) {
     size_t o = 0;
     L.header = o; o += align256(sizeof(WsHeader));
     L.hdone = o;  o += align256(sizeof(uint32_t) * (N + (size_t)B * kslots / 16 + 1));   // per token chunk
-    L.gflag = o;  o += align256(sizeof(uint32_t) * kMaxGrid);
     L.exinfo = o; o += align256(sizeof(uint32_t) * 2 * N);   // per active expert: info, token mask
     L.pos_of = o; o += align256(sizeof(int32_t) * (size_t)B * kslots + 4);
     L.nused = o;  o += align256(sizeof(int32_t) * (size_t)B + 4);                  // kept slots per token
@@ -107,7 +106,6 @@ struct FfnArgs {
     uint32_t* hdone;        // [token chunks] phase-A tiles of the chunk whose h rows are written
     const int32_t* nused;   // [B] kept slots of each token (routing kernel)
     uint32_t* ycnt;         // [B][ceil(d / 128)] y slices still missing; the last writer combines
-    uint32_t* gflag;        // [grid] CTA finished its share of the gather
     WsHeader* hdr;
     const void* w_gate;     // [N][F][d]   (fp32 path)
     const void* w_up;

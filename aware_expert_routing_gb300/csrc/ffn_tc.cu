@@ -99,7 +99,9 @@ constexpr int kQ = 16;                   // tile queue entries
 constexpr int kAcc = 4;                  // accumulator buffers
 constexpr uint32_t kTmemCols = kAcc * kNMax;   // fp32 columns (batches over 16 tokens)
 constexpr uint32_t kTmemColsSmall = kAcc * 16;  // batches of up to 16 tokens
-constexpr uint32_t kBarEpi = 1;          // named barrier of the four epilogue warps
+constexpr uint32_t kBarGather = 2;       // named barrier of the warps that copy grouped rows
+constexpr int kGatherThreads = (kEpiWarps + kConvWarps + 1) * 32;   // warps 0-3 and 7-15
+constexpr int kGatherRows = 64;          // grouped rows per pass
 constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
 static_assert(kTmemCols <= 512, "tensor memory has 512 columns");
 
@@ -121,6 +123,7 @@ struct Smem {
     uint32_t raw_info[kRaw];             // ring slot | phase A << 8 | K block << 9 | last << 13, or ~0u
     int tq[kQ];                          // tile index, or -1 once the list is exhausted
     int fast_ops;                        // stages of the first tile whose token rows warp 4 has loaded
+    int gtok[kGatherRows];               // tokens of the grouped rows this CTA copies in one pass
     uint32_t tmem_base;
     int nmax;                            // tokens per chunk for this launch (multiple of 16)
     int abort_flag;
@@ -440,6 +443,48 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     tmem_fence_after_sync();
     const uint32_t tmem = S.tmem_base;
 
+    // Batches over 16 tokens: the expert-grouped copy of the hidden states.
+    // Warps 0-3 and 7-15 copy this CTA's rows b, b+G, ... (their tokens
+    // first, so that every 16-byte load depends on shared memory only), then
+    // one thread counts the CTA in; the operand warp starts phase A once all
+    // CTAs have.
+    if (!small_b && (warp < kEpiWarps || warp >= kWarpC)) {
+        const int gt = warp < kEpiWarps ? (int)threadIdx.x : (int)threadIdx.x - (kWarpC - kEpiWarps) * 32;
+        const int P = A.offsets[A.N];
+        const int vpr = d / 8;   // 16-byte vectors per row
+        const int nrow = P > (int)blockIdx.x ? (P - 1 - (int)blockIdx.x) / (int)G + 1 : 0;
+        const uint4* xs = static_cast<const uint4*>(A.x);
+        uint4* xp = static_cast<uint4*>(A.xperm);
+        for (int r0 = 0; r0 < nrow; r0 += kGatherRows) {
+            const int nr = min(kGatherRows, nrow - r0);
+            if (gt < nr) S.gtok[gt] = A.perm[(int)blockIdx.x + (r0 + gt) * (int)G] / A.kslots;
+            named_barrier(kBarGather, kGatherThreads);
+            const int nvec = nr * vpr;
+            for (int v0 = 0; v0 < nvec; v0 += 4 * kGatherThreads) {
+                uint4 val[4];
+                size_t dst[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int v = v0 + u * kGatherThreads + gt;
+                    dst[u] = ~size_t(0);
+                    if (v < nvec) {
+                        const int r = v / vpr, c = v - r * vpr;
+                        val[u] = __ldg(xs + (size_t)S.gtok[r] * vpr + c);
+                        dst[u] = (size_t)((int)blockIdx.x + (r0 + r) * (int)G) * vpr + c;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (dst[u] != ~size_t(0)) xp[dst[u]] = val[u];
+            }
+            named_barrier(kBarGather, kGatherThreads);   // every row stored; gtok is free again
+        }
+        if (gt == 0) {
+            __threadfence();
+            atomicAdd(&A.hdr->gathered, 1u);
+        }
+    }
+
     // Tiles: phase A (expert, 64 rows of d_ff, chunk) first, then phase B
     // (expert, 128 rows of d, chunk), both in active-expert order.
     const int rbA = F / 64, rbB = (d + kM - 1) / kM;
@@ -550,9 +595,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const bool ph_a = tile < TA;
             const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
             if (ph_a && !gathered) {   // every CTA has copied its rows of the grouped hidden states
-                for (int c = lane; c < (int)G; c += 32) wait_counter(&A.gflag[c], 1u, S, flags);
+                if (lane == 0) {
+                    wait_counter(&A.hdr->gathered, G, S, flags);
+                    fence_proxy_async_global();
+                }
                 __syncwarp();
-                fence_proxy_async_global();
                 gathered = true;
             }
             if (lane == 0) {
@@ -683,41 +730,6 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     } else {
         // ------------------------------- epilogue --------------------------------
         const int tid = threadIdx.x;   // 0..127
-
-        // Prologue (batches over 16 tokens): this CTA's rows of the
-        // expert-grouped hidden states (rows b, b+G, ...), eight 16-byte
-        // loads in flight per thread.
-        if (!small_b) {
-            const int P = A.offsets[A.N];
-            const int vpr = d / 8;   // 16-byte vectors per row
-            const int nrow = P > (int)blockIdx.x ? (P - 1 - (int)blockIdx.x) / (int)G + 1 : 0;
-            const int nvec = nrow * vpr;
-            const uint4* xs = static_cast<const uint4*>(A.x);
-            uint4* xp = static_cast<uint4*>(A.xperm);
-            for (int v0 = 0; v0 < nvec; v0 += 8 * kEpiWarps * 32) {
-                uint4 val[8];
-                size_t dst[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int v = v0 + u * kEpiWarps * 32 + tid;
-                    dst[u] = ~size_t(0);
-                    if (v < nvec) {
-                        const int r = v / vpr, c = v - r * vpr;
-                        const int pr = (int)blockIdx.x + r * (int)G;
-                        val[u] = __ldg(xs + (size_t)(A.perm[pr] / A.kslots) * vpr + c);
-                        dst[u] = (size_t)pr * vpr + c;
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (dst[u] != ~size_t(0)) xp[dst[u]] = val[u];
-            }
-            named_barrier(kBarEpi, kEpiWarps * 32);
-            if (tid == 0) {
-                __threadfence();
-                atomicExch(&A.gflag[blockIdx.x], 1u);
-            }
-        }
 
         __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
         const int i = 32 * warp + lane;                    // this thread's D row (tensor-memory lane)
@@ -886,11 +898,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     __syncthreads();
     if (S.last_flag) {
         __threadfence();
-        for (int k = threadIdx.x; k < (int)G; k += kThreads) A.gflag[k] = 0;
         for (int k = threadIdx.x; k < X.chunk_off[Tn]; k += kThreads) A.hdone[k] = 0;
     }
     if (S.last_flag && threadIdx.x == 0) {
         A.hdr->next_tile = 0;
+        A.hdr->gathered = 0;
         A.hdr->ctas_done = 0;
     }
 }
