@@ -671,19 +671,27 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         __syncwarp();
     } else if (warp == kWarpN) {
         // ----------------------------- count-down warp ----------------------------
-        // Each finished phase-B tile's tokens count down their counters for
-        // the tile's 128 rows of d.  The release (after the acquire of the
-        // epilogue warps' barrier) makes their y stores visible first.
+        // Each finished phase-B tile's tokens (at most kNMax, four per lane)
+        // count down their counters for the tile's 128 rows of d: all the
+        // tokens are looked up at once, then one fence (after the acquire of
+        // the epilogue warps' barrier) makes their y stores visible before
+        // the plain atomic subtractions -- a release.
         for (uint32_t p = 0;; ++p) {
             const int slot = (int)(p % kNQ);
             wait_bar(&S.nt_full[slot], (p / kNQ) & 1, S, flags);
             if (*(volatile int*)&S.abort_flag) break;
             const int4 inf = S.nt_info[slot];
             if (inf.y < 0) break;
-            for (int j = lane; j < inf.y; j += 32) {
-                const int tok = A.perm[inf.x + j] / A.kslots;
-                red_release_gpu_add(&A.ycnt[(size_t)tok * rbB + inf.z], 0xffffffffu);
+            int tk[kNMax / 32];
+#pragma unroll
+            for (int u = 0; u < kNMax / 32; ++u) {
+                const int j = lane + 32 * u;
+                tk[u] = j < inf.y ? A.perm[inf.x + j] / A.kslots : -1;
             }
+            __threadfence();
+#pragma unroll
+            for (int u = 0; u < kNMax / 32; ++u)
+                if (tk[u] >= 0) atomicAdd(&A.ycnt[(size_t)tk[u] * rbB + inf.z], 0xffffffffu);
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.nt_empty[slot]);
         }
