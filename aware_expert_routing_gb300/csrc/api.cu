@@ -185,11 +185,16 @@ int small_batch_blocks(int d, int F) {
     return 1;
 }
 
+// Blocks per stage for larger batches (token rows of up to 128 per stage
+// share the ring): 2 where d / 64 and d_ff / 64 are even, else 1.
+int large_batch_blocks(int d, int F) { return ((d / 64) % 2 == 0 && (F / 64) % 2 == 0) ? 2 : 1; }
+
 struct TcMapEntry {
     MapKey key;
     // gate/up 5D (or W_gate 8-row boxes), W_up 8-row boxes, W_down 128-row boxes
-    // (one block wide); gate/up 5D and W_down kb blocks wide
-    CUtensorMap maps[5];
+    // (one block wide); gate/up 5D and W_down as many blocks wide as small
+    // batches use, then as many as larger batches use
+    CUtensorMap maps[7];
     bool fused, swap, used;
 };
 TcMapEntry g_tc_maps[64];
@@ -226,6 +231,12 @@ moe_status tc_expert_maps(const void* g, const void* u, const void* dn, int N, i
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_gate / W_up, wide boxes)");
     if (!encode_3d(&e.maps[4], dn, F, (uint64_t)N * d, 128, kb))
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_down, wide boxes)");
+    const uint32_t kbl = (uint32_t)large_batch_blocks(d, F);
+    e.maps[5] = e.maps[0];
+    if (e.fused && !encode_gate_up_5d(&e.maps[5], g, u, d, (uint64_t)N * F, &swap4, kbl))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_gate / W_up, 2-block boxes)");
+    if (!encode_3d(&e.maps[6], dn, F, (uint64_t)N * d, 128, kbl))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_down, 2-block boxes)");
     e.used = true;
     memcpy(out, e.maps, sizeof e.maps);
     *fused = e.fused;
@@ -375,9 +386,9 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
     if (sms > kMaxGrid) sms = kMaxGrid;
     {   // the tcgen05 expert kernel (bf16 experts, and INT4 experts through its converter warps)
-        CUtensorMap maps[11];
+        CUtensorMap maps[13];
         bool fused = false, swap = false;
-        CUtensorMap wm[5], om[5];
+        CUtensorMap wm[7], om[5];
         if ((st = tc_expert_maps(w_gate, w_up, w_down, n_hot, d_ff, P.d, dev, wm, &fused, &swap)) != MOE_OK) return st;
         if ((st = tc_operand_maps(ws, L, hidden, P.B * P.kslots, P.B, P.d, d_ff, dev, om)) != MOE_OK) return st;
         maps[0] = wm[0];                       // gate/up 5D, or W_gate
@@ -391,9 +402,12 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
         maps[8] = wm[4];                       // W_down, kb blocks wide
         maps[9] = om[3];                       // hidden states, kb blocks wide
         maps[10] = om[4];                      // h, kb blocks wide
+        maps[11] = wm[5];                      // gate/up 5D, 2 blocks wide (larger batches)
+        maps[12] = wm[6];                      // W_down, 2 blocks wide (larger batches)
         a.gu_fused = fused ? 1 : 0;
         a.gu_swap = swap ? 1 : 0;
         a.kbs = small_batch_blocks(P.d, d_ff);
+        a.kbl = large_batch_blocks(P.d, d_ff);
         e = launch_ffn_tc(a, maps, sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
         return MOE_OK;

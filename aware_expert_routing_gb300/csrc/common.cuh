@@ -119,6 +119,7 @@ struct FfnArgs {
     int gu_fused;           // tcgen05 kernel: W_gate and W_up through one interleaving 5D map
     int gu_swap;            // that map starts at W_up (the lower address): up rows come first
     int kbs;                // tcgen05 kernel: 64-column blocks per stage for batches of up to 16 tokens
+    int kbl;                // tcgen05 kernel: 64-column blocks per stage for larger batches
     int smem_bytes;         // tcgen05 kernel: dynamic shared memory of the launch (set by the launcher)
 };
 
@@ -130,7 +131,8 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 // (8-row boxes), W_down (128-row boxes), gathered hidden states, h and the
 // hidden states (16-row boxes), all one 64-column block wide; maps[7..10]:
 // the 5D gate/up map, W_down, the hidden states and h with boxes kbs blocks
-// wide (batches of up to 16 tokens).
+// wide (batches of up to 16 tokens); maps[11..12]: the 5D gate/up map and
+// W_down with boxes kbl blocks wide (larger batches).
 cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s);
 cudaError_t launch_ffn_f32(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_synth(void* dst, int dtype, uint64_t n, uint64_t start, uint64_t seed,

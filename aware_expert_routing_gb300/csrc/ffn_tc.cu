@@ -288,7 +288,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
               const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_h,
               const __grid_constant__ CUtensorMap tm_hid, const __grid_constant__ CUtensorMap tm_gu4,
               const __grid_constant__ CUtensorMap tm_down4, const __grid_constant__ CUtensorMap tm_hid4,
-              const __grid_constant__ CUtensorMap tm_h4) {
+              const __grid_constant__ CUtensorMap tm_h4, const __grid_constant__ CUtensorMap tm_gu2,
+              const __grid_constant__ CUtensorMap tm_down2) {
     extern __shared__ unsigned char smem_raw[];
     // [stage ring][kRaw packed INT4 slots, with INT4 experts][Smem][tables]
     const bool has_q4 = A.n_cold > 0;
@@ -307,11 +308,14 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     const int d = A.d, F = A.F;
     uint32_t* flags = &A.hdr->flags;
     const uint32_t G = gridDim.x;
-    // K blocks (64 columns) per stage: batches of up to 16 tokens move
-    // A.kbs blocks per TMA operation, since the TMA unit's rate per SM grows
-    // with the size of each operation; larger batches one block.
+    // K blocks (64 columns) per stage, moved by one TMA operation for the
+    // weights, since the TMA unit's rate per SM grows with the size of each
+    // operation: A.kbs (up to 4) for batches of up to 16 tokens, A.kbl (up to
+    // 2) for larger batches, whose token rows share the ring.
     const bool small_b = A.B <= 16;                 // phase-A operand: the whole batch
-    const int KB = (small_b && A.gu_fused) ? A.kbs : 1;
+    const int KB = A.gu_fused ? (small_b ? A.kbs : A.kbl) : 1;
+    const CUtensorMap* const m_gu = KB == 1 ? &tm_gu : small_b ? &tm_gu4 : &tm_gu2;       // weight maps, KB wide
+    const CUtensorMap* const m_down = KB == 1 ? &tm_down : small_b ? &tm_down4 : &tm_down2;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kMaxStages; ++i) {
@@ -375,7 +379,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     tma_load_3d(dst + KB * kWBytes, KB > 1 ? &tm_hid4 : &tm_hid, 0, 0, s * KB, &S.full[s], pol_x);
                     mbar_arrive_expect_tx(&S.full[s], KB * kWBytes);
                     if (A.gu_fused) {
-                        tma_load_5d(dst, KB > 1 ? &tm_gu4 : &tm_gu, 0, 0, 0, row0 / 8, s * KB, &S.full[s], pol);
+                        tma_load_5d(dst, m_gu, 0, 0, 0, row0 / 8, s * KB, &S.full[s], pol);
                     } else {
                         for (int g = 0; g < 8; ++g) {
                             tma_load_3d(dst + (2 * g) * 1024, &tm_gate, 0, row0 + 8 * g, s, &S.full[s], pol);
@@ -425,9 +429,9 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         }
     }
     if (warp == kWarpW && lane == 0) {
-        prefetch_tensormap(A.gu_fused ? (KB > 1 ? &tm_gu4 : &tm_gu) : &tm_gate);
+        prefetch_tensormap(A.gu_fused ? m_gu : &tm_gate);
         if (!A.gu_fused) prefetch_tensormap(&tm_up);
-        prefetch_tensormap(KB > 1 ? &tm_down4 : &tm_down);
+        prefetch_tensormap(m_down);
     }
     if (warp == kWarpO && lane == 0) {
         if (small_b) {
@@ -557,10 +561,10 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     mbar_arrive_expect_tx(&S.full[slot], KB * kWBytes);
                     if (!ph_a) {
                         // 128 W_down rows (rows past the expert's d are computed and dropped)
-                        tma_load_3d(dst, KB > 1 ? &tm_down4 : &tm_down, 0, row0, s * KB, &S.full[slot], pol);
+                        tma_load_3d(dst, m_down, 0, row0, s * KB, &S.full[slot], pol);
                     } else if (A.gu_fused) {
                         // 8 row groups x {8 rows of the lower matrix, 8 rows of the other}
-                        tma_load_5d(dst, KB > 1 ? &tm_gu4 : &tm_gu, 0, 0, 0, row0 / 8, s * KB, &S.full[slot], pol);
+                        tma_load_5d(dst, m_gu, 0, 0, 0, row0 / 8, s * KB, &S.full[slot], pol);
                     } else {   // KB = 1
 #pragma unroll 1
                         for (int g = 0; g < 8; ++g) {
@@ -607,10 +611,12 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     wait_counter(&A.hdone[X.chunk_off[T.a] + T.c], (uint32_t)rbA, S, flags);
                     fence_proxy_async_global();
                 }
-                // KB > 1 only for batches of up to 16 tokens: one 16-row box of KB
-                // blocks, which lands as KB consecutive [16 rows][64] operand blocks
+                // Batches of up to 16 tokens: one 16-row box of KB blocks, which
+                // lands as KB consecutive [16 rows][64] operand blocks.  Larger
+                // batches: one 16-row box per 16 tokens and block, block kb at
+                // kb x nmax rows.
                 const CUtensorMap* map = ph_a ? (small_b ? (KB > 1 ? &tm_hid4 : &tm_hid) : &tm_x)
-                                              : (KB > 1 ? &tm_h4 : &tm_h);
+                                              : (small_b && KB > 1 ? &tm_h4 : &tm_h);
                 const int row = (ph_a && small_b) ? 0 : T.off + nmax * T.c;
                 const int nb = (ph_a && small_b) ? 1 : (T.ntok + 15) >> 4;   // 16-row boxes = MMA N / 16
                 const int ns = ph_a ? SA : SB;
@@ -619,8 +625,15 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
                     mbar_arrive_expect_tx(&S.full[slot], nb * 2048 * KB);   // rows past the end read as zeros
                     unsigned char* dst = ring + (size_t)slot * slot_bytes + KB * kWBytes;
-                    for (int j = 0; j < nb; ++j)
-                        tma_load_3d(dst + j * 2048, map, 0, row + 16 * j, s * KB, &S.full[slot], pol);
+                    if (small_b) {
+                        for (int j = 0; j < nb; ++j)
+                            tma_load_3d(dst + j * 2048, map, 0, row + 16 * j, s * KB, &S.full[slot], pol);
+                    } else {
+                        for (int kb = 0; kb < KB; ++kb)
+                            for (int j = 0; j < nb; ++j)
+                                tma_load_3d(dst + kb * obytes + j * 2048, map, 0, row + 16 * j, s * KB + kb,
+                                            &S.full[slot], pol);
+                    }
                 }
             }
             __syncwarp();
@@ -935,8 +948,8 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
     FfnArgs a = a_in;
     a.smem_bytes = smem_optin[dev];
     // the ring must hold two stages of the largest slot this launch can use
-    const int kb = (a.B <= 16 && a.gu_fused) ? a.kbs : 1;
-    const size_t slot = a.B <= 16 ? (size_t)kb * (kWBytes + 16 * 128) : (size_t)kWBytes + kNMax * 128;
+    const int kb = a.gu_fused ? (a.B <= 16 ? a.kbs : a.kbl) : 1;
+    const size_t slot = (size_t)kb * (kWBytes + (a.B <= 16 ? 16 : kNMax) * 128);
     if ((size_t)a.smem_bytes < 4096 + tabs_bytes(a.N) + (size_t)kRaw * kRawBytes ||
         ring_bytes_for((size_t)a.smem_bytes, a.N, a.n_cold > 0) < 2 * slot)
         return cudaErrorInvalidConfiguration;
@@ -954,7 +967,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, ffn_tc_kernel, a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                              maps[6], maps[7], maps[8], maps[9], maps[10]);
+                              maps[6], maps[7], maps[8], maps[9], maps[10], maps[11], maps[12]);
 }
 
 }  // namespace moe
