@@ -361,6 +361,11 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
 
     def step(i, ev_pre=None, ev_post=None):
         D = layers[i % N_LAYERS]
+        if ev_pre is None and "mixed" not in D:
+            # the whole layer through the public call (routing, then experts)
+            moe.moe_decode_layer(D["x"], D["w_router"], D["bias"], D["w_gate"], D["w_up"], D["w_down"], w.F, prm,
+                                 routing, out, ws, stream)
+            return
         moe.moe_route(D["x"], D["w_router"], D["bias"], prm, routing, ws, stream)
         if ev_pre is not None:
             ev_pre.record(stream)
