@@ -203,6 +203,21 @@ def test_identical_tokens():
     assert g["T"] == 8
 
 
+@pytest.mark.parametrize("N", [64, 128, 256])
+def test_tied_scores(N):
+    # Experts 2j and 2j+1 have the same router row (and no bias), so every
+    # token scores them exactly alike: the ranking must put the lower id
+    # first, and the selections must match the oracle's bit for bit.
+    w = W("t_ties", N=N, k=8, d=256, F=128, seed=N + 3)
+    L = synth.make_layer(w, 0, 24)
+    L["w_router"] = np.repeat(L["w_router"][::2], 2, axis=0)
+    L["bias"] = None if L["bias"] is None else np.zeros_like(L["bias"])
+    g, _, _ = run_case(w, 24, OEA, 3, 1.0, L=L, check_e2e=False)
+    assert (g["logits"][:, ::2] == g["logits"][:, 1::2]).all()
+    run_case(w, 24, OEA, 5, 0.8, maxP=9, kmax=8, L=L, check_e2e=False)
+    run_case(w, 24, TOPK, L=L, check_e2e=False)
+
+
 def test_empty_batch():
     w = W("t_empty")
     run_case(w, 0, OEA, 3, 1.0)
