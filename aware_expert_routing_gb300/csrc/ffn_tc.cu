@@ -46,11 +46,14 @@
 //     tcgen05.commit frees each stage when its MMAs have completed and marks
 //     a tile's accumulator full.
 //   * INT4 experts (DynaExq page, section 3.2): warp 4 bulk-copies the
-//     packed chunks of a stage into a 4-slot raw ring; warps 7-14 decode
-//     them (exact integer codes, times the row's group scale, rounded once
-//     to bf16) into the stage's 128-byte-swizzled A operand, fence it for
-//     the tensor core's async proxy and arrive on the stage's barrier in
-//     place of warp 4.
+//     packed chunk of each K block of a stage into a raw ring of 4 to 16
+//     slots (the stage ring's unused tail holds all but 4) and arrives on
+//     the stage barrier without bytes; warps 7-14 decode each
+//     chunk together (exact integer codes, times the row's group scale,
+//     rounded once to bf16) into the stage's 128-byte-swizzled A operand,
+//     fence it for the tensor core's async proxy, and after the stage's last
+//     block each arrives on the stage's cfull barrier, which the MMA thread
+//     waits on besides the stage barrier.
 //   * Warps 0-3 (tensor-memory lanes 32w..32w+31, one D row per thread)
 //     read a finished accumulator with tcgen05.ld and free it; phase A:
 //     the lane holding gate row r takes the matching up row from the lane
@@ -90,7 +93,8 @@ constexpr int kM = 128;                  // weight rows per tile (MMA M)
 constexpr int kNMax = 128;               // most token columns per tile (MMA N)
 constexpr int kWBytes = kM * 128;        // one K block: 128 rows x 64 bf16
 constexpr int kMaxStages = 12;
-constexpr int kRaw = 4;                  // packed INT4 chunks in flight
+constexpr int kRaw = 4;                  // packed INT4 chunk slots after the stage ring (at least)
+constexpr int kRawMax = 16;              // slots in all: the ring's unused tail holds the others
 constexpr int kQ4A = 64 * 32 + 64 * 2;   // INT4 chunk of W_gate / W_up: 64 rows x 64 columns + scales
 constexpr int kQ4B = 128 * 32 + 128 * 2; // INT4 chunk of W_down: 128 rows x 64 columns + scales
 constexpr int kRawBytes = 2 * kQ4A;      // a phase-A stage needs a W_gate and a W_up chunk
@@ -117,10 +121,10 @@ struct Smem {
     uint64_t nt_full[kNQ];               // the four epilogue warps stored a phase-B tile's y rows
     uint64_t nt_empty[kNQ];              // warp 15 has counted them down
     int4 nt_info[kNQ];                   // first pair, pairs (-1: no more tiles), row block
-    uint64_t raw_full[kRaw];             // packed INT4 chunks landed (bulk copies)
-    uint64_t raw_empty[kRaw];            // the four converter warps have read them
-    uint64_t conv_bar;                   // the four converter warps meet (bounded wait)
-    uint32_t raw_info[kRaw];             // ring slot | phase A << 8 | K block << 9 | last << 13, or ~0u
+    uint64_t raw_full[kRawMax];          // packed INT4 chunks landed (bulk copies)
+    uint64_t raw_empty[kRawMax];         // the converter warps have read them
+    uint64_t cfull[kMaxStages];          // each converter warp wrote its rows of a stage's blocks (INT4 stages)
+    uint32_t raw_info[kRawMax];          // ring slot | phase A << 8 | K block << 9, or ~0u
     int tq[kQ];                          // tile index, or -1 once the list is exhausted
     int fast_ops;                        // stages of the first tile whose token rows warp 4 has loaded
     int gtok[kGatherRows];               // tokens of the grouped rows this CTA copies in one pass
@@ -248,15 +252,6 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// The four converter warps meet; every warp calls this the same number of
-// times, and the wait is bounded.
-__device__ __forceinline__ void conv_sync(Smem& S, uint32_t& nsync, uint32_t* flags, int lane) {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.conv_bar);
-    wait_bar(&S.conv_bar, nsync & 1, S, flags);
-    ++nsync;
-}
-
 // The four epilogue warps meet (bounded wait); every warp calls this the
 // same number of times.
 __device__ __forceinline__ void epi_meet(Smem& S, uint32_t& nm, uint32_t* flags, int lane) {
@@ -337,11 +332,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             mbar_init(&S.nt_empty[i], 1);
             S.nt_info[i] = make_int4(0, 0, 0, 0);
         }
-        for (int i = 0; i < kRaw; ++i) {
+        for (int i = 0; i < kRawMax; ++i) {
             mbar_init(&S.raw_full[i], 1);
             mbar_init(&S.raw_empty[i], kConvWarps);
         }
-        mbar_init(&S.conv_bar, kConvWarps);
+        for (int i = 0; i < kMaxStages; ++i) mbar_init(&S.cfull[i], kConvWarps);
         fence_barrier_init();
         S.abort_flag = 0;
         S.fast_ops = 0;
@@ -500,6 +495,13 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     const int slot_bytes = KB * (kWBytes + nmax * 128);
     const int obytes = nmax * 128;                  // one operand block
     const int nst = min(kMaxStages, ring_bytes / slot_bytes);
+    // Packed INT4 chunk slots: kRaw after the ring, more in the ring's tail
+    // that the whole stages leave unused (deeper raw rings keep more bytes in
+    // flight for the converter warps without costing a stage).
+    const int nraw = kRaw + min(kRawMax - kRaw, (ring_bytes - nst * slot_bytes) / kRawBytes);
+    auto raw_slot = [&](int r) -> unsigned char* {
+        return r < kRaw ? raw + (size_t)r * kRawBytes : ring + (size_t)nst * slot_bytes + (size_t)(r - kRaw) * kRawBytes;
+    };
 
     if (warp == kWarpW) {
         // ---------------------------- weight producer ----------------------------
@@ -534,15 +536,16 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     if (sl < 0) {
                         // INT4 expert: the packed chunks of the stage's K blocks go to
                         // raw slots; the converter warps write the bf16 blocks and
-                        // arrive on the stage's barrier after its last one.
+                        // each arrives on the stage's cfull barrier after the last
+                        // one.  This warp's arrival on full carries no bytes.
                         const int c = -1 - sl;
+                        mbar_arrive(&S.full[slot]);
 #pragma unroll 1
                         for (int kb = 0; kb < KB; ++kb) {
                             const int r = rq.slot;
                             if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
-                            S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u) | ((uint32_t)kb << 9) |
-                                            (kb == KB - 1 ? (1u << 13) : 0u);
-                            unsigned char* rdst = raw + (size_t)r * kRawBytes;
+                            S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u) | ((uint32_t)kb << 9);
+                            unsigned char* rdst = raw_slot(r);
                             const int kblk = s * KB + kb;
                             if (ph_a) {
                                 const size_t off = (size_t)c * q4_mat_a + ((size_t)T.rb * (d / 64) + kblk) * kQ4A;
@@ -554,7 +557,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                                 mbar_arrive_expect_tx(&S.raw_full[r], kQ4B);
                                 bulk_load(rdst, A.q_down + off, kQ4B, &S.raw_full[r], pol);
                             }
-                            rq.next(kRaw);
+                            rq.next(nraw);
                         }
                         continue;
                     }
@@ -642,6 +645,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         // ------------------------------ MMA issuer -------------------------------
         if (lane == 0) {
             RingPos rp;
+            uint32_t cpar = 0;   // per ring slot: parity of its next cfull phase (INT4 stages)
             for (int n = 0;; ++n) {
                 const int q = n % kQ;
                 wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
@@ -649,9 +653,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 if (tile < 0) break;
                 const bool ph_a = tile < TA;
                 int ntile = 16;   // MMA N: batches of up to 16 always use 16 columns
-                if (!small_b) {
+                bool q4 = false;  // INT4 expert: the converter warps write the A operand
+                if (!small_b || A.n_cold > 0) {
                     const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
-                    ntile = (T.ntok + 15) & ~15;
+                    if (!small_b) ntile = (T.ntok + 15) & ~15;
+                    q4 = X.ex_slot[T.a] < 0;
                 }
                 const uint32_t idesc = umma_idesc_bf16(kM, ntile);
                 const int ns = ph_a ? SA : SB;
@@ -664,6 +670,10 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 for (int s = 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     wait_bar(&S.full[slot], rp.phase, S, flags);
+                    if (q4) {
+                        wait_bar(&S.cfull[slot], (cpar >> slot) & 1u, S, flags);
+                        cpar ^= 1u << slot;
+                    }
                     tmem_fence_after_sync();
                     const uint32_t a0 = smem_u32(ring + (size_t)slot * slot_bytes);
                     const uint32_t b0 = a0 + KB * kWBytes;
@@ -716,18 +726,24 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         // (2g + m)*8 + r is row 8g + r of W_gate (m = 0) or W_up (m = 1).
         const int ct = threadIdx.x - kWarpC * 32;   // 0..kConvWarps*32-1
         RingPos rq;
-        uint32_t nsync = 0;
         for (;;) {
             if (A.n_cold == 0) break;                  // no INT4 experts in this launch
             const int r = rq.slot;
             wait_bar(&S.raw_full[r], rq.phase, S, flags);
+            if (*(volatile int*)&S.abort_flag) break;
             const uint32_t info = S.raw_info[r];
             if (info == ~0u) break;
             const int slot = (int)(info & 255u);
             const bool ph_a = (info >> 8) & 1u;
             const int kb = (int)((info >> 9) & 15u);
-            const bool last = (info >> 13) & 1u;
-            const unsigned char* src = raw + (size_t)r * kRawBytes;
+            if (slot >= nst || kb >= KB) {   // never posted so: flag it and write nothing
+                if (lane == 0) {
+                    raise_flag(flags, kFlagBadIndex);
+                    give_up(S, flags);
+                }
+                break;
+            }
+            const unsigned char* src = raw_slot(r);
             unsigned char* dstA = ring + (size_t)slot * slot_bytes + kb * kWBytes;
 #pragma unroll
             for (int it = 0; it < 1024 / (kConvWarps * 32); ++it) {   // 128 rows x 8 units
@@ -743,10 +759,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             }
             fence_proxy_async_shared();   // the tensor core reads the stage through the async proxy
             __syncwarp();
-            if (lane == 0) mbar_arrive(&S.raw_empty[r]);   // this warp has read the packed chunk
-            conv_sync(S, nsync, flags, lane);              // all the converter warps have written their rows
-            if (ct == 0 && last) mbar_arrive(&S.full[slot]);   // in place of the weight warp
-            rq.next(kRaw);
+            if (lane == 0) {
+                mbar_arrive(&S.raw_empty[r]);                   // this warp has read the packed chunk
+                if (kb == KB - 1) mbar_arrive(&S.cfull[slot]);  // and written its rows of the stage
+            }
+            rq.next(nraw);
         }
     } else {
         // ------------------------------- epilogue --------------------------------
