@@ -93,8 +93,8 @@ constexpr int kM = 128;                  // weight rows per tile (MMA M)
 constexpr int kNMax = 128;               // most token columns per tile (MMA N)
 constexpr int kWBytes = kM * 128;        // one K block: 128 rows x 64 bf16
 constexpr int kMaxStages = 12;
-constexpr int kRaw = 4;                  // packed INT4 chunk slots after the stage ring (at least)
-constexpr int kRawMax = 16;              // slots in all: the ring's unused tail holds the others
+constexpr int kRaw = 4;                  // packed INT4 chunks' worth of bytes after the stage ring
+constexpr int kRawMax = 16;              // raw slots (one stage's chunks each) at most; the ring's unused tail holds more
 constexpr int kQ4A = 64 * 32 + 64 * 2;   // INT4 chunk of W_gate / W_up: 64 rows x 64 columns + scales
 constexpr int kQ4B = 128 * 32 + 128 * 2; // INT4 chunk of W_down: 128 rows x 64 columns + scales
 constexpr int kRawBytes = 2 * kQ4A;      // a phase-A stage needs a W_gate and a W_up chunk
@@ -124,7 +124,7 @@ struct Smem {
     uint64_t raw_full[kRawMax];          // packed INT4 chunks landed (bulk copies)
     uint64_t raw_empty[kRawMax];         // the converter warps have read them
     uint64_t cfull[kMaxStages];          // each converter warp wrote its rows of a stage's blocks (INT4 stages)
-    uint32_t raw_info[kRawMax];          // ring slot | phase A << 8 | K block << 9, or ~0u
+    uint32_t raw_info[kRawMax];          // ring slot | phase A << 8, or ~0u
     int tq[kQ];                          // tile index, or -1 once the list is exhausted
     int fast_ops;                        // stages of the first tile whose token rows warp 4 has loaded
     int gtok[kGatherRows];               // tokens of the grouped rows this CTA copies in one pass
@@ -498,9 +498,13 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // Packed INT4 chunk slots: kRaw after the ring, more in the ring's tail
     // that the whole stages leave unused (deeper raw rings keep more bytes in
     // flight for the converter warps without costing a stage).
-    const int nraw = kRaw + min(kRawMax - kRaw, (ring_bytes - nst * slot_bytes) / kRawBytes);
+    // A raw slot holds one stage's KB packed chunks (W_gate's, then W_up's,
+    // in phase A), each matrix's moved by one bulk copy.
+    const int rslot = KB * kRawBytes;
+    const int nraw_a = kRaw * kRawBytes / rslot;   // slots after the ring
+    const int nraw = nraw_a + min(kRawMax - nraw_a, (ring_bytes - nst * slot_bytes) / rslot);
     auto raw_slot = [&](int r) -> unsigned char* {
-        return r < kRaw ? raw + (size_t)r * kRawBytes : ring + (size_t)nst * slot_bytes + (size_t)(r - kRaw) * kRawBytes;
+        return r < nraw_a ? raw + (size_t)r * rslot : ring + (size_t)nst * slot_bytes + (size_t)(r - nraw_a) * rslot;
     };
 
     if (warp == kWarpW) {
@@ -534,31 +538,28 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
                     unsigned char* dst = ring + (size_t)slot * slot_bytes;
                     if (sl < 0) {
-                        // INT4 expert: the packed chunks of the stage's K blocks go to
-                        // raw slots; the converter warps write the bf16 blocks and
-                        // each arrives on the stage's cfull barrier after the last
-                        // one.  This warp's arrival on full carries no bytes.
+                        // INT4 expert: the packed chunks of the stage's KB blocks are
+                        // contiguous per matrix and go to one raw slot; the converter
+                        // warps write the bf16 blocks and each arrives on the stage's
+                        // cfull barrier.  This warp's arrival on full carries no bytes.
                         const int c = -1 - sl;
                         mbar_arrive(&S.full[slot]);
-#pragma unroll 1
-                        for (int kb = 0; kb < KB; ++kb) {
-                            const int r = rq.slot;
-                            if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
-                            S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u) | ((uint32_t)kb << 9);
-                            unsigned char* rdst = raw_slot(r);
-                            const int kblk = s * KB + kb;
-                            if (ph_a) {
-                                const size_t off = (size_t)c * q4_mat_a + ((size_t)T.rb * (d / 64) + kblk) * kQ4A;
-                                mbar_arrive_expect_tx(&S.raw_full[r], 2 * kQ4A);
-                                bulk_load(rdst, A.q_gate + off, kQ4A, &S.raw_full[r], pol);
-                                bulk_load(rdst + kQ4A, A.q_up + off, kQ4A, &S.raw_full[r], pol);
-                            } else {
-                                const size_t off = (size_t)c * q4_mat_b + ((size_t)T.rb * (F / 64) + kblk) * kQ4B;
-                                mbar_arrive_expect_tx(&S.raw_full[r], kQ4B);
-                                bulk_load(rdst, A.q_down + off, kQ4B, &S.raw_full[r], pol);
-                            }
-                            rq.next(nraw);
+                        const int r = rq.slot;
+                        if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
+                        S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u);
+                        unsigned char* rdst = raw_slot(r);
+                        const int kblk = s * KB;
+                        if (ph_a) {
+                            const size_t off = (size_t)c * q4_mat_a + ((size_t)T.rb * (d / 64) + kblk) * kQ4A;
+                            mbar_arrive_expect_tx(&S.raw_full[r], 2 * KB * kQ4A);
+                            bulk_load(rdst, A.q_gate + off, KB * kQ4A, &S.raw_full[r], pol);
+                            bulk_load(rdst + KB * kQ4A, A.q_up + off, KB * kQ4A, &S.raw_full[r], pol);
+                        } else {
+                            const size_t off = (size_t)c * q4_mat_b + ((size_t)T.rb * (F / 64) + kblk) * kQ4B;
+                            mbar_arrive_expect_tx(&S.raw_full[r], KB * kQ4B);
+                            bulk_load(rdst, A.q_down + off, KB * kQ4B, &S.raw_full[r], pol);
                         }
+                        rq.next(nraw);
                         continue;
                     }
                     mbar_arrive_expect_tx(&S.full[slot], KB * kWBytes);
@@ -724,6 +725,9 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         // stage, 128-byte swizzled like a TMA box: output row i, 16-byte unit u
         // (8 columns) at i*128 + ((u ^ (i & 7)) << 4).  Phase A: row i =
         // (2g + m)*8 + r is row 8g + r of W_gate (m = 0) or W_up (m = 1).
+        // A stage's KB chunks sit in one raw slot: the warps decode them in
+        // one pass (KB x 4 units per lane), then fence once and arrive on the
+        // slot and on the stage.
         const int ct = threadIdx.x - kWarpC * 32;   // 0..kConvWarps*32-1
         RingPos rq;
         for (;;) {
@@ -732,36 +736,40 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             wait_bar(&S.raw_full[r], rq.phase, S, flags);
             if (*(volatile int*)&S.abort_flag) break;
             const uint32_t info = S.raw_info[r];
-            if (info == ~0u) break;
+            if (info == ~0u) break;                    // no more chunks
             const int slot = (int)(info & 255u);
-            const bool ph_a = (info >> 8) & 1u;
-            const int kb = (int)((info >> 9) & 15u);
-            if (slot >= nst || kb >= KB) {   // never posted so: flag it and write nothing
+            if (slot >= nst) {   // never posted so: flag it and write nothing
                 if (lane == 0) {
                     raise_flag(flags, kFlagBadIndex);
                     give_up(S, flags);
                 }
                 break;
             }
+            const bool ph_a = (info >> 8) & 1u;
+            const int rows = ph_a ? 64 : kM;
             const unsigned char* src = raw_slot(r);
-            unsigned char* dstA = ring + (size_t)slot * slot_bytes + kb * kWBytes;
 #pragma unroll
-            for (int it = 0; it < 1024 / (kConvWarps * 32); ++it) {   // 128 rows x 8 units
-                const int k = it * (kConvWarps * 32) + ct;
-                const int i = k >> 3, u = k & 7;
-                const unsigned char* ch = ph_a ? src + ((i >> 3) & 1) * kQ4A : src;
-                const int srow = ph_a ? 8 * (i >> 4) + (i & 7) : i;
-                const int rows = ph_a ? 64 : kM;
-                const uint32_t w = *reinterpret_cast<const uint32_t*>(ch + srow * 32 + u * 4);
-                const __nv_bfloat16 sc = *reinterpret_cast<const __nv_bfloat16*>(ch + rows * 32 + srow * 2);
-                *reinterpret_cast<uint4*>(dstA + i * 128 + ((u ^ (i & 7)) << 4)) =
-                    decode_q4_row8(w, __bfloat162bfloat162(sc));
+            for (int kb = 0; kb < 4; ++kb) {
+                if (kb >= KB) break;
+                unsigned char* dstA = ring + (size_t)slot * slot_bytes + kb * kWBytes;
+#pragma unroll
+                for (int it = 0; it < 1024 / (kConvWarps * 32); ++it) {   // 128 rows x 8 units
+                    const int k = it * (kConvWarps * 32) + ct;
+                    const int i = k >> 3, u = k & 7;
+                    // phase A: W_gate's chunk kb, or W_up's (after W_gate's KB)
+                    const unsigned char* ch = ph_a ? src + (((i >> 3) & 1) * KB + kb) * kQ4A : src + kb * kQ4B;
+                    const int srow = ph_a ? 8 * (i >> 4) + (i & 7) : i;
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(ch + srow * 32 + u * 4);
+                    const __nv_bfloat16 sc = *reinterpret_cast<const __nv_bfloat16*>(ch + rows * 32 + srow * 2);
+                    *reinterpret_cast<uint4*>(dstA + i * 128 + ((u ^ (i & 7)) << 4)) =
+                        decode_q4_row8(w, __bfloat162bfloat162(sc));
+                }
             }
             fence_proxy_async_shared();   // the tensor core reads the stage through the async proxy
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&S.raw_empty[r]);                   // this warp has read the packed chunk
-                if (kb == KB - 1) mbar_arrive(&S.cfull[slot]);  // and written its rows of the stage
+                mbar_arrive(&S.raw_empty[r]);    // this warp has read the packed chunks
+                mbar_arrive(&S.cfull[slot]);     // and written its rows of the stage
             }
             rq.next(nraw);
         }
