@@ -8,6 +8,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 
 #include "common.cuh"
 
@@ -128,6 +129,26 @@ struct MapKey {
 };
 
 std::mutex g_map_mu;
+
+// Routing calls per workspace.  Each routing launch publishes its early
+// union of activated experts under a new epoch (never 0); the expert kernel
+// that follows on the same workspace waits for that epoch, so a union left
+// by an earlier call never passes for the current one.
+std::mutex g_epoch_mu;
+std::unordered_map<const void*, uint32_t> g_epoch;
+
+uint32_t next_epoch(const void* ws) {
+    std::lock_guard<std::mutex> lk(g_epoch_mu);
+    uint32_t& e = g_epoch[ws];
+    e = e + 1u == 0u ? 1u : e + 1u;
+    return e;
+}
+
+uint32_t current_epoch(const void* ws) {   // 0: no routing call recorded for this workspace
+    std::lock_guard<std::mutex> lk(g_epoch_mu);
+    const auto it = g_epoch.find(ws);
+    return it == g_epoch.end() ? 0u : it->second;
+}
 
 // A row-major bf16 matrix [rows][cols] (cols a multiple of 64) viewed as 3D
 // {64 columns, rows, cols/64 column blocks}: one box {64, box_rows, 4} moves
@@ -358,6 +379,10 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     a.nused = reinterpret_cast<const int32_t*>(ws + L.nused);
     a.ycnt = reinterpret_cast<uint32_t*>(ws + L.ycnt);
     a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
+    a.ubits = a.hdr->union_bits;
+    a.uflag = &a.hdr->union_epoch;
+    // the early start serves OEA routing of batches of up to 16 tokens
+    a.epoch = P.B <= 16 && P.mode == MOE_MODE_OEA ? current_epoch(workspace) : 0u;
     a.w_gate = w_gate;
     a.w_up = w_up;
     a.w_down = w_down;
@@ -483,7 +508,13 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
     a.nused = reinterpret_cast<int32_t*>(ws + L.nused);
     a.ycnt = reinterpret_cast<uint32_t*>(ws + L.ycnt);
     a.rbd = (P.d + 127) / 128;
-    a.flags = &reinterpret_cast<WsHeader*>(ws + L.header)->flags;
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
+    a.flags = &hdr->flags;
+    if (P.B <= 32 && P.mode == MOE_MODE_OEA) {   // one routing CTA: it publishes S_base after phase 1
+        a.ubits = hdr->union_bits;
+        a.uflag = &hdr->union_epoch;
+        a.epoch = next_epoch(workspace);
+    }
     e = launch_route(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
     return MOE_OK;

@@ -26,8 +26,11 @@ struct WsHeader {
     uint32_t next_tile;    // expert kernel: tiles claimed beyond each CTA's first
     uint32_t unused0;
     uint32_t gathered;     // expert kernel: CTAs that copied their rows of the grouped hidden states
-    uint32_t pad[59];
+    uint32_t union_epoch;  // routing kernel: epoch of the call whose union_bits are complete
+    uint32_t pad[26];
+    uint32_t union_bits[32];   // routing kernel (OEA, batches of up to 32): S_base, one bit per expert
 };
+static_assert(sizeof(WsHeader) == 256, "the header is one 256-byte block");
 
 struct WsLayout {
     size_t header, hdone, exinfo, pos_of, nused, ycnt, logits, hbuf, ybuf, xperm, total;
@@ -86,6 +89,12 @@ struct RouteArgs {
     uint32_t* ycnt;         // [B][rbd] set to nused: the expert kernel counts each row block's y slices down
     int rbd;                // row blocks of 128 in d
     uint32_t* flags;
+    // OEA, batches of up to 32 tokens: S_base (one bit per expert), published
+    // with `epoch` once phase 1 is done, so the expert kernel can start on
+    // the activated experts' weights before the routing ends.
+    uint32_t* ubits;        // [32] or null: not published
+    uint32_t* uflag;        // set to epoch (release) once ubits is complete
+    uint32_t epoch;         // nonzero, distinct per routing call on this workspace
 };
 
 struct FfnArgs {
@@ -121,6 +130,12 @@ struct FfnArgs {
     int kbs;                // tcgen05 kernel: 64-column blocks per stage for batches of up to 16 tokens
     int kbl;                // tcgen05 kernel: 64-column blocks per stage for larger batches
     int smem_bytes;         // tcgen05 kernel: dynamic shared memory of the launch (set by the launcher)
+    // OEA, batches of up to 16 tokens: the routing kernel's early S_base
+    // (RouteArgs::ubits) and the epoch of the routing call that this launch
+    // follows; epoch 0: wait for the whole routing instead.
+    const uint32_t* ubits;
+    const uint32_t* uflag;
+    uint32_t epoch;
 };
 
 // Launchers (defined in the .cu files).
@@ -374,6 +389,10 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 // thread has made or observed are visible before it) and no result.
 __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Atomic add at GPU scope with acquire and release semantics; returns the old value.

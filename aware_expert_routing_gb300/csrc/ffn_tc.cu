@@ -117,6 +117,9 @@ struct Smem {
     uint64_t tq_full[kQ];                // tile queue entry posted by the weight warp
     uint64_t tq_empty[kQ];               // entry released by the four epilogue warps
     uint64_t mma_done;                   // every MMA issued has completed
+    uint64_t meta_full;                  // early start: counts, first pairs and token masks are in the tables
+    uint64_t union_full;                 // early start: warp 4 has put the union's words in uw
+    uint32_t uw[32];                     // early start: the routing kernel's union (bit b of word j: expert 32j + b)
     uint64_t epi_bar;                    // the four epilogue warps meet (bounded wait)
     uint64_t nt_full[kNQ];               // the four epilogue warps stored a phase-B tile's y rows
     uint64_t nt_empty[kNQ];              // warp 15 has counted them down
@@ -130,6 +133,7 @@ struct Smem {
     int gtok[kGatherRows];               // tokens of the grouped rows this CTA copies in one pass
     uint32_t tmem_base;
     int nmax;                            // tokens per chunk for this launch (multiple of 16)
+    int tn;                              // activated experts (T)
     int abort_flag;
     int last_flag;
 };
@@ -225,6 +229,22 @@ __device__ __forceinline__ void wait_zero(const uint32_t* p, Smem& S, uint32_t* 
         __nanosleep(ns);
         if (ns < 128) ns <<= 1;
     }
+}
+
+// Early start (batches of up to 16): waits (bounded) until the routing call
+// that this launch follows has published its activated experts, then
+// returns word `lane` of that union (bit b: expert 32 * lane + b).
+__device__ __forceinline__ uint32_t early_union_word(const FfnArgs& A, int lane, Smem& S, uint32_t* flags) {
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(A.uflag) != A.epoch) {
+        if (*(volatile int*)&S.abort_flag) return 0u;
+        if (clock64() - t0 > kWaitCycles) {
+            give_up(S, flags);
+            return 0u;
+        }
+        __nanosleep(64);
+    }
+    return lane < (A.N + 31) / 32 ? A.ubits[lane] : 0u;
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
@@ -326,6 +346,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             mbar_init(&S.tq_empty[i], kEpiWarps);
         }
         mbar_init(&S.mma_done, 1);
+        mbar_init(&S.meta_full, 1);
+        mbar_init(&S.union_full, 1);
         mbar_init(&S.epi_bar, kEpiWarps);
         for (int i = 0; i < kNQ; ++i) {
             mbar_init(&S.nt_full[i], kEpiWarps);
@@ -346,21 +368,60 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     const int acc_stride = small_b ? 16 : kNMax;
     if (warp == kWarpM) tmem_alloc(&S.tmem_base, tmem_cols);
     __syncthreads();             // barriers initialised (this overlaps the routing kernel)
-    grid_dependency_wait();      // routing comes from the preceding kernel
-    int Tn = *A.T;
-    if (Tn < 0 || Tn > A.N) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) raise_flag(flags, kFlagBadIndex);
-        Tn = 0;
+    // Early start (OEA routing of batches of up to 16 tokens, whose routing
+    // call publishes S_base after phase 1): the activated experts are fixed
+    // before the routing kernel ends, and they are all that phase A needs (its operand
+    // is the whole batch; the token masks and first pairs are read only by
+    // the epilogue and phase B).  The tables start from the union, in
+    // ascending expert id like the routing kernel's active list, and the
+    // weights stream while the routing finishes; warp 0 then adds the counts,
+    // first pairs and token masks once the routing kernel has completed.
+    // Every warp that reads the routing's other outputs waits for its
+    // completion first.
+    const bool early = small_b && A.epoch != 0u;
+    int Tn = 0;
+    if (!early) {
+        grid_dependency_wait();      // routing comes from the preceding kernel
+        Tn = *A.T;
+        if (Tn < 0 || Tn > A.N) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) raise_flag(flags, kFlagBadIndex);
+            Tn = 0;
+        }
     }
     // Batches of up to 16 tokens: the CTA's first tile is phase-A tile
     // blockIdx.x of a one-chunk-per-expert list, so the weight warp starts
     // its stages now (each stage's token rows first, then its weights), while
     // warp 0 builds the per-expert records.
     int fast_stages = 0;
-    if (warp == kWarpW && lane == 0 && small_b) {
+    if (warp == kWarpW && small_b) {
         const int rbA0 = F / 64, t0 = (int)blockIdx.x;
-        if (t0 < Tn * rbA0) {
-            const int e = (int)(A.exinfo[t0 / rbA0] & 1023u);
+        int e = -1;   // expert of phase-A tile t0 (active index t0 / rbA0), if there is one
+        if (early) {
+            const uint32_t word = early_union_word(A, lane, S, flags);
+            S.uw[lane] = word;   // for warp 0's tables
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.union_full);
+            const int c = __popc(word);
+            int inc = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, inc, off);
+                if (lane >= off) inc += u;
+            }
+            const int a0 = t0 / rbA0;
+            const bool mine = a0 >= inc - c && a0 < inc;   // active index a0 is a bit of this lane's word
+            int eo = -1;
+            if (mine) {
+                uint32_t w = word;
+                for (int k = inc - c; k < a0; ++k) w &= w - 1u;   // drop the lower set bits
+                eo = 32 * lane + __ffs(w) - 1;
+            }
+            const uint32_t who = __ballot_sync(0xffffffffu, mine);
+            e = who ? __shfl_sync(0xffffffffu, eo, __ffs(who) - 1) : -1;
+        } else if (t0 < Tn * rbA0) {
+            e = (int)(A.exinfo[t0 / rbA0] & 1023u);
+        }
+        if (lane == 0 && e >= 0) {
             const int sl = A.slot ? A.slot[e] : e;
             if (sl >= 0 && sl < A.n_hot) {
                 const uint64_t pol = l2_evict_first_policy();
@@ -386,7 +447,37 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             }
         }
     }
-    if (warp == 0) {   // per-expert records, chunk width and chunk offsets of the active experts
+    if (warp == 0 && early) {   // the tables from the union: one chunk per expert
+        wait_bar(&S.union_full, 0, S, flags);
+        const uint32_t word = S.uw[lane];
+        const int c = __popc(word);
+        int inc = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += u;
+        }
+        const int tot = __shfl_sync(0xffffffffu, inc, 31);
+        uint32_t w = word;
+        for (int a = inc - c; w; ++a, w &= w - 1u) {
+            const int e = 32 * lane + __ffs(w) - 1;
+            int sl = A.slot ? A.slot[e] : e;
+            if (sl >= A.n_hot || -1 - sl >= A.n_cold) {   // out of range: flag it, read expert 0
+                raise_flag(flags, kFlagBadIndex);
+                sl = A.n_hot > 0 ? 0 : -1;
+            }
+            X.ex_info[a] = (uint32_t)e;   // the count and first pair follow with the routing's completion
+            X.tokmask[a] = 0;
+            X.ex_slot[a] = sl;
+            X.chunk_off[a] = a;
+        }
+        if (lane == 0) {
+            X.chunk_off[tot] = tot;
+            S.nmax = 16;
+            S.tn = tot;
+        }
+    } else if (warp == 0) {   // per-expert records, chunk width and chunk offsets of the active experts
+        if (lane == 0) S.tn = Tn;
         int maxcnt = 0;
         for (int a = lane; a < Tn; a += 32) {
             const uint32_t info = A.exinfo[a];   // written by the routing kernel
@@ -441,6 +532,21 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     __syncthreads();
     tmem_fence_after_sync();
     const uint32_t tmem = S.tmem_base;
+    Tn = S.tn;
+    if (early && warp == 0) {
+        // The routing kernel has completed: the counts, first pairs and token
+        // masks join the union's tables (the same experts, in the same order).
+        grid_dependency_wait();
+        if (lane == 0 && *A.T != Tn) raise_flag(flags, kFlagBadIndex);
+        for (int a = lane; a < Tn; a += 32) {
+            const uint32_t info = A.exinfo[a];
+            if ((info & 1023u) != X.ex_info[a]) raise_flag(flags, kFlagBadIndex);
+            X.ex_info[a] = info;
+            X.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.meta_full);
+    }
 
     // Batches over 16 tokens: the expert-grouped copy of the hidden states.
     // Warps 0-3 and 7-15 copy this CTA's rows b, b+G, ... (their tokens
@@ -595,12 +701,17 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         const int fast_ops = S.fast_ops;   // stages of the first tile already loaded by warp 4
         for (int s = 0; s < fast_ops; ++s) rp.next(nst);
         bool gathered = small_b;
+        bool meta = !early;   // the tables hold the counts and first pairs
         for (int n = 0;; ++n) {
             const int q = n % kQ;
             wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
             const int tile = S.tq[q];
             if (tile < 0) break;
             const bool ph_a = tile < TA;
+            if (!ph_a && !meta) {   // phase B reads the chunk's first pair and tokens
+                wait_bar(&S.meta_full, 0, S, flags);
+                meta = true;
+            }
             const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
             if (ph_a && !gathered) {   // every CTA has copied its rows of the grouped hidden states
                 if (lane == 0) {
@@ -700,6 +811,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         // tokens are looked up at once, then one fence (after the acquire of
         // the epilogue warps' barrier) makes their y stores visible before
         // the plain atomic subtractions -- a release.
+        if (early) grid_dependency_wait();   // the pairs and counters come from the routing kernel
         for (uint32_t p = 0;; ++p) {
             const int slot = (int)(p % kNQ);
             wait_bar(&S.nt_full[slot], (p / kNQ) & 1, S, flags);
@@ -776,6 +888,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     } else {
         // ------------------------------- epilogue --------------------------------
         const int tid = threadIdx.x;   // 0..127
+        if (early) wait_bar(&S.meta_full, 0, S, flags);   // token masks and first pairs
 
         __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
         const int i = 32 * warp + lane;                    // this thread's D row (tensor-memory lane)
@@ -873,6 +986,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // sets the counter back to the token's kept slots for the next launch.
     // Tokens that keep no expert find zero at once and get rows of zeros.
     {
+        if (early) grid_dependency_wait();   // slot positions, weights and counters come from the routing kernel
         // converters 0-7, producers and MMA 8-10, count-down warp 11, epilogue 12-15
         const int widx = warp == kWarpN ? kConvWarps + 3
                        : warp >= kWarpC ? warp - kWarpC

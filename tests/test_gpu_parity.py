@@ -248,6 +248,41 @@ def test_deterministic_and_repeatable():
         assert torch.equal(o1, o3)
 
 
+@pytest.mark.parametrize("mode", [OEA, TOPK])
+def test_early_union_follows_the_latest_routing(mode):
+    """With OEA routing, batches of up to 16 start the expert kernel from
+    S_base, which the routing kernel publishes after phase 1 tagged with the
+    routing call's epoch.  An expert call must use the union of the latest
+    routing call on its workspace -- also after routing calls that no expert
+    call followed -- and expert calls after a host synchronisation (no
+    overlap with the routing kernel) must give the same bits.  Top-k routing
+    (which waits for the whole routing) must behave the same way."""
+    w = W("t_epoch", N=128, d=512, F=256, seed=21)
+    B = 12
+    prm = gu.params_for(w, B, mode, 3 if mode == OEA else None, 1.0)
+    Ls = [synth.make_layer(w, layer, B) for layer in range(3)]
+    Ds = [gu.device_inputs(L, True) for L in Ls]
+    g2, ref2, _ = run_case(w, B, mode, 3 if mode == OEA else None, 1.0, L=Ls[2])   # checked against the oracle
+    Ts = [run_case(w, B, mode, 3 if mode == OEA else None, 1.0, L=L)[0]["active"] for L in Ls[:2]]
+    assert any(not np.array_equal(t, g2["active"]) for t in Ts)   # the earlier unions differ
+    ws = moe.alloc_workspace(prm, w.F, gu.DEV)
+    r = moe.Routing(prm, gu.DEV, with_logits=True)
+    out = torch.empty_like(ref2)
+    for D in Ds[:2]:   # routing calls that no expert call follows
+        moe.moe_route(D["x"], D["w_router"], D["bias"], prm, r, ws)
+    D = Ds[2]
+    moe.moe_route(D["x"], D["w_router"], D["bias"], prm, r, ws)
+    moe.moe_expert_ffn(D["x"], D["w_gate"], D["w_up"], D["w_down"], w.F, prm, r, out, ws)
+    assert moe.moe_device_status(ws) == 0
+    assert torch.equal(out, ref2)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        moe.moe_expert_ffn(D["x"], D["w_gate"], D["w_up"], D["w_down"], w.F, prm, r, out, ws)
+        assert moe.moe_device_status(ws) == 0
+        assert torch.equal(out, ref2)
+
+
 def test_nonfinite_scores_are_flagged():
     w = W("t_inf", N=32, d=128, F=64)
     L = synth.make_layer(w, 0, 4)
