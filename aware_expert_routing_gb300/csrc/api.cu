@@ -379,8 +379,7 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     a.nused = reinterpret_cast<const int32_t*>(ws + L.nused);
     a.ycnt = reinterpret_cast<uint32_t*>(ws + L.ycnt);
     a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
-    a.ubits = a.hdr->union_bits;
-    a.uflag = &a.hdr->union_epoch;
+    a.uwords = a.hdr->union_words;
     // the early start serves OEA routing of batches of up to 16 tokens
     a.epoch = P.B <= 16 && P.mode == MOE_MODE_OEA ? current_epoch(workspace) : 0u;
     a.w_gate = w_gate;
@@ -511,8 +510,7 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
     a.flags = &hdr->flags;
     if (P.B <= 32 && P.mode == MOE_MODE_OEA) {   // one routing CTA: it publishes S_base after phase 1
-        a.ubits = hdr->union_bits;
-        a.uflag = &hdr->union_epoch;
+        a.uwords = hdr->union_words;
         a.epoch = next_epoch(workspace);
     }
     e = launch_route(a, s);

@@ -26,11 +26,13 @@ struct WsHeader {
     uint32_t next_tile;    // expert kernel: tiles claimed beyond each CTA's first
     uint32_t unused0;
     uint32_t gathered;     // expert kernel: CTAs that copied their rows of the grouped hidden states
-    uint32_t union_epoch;  // routing kernel: epoch of the call whose union_bits are complete
-    uint32_t pad[26];
-    uint32_t union_bits[32];   // routing kernel (OEA, batches of up to 32): S_base, one bit per expert
+    uint32_t pad[59];
+    // routing kernel (OEA, batches of up to 32): S_base, word j (experts
+    // 32j ... 32j + 31, one bit each) in the low half and the epoch of the
+    // routing call in the high half, each stored at once with release
+    uint64_t union_words[32];
 };
-static_assert(sizeof(WsHeader) == 256, "the header is one 256-byte block");
+static_assert(sizeof(WsHeader) == 512, "the header is two 256-byte blocks");
 
 struct WsLayout {
     size_t header, hdone, exinfo, pos_of, nused, ycnt, logits, hbuf, ybuf, xperm, total;
@@ -92,8 +94,7 @@ struct RouteArgs {
     // OEA, batches of up to 32 tokens: S_base (one bit per expert), published
     // with `epoch` once phase 1 is done, so the expert kernel can start on
     // the activated experts' weights before the routing ends.
-    uint32_t* ubits;        // [32] or null: not published
-    uint32_t* uflag;        // set to epoch (release) once ubits is complete
+    uint64_t* uwords;       // [32] epoch << 32 | word, or null: not published
     uint32_t epoch;         // nonzero, distinct per routing call on this workspace
 };
 
@@ -131,10 +132,9 @@ struct FfnArgs {
     int kbl;                // tcgen05 kernel: 64-column blocks per stage for larger batches
     int smem_bytes;         // tcgen05 kernel: dynamic shared memory of the launch (set by the launcher)
     // OEA, batches of up to 16 tokens: the routing kernel's early S_base
-    // (RouteArgs::ubits) and the epoch of the routing call that this launch
+    // (RouteArgs::uwords) and the epoch of the routing call that this launch
     // follows; epoch 0: wait for the whole routing instead.
-    const uint32_t* ubits;
-    const uint32_t* uflag;
+    const uint64_t* uwords;
     uint32_t epoch;
 };
 
@@ -391,8 +391,14 @@ __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_release_gpu_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // Atomic add at GPU scope with acquire and release semantics; returns the old value.

@@ -233,18 +233,22 @@ __device__ __forceinline__ void wait_zero(const uint32_t* p, Smem& S, uint32_t* 
 
 // Early start (batches of up to 16): waits (bounded) until the routing call
 // that this launch follows has published its activated experts, then
-// returns word `lane` of that union (bit b: expert 32 * lane + b).
+// returns word `lane` of that union (bit b: expert 32 * lane + b).  Each
+// lane polls its own word, which carries the epoch in its high half; the
+// whole warp calls this.
 __device__ __forceinline__ uint32_t early_union_word(const FfnArgs& A, int lane, Smem& S, uint32_t* flags) {
     const long long t0 = clock64();
-    while (ld_acquire_gpu(A.uflag) != A.epoch) {
-        if (*(volatile int*)&S.abort_flag) return 0u;
-        if (clock64() - t0 > kWaitCycles) {
-            give_up(S, flags);
+    uint64_t v = ld_acquire_gpu_u64(&A.uwords[lane]);
+    while (!__all_sync(0xffffffffu, (uint32_t)(v >> 32) == A.epoch)) {
+        if (__any_sync(0xffffffffu, *(volatile int*)&S.abort_flag != 0)) return 0u;
+        if (__any_sync(0xffffffffu, clock64() - t0 > kWaitCycles)) {
+            if (lane == 0) give_up(S, flags);
             return 0u;
         }
         __nanosleep(64);
+        v = ld_acquire_gpu_u64(&A.uwords[lane]);
     }
-    return lane < (A.N + 31) / 32 ? A.ubits[lane] : 0u;
+    return (uint32_t)v;
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }

@@ -126,17 +126,15 @@ __device__ __forceinline__ void finish_token(const RouteArgs& a, RouteSmem& sm, 
     }
 }
 
-// Publishes the OEA union S_base (lane j: bit b of word j is expert 32j + b),
-// then the call's epoch with release semantics.  The activated set is S_base
+// Publishes the OEA union S_base: lane j stores word j (bit b: expert
+// 32j + b) together with the call's epoch, at once and with release
+// semantics, so a reader that sees the epoch sees the word.  The activated set is S_base
 // as soon as phase 1 is done: phase 2 only adds tokens to experts inside it,
 // and every expert in it keeps the token whose baseline put it there.  The
 // expert kernel, launched early, starts on those experts' weights from it
 // while phase 2 and the grouping run.  Warp 0 of a one-CTA launch.
 __device__ __forceinline__ void publish_union(const RouteArgs& a, uint32_t word, int lane) {
-    if (lane < (a.N + 31) / 32) a.ubits[lane] = word;
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release_gpu(a.uflag, a.epoch);
+    st_release_gpu_u64(&a.uwords[lane], ((uint64_t)a.epoch << 32) | (lane < (a.N + 31) / 32 ? word : 0u));
 }
 
 template <int NPL>
@@ -261,7 +259,7 @@ __global__ void route_kernel(RouteArgs a) {
             sb = sm.sball;
         }
         __syncthreads();
-        if (ncta == 1 && a.ubits && warp == 0) publish_union(a, sb[lane], lane);   // S_base
+        if (ncta == 1 && a.uwords && warp == 0) publish_union(a, sb[lane], lane);   // S_base
         uint32_t notin = 0;
 #pragma unroll
         for (int j = 0; j < NPL; ++j)
