@@ -25,7 +25,7 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 FLAG_NONFINITE_SCORE, FLAG_WAIT_TIMEOUT, FLAG_BAD_INDEX = 0x1, 0x2, 0x4
 MAX_TOKENS, MAX_EXPERTS, MAX_SLOTS = 256, 1024, 32
 
-EXPORTED = ["moe_num_slots", "moe_workspace_bytes", "moe_route", "moe_expert_ffn",
+EXPORTED = ["moe_num_slots", "moe_layer_launches", "moe_workspace_bytes", "moe_route", "moe_expert_ffn",
             "moe_expert_ffn_mixed", "moe_decode_layer", "moe_decode_layer_static", "moe_device_status",
             "moe_synth_normal", "moe_status_string", "moe_last_error"]
 STATIC_SCRATCH_BYTES = 32 << 20
@@ -70,6 +70,8 @@ def load(path: str | None = None):
     V, P = ctypes.c_void_p, ctypes.POINTER
     lib.moe_num_slots.argtypes = [P(_Params)]
     lib.moe_num_slots.restype = ctypes.c_int32
+    lib.moe_layer_launches.argtypes = [P(_Params), ctypes.c_int32]
+    lib.moe_layer_launches.restype = ctypes.c_int32
     lib.moe_workspace_bytes.argtypes = [P(_Params), ctypes.c_int32]
     lib.moe_workspace_bytes.restype = ctypes.c_size_t
     lib.moe_route.argtypes = [V, V, V, P(_Params), P(_Routing), V, ctypes.c_size_t, V]
@@ -145,6 +147,13 @@ def moe_num_slots(params: RouteParams) -> int:
     n = load().moe_num_slots(ctypes.byref(params.c()))
     if n < 0:
         raise MoeError(MOE_ERR_ARG, "moe_num_slots", load().moe_last_error().decode())
+    return n
+
+
+def moe_layer_launches(params: RouteParams, d_ff: int) -> int:
+    n = load().moe_layer_launches(ctypes.byref(params.c()), d_ff)
+    if n < 0:
+        raise MoeError(MOE_ERR_ARG, "moe_layer_launches", load().moe_last_error().decode())
     return n
 
 

@@ -448,6 +448,15 @@ int32_t moe_num_slots(const moe_route_params* params) {
     return P.kslots;
 }
 
+int32_t moe_layer_launches(const moe_route_params* params, int32_t d_ff) {
+    Params P;
+    if (resolve(params, P) != MOE_OK) return -1;
+    if (d_ff <= 0 || d_ff % 64 != 0 || d_ff > 16384) return -1;
+    int32_t n = route_fused_supported(P.dtype, P.B, P.N, P.kslots) ? 1 : (P.B > 0 ? 2 : 1);
+    if (P.B > 0) n += P.dtype == MOE_DTYPE_F32 ? 3 : 1;
+    return n;
+}
+
 size_t moe_workspace_bytes(const moe_route_params* params, int32_t d_ff) {
     Params P;
     if (resolve(params, P) != MOE_OK) return 0;
@@ -479,7 +488,9 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
     ra.B = P.B;
     ra.N = P.N;
     ra.d = P.d;
-    cudaError_t e = launch_router(ra, P.dtype, s);
+    // batches of up to 32 tokens (bf16, N <= 128): scores and routing in one cluster launch
+    const bool fused = route_fused_supported(P.dtype, P.B, P.N, P.kslots);
+    cudaError_t e = fused ? cudaSuccess : launch_router(ra, P.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
 
     RouteArgs a{};
@@ -513,7 +524,7 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
         a.uwords = hdr->union_words;
         a.epoch = next_epoch(workspace);
     }
-    e = launch_route(a, s);
+    e = fused ? launch_route_fused(ra, a, s) : launch_route(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
     return MOE_OK;
 }

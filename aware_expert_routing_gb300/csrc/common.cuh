@@ -141,6 +141,10 @@ struct FfnArgs {
 // Launchers (defined in the .cu files).
 cudaError_t launch_router(const RouterArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+// Router scores and routing in one cluster launch (bf16, up to 32 tokens,
+// N <= 128); launch_router + launch_route otherwise.
+bool route_fused_supported(int dtype, int B, int N, int kslots);
+cudaError_t launch_route_fused(const RouterArgs& r, const RouteArgs& a, cudaStream_t s);
 // tcgen05 expert kernel (bf16 weights).  maps[0..6]: W_gate/W_up
 // interleaved 8 rows at a time (5D, gu_fused) or W_gate and W_up alone
 // (8-row boxes), W_down (128-row boxes), gathered hidden states, h and the

@@ -137,15 +137,15 @@ __device__ __forceinline__ void publish_union(const RouteArgs& a, uint32_t word,
     st_release_gpu_u64(&a.uwords[lane], ((uint64_t)a.epoch << 32) | (lane < (a.N + 31) / 32 ? word : 0u));
 }
 
+// The routing of tokens [32 rank, 32 rank + 32) by one CTA of `ncta` in a
+// cluster; a.logits may point to shared memory.
 template <int NPL>
-__global__ void route_kernel(RouteArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+__device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* smem_raw, const uint32_t rank,
+                                           const uint32_t ncta) {
     const int nthreads = blockDim.x;
     const int nwarps = nthreads >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int N = a.N, B = a.B;
-    const uint32_t rank = cluster_ctarank();
-    const uint32_t ncta = gridDim.x;                 // the whole grid is one cluster
     const int tb = 32 * (int)rank;                   // this CTA's tokens: [tb, te)
     const int te = min(B, tb + 32);
     const int bv = min(te, max(tb, a.B_valid));      // valid tokens of this CTA: [tb, bv)
@@ -409,6 +409,162 @@ __global__ void route_kernel(RouteArgs a) {
 }
 
 template <int NPL>
+__global__ void route_kernel(RouteArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    route_body<NPL>(a, smem_raw, cluster_ctarank(), gridDim.x);   // the whole grid is one cluster
+}
+
+// ---- scores and routing in one cluster (bf16, up to 32 tokens, N <= 128) ----
+// CTA r of the cluster scores experts [16r, 16r + 16) for all tokens over
+// the whole hidden dimension: its 32 warps take the 64-column blocks w,
+// w + 32, ... with warp-level bf16 MMAs (the operand loads and the K-index
+// permutation of the separate router kernel), then sum their partial tiles
+// in warp order.  CTA 0 gathers every CTA's tile through distributed shared
+// memory and runs the routing above on the scores in its own shared memory,
+// so the scores never make a round trip through global memory between two
+// kernels (they are still written there, as the routing's logits output).
+constexpr int kFusedWarps = 32;
+
+// Opt-in dynamic shared memory per block of the current device.
+size_t smem_cap() {
+    static int cap[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 48 * 1024;
+    if (!cap[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 48 * 1024;
+        cap[dev] = v;
+    }
+    return (size_t)cap[dev];
+}
+
+__device__ __forceinline__ uint4 ldg16(const __nv_bfloat16* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__host__ __device__ constexpr size_t route_smem_bytes(int N, int kslots) {
+    return 4 * 32 * 4 + 3 * (size_t)N * 4 + 32 * (size_t)kslots * 4;
+}
+
+// Shared memory of the fused kernel: the routing's, the gathered scores
+// [32][N], the warps' partial tiles [32][512] and the CTA's tile [32][16].
+__host__ __device__ constexpr size_t fused_smem_bytes(int N, int kslots) {
+    return ((route_smem_bytes(N, kslots) + 15) & ~size_t(15)) + 32 * (size_t)N * 4 +
+           (size_t)kFusedWarps * 512 * 4 + 512 * 4;
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(kFusedWarps * 32, 1) route_fused_kernel(RouterArgs r, RouteArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const size_t rsm = (route_smem_bytes(a.N, a.kslots) + 15) & ~size_t(15);
+    float* lg = reinterpret_cast<float*>(smem_raw + rsm);             // [32][N] scores (CTA 0)
+    float* red = lg + 32 * a.N;                                        // [32 warps][512] partial tiles
+    float* lt = red + kFusedWarps * 512;                               // [32 tokens][16 experts] this CTA's tile
+    grid_launch_dependents();    // the expert kernel may start its prologue
+    grid_dependency_wait();      // hidden states come from the preceding kernel
+    const uint32_t rank = cluster_ctarank();   // the whole grid is one cluster
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const int e0 = 16 * (int)rank;
+    const int ntv = min(4, (r.B + 7) / 8);   // 8-token n-tiles holding real tokens
+    const int kbtot = r.d / 64;
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(r.x);
+    const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(r.w);
+
+    float acc[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
+    const int r0 = e0 + g, r1 = e0 + g + 8;
+    for (int kb = warp; kb < kbtot; kb += kFusedWarps) {
+        const int col = kb * 64 + 16 * t;
+        uint4 wa0 = make_uint4(0, 0, 0, 0), wa1 = wa0, wb0 = wa0, wb1 = wa0;
+        if (r0 < r.N) { wa0 = ldg16(w + (size_t)r0 * r.d + col); wa1 = ldg16(w + (size_t)r0 * r.d + col + 8); }
+        if (r1 < r.N) { wb0 = ldg16(w + (size_t)r1 * r.d + col); wb1 = ldg16(w + (size_t)r1 * r.d + col + 8); }
+        const uint32_t A0[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
+        const uint32_t A1[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j >= ntv) break;
+            const int tok = 8 * j + g;
+            uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+            if (tok < r.B) { xa = ldg16(x + (size_t)tok * r.d + col); xb = ldg16(x + (size_t)tok * r.d + col + 8); }
+            const uint32_t X[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16_16816(acc[j], A0[2 * s], A1[2 * s], A0[2 * s + 1], A1[2 * s + 1], X[2 * s], X[2 * s + 1]);
+        }
+    }
+    // the warps' partial tiles (fragment-linear), summed in warp order
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) red[warp * 512 + j * 128 + lane * 4 + q2] = acc[j][q2];
+    __syncthreads();
+    if (threadIdx.x < 512) {
+        const int l = threadIdx.x;
+        float sum = 0.f;
+        for (int w2 = 0; w2 < kFusedWarps; ++w2) sum += red[w2 * 512 + l];
+        const int j = l >> 7, ln = (l >> 2) & 31, q2 = l & 3;
+        const int row = (ln >> 2) + 8 * (q2 >> 1);
+        const int tok = 8 * j + 2 * (ln & 3) + (q2 & 1);
+        const int e = e0 + row;
+        if (tok < r.B && e < r.N) {
+            if (r.bias) sum += r.bias[e];
+            r.logits[(size_t)tok * r.N + e] = sum;
+        }
+        lt[tok * 16 + row] = sum;
+    }
+    const bool clustered = gridDim.x > 1;   // one CTA (N <= 16) is launched without a cluster
+    if (clustered) cluster_sync(); else __syncthreads();   // every CTA's tile is complete
+    if (rank == 0) {
+        for (int q = threadIdx.x; q < r.B * r.N; q += blockDim.x) {
+            const int tok = q / r.N, e = q - tok * r.N;
+            const uint32_t src = (uint32_t)(e >> 4);
+            const float* p = &lt[tok * 16 + (e & 15)];
+            lg[q] = src == 0 ? *p : ld_dsmem_f32(p, src);
+        }
+    }
+    if (clustered) cluster_sync(); else __syncthreads();   // CTA 0 has read every tile: the others may leave
+    if (rank != 0) return;
+    RouteArgs ra = a;
+    ra.logits = lg;
+    route_body<NPL>(ra, smem_raw, 0u, 1u);
+}
+
+template <int NPL>
+cudaError_t launch_route_fused_t(const RouterArgs& r, const RouteArgs& a, cudaStream_t s) {
+    const int ncta = (a.N + 15) / 16;
+    const size_t smem = fused_smem_bytes(a.N, a.kslots);
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(route_fused_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_cap());
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ncta);
+    cfg.blockDim = dim3(kFusedWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = ncta;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ncta > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, route_fused_kernel<NPL>, r, a);
+}
+
+template <int NPL>
 cudaError_t launch_route_t(const RouteArgs& a, cudaStream_t s) {
     const int threads = NPL <= 8 ? 1024 : 512;
     const int ncta = a.B > 0 ? (a.B + 31) / 32 : 1;
@@ -432,6 +588,17 @@ cudaError_t launch_route_t(const RouteArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool route_fused_supported(int dtype, int B, int N, int kslots) {
+    return dtype == MOE_DTYPE_BF16 && B > 0 && B <= 32 && N <= 128 && fused_smem_bytes(N, kslots) <= smem_cap();
+}
+
+cudaError_t launch_route_fused(const RouterArgs& r, const RouteArgs& a, cudaStream_t s) {
+    const int nw = (a.N + 31) / 32;
+    if (nw <= 1) return launch_route_fused_t<1>(r, a, s);
+    if (nw <= 2) return launch_route_fused_t<2>(r, a, s);
+    return launch_route_fused_t<4>(r, a, s);
+}
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     const int nw = (a.N + 31) / 32;

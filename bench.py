@@ -436,7 +436,7 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
         "ffn_us_mean": float(np.mean(ffn_us)),
         "ffn_gbs": ffn_b / (sum(ffn_us) * 1e-6) / 1e9,
         "ffn_bytes_per_launch": ffn_b / n2,
-        "clocks": clk, "launches": 3 * steps,
+        "clocks": clk, "launches": moe.moe_layer_launches(prm, w.F) * steps,
         "objs": (prm, routing, ws, out),
     }
 

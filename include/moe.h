@@ -145,6 +145,16 @@ typedef struct {
 int32_t moe_num_slots(const moe_route_params *params);
 
 /*
+ * Kernels that one moe_decode_layer() call launches for these parameters
+ * and expert FFN width on the current device, or -1 if the parameters are
+ * invalid.  bf16 batches of up to 32 tokens with N <= 128 score and route
+ * in one cluster launch, so a layer is two kernels; otherwise the router
+ * and the routing are separate (three kernels; no router for an empty
+ * batch, and three expert kernels on the fp32 path).
+ */
+int32_t moe_layer_launches(const moe_route_params *params, int32_t d_ff);
+
+/*
  * Bytes of device workspace needed by moe_route / moe_expert_ffn /
  * moe_decode_layer for these parameters and expert FFN width d_ff (pass
  * d_ff = 0 when only moe_route is used).  Returns 0 if the parameters are

@@ -46,6 +46,12 @@ def P(**kw):
 
 def test_slots_and_workspace(lib):
     assert moe.moe_num_slots(P()) == 8
+    # router + routing (one cluster launch where the device allows it) + experts
+    assert moe.moe_layer_launches(P(), 768) in (2, 3)
+    assert moe.moe_layer_launches(P(B=0), 768) == 1            # the routing kernel only
+    assert moe.moe_layer_launches(P(B=64), 768) == 3           # router, routing, experts
+    with pytest.raises(moe.MoeError):
+        moe.moe_layer_launches(P(), 100)                       # d_ff not a multiple of 64
     assert moe.moe_num_slots(P(mode=moe.MODE_OEA, k0=3)) == 8
     assert moe.moe_num_slots(P(mode=moe.MODE_OEA, k0=3, kmax=11)) == 11
     a = moe.moe_workspace_bytes(P(), 768)
