@@ -148,9 +148,10 @@ int32_t moe_num_slots(const moe_route_params *params);
  * Kernels that one moe_decode_layer() call launches for these parameters
  * and expert FFN width on the current device, or -1 if the parameters are
  * invalid.  bf16 batches of up to 32 tokens with N <= 128 score and route
- * in one cluster launch, so a layer is two kernels; otherwise the router
- * and the routing are separate (three kernels; no router for an empty
- * batch, and three expert kernels on the fp32 path).
+ * in one cluster launch, so a layer is two kernels.  Otherwise the router
+ * and the routing are separate launches: three kernels with bf16 experts,
+ * five on the fp32 path (three expert kernels).  An empty batch launches
+ * only the routing kernel.
  */
 int32_t moe_layer_launches(const moe_route_params *params, int32_t d_ff);
 
