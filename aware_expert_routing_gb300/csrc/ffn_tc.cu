@@ -30,15 +30,19 @@
 //     from one 5D tensor map over both matrices).  A TMA unit's rate per SM
 //     grows with the bytes of each operation, so batches of up to 16 tokens
 //     use KB = 4 (64 KB per operation) where d and d_ff allow it, larger
-//     batches KB = 1.  Warp 5 streams the token rows of each stage (16-row
-//     boxes): the whole batch of up to 16 tokens straight from the hidden
-//     states, or rows of the expert-grouped copy of the hidden states, or
-//     (phase B) rows of h once every phase-A tile of the chunk has written
-//     them (a per-chunk counter).  The stage ring takes the shared memory
+//     batches KB = 2 where both are even.  Warp 5 streams the token rows of
+//     each stage (16-row boxes): the whole batch of up to 16 tokens
+//     straight from the hidden states, or rows of the expert-grouped copy
+//     of the hidden states, or (phase B) rows of h once every phase-A tile
+//     of the chunk has written them (a per-chunk counter).  The stage ring takes the shared memory
 //     that the barriers and per-expert tables leave (3 stages of 72 KB at
-//     KB = 4, up to 12 of 18 KB at KB = 1 and nmax = 16).  For batches of up
-//     to 16 tokens warp 4 also loads the first tile's first stages (token
-//     rows, then weights) right after the routing kernel ends.
+//     KB = 4; 3 to 6 stages at KB = 2, by the chunk width).  For batches of
+//     up to 16 tokens warp 4 also loads the first tile's first stages (token
+//     rows, then weights) as soon as the activated experts are known: with
+//     OEA routing, from the S_base that the routing kernel publishes after
+//     phase 1 (the early start: the weights stream while phase 2 and the
+//     grouping run; warp 0 adds the counts, first pairs and token masks
+//     once the routing kernel has completed), else after it ends.
 //   * Warp 6, lane 0, issues the MMAs: four K=16 steps per stage straight
 //     from the swizzled shared memory (no register staging), fp32
 //     accumulators in tensor memory, four accumulator buffers (16 columns
