@@ -28,6 +28,17 @@
 // experts each, turn them into per-expert counts, offsets and the pairs of
 // earlier CTAs, which give each pair's position directly (tokens ascending
 // within an expert).  CTA 0 writes the per-expert arrays.
+//
+// With OEA and one CTA (up to 32 tokens), S_base is published to the
+// workspace as soon as phase 1 is done, each word with the routing call's
+// epoch: the expert kernel, already resident, starts on the activated
+// experts' weights while phase 2 and the grouping run.
+//
+// For bf16 batches of up to 32 tokens with N <= 128, route_fused_kernel
+// also computes the router scores (page section 2 Q1/Q2: every token scores
+// all N experts), in one cluster of N/16 CTAs, and runs the same selection
+// and grouping on them from shared memory, so a layer needs no separate
+// router kernel.
 #include <limits.h>
 
 #include "common.cuh"
