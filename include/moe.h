@@ -185,7 +185,11 @@ moe_status moe_route(const void *hidden, const void *w_router, const float *rout
  * workspace, so no other call may use that workspace in between.  A
  * completed call leaves them as it found them, so it may be repeated on the
  * same routing.  Reads only activated experts, each expert's three
- * matrices once from HBM.
+ * matrices once from HBM.  With OEA routing of up to 16 tokens, the call
+ * starts on the activated experts' weights as soon as the preceding
+ * moe_route() on this workspace and stream has fixed them (its phase 1),
+ * before that routing call's kernel ends; it recognises that call's
+ * published set by a per-call tag the library keeps for the workspace.
  *   hidden  [B][d]        dtype  the hidden states given to moe_route.
  *   w_gate  [N][d_ff][d]  dtype  expert gate projections.
  *   w_up    [N][d_ff][d]  dtype  expert up projections.
