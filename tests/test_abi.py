@@ -50,6 +50,7 @@ def test_slots_and_workspace(lib):
     assert moe.moe_layer_launches(P(), 768) in (2, 3)
     assert moe.moe_layer_launches(P(B=0), 768) == 1            # the routing kernel only
     assert moe.moe_layer_launches(P(B=64), 768) == 3           # router, routing, experts
+    assert moe.moe_layer_launches(P(dtype=moe.DTYPE_F32), 768) == 5   # router, routing, three fp32 expert kernels
     with pytest.raises(moe.MoeError):
         moe.moe_layer_launches(P(), 100)                       # d_ff not a multiple of 64
     assert moe.moe_num_slots(P(mode=moe.MODE_OEA, k0=3)) == 8
