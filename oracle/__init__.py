@@ -46,9 +46,11 @@ def _load():
             i = ctypes.c_int
             lib.oracle_router_logits.argtypes = [P, P, P, i, i, i, P]
             lib.oracle_router_logits.restype = None
-            lib.oracle_route.argtypes = [P, i, i, i, i, i, ctypes.c_float, i, i, i,
+            lib.oracle_route.argtypes = [P, i, i, i, i, i, ctypes.c_float, i, i, i, P,
                                          P, P, P, P, P, P, P, P]
             lib.oracle_route.restype = i
+            lib.oracle_policy_k0.argtypes = [i, i, ctypes.POINTER(ctypes.c_float)]
+            lib.oracle_policy_k0.restype = i
             lib.oracle_expert_ffn.argtypes = [P, P, P, P, i, i, P]
             lib.oracle_expert_ffn.restype = None
             lib.oracle_moe_experts.argtypes = [P, P, P, P, i, i, i, i, P, P, P]
@@ -78,11 +80,23 @@ def router_logits(x, w_router, bias=None) -> np.ndarray:
     return out
 
 
+def policy_k0(B_valid: int, k: int, p: float = 1.0) -> tuple:
+    """(k0, p) of the batch-size-dependent policy (OEA page, section 7,
+    implementation detail 2): plain top-k for at most one real token,
+    ceil(5k/8) below 16 tokens, ceil(3k/8) from 16 tokens on."""
+    pp = ctypes.c_float(p)
+    k0 = _load().oracle_policy_k0(B_valid, k, ctypes.byref(pp))
+    return k0, float(pp.value)
+
+
 def route(logits, mode: int, k: int, k0: int | None = None, p: float = 1.0,
           maxP: int | None = None, kmax: int | None = None,
-          B_valid: int | None = None) -> dict:
+          B_valid: int | None = None, nbase=None) -> dict:
     """Plain top-k or OEA routing of fp32 logits (OEA page, sections 2-5, 7).
 
+    k0 <= 0 (OEA) takes k0 from ``policy_k0``.  ``nbase`` (OEA, optional,
+    [B] ints): phase 1 uses these n_i for the real tokens instead of the
+    top-p count.
     Returns idx [B, kslots] int32, w [B, kslots] fp64, nbase [B], T,
     counts [N], offsets [N+1], active [T], perm [sum counts].
     """
@@ -93,6 +107,9 @@ def route(logits, mode: int, k: int, k0: int | None = None, p: float = 1.0,
     kmax = k if kmax is None else kmax
     B_valid = B if B_valid is None else B_valid
     kslots = k if mode == TOPK else kmax
+    nb_in = None if nbase is None else np.ascontiguousarray(nbase, dtype=np.int32)
+    if nb_in is not None and nb_in.shape != (B,):
+        raise ValueError("nbase must hold one n_i per token")
     idx = np.empty((B, kslots), np.int32)
     w = np.empty((B, kslots), np.float64)
     nbase = np.empty(B, np.int32)
@@ -102,8 +119,8 @@ def route(logits, mode: int, k: int, k0: int | None = None, p: float = 1.0,
     active = np.empty(N, np.int32)
     perm = np.empty(max(B * kslots, 1), np.int32)
     rc = _load().oracle_route(_ptr(logits), B, N, mode, k, k0, ctypes.c_float(p), maxP,
-                              kmax, B_valid, _ptr(idx), _ptr(w), _ptr(nbase), _ptr(T),
-                              _ptr(counts), _ptr(offsets), _ptr(active), _ptr(perm))
+                              kmax, B_valid, _ptr(nb_in), _ptr(idx), _ptr(w), _ptr(nbase),
+                              _ptr(T), _ptr(counts), _ptr(offsets), _ptr(active), _ptr(perm))
     if rc != 0:
         raise ValueError("oracle_route: invalid arguments")
     t = int(T[0])

@@ -95,14 +95,40 @@ static int top_p_count(const float *l, const int *order, int N, float p)
 }
 
 /*
+ * Batch-size-dependent k0 (OEA page, section 7, implementation detail 2):
+ * piggybacking adds nothing for a single token and OEA belongs only to
+ * non-trivial batches, so a batch with at most one real token routes by
+ * plain top-k (k0 = k, top-p off: *p is set to 1); smaller batches take
+ * the larger, safer k0 = ceil(5k/8) and batches of 16 or more tokens the
+ * aggressive k0 = ceil(3k/8).  For k = 8 these are the page's two settings,
+ * k0 = 5 and k0 = 3, whose results the page reports at B = 16 (section 5,
+ * Figs. 2-3, Table 3).
+ */
+int oracle_policy_k0(int B_valid, int k, float *p)
+{
+    if (B_valid <= 1) {
+        *p = 1.0f;
+        return k;
+    }
+    if (B_valid < 16)
+        return (5 * k + 7) / 8;
+    return (3 * k + 7) / 8;
+}
+
+/*
  * Routing for one batch.
  *   logits   [B][N] fp32 (row i of token i)
  *   mode     ORACLE_TOPK or ORACLE_OEA
  *   k        top-k of the plain router (slots per token when mode is top-k)
- *   k0, p    OEA baseline cap and top-p threshold (p >= 1: top-p off)
+ *   k0, p    OEA baseline cap and top-p threshold (p >= 1: top-p off);
+ *            k0 <= 0 takes k0 (and possibly p) from oracle_policy_k0
  *   maxP     deepest rank phase 2 may take an expert from (>= N: no limit)
  *   kmax     experts per token after phase 2 (slots per token in OEA mode)
  *   B_valid  tokens i >= B_valid are padding and select nothing
+ *   nbase_in [B] or NULL (OEA only): phase 1 takes n_i = nbase_in[i]
+ *            (1..k0) for every real token instead of computing t_i; for
+ *            comparing with a router whose fp32 prefix sums land on the
+ *            other side of p for a token whose prefix lies at p
  * Outputs (kslots = k for top-k, kmax for OEA):
  *   idx   [B][kslots] expert ids in ranked order, -1 in unused slots
  *   w     [B][kslots] renormalised weights, 0 in unused slots
@@ -115,17 +141,23 @@ static int top_p_count(const float *l, const int *order, int N, float p)
  * Returns 0, or -1 on invalid arguments.
  */
 int oracle_route(const float *logits, int B, int N, int mode, int k, int k0,
-                 float p, int maxP, int kmax, int B_valid,
+                 float p, int maxP, int kmax, int B_valid, const int *nbase_in,
                  int *idx, double *w, int *nbase, int *T, int *counts,
                  int *offsets, int *active, int *perm)
 {
     if (B < 0 || N < 1 || k < 1 || k > N || B_valid < 0 || B_valid > B)
         return -1;
+    if (mode == ORACLE_OEA && k0 <= 0)
+        k0 = oracle_policy_k0(B_valid, k, &p);
     if (mode == ORACLE_OEA && (k0 < 1 || k0 > k || kmax < k0 || kmax > N ||
                                maxP < 1 || !(p > 0.0f)))
         return -1;
     if (mode != ORACLE_TOPK && mode != ORACLE_OEA)
         return -1;
+    if (mode == ORACLE_OEA && nbase_in)
+        for (int i = 0; i < B_valid; ++i)
+            if (nbase_in[i] < 1 || nbase_in[i] > k0)
+                return -1;
     const int kslots = (mode == ORACLE_TOPK) ? k : kmax;
 
     int *order = malloc(sizeof(int) * (size_t)N * (B > 0 ? B : 1));
@@ -156,8 +188,12 @@ int oracle_route(const float *logits, int B, int N, int mode, int k, int k0,
             }
             const float *l = logits + (size_t)i * N;
             const int *o = order + (size_t)i * N;
-            int t = top_p_count(l, o, N, p);
-            nbase[i] = t < k0 ? t : k0;
+            if (nbase_in) {
+                nbase[i] = nbase_in[i];
+            } else {
+                int t = top_p_count(l, o, N, p);
+                nbase[i] = t < k0 ? t : k0;
+            }
             for (int j = 0; j < nbase[i]; ++j)
                 in_base[o[j]] = 1;             /* S_base = union of baselines */
         }

@@ -37,6 +37,10 @@ MUTANTS = {
                                   "const int bit = 16 * (o / 2 % 2) + 4 * (o % 2) + 8 * (o / 4);"),
     "int4_scale_row_ignored": ("(size_t)rb * 32 + (size_t)rr * 2;", "(size_t)rb * 32;"),
     "int4_chunk_order_swapped": ("((size_t)rbi * nkb + kb) * chunk", "((size_t)kb * (rows / rb) + rbi) * chunk"),
+    "given_baseline_sizes_ignored": ("nbase[i] = nbase_in[i];", "nbase[i] = k0;"),
+    "policy_keeps_oea_for_one_token": ("if (B_valid <= 1) {", "if (B_valid < 1) {"),
+    "policy_smaller_k0_at_small_batches": ("if (B_valid < 16)\n        return (5 * k + 7) / 8;",
+                                           "if (B_valid < 16)\n        return (3 * k + 7) / 8;"),
 }
 
 
@@ -44,7 +48,7 @@ def pins():
     """Every pin test, bound to fixed parameters."""
     out = [R.test_topk_invariants_and_grouping, R.test_weights_are_renormalised_scores,
            R.test_top_p_worked_example, R.test_special_cases_reduce_to_known_routers,
-           R.test_padding_tokens_select_nothing,
+           R.test_padding_tokens_select_nothing, R.test_batch_size_policy,
            FFN.test_swiglu_worked_example, FFN.test_expert_algebra,
            FFN.test_combine_is_weighted_sum_in_slot_order, FFN.test_router_logits_match_library,
            FFN.test_dequant_int4_codes_and_layout, FFN.test_int4_round_trip_within_half_step]
@@ -54,6 +58,7 @@ def pins():
     for d, F in [(8, 5), (96, 40)]:
         out.append(lambda d=d, F=F: FFN.test_expert_matches_library_fp64(d, F))
     out.append(lambda: R.test_union_size_monte_carlo(16, R.OEA, 3))
+    out += [lambda s=s: R.test_given_baseline_sizes_follow_the_definitions(s, 2, 12, 4) for s in range(3)]
     return out
 
 

@@ -80,6 +80,14 @@ def test_oea_matches_brute_force(seed, k0, p, maxP, kmax):
             pytest.skip("prefix within 1e-4 of p: decided by rounding")
         n.append(min(k0, t))
     assert list(r["nbase"]) == n
+    check_union_and_phase2(lg, r, n, maxP, kmax)
+
+
+def check_union_and_phase2(lg, r, n, maxP, kmax):
+    """The union of the top-n_i baselines and the phase-2 picks, rebuilt
+    from the OEA page's definitions (section 2 Q2, section 3) by subset
+    enumeration, for given baseline sizes n_i."""
+    B, N = lg.shape
     base = [brute_top(lg[i], range(N), n[i]) for i in range(B)]
     S_base = set().union(*base)
     assert r["T"] == len(S_base)
@@ -242,6 +250,59 @@ def test_union_size_monte_carlo(B, mode, kk):
     assert abs(Ts.mean() - want) < 4.5 * se + 1e-9, (Ts.mean(), want, se)
 
 
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("k0,maxP,kmax", [(2, 12, 4), (3, 6, 4), (3, 12, 6)])
+def test_given_baseline_sizes_follow_the_definitions(seed, k0, maxP, kmax):
+    """Phase 1 with the baseline sizes n_i given (the n_base input): the
+    union and phase 2 follow the definitions for those n_i, and passing the
+    oracle's own n_i reproduces its routing exactly."""
+    rng = np.random.default_rng(300 + seed)
+    B, N, k = 5, 12, 4
+    lg = (tied_logits(rng, B, N, 6) if seed % 3 == 0
+          else (rng.standard_normal((B, N)) * 1.5).astype(np.float32))
+    nb = rng.integers(1, k0 + 1, size=B).astype(np.int32)
+    r = oracle.route(lg, OEA, k, k0, 0.6, maxP, kmax, nbase=nb)
+    assert list(r["nbase"]) == list(nb)
+    check_union_and_phase2(lg, r, list(nb), maxP, kmax)
+    own = oracle.route(lg, OEA, k, k0, 0.6, maxP, kmax)
+    again = oracle.route(lg, OEA, k, k0, 0.6, maxP, kmax, nbase=own["nbase"])
+    for key in ("idx", "nbase", "counts", "offsets", "active", "perm"):
+        assert np.array_equal(own[key], again[key])
+    assert own["T"] == again["T"] and np.array_equal(own["w"], again["w"])
+    with pytest.raises(ValueError):
+        oracle.route(lg, OEA, k, k0, 0.6, maxP, kmax, nbase=np.full(B, k0 + 1, np.int32))
+
+
+def test_batch_size_policy():
+    """Batch-size-dependent k0 (OEA page, section 7, implementation detail 2):
+    piggybacking adds nothing for one token, so OEA is off there (plain
+    top-k, top-p off); smaller batches keep a larger, safer k0 than larger
+    ones; for k = 8 the two values are the page's settings k0 = 5 and
+    k0 = 3.  k0 <= 0 in a routing call applies the policy."""
+    for k in (1, 4, 8, 16):
+        assert oracle.policy_k0(1, k, 0.7) == (k, 1.0)
+        assert oracle.policy_k0(0, k, 0.7) == (k, 1.0)
+        ks = [oracle.policy_k0(B, k, 0.7)[0] for B in range(1, 257)]
+        assert all(a >= b for a, b in zip(ks, ks[1:])) and all(1 <= x <= k for x in ks)
+    assert {oracle.policy_k0(B, 8)[0] for B in range(2, 16)} == {5}
+    assert {oracle.policy_k0(B, 8)[0] for B in range(16, 257)} == {3}
+    k0, p = oracle.policy_k0(4, 8, 0.7)
+    assert abs(p - 0.7) < 1e-7
+    rng = np.random.default_rng(17)
+    lg = rng.standard_normal((64, 128)).astype(np.float32)
+    one = oracle.route(lg[:1], OEA, 8, 0, 0.7)
+    plain = oracle.route(lg[:1], TOPK, 8)
+    assert one["T"] == 8 and np.array_equal(one["idx"], plain["idx"])
+    assert np.allclose(one["w"], plain["w"], rtol=0, atol=1e-15)
+    padded = oracle.route(lg[:5], OEA, 8, 0, 1.0, B_valid=1)   # one real token, four padding
+    assert padded["T"] == 8 and np.array_equal(padded["idx"][0], plain["idx"][0])
+    for B in (2, 4, 15, 16, 64):
+        k0, _ = oracle.policy_k0(B, 8, 0.9)
+        a, b = oracle.route(lg[:B], OEA, 8, 0, 0.9), oracle.route(lg[:B], OEA, 8, k0, 0.9)
+        assert np.array_equal(a["idx"], b["idx"]) and a["T"] == b["T"]
+        assert (a["nbase"] <= k0).all()
+
+
 def test_invalid_arguments_rejected():
     lg = np.zeros((2, 8), np.float32)
     with pytest.raises(ValueError):
@@ -249,6 +310,6 @@ def test_invalid_arguments_rejected():
     with pytest.raises(ValueError):
         oracle.route(lg, OEA, 4, 5, 1.0)
     with pytest.raises(ValueError):
-        oracle.route(lg, OEA, 4, 0, 1.0)
-    with pytest.raises(ValueError):
         oracle.route(lg, OEA, 4, 2, 0.0)
+    with pytest.raises(ValueError):
+        oracle.route(lg, OEA, 4, 2, 1.0, nbase=np.zeros(2, np.int32))
