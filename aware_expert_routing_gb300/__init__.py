@@ -26,8 +26,8 @@ FLAG_NONFINITE_SCORE, FLAG_WAIT_TIMEOUT, FLAG_BAD_INDEX = 0x1, 0x2, 0x4
 MAX_TOKENS, MAX_EXPERTS, MAX_SLOTS = 256, 1024, 32
 
 EXPORTED = ["moe_num_slots", "moe_layer_launches", "moe_workspace_bytes", "moe_route", "moe_expert_ffn",
-            "moe_expert_ffn_mixed", "moe_decode_layer", "moe_decode_layer_static", "moe_device_status",
-            "moe_synth_normal", "moe_status_string", "moe_last_error"]
+            "moe_expert_ffn_mixed", "moe_decode_layer", "moe_decode_layer_mixed", "moe_decode_layer_static",
+            "moe_device_status", "moe_device_status_static", "moe_set_wait_timeout_us", "moe_synth_normal", "moe_status_string", "moe_last_error"]
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -85,11 +85,18 @@ def load(path: str | None = None):
     lib.moe_decode_layer.argtypes = [V, V, V, V, V, V, ctypes.c_int32, P(_Params), P(_Routing), V,
                                      V, ctypes.c_size_t, V]
     lib.moe_decode_layer.restype = ctypes.c_int
+    lib.moe_decode_layer_mixed.argtypes = [V, V, V, V, V, V, P(_Mixed), ctypes.c_int32, P(_Params), P(_Routing),
+                                           V, V, ctypes.c_size_t, V]
+    lib.moe_decode_layer_mixed.restype = ctypes.c_int
     lib.moe_decode_layer_static.argtypes = [V, V, V, V, V, V, ctypes.c_int32, P(_Params), P(_Routing),
                                             V, V]
     lib.moe_decode_layer_static.restype = ctypes.c_int
     lib.moe_device_status.argtypes = [V, V, P(ctypes.c_uint32)]
     lib.moe_device_status.restype = ctypes.c_int
+    lib.moe_device_status_static.argtypes = [V, P(ctypes.c_uint32)]
+    lib.moe_device_status_static.restype = ctypes.c_int
+    lib.moe_set_wait_timeout_us.argtypes = [ctypes.c_uint32]
+    lib.moe_set_wait_timeout_us.restype = ctypes.c_int
     lib.moe_synth_normal.argtypes = [V, ctypes.c_int32, ctypes.c_uint64, ctypes.c_uint64,
                                      ctypes.c_uint64, ctypes.c_float, V]
     lib.moe_synth_normal.restype = ctypes.c_int
@@ -286,6 +293,24 @@ def moe_decode_layer(hidden, w_router, router_bias, w_gate, w_up, w_down, d_ff: 
     return out
 
 
+def moe_decode_layer_mixed(hidden, w_router, router_bias, w_gate, w_up, w_down, mixed: MixedExperts,
+                           d_ff: int, params: RouteParams, routing: Routing, out, workspace: torch.Tensor,
+                           stream=None):
+    """The whole layer with bf16 hot and INT4 cold experts in one call."""
+    for t, n in ((hidden, "hidden"), (w_router, "w_router"), (w_gate, "w_gate"), (w_up, "w_up"),
+                 (w_down, "w_down"), (out, "out")):
+        _need(t, torch.bfloat16, n)
+    if router_bias is not None:
+        _need(router_bias, torch.float32, "router_bias")
+    _need(mixed.slot, torch.int32, "slot")
+    st = load().moe_decode_layer_mixed(_ptr(hidden), _ptr(w_router), _ptr(router_bias), _ptr(w_gate),
+                                       _ptr(w_up), _ptr(w_down), ctypes.byref(mixed.c()), d_ff,
+                                       ctypes.byref(params.c()), ctypes.byref(routing.c()), _ptr(out),
+                                       _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "moe_decode_layer_mixed")
+    return out
+
+
 def moe_decode_layer_static(hidden, w_router, router_bias, w_gate, w_up, w_down, d_ff: int,
                             params: RouteParams, routing: Routing, out, stream=None):
     """moe_decode_layer without a workspace, for callers that cannot
@@ -309,6 +334,19 @@ def moe_device_status(workspace: torch.Tensor, stream=None) -> int:
     f = ctypes.c_uint32(0)
     load().moe_device_status(_ptr(workspace), _stream(stream), ctypes.byref(f))
     return int(f.value)
+
+
+def moe_device_status_static(stream=None) -> int:
+    """Synchronises the stream; returns and clears the flag word of the
+    calls of moe_decode_layer_static on the current device."""
+    f = ctypes.c_uint32(0)
+    load().moe_device_status_static(_stream(stream), ctypes.byref(f))
+    return int(f.value)
+
+
+def moe_set_wait_timeout_us(microseconds: int):
+    """Bound of every in-kernel wait (0: the default of two seconds)."""
+    _check(load().moe_set_wait_timeout_us(int(microseconds)), "moe_set_wait_timeout_us")
 
 
 def moe_synth_normal(dst: torch.Tensor, seed: int, scale: float, start: int = 0, stream=None):

@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <unordered_map>
@@ -39,6 +40,21 @@ struct Params {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// k0 chosen from the batch (OEA page, section 7, implementation detail 2:
+// piggybacking is redundant for a single token and pays only for
+// non-trivial batches, where a larger, safer k0 suits smaller batches).
+// At most one real token: OEA is off, i.e. k0 = k with top-p off, which
+// routes exactly as plain top-k.  2..15 tokens: ceil(5k/8); 16 or more:
+// ceil(3k/8) -- for k = 8 the page's two settings, 5 and 3, whose results
+// it reports at 16 tokens.
+int policy_k0(int B_valid, int k, float* p) {
+    if (B_valid <= 1) {
+        *p = 1.f;
+        return k;
+    }
+    return B_valid < 16 ? (5 * k + 7) / 8 : (3 * k + 7) / 8;
+}
+
 moe_status resolve(const moe_route_params* in, Params& P) {
     if (!in) return fail(MOE_ERR_ARG, "params is NULL");
     P.B = in->B;
@@ -65,8 +81,9 @@ moe_status resolve(const moe_route_params* in, Params& P) {
         P.kmax = P.k;
         P.kslots = P.k;
     } else if (P.mode == MOE_MODE_OEA) {
-        if (P.k0 < 1 || P.k0 > P.k) return fail(MOE_ERR_ARG, "k0=%d outside 1..k=%d", P.k0, P.k);
         if (!(P.p > 0.f) || !(P.p <= 1.f)) return fail(MOE_ERR_ARG, "p=%g outside (0, 1]", (double)P.p);
+        if (P.k0 <= 0) P.k0 = policy_k0(P.B_valid, P.k, &P.p);
+        if (P.k0 < 1 || P.k0 > P.k) return fail(MOE_ERR_ARG, "k0=%d outside 1..k=%d", P.k0, P.k);
         P.maxP = (in->maxP <= 0 || in->maxP >= P.N) ? P.N : in->maxP;
         P.kmax = in->kmax <= 0 ? P.k : in->kmax;
         if (P.kmax < P.k0 || P.kmax > slot_cap)
@@ -137,11 +154,18 @@ std::mutex g_map_mu;
 std::mutex g_epoch_mu;
 std::unordered_map<const void*, uint32_t> g_epoch;
 
+// The epoch the next routing call on `ws` publishes under; recorded by
+// commit_epoch() once that call's kernel has been launched.
 uint32_t next_epoch(const void* ws) {
     std::lock_guard<std::mutex> lk(g_epoch_mu);
-    uint32_t& e = g_epoch[ws];
-    e = e + 1u == 0u ? 1u : e + 1u;
-    return e;
+    const auto it = g_epoch.find(ws);
+    const uint32_t e = it == g_epoch.end() ? 0u : it->second;
+    return e + 1u == 0u ? 1u : e + 1u;
+}
+
+void commit_epoch(const void* ws, uint32_t e) {
+    std::lock_guard<std::mutex> lk(g_epoch_mu);
+    g_epoch[ws] = e;
 }
 
 uint32_t current_epoch(const void* ws) {   // 0: no routing call recorded for this workspace
@@ -322,12 +346,36 @@ int num_sms() {
 
 }  // namespace
 
+namespace {
+// Bound of every in-kernel wait (moe_set_wait_timeout_us), microseconds.
+constexpr uint32_t kDefaultWaitUs = 2000000u;
+std::atomic<uint32_t> g_wait_us{kDefaultWaitUs};
+}  // namespace
+
 namespace moe {
+// SM cycles per microsecond assumed for the wait bound: the GB300's SM
+// clock is at most 2.07 GHz, so a bound of t microseconds lasts at least
+// about t microseconds.
+long long wait_cycles_now() { return (long long)g_wait_us.load() * 2000LL; }
+
 // Records `message` as this thread's last error and returns `status`.
 moe_status report_error(moe_status status, const char* message) { return fail(status, "%s", message); }
 }  // namespace moe
 
 namespace {
+// The mixed-precision expert descriptor (slot table and INT4 images).
+moe_status check_mixed(const moe_mixed_experts* mixed, const Params& P, int d_ff) {
+    if (P.dtype != MOE_DTYPE_BF16) return fail(MOE_ERR_ARG, "mixed experts need bf16 activations");
+    if (P.d % 128 != 0 || d_ff % 128 != 0) return fail(MOE_ERR_ARG, "mixed experts need d and d_ff multiples of 128");
+    if (!mixed->slot || !aligned(mixed->slot, 4)) return fail(MOE_ERR_ARG, "mixed->slot is NULL or misaligned");
+    if (mixed->n_hot < 1 || mixed->n_cold < 0) return fail(MOE_ERR_ARG, "need n_hot >= 1 and n_cold >= 0");
+    const void* q[] = {mixed->q_gate, mixed->q_up, mixed->q_down};
+    for (const void* p : q)
+        if ((mixed->n_cold > 0 && !p) || !aligned(p, 16))
+            return fail(MOE_ERR_ARG, "an INT4 image is NULL or not 16-byte aligned");
+    return MOE_OK;
+}
+
 moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w_up, const void* w_down,
                            const moe_mixed_experts* mixed, int32_t d_ff, const moe_route_params* params,
                            const moe_routing* routing, void* out, void* workspace, size_t workspace_bytes,
@@ -339,17 +387,7 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     if (d_ff < 64 || d_ff % 64 != 0 || d_ff > 16384)
         return fail(MOE_ERR_ARG, "d_ff=%d must be a multiple of 64 in 64..16384", d_ff);
     const int n_hot = mixed ? mixed->n_hot : P.N;
-    if (mixed) {
-        if (P.dtype != MOE_DTYPE_BF16) return fail(MOE_ERR_ARG, "mixed experts need bf16 activations");
-        if (P.d % 128 != 0 || d_ff % 128 != 0)
-            return fail(MOE_ERR_ARG, "mixed experts need d and d_ff multiples of 128");
-        if (!mixed->slot || !aligned(mixed->slot, 4)) return fail(MOE_ERR_ARG, "mixed->slot is NULL or misaligned");
-        if (mixed->n_hot < 1 || mixed->n_cold < 0) return fail(MOE_ERR_ARG, "need n_hot >= 1 and n_cold >= 0");
-        const void* q[] = {mixed->q_gate, mixed->q_up, mixed->q_down};
-        for (const void* p : q)
-            if ((mixed->n_cold > 0 && !p) || !aligned(p, 16))
-                return fail(MOE_ERR_ARG, "an INT4 image is NULL or not 16-byte aligned");
-    }
+    if (mixed && (st = check_mixed(mixed, P, d_ff)) != MOE_OK) return st;
     const void* req[] = {w_gate, w_up, w_down, hidden, out};
     for (int i = 0; i < 5; ++i) {
         if (!req[i] && (i < 3 || P.B > 0)) return fail(MOE_ERR_ARG, "a tensor pointer is NULL");
@@ -396,6 +434,7 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     a.d = P.d;
     a.F = d_ff;
     a.kslots = P.kslots;
+    a.wait_cycles = wait_cycles_now();
 
     cudaError_t e;
     if (P.dtype == MOE_DTYPE_F32) {
@@ -526,6 +565,7 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
     }
     e = fused ? launch_route_fused(ra, a, s) : launch_route(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    if (a.epoch) commit_epoch(workspace, a.epoch);   // an expert call on this workspace now waits for it
     return MOE_OK;
 }
 
@@ -555,6 +595,22 @@ moe_status moe_decode_layer(const void* hidden, const void* w_router, const floa
                           stream);
 }
 
+moe_status moe_decode_layer_mixed(const void* hidden, const void* w_router, const float* router_bias,
+                                  const void* w_gate, const void* w_up, const void* w_down,
+                                  const moe_mixed_experts* mixed, int32_t d_ff, const moe_route_params* params,
+                                  const moe_routing* routing, void* out, void* workspace, size_t workspace_bytes,
+                                  moe_stream_t stream) {
+    if (!mixed) return fail(MOE_ERR_ARG, "mixed is NULL");
+    Params P;
+    moe_status st = resolve(params, P);
+    if (st != MOE_OK) return st;
+    if ((st = check_mixed(mixed, P, d_ff)) != MOE_OK) return st;   // before the routing launches
+    if ((st = moe_route(hidden, w_router, router_bias, params, routing, workspace, workspace_bytes, stream)) != MOE_OK)
+        return st;
+    return expert_ffn_impl(hidden, w_gate, w_up, w_down, mixed, d_ff, params, routing, out, workspace,
+                           workspace_bytes, stream);
+}
+
 moe_status moe_device_status(void* workspace, moe_stream_t stream, uint32_t* flags) {
     if (!workspace || !aligned(workspace, 256)) return fail(MOE_ERR_WORKSPACE, "bad workspace");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -576,6 +632,11 @@ moe_status moe_synth_normal(void* dst, int32_t dtype, uint64_t n, uint64_t start
     if (!std::isfinite(scale)) return fail(MOE_ERR_ARG, "scale is not finite");
     cudaError_t e = launch_synth(dst, dtype, n, start, seed, scale, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "synth launch");
+    return MOE_OK;
+}
+
+moe_status moe_set_wait_timeout_us(uint32_t microseconds) {
+    g_wait_us.store(microseconds ? microseconds : kDefaultWaitUs);
     return MOE_OK;
 }
 

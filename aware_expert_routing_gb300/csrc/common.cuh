@@ -136,7 +136,14 @@ struct FfnArgs {
     // follows; epoch 0: wait for the whole routing instead.
     const uint64_t* uwords;
     uint32_t epoch;
+    // Bound of every wait in the expert kernel, in SM clock cycles (about
+    // 2000 per microsecond); a wait that runs longer gives up and raises
+    // MOE_FLAG_WAIT_TIMEOUT.
+    long long wait_cycles;
 };
+
+// Bound of in-kernel waits set with moe_set_wait_timeout_us, in cycles.
+long long wait_cycles_now();
 
 // Launchers (defined in the .cu files).
 cudaError_t launch_router(const RouterArgs& a, int dtype, cudaStream_t s);

@@ -110,7 +110,6 @@ constexpr uint32_t kTmemColsSmall = kAcc * 16;  // batches of up to 16 tokens
 constexpr uint32_t kBarGather = 2;       // named barrier of the warps that copy grouped rows
 constexpr int kGatherThreads = (kEpiWarps + kConvWarps + 1) * 32;   // warps 0-3 and 7-15
 constexpr int kGatherRows = 64;          // grouped rows per pass
-constexpr long long kWaitCycles = 4000000000LL;   // about two seconds
 static_assert(kTmemCols <= 512, "tensor memory has 512 columns");
 
 struct Smem {
@@ -140,6 +139,7 @@ struct Smem {
     int tn;                              // activated experts (T)
     int abort_flag;
     int last_flag;
+    long long wait_cycles;               // bound of every wait (FfnArgs::wait_cycles)
 };
 
 // Per-expert tables in shared memory, after Smem, sized by N at launch.
@@ -185,6 +185,8 @@ __device__ __forceinline__ Tile decode_tile(int t, int rbn, const Tabs& X, int T
     return T;
 }
 
+__device__ __forceinline__ bool aborted(Smem& S) { return *(volatile int*)&S.abort_flag != 0; }
+
 __device__ __forceinline__ void give_up(Smem& S, uint32_t* flags) {
     *(volatile int*)&S.abort_flag = 1;
     raise_flag(flags, kFlagTimeout);
@@ -197,7 +199,7 @@ __device__ __forceinline__ void wait_bar(uint64_t* bar, uint32_t parity, Smem& S
     const long long t0 = clock64();
     while (!*(volatile int*)&S.abort_flag) {
         if (mbar_try_wait(bar, parity)) return;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > S.wait_cycles) {
             give_up(S, flags);
             return;
         }
@@ -210,7 +212,7 @@ __device__ __forceinline__ void wait_counter(const uint32_t* p, uint32_t need, S
     const long long t0 = clock64();
     while (!*(volatile int*)&S.abort_flag) {
         if (ld_acquire_gpu(p) >= need) return;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > S.wait_cycles) {
             give_up(S, flags);
             return;
         }
@@ -226,7 +228,7 @@ __device__ __forceinline__ void wait_zero(const uint32_t* p, Smem& S, uint32_t* 
     uint32_t ns = 32;
     while (!*(volatile int*)&S.abort_flag) {
         if (ld_acquire_gpu(p) == 0u) return;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > S.wait_cycles) {
             give_up(S, flags);
             return;
         }
@@ -245,7 +247,7 @@ __device__ __forceinline__ uint32_t early_union_word(const FfnArgs& A, int lane,
     uint64_t v = ld_acquire_gpu_u64(&A.uwords[lane]);
     while (!__all_sync(0xffffffffu, (uint32_t)(v >> 32) == A.epoch)) {
         if (__any_sync(0xffffffffu, *(volatile int*)&S.abort_flag != 0)) return 0u;
-        if (__any_sync(0xffffffffu, clock64() - t0 > kWaitCycles)) {
+        if (__any_sync(0xffffffffu, clock64() - t0 > S.wait_cycles)) {
             if (lane == 0) give_up(S, flags);
             return 0u;
         }
@@ -370,6 +372,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         fence_barrier_init();
         S.abort_flag = 0;
         S.fast_ops = 0;
+        S.wait_cycles = A.wait_cycles;
+        for (int i = 0; i < 32; ++i) S.uw[i] = 0u;   // read as "no expert" if a wait gives up first
     }
     // accumulator buffers: kAcc x nmax columns, nmax = 16 for batches of up to 16
     const uint32_t tmem_cols = small_b ? kTmemColsSmall : kTmemCols;
@@ -405,7 +409,10 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         const int rbA0 = F / 64, t0 = (int)blockIdx.x;
         int e = -1;   // expert of phase-A tile t0 (active index t0 / rbA0), if there is one
         if (early) {
-            const uint32_t word = early_union_word(A, lane, S, flags);
+            // experts N and above do not exist: their bits are dropped
+            const int nb = A.N - 32 * lane;
+            const uint32_t word = early_union_word(A, lane, S, flags) &
+                                  (nb >= 32 ? 0xffffffffu : nb > 0 ? (1u << nb) - 1u : 0u);
             S.uw[lane] = word;   // for warp 0's tables
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.union_full);
@@ -457,7 +464,9 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     }
     if (warp == 0 && early) {   // the tables from the union: one chunk per expert
         wait_bar(&S.union_full, 0, S, flags);
-        const uint32_t word = S.uw[lane];
+        const int nbits = A.N - 32 * lane;   // at most N experts, so the tables stay in bounds
+        const uint32_t word = *(volatile uint32_t*)&S.uw[lane] &
+                              (nbits >= 32 ? 0xffffffffu : nbits > 0 ? (1u << nbits) - 1u : 0u);
         const int c = __popc(word);
         int inc = c;
 #pragma unroll
@@ -636,7 +645,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             for (int n = 0;; ++n) {
                 const int q = n % kQ;
                 if (n >= kQ) wait_bar(&S.tq_empty[q], ((n / kQ) - 1) & 1, S, flags);
-                const int tile = next0 < Ttot ? next0 : -1;
+                const int tile = next0 < Ttot && !aborted(S) ? next0 : -1;   // no new copies once a wait gave up
                 S.tq[q] = tile;
                 mbar_arrive(&S.tq_full[q]);
                 if (tile < 0) break;
@@ -650,6 +659,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 for (int s = n == 0 ? fast_stages : 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
+                    if (aborted(S)) break;
                     unsigned char* dst = ring + (size_t)slot * slot_bytes;
                     if (sl < 0) {
                         // INT4 expert: the packed chunks of the stage's KB blocks are
@@ -713,6 +723,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         for (int n = 0;; ++n) {
             const int q = n % kQ;
             wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
+            if (aborted(S)) break;
             const int tile = S.tq[q];
             if (tile < 0) break;
             const bool ph_a = tile < TA;
@@ -746,6 +757,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 for (int s = n == 0 ? fast_ops : 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
+                    if (aborted(S)) break;
                     mbar_arrive_expect_tx(&S.full[slot], nb * 2048 * KB);   // rows past the end read as zeros
                     unsigned char* dst = ring + (size_t)slot * slot_bytes + KB * kWBytes;
                     if (small_b) {
@@ -769,6 +781,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             for (int n = 0;; ++n) {
                 const int q = n % kQ;
                 wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
+                if (aborted(S)) break;
                 const int tile = S.tq[q];
                 if (tile < 0) break;
                 const bool ph_a = tile < TA;
@@ -794,6 +807,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                         wait_bar(&S.cfull[slot], (cpar >> slot) & 1u, S, flags);
                         cpar ^= 1u << slot;
                     }
+                    if (aborted(S)) break;   // the stage may not have landed: issue nothing more
                     tmem_fence_after_sync();
                     const uint32_t a0 = smem_u32(ring + (size_t)slot * slot_bytes);
                     const uint32_t b0 = a0 + KB * kWBytes;
@@ -809,7 +823,10 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 umma_commit(&S.acc_full[b]);
             }
             umma_commit(&S.mma_done);
-            wait_bar(&S.mma_done, 0, S, flags);
+            // Every MMA issued has completed before the tensor memory is
+            // freed, also after a wait gave up (bounded, not cut short).
+            for (const long long t0 = clock64(); !mbar_try_wait(&S.mma_done, 0) && clock64() - t0 < S.wait_cycles;) {
+            }
         }
         __syncwarp();
     } else if (warp == kWarpN) {
@@ -915,6 +932,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         for (int n = 0;; ++n) {
             const int q = n % kQ;
             wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
+            if (aborted(S)) break;
             const int tile = S.tq[q];
             if (tile < 0) break;
             const bool ph_a = tile < TA;
@@ -922,6 +940,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const int b = n % kAcc;
             const int ngroups = (ph_a && small_b) ? 1 : (T.ntok + 15) >> 4;   // 16-column groups of D
             wait_bar(&S.acc_full[b], (n / kAcc) & 1, S, flags);
+            if (aborted(S)) break;
             tmem_fence_after_sync();
             if (ph_a) {
                 // D row i = (2g + m) * 8 + r holds gate (m = 0) or up (m = 1) row
@@ -1052,6 +1071,13 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     }
 
     // ---- release the tensor memory; the last CTA resets the counters ----
+    // After a wait gave up, stages may have been issued that no MMA waited
+    // for: give their TMA copies (a few, each landing within microseconds)
+    // a bounded 20 us to land before the CTA's shared memory is released.
+    if (aborted(S)) {
+        const long long t0 = clock64();
+        while (clock64() - t0 < 40000) __nanosleep(1000);
+    }
     tmem_fence_before_sync();
     __syncthreads();
     if (warp == kWarpM) {
@@ -1090,6 +1116,13 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
         if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
         if ((e = cudaFuncSetAttribute(ffn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, v)) != cudaSuccess)
             return e;
+        // The CTAs wait for one another, so the grid (one CTA per SM) must be
+        // able to be resident at once: one CTA of this size has to fit an SM.
+        int per_sm = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_tc_kernel, kThreads, (size_t)v)) !=
+            cudaSuccess)
+            return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
         smem_optin[dev] = v;
     }
     FfnArgs a = a_in;

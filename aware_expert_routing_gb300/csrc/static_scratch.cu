@@ -9,6 +9,7 @@
 // taken from one fixed array in the library's device memory instead of the
 // caller's workspace.  It allocates nothing: no cudaMalloc, no cudaFree, no
 // allocating library routine.
+#include <cstddef>
 #include <cstdio>
 #include <mutex>
 
@@ -63,11 +64,22 @@ extern "C" moe_status moe_decode_layer_static(const void* hidden, const void* w_
     void* ws = nullptr;
     moe_status st = scratch_address(&ws);
     if (st != MOE_OK) return st;
-    // The counters and flags at the front of the scratch must start at zero.
+    // The counters at the front of the scratch must start at zero.  The flag
+    // word (the header's first four bytes) is kept, so that flags raised by
+    // earlier calls stay readable with moe_device_status_static().
     const moe::WsLayout L = moe::ws_layout(params->B, params->N, params->d, moe_num_slots(params), d_ff,
                                            params->dtype == MOE_DTYPE_BF16 ? 2 : 4);
-    cudaError_t e = cudaMemsetAsync(ws, 0, L.pos_of, reinterpret_cast<cudaStream_t>(stream));
+    static_assert(offsetof(moe::WsHeader, flags) == 0, "the flag word leads the header");
+    cudaError_t e = cudaMemsetAsync(static_cast<unsigned char*>(ws) + sizeof(uint32_t), 0,
+                                    L.pos_of - sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return moe::report_error(MOE_ERR_CUDA, cudaGetErrorString(e));
     return moe_decode_layer(hidden, w_router, router_bias, w_gate, w_up, w_down, d_ff, params, routing, out, ws,
                             kScratchBytes, stream);
+}
+
+extern "C" moe_status moe_device_status_static(moe_stream_t stream, uint32_t* flags) {
+    void* ws = nullptr;
+    moe_status st = scratch_address(&ws);
+    if (st != MOE_OK) return st;
+    return moe_device_status(ws, stream, flags);
 }

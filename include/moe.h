@@ -83,7 +83,12 @@ typedef enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 } moe_dtype;
  *   N        experts, 1..MOE_MAX_EXPERTS.
  *   k        experts per token of the plain router, 1..min(N, 32).
  *   mode     MOE_MODE_TOPK or MOE_MODE_OEA.
- *   k0       OEA baseline cap, 1..k.
+ *   k0       OEA baseline cap, 1..k; <= 0 chooses it from the batch
+ *            (section 7, implementation detail 2: piggybacking adds nothing
+ *            for a single token, and smaller batches want a larger, safer
+ *            k0): B_valid <= 1 routes as plain top-k (k0 = k, top-p off),
+ *            2..15 real tokens take k0 = ceil(5k/8), 16 or more
+ *            ceil(3k/8) -- for k = 8 the page's settings 5 and 3.
  *   p        OEA top-p threshold in (0, 1]; p >= 1 switches top-p off
  *            (t_i = N), as in the simplified router of section 5.
  *   maxP     OEA: deepest rank of the token's own list that phase 2 may
@@ -245,6 +250,27 @@ moe_status moe_expert_ffn_mixed(const void *hidden, const void *w_gate, const vo
                                 const moe_routing *routing, void *out, void *workspace, size_t workspace_bytes,
                                 moe_stream_t stream);
 
+/*
+ * The whole layer with mixed-precision experts in one call: moe_route, then
+ * moe_expert_ffn_mixed, on the same stream and workspace.  `mixed` is the
+ * per-expert descriptor of the DynaExq page's stable expert handles
+ * (section 2.2; section 3.2 for the precision tiers): for every expert id,
+ * its slot says where its current version lives -- a bf16 expert of
+ * w_gate / w_up / w_down, or a packed INT4 image -- so the kernels resolve
+ * each activated expert through the table and a caller switches an
+ * expert's version by rewriting its slot (and image) between calls.
+ * Arguments, layouts and results as moe_route and moe_expert_ffn_mixed;
+ * every argument, the descriptor included, is checked before anything is
+ * launched.  With OEA routing of up to 16 tokens the expert kernel starts
+ * on the activated experts before the routing kernel ends, as for
+ * moe_expert_ffn.
+ */
+moe_status moe_decode_layer_mixed(const void *hidden, const void *w_router, const float *router_bias,
+                                  const void *w_gate, const void *w_up, const void *w_down,
+                                  const moe_mixed_experts *mixed, int32_t d_ff,
+                                  const moe_route_params *params, const moe_routing *routing, void *out,
+                                  void *workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* moe_route followed by moe_expert_ffn on the same stream. */
 moe_status moe_decode_layer(const void *hidden, const void *w_router, const float *router_bias,
                             const void *w_gate, const void *w_up, const void *w_down,
@@ -266,14 +292,17 @@ moe_status moe_decode_layer(const void *hidden, const void *w_router, const floa
  *     MOE_STATIC_SCRATCH_BYTES is rejected with MOE_ERR_WORKSPACE before
  *     anything is launched.
  *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before
- *     any stream capture.
+ *     per device, with that device current) and keeps it for the life of
+ *     the process; make that first call before any stream capture, and do
+ *     not use this call across a reset of the device (cudaDeviceReset, or
+ *     the primary context torn down and recreated), after which the kept
+ *     address no longer names the array.
  *   - All calls on a device share its array, which keeps the last call's
  *     contents; the counters at its front are cleared on `stream` at every
  *     call.  Calls that overlap on the GPU (for example on two streams) race
  *     with each other: serialise them.
- *   - Device flags are not kept between calls; use moe_decode_layer with a
- *     workspace and moe_device_status() to read them.
+ *   - Device flags raised by these calls accumulate in the array until
+ *     moe_device_status_static() reads and clears them.
  */
 #define MOE_STATIC_SCRATCH_BYTES (32u << 20)
 moe_status moe_decode_layer_static(const void *hidden, const void *w_router, const float *router_bias,
@@ -282,11 +311,39 @@ moe_status moe_decode_layer_static(const void *hidden, const void *w_router, con
                                    const moe_routing *routing, void *out, moe_stream_t stream);
 
 /*
+ * moe_device_status for moe_decode_layer_static: synchronises `stream`,
+ * returns the device flag word (MOE_FLAG_*) that calls of
+ * moe_decode_layer_static raised on the current device since the last
+ * read, and clears it.  Returns MOE_ERR_DEVICE_CHECK if any flag was set.
+ * Allocates nothing.  (No counterpart on the pages.)
+ */
+moe_status moe_device_status_static(moe_stream_t stream, uint32_t *flags);
+
+/*
  * Synchronises `stream`, returns the device flag word (MOE_FLAG_*) that the
  * calls on this workspace raised since the last read, and clears it.
  * Returns MOE_ERR_DEVICE_CHECK if any flag was set.
  */
 moe_status moe_device_status(void *workspace, moe_stream_t stream, uint32_t *flags);
+
+/*
+ * Bound, in microseconds, of every wait inside the library's kernels: the
+ * expert kernel's CTAs wait for one another (hidden states copied, h rows
+ * written, y slices stored) and, with the early start, for the routing
+ * kernel's published union.  A healthy layer's waits last microseconds.  A
+ * wait that reaches the bound gives up: the kernel raises
+ * MOE_FLAG_WAIT_TIMEOUT, every later wait in the same CTA returns at once,
+ * the call's output is not valid, and the kernel still ends and leaves the
+ * workspace ready for the next call.  Default 2,000,000 (two seconds);
+ * 0 restores it.  The bound is counted in SM clock cycles at 2,000 per
+ * microsecond (the clock runs at up to 2.07 GHz), so it lasts at least
+ * about the given time.  Applies to calls launched afterwards, process
+ * wide.  Short bounds are for tests of the failure path: a layer whose CTA
+ * is delayed for longer than the bound (for example by a long kernel on
+ * another stream occupying its SM) would fail with the flag.
+ * (No counterpart on the pages.)
+ */
+moe_status moe_set_wait_timeout_us(uint32_t microseconds);
 
 /*
  * Seeded synthetic tensor fill (for benchmarks and tests; not part of the

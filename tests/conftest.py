@@ -27,3 +27,13 @@ def read_golden(name):
             key, val = (s.strip() for s in line.split("=", 1))
             vals[key] = val
     return vals
+
+
+@pytest.fixture(scope="session")
+def pool():
+    """A spawn-started process pool that runs the oracle on full-size
+    batches (tests/oracle_pool.py)."""
+    from oracle_pool import OraclePool
+    p = OraclePool()
+    yield p
+    p.close()

@@ -32,9 +32,18 @@ def device_inputs(L: dict, bf16: bool) -> dict:
 
 
 def params_for(w: synth.Workload, B: int, mode: int, k0=None, p=1.0, maxP=0, kmax=0, B_valid=-1):
-    return moe.RouteParams(B=B, d=w.d, N=w.N, k=w.k, mode=mode, k0=k0 if k0 else w.k, p=p, maxP=maxP,
+    """k0 None: k; k0 <= 0 (OEA): the library's batch-size policy."""
+    return moe.RouteParams(B=B, d=w.d, N=w.N, k=w.k, mode=mode, k0=w.k if k0 is None else k0, p=p, maxP=maxP,
                            kmax=kmax, B_valid=B_valid,
                            dtype=moe.DTYPE_BF16 if w.bf16 else moe.DTYPE_F32)
+
+
+def resolved_k0_p(prm: moe.RouteParams, B_valid: int):
+    """(k0, p) the routing runs with: the oracle's batch-size policy when
+    prm.k0 <= 0 in OEA mode."""
+    if prm.mode == moe.MODE_OEA and prm.k0 <= 0:
+        return oracle.policy_k0(B_valid, prm.k, prm.p)
+    return prm.k0, prm.p
 
 
 def run_layer(w: synth.Workload, D: dict, prm: moe.RouteParams, ws=None, stream=None):
@@ -55,38 +64,52 @@ def to_np(r: moe.Routing) -> dict:
     return g
 
 
-def near_tie_tokens(logits: np.ndarray, p: float, k0: int, B_valid: int) -> set:
-    """Tokens whose top-p prefix (fp64) over the first k0 ranks lies within
-    NEAR_TIE_P of p: there fp32 rounding order decides t_i."""
+def near_tie_choices(logits: np.ndarray, p: float, k0: int, B_valid: int) -> dict:
+    """Tokens whose top-p prefix (fp64) at one of the first k0 ranks lies
+    within NEAR_TIE_P of p, where fp32 rounding order decides t_i, each with
+    the baseline sizes that decision can give: stopping at that rank, or
+    one rank later (capped at k0)."""
     if p >= 1:
-        return set()
-    out = set()
+        return {}
+    out = {}
     for i in range(min(B_valid, logits.shape[0])):
         l = logits[i].astype(np.float64)
         P = np.exp(l - l.max())
         P /= P.sum()
         c = np.cumsum(np.sort(P)[::-1])[:k0]
-        if np.min(np.abs(c - p)) < NEAR_TIE_P:
-            out.add(i)
+        near = np.nonzero(np.abs(c - p) < NEAR_TIE_P)[0]
+        if len(near):
+            out[i] = {int(t) + 1 for t in near} | {min(int(t) + 2, k0) for t in near}
     return out
 
 
+def near_tie_tokens(logits: np.ndarray, p: float, k0: int, B_valid: int) -> set:
+    return set(near_tie_choices(logits, p, k0, B_valid))
+
+
 def check_routing(g: dict, prm: moe.RouteParams, B_valid: int):
-    """The GPU routing equals the oracle's routing of the GPU's own scores
-    (bit-exact for indices, counts, offsets, active list, grouping; weights
-    within TOL_W).  Returns the oracle result."""
+    """The GPU routing equals the oracle's routing of the GPU's own scores,
+    for the whole batch: bit-exact for n_i, T, indices, counts, offsets,
+    active list and grouping; weights within TOL_W.  A token whose top-p
+    prefix lies within NEAR_TIE_P of p (a near-tie: fp32 rounding order
+    decides its t_i) may take either baseline size that rounding can give;
+    every other token's n_i must be the oracle's, and the oracle is then
+    rerun with the GPU's n_i so that the rest of the batch is compared
+    exactly.  Returns the oracle result and the near-tie count."""
     mode = oracle.OEA if prm.mode == moe.MODE_OEA else oracle.TOPK
     kmax = prm.kmax if prm.kmax > 0 else prm.k
     maxP = prm.maxP if 0 < prm.maxP < prm.N else prm.N
+    k0, p = resolved_k0_p(prm, B_valid)
     ref = oracle.route(g["logits"], mode, prm.k, prm.k0, prm.p, maxP, kmax, B_valid)
-    ties = near_tie_tokens(g["logits"], prm.p, prm.k0, B_valid) if mode == oracle.OEA else set()
+    ties = near_tie_choices(g["logits"], p, k0, B_valid) if mode == oracle.OEA else {}
     if ties:
-        # accept either decision for those tokens; the rest must match
-        for i in range(prm.B):
+        nb = g["n_base"][:prm.B].astype(np.int32)
+        for i in range(B_valid):
             if i in ties:
-                continue
-            assert g["n_base"][i] == ref["nbase"][i]
-        return ref
+                assert nb[i] in ties[i] | {int(ref["nbase"][i])}, (i, nb[i], ties[i])
+            else:
+                assert nb[i] == ref["nbase"][i], (i, nb[i], ref["nbase"][i])
+        ref = oracle.route(g["logits"], mode, prm.k, prm.k0, prm.p, maxP, kmax, B_valid, nbase=nb)
     assert g["T"] == ref["T"]
     assert np.array_equal(g["n_base"][:prm.B], ref["nbase"])
     assert np.array_equal(g["expert_idx"], ref["idx"])
@@ -97,6 +120,7 @@ def check_routing(g: dict, prm: moe.RouteParams, B_valid: int):
     assert (g["active"][g["T"]:] == -1).all()
     n = int(ref["offsets"][-1])
     assert np.array_equal(g["perm"][:n], ref["perm"])
+    ref["near_ties"] = len(ties)
     return ref
 
 

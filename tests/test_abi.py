@@ -65,7 +65,7 @@ def test_slots_and_workspace(lib):
 @pytest.mark.parametrize("kw", [
     dict(B=257), dict(B=-1), dict(d=100), dict(d=32), dict(N=0), dict(N=1025), dict(k=0),
     dict(k=33, N=64), dict(k=9, N=8), dict(mode=2), dict(dtype=3),
-    dict(mode=moe.MODE_OEA, k0=0), dict(mode=moe.MODE_OEA, k0=9),
+    dict(mode=moe.MODE_OEA, k0=9), dict(mode=moe.MODE_OEA, k0=0, p=0.0),
     dict(mode=moe.MODE_OEA, k0=3, p=0.0), dict(mode=moe.MODE_OEA, k0=3, p=1.5),
     dict(mode=moe.MODE_OEA, k0=3, p=float("nan")),
     dict(mode=moe.MODE_OEA, k0=4, kmax=3), dict(mode=moe.MODE_OEA, k0=4, kmax=40),
@@ -101,3 +101,33 @@ def test_bad_buffers_rejected_on_host(lib):
                               None) == moe.MOE_ERR_ARG
     assert b"d_ff" in lib.moe_last_error()
     assert lib.moe_status_string(moe.MOE_ERR_WORKSPACE) == b"MOE_ERR_WORKSPACE"
+
+
+def test_batch_size_policy_is_accepted(lib):
+    """k0 <= 0 in OEA mode chooses k0 from the batch instead of failing."""
+    for B in (0, 1, 4, 16, 256):
+        for k0 in (0, -3):
+            assert moe.moe_num_slots(P(B=B, mode=moe.MODE_OEA, k0=k0, p=0.7)) == 8
+    assert moe.moe_num_slots(P(mode=moe.MODE_OEA, k0=0, kmax=4)) == 4    # k0 = 3 at B = 16
+    assert lib.moe_num_slots(ctypes.byref(P(B=4, mode=moe.MODE_OEA, k0=0, kmax=4).c())) == -1   # k0 = 5 > kmax
+
+
+def test_mixed_layer_checks_its_descriptor_before_launching(lib):
+    """moe_decode_layer_mixed rejects a bad expert descriptor on the host,
+    so not even the routing kernel is launched."""
+    prm = P(mode=moe.MODE_OEA, k0=3).c()
+    fake = ctypes.c_void_p(4096)
+    r = moe._Routing(*([fake] * 7 + [None, None]))
+    ws = moe.moe_workspace_bytes(P(mode=moe.MODE_OEA, k0=3), 768)
+    bad = [moe._Mixed(None, fake, fake, fake, 32, 96),            # no slot table
+           moe._Mixed(fake, ctypes.c_void_p(4100), fake, fake, 32, 96),   # misaligned image
+           moe._Mixed(fake, fake, fake, fake, 0, 128),            # no bf16 expert
+           moe._Mixed(fake, None, fake, fake, 32, 96)]            # missing image
+    for m in bad:
+        assert lib.moe_decode_layer_mixed(fake, fake, None, fake, fake, fake, ctypes.byref(m), 768,
+                                          ctypes.byref(prm), ctypes.byref(r), fake, fake, ws, None) == moe.MOE_ERR_ARG
+    assert lib.moe_decode_layer_mixed(fake, fake, None, fake, fake, fake, None, 768, ctypes.byref(prm),
+                                      ctypes.byref(r), fake, fake, ws, None) == moe.MOE_ERR_ARG
+    m = moe._Mixed(fake, fake, fake, fake, 32, 96)
+    assert lib.moe_decode_layer_mixed(fake, fake, None, fake, fake, fake, ctypes.byref(m), 100,   # d_ff % 128
+                                      ctypes.byref(prm), ctypes.byref(r), fake, fake, ws, None) == moe.MOE_ERR_ARG

@@ -105,31 +105,64 @@ def test_mixed_small_batches(d, F, B):
     gu.check_output(out, ref, True)
 
 
-def test_bad_slot_is_flagged():
+@pytest.mark.parametrize("mode,k0", [(TOPK, 2), (OEA, 1)])
+def test_bad_slot_is_flagged(mode, k0):
+    """An out-of-range slot of an activated expert raises MOE_FLAG_BAD_INDEX.
+    A router bias far above the score spread puts expert 5 first for every
+    token, so the bad slot is always read."""
     w = synth.Workload("t_mixed_bad", N=16, k=2, d=256, F=256, B=8, seed=3)
     L = synth.make_layer(w, 0, 8)
+    L["bias"] = np.zeros(16, np.float32)
+    L["bias"][5] = 30.0
     hot_w, mixed, _ = build_mixed(w, L, range(8))
     mixed.slot[5] = 100          # out of range
     D = gu.device_inputs(L, True)
-    prm = gu.params_for(w, 8, TOPK)
+    prm = gu.params_for(w, 8, mode, k0)
     r = moe.Routing(prm, gu.DEV)
     ws = moe.alloc_workspace(prm, w.F, gu.DEV)
     out = torch.empty(8, w.d, dtype=torch.bfloat16, device=gu.DEV)
     moe.moe_route(D["x"], D["w_router"], D["bias"], prm, r, ws)
     moe.moe_expert_ffn_mixed(D["x"], hot_w["w_gate"], hot_w["w_up"], hot_w["w_down"], mixed, w.F, prm, r, out, ws)
     flags = moe.moe_device_status(ws)
-    if int((r.expert_idx == 5).sum().item()) > 0:
-        assert flags & moe.FLAG_BAD_INDEX
+    assert int((r.expert_idx[:, 0] == 5).sum().item()) == 8
+    assert flags & moe.FLAG_BAD_INDEX
 
 
-def test_full_size_mixed_sampled():
-    """The 30B mixed workload (B=32): hot set from a 200-step EMA trace, cold
-    experts INT4; sampled tokens against the oracle.  The hot experts are
-    generated on the device (the generator is bit-identical to the host's);
-    the host packs the cold experts of the sampled tokens (other cold slots
-    hold zero images and contribute nothing to the checked tokens)."""
+@pytest.mark.parametrize("mode,k0,p,B", [(OEA, 2, 0.7, 12), (TOPK, 4, 1.0, 20), (OEA, 0, 1.0, 37)])
+def test_mixed_layer_one_call(mode, k0, p, B):
+    """moe_decode_layer_mixed (routing and mixed experts in one call) against
+    the oracle, and bit for bit against the two-call sequence."""
+    w = synth.Workload("t_mixed_one", N=32, k=4, d=512, F=256, B=B, seed=43, zipf=True)
+    L = synth.make_layer(w, 0, B)
+    hot = [0, 2, 6, 7, 12, 19, 22, 30]
+    hot_w, mixed, eff = build_mixed(w, L, hot)
+    D = gu.device_inputs(L, True)
+    prm = gu.params_for(w, B, mode, k0, p)
+    r = moe.Routing(prm, gu.DEV, with_logits=True)
+    ws = moe.alloc_workspace(prm, w.F, gu.DEV)
+    out = torch.full((B, w.d), float("nan"), dtype=torch.bfloat16, device=gu.DEV)
+    for _ in range(2):
+        moe.moe_decode_layer_mixed(D["x"], D["w_router"], D["bias"], hot_w["w_gate"], hot_w["w_up"],
+                                   hot_w["w_down"], mixed, w.F, prm, r, out, ws)
+        assert moe.moe_device_status(ws) == 0
+        g = gu.to_np(r)
+        gu.check_routing(g, prm, B)
+        ref = oracle.moe_experts(L["x"], eff["w_gate"], eff["w_up"], eff["w_down"], g["expert_idx"],
+                                 g["weights"].astype(np.float64))
+        gu.check_output(out, ref, True)
+    r2, out2 = run_mixed(w, L, D, hot_w, mixed, prm)
+    assert torch.equal(out, out2) and torch.equal(r.expert_idx, r2.expert_idx)
+
+
+def test_full_size_mixed_every_token(pool):
+    """The 30B mixed workload (B=32): hot set from a 200-step EMA trace,
+    every cold expert packed to INT4 from its real weights, the whole layer
+    in one call (moe_decode_layer_mixed); routing and every output element
+    of every token against the oracle on the same packed bytes.  The hot
+    experts are generated on the device (the generator is bit-identical to
+    the host's)."""
     w = synth.WORKLOADS["qwen3_30b_a3b_mixed_int4_b32"]
-    B, N, d, F = w.B, w.N, w.d, w.F
+    B, N, d = w.B, w.N, w.d
     dev = gu.DEV
     bf = torch.bfloat16
     x = synth.make_tensor(w, 0, synth.T_X, B)
@@ -156,7 +189,6 @@ def test_full_size_mixed_sampled():
         slot[e] = i
     for i, e in enumerate(cold):
         slot[e] = -1 - i
-    # hot pool on the device
     hot_w = {}
     for name, tid in (("w_gate", synth.T_GATE), ("w_up", synth.T_UP), ("w_down", synth.T_DOWN)):
         t = torch.empty((len(hot),) + synth.tensor_shape(w, tid)[1:], dtype=bf, device=dev)
@@ -165,38 +197,23 @@ def test_full_size_mixed_sampled():
             moe.moe_synth_normal(t[i], synth.tensor_seed(w.seed, 0, tid),
                                  float(synth.scale_f32(synth.tensor_std(w, tid))), start=e * per)
         hot_w[name] = t
-    # routing of the layer, then the cold experts the sampled tokens use
-    prm = gu.params_for(w, B, OEA, 5, 1.0)
-    r0 = moe.Routing(prm, dev)
-    ws0 = moe.alloc_workspace(prm, 0, dev)
-    moe.moe_route(D["x"], D["w_router"], D["bias"], prm, r0, ws0)
-    idx0 = r0.expert_idx.cpu().numpy()
-    sample = (0, 13, B - 1)
-    used = {int(e) for i in sample for e in idx0[i] if e >= 0}
-    na, nd = F * d // 2 + F * (d // 64) * 2, d * F // 2 + d * (F // 64) * 2   # codes + a scale per 64-column chunk
-    qg = np.zeros((len(cold), na), np.uint8)
-    qu = np.zeros((len(cold), na), np.uint8)
-    qd = np.zeros((len(cold), nd), np.uint8)
-    eff = {}
-    for e in used:
-        g, u, dn = synth.make_expert(w, 0, e)
-        if e in hot:
-            eff[e] = (g, u, dn)
-        else:
-            (pg, pu, pd), _ = synth.pack_int4_expert(g, u, dn)
-            i = cold.index(e)
-            qg[i], qu[i], qd[i] = pg, pu, pd
-            eff[e] = (oracle.dequant_int4(pg, F, d, synth.INT4_RB_GATE_UP), oracle.dequant_int4(pu, F, d, synth.INT4_RB_GATE_UP),
-                      oracle.dequant_int4(pd, d, F, synth.INT4_RB_DOWN))
-    mixed = moe.MixedExperts(torch.from_numpy(slot).to(dev), torch.from_numpy(qg).to(dev),
-                             torch.from_numpy(qu).to(dev), torch.from_numpy(qd).to(dev), len(hot), len(cold))
-    r, out = run_mixed(w, L, D, hot_w, mixed, prm)
-    g = gu.to_np(r)
-    gu.check_routing(g, prm, B)
-    got = out.float().cpu().numpy()
-    for i in sample:
-        ref = np.zeros(d)
-        for j, e in enumerate(g["expert_idx"][i]):
-            if e >= 0:
-                ref += float(g["weights"][i, j]) * oracle.expert_ffn(x[i], *eff[int(e)])
-        assert np.abs(got[i] - ref).max() <= gu.TOL_BF16 * np.abs(ref).max()
+    packed = pool.pack_cold(w, 0, cold)
+    q = [torch.from_numpy(np.stack([pk[m] for pk in packed])).to(dev) for m in range(3)]
+    mixed = moe.MixedExperts(torch.from_numpy(slot).to(dev), q[0], q[1], q[2], len(hot), len(cold))
+    res = []
+    for mode, k0, p in ((OEA, 5, 1.0), (TOPK, 8, 1.0)):
+        prm = gu.params_for(w, B, mode, k0, p)
+        r = moe.Routing(prm, dev, with_logits=True)
+        ws = moe.alloc_workspace(prm, w.F, dev)
+        out = torch.full((B, d), float("nan"), dtype=bf, device=dev)
+        moe.moe_decode_layer_mixed(D["x"], D["w_router"], D["bias"], hot_w["w_gate"], hot_w["w_up"],
+                                   hot_w["w_down"], mixed, w.F, prm, r, out, ws)
+        assert moe.moe_device_status(ws) == 0
+        g = gu.to_np(r)
+        gu.check_routing(g, prm, B)
+        res.append((g, out))
+    assert any(slot[e] < 0 for g, _ in res for e in g["active"][:g["T"]])   # INT4 experts are activated
+    refs = pool.layer_outputs(w, 0, x, [(g["expert_idx"], g["weights"].astype(np.float64)) for g, _ in res],
+                              cold=frozenset(cold))
+    for (g, out), ref in zip(res, refs):
+        gu.check_output(out, ref, True)

@@ -22,23 +22,40 @@ def built():
     moe.load()
 
 
-@pytest.mark.parametrize("mode,k0,p,B", [(1, 3, 0.7, 24), (0, 8, 1.0, 16), (1, 5, 1.0, 40)])
+def static_call(w, D, prm):
+    r = moe.Routing(prm, gu.DEV, with_logits=True)
+    out = torch.full((prm.B, w.d), float("nan"), dtype=torch.bfloat16, device=gu.DEV)
+    moe.moe_decode_layer_static(D["x"], D["w_router"], D["bias"], D["w_gate"], D["w_up"], D["w_down"],
+                                w.F, prm, r, out)
+    return r, out
+
+
+@pytest.mark.parametrize("mode,k0,p,B", [(1, 3, 0.7, 8), (1, 5, 1.0, 16), (1, 3, 0.7, 24), (0, 8, 1.0, 16),
+                                         (1, 5, 1.0, 40)])
 def test_static_scratch_matches_workspace_call(mode, k0, p, B):
+    """Two calls in a row give the workspace call's bits (routing and
+    output), with a call of another batch shape in between, so a union,
+    epoch or counter left in the shared array by a different call would be
+    caught.  OEA batches of up to 16 tokens take the early start, which
+    reads the union words the routing kernel publishes in the array."""
     w = synth.Workload("t_static", N=128, k=8, d=512, F=256, B=B, seed=77, zipf=True)
     D = gu.device_inputs(synth.make_layer(w, 0, B), True)
     prm = gu.params_for(w, B, mode, k0, p)
     r_ref, out_ref, _, flags = gu.run_layer(w, D, prm)
     assert flags == 0
-    ref = out_ref.float().cpu().numpy().astype(np.float64)
-    for _ in range(2):   # two calls in a row: the shared array keeps the last contents
-        r = moe.Routing(prm, gu.DEV, with_logits=True)
-        out = torch.full((B, w.d), float("nan"), dtype=torch.bfloat16, device=gu.DEV)
-        moe.moe_decode_layer_static(D["x"], D["w_router"], D["bias"], D["w_gate"], D["w_up"], D["w_down"],
-                                    w.F, prm, r, out)
-        torch.cuda.synchronize()
-        assert torch.equal(r.expert_idx, r_ref.expert_idx) and int(r.T.item()) == int(r_ref.T.item())
-        got = out.float().cpu().numpy().astype(np.float64)
-        assert np.abs(got - ref).max() <= gu.TOL_BF16 * np.abs(ref).max()
+    wo = synth.Workload("t_static_other", N=128, k=8, d=512, F=256, B=40, seed=78, zipf=True)
+    Do = gu.device_inputs(synth.make_layer(wo, 0, 40), True)
+    prm_o = gu.params_for(wo, 40, 1, 5, 1.0)
+    assert moe.moe_device_status_static() == 0
+    for call in range(2):
+        r, out = static_call(w, D, prm)
+        assert moe.moe_device_status_static() == 0
+        for name in ("expert_idx", "weights", "T", "active", "counts", "offsets", "perm", "n_base", "logits"):
+            assert torch.equal(getattr(r, name), getattr(r_ref, name)), name
+        assert torch.equal(out, out_ref)
+        if call == 0:   # another batch shape in between
+            static_call(wo, Do, prm_o)
+            assert moe.moe_device_status_static() == 0
 
 
 def test_static_scratch_rejects_oversized_batch():
