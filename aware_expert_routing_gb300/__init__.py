@@ -26,7 +26,7 @@ FLAG_NONFINITE_SCORE, FLAG_WAIT_TIMEOUT, FLAG_BAD_INDEX = 0x1, 0x2, 0x4
 MAX_TOKENS, MAX_EXPERTS, MAX_SLOTS = 256, 1024, 32
 
 EXPORTED = ["moe_num_slots", "moe_layer_launches", "moe_workspace_bytes", "moe_route", "moe_expert_ffn",
-            "moe_expert_ffn_mixed", "moe_decode_layer", "moe_decode_layer_mixed", "moe_decode_layer_static",
+            "moe_expert_ffn_mixed", "moe_pack_int4", "moe_decode_layer", "moe_decode_layer_mixed", "moe_decode_layer_static",
             "moe_device_status", "moe_device_status_static", "moe_set_wait_timeout_us", "moe_synth_normal", "moe_status_string", "moe_last_error"]
 STATIC_SCRATCH_BYTES = 32 << 20
 
@@ -95,6 +95,8 @@ def load(path: str | None = None):
     lib.moe_device_status.restype = ctypes.c_int
     lib.moe_device_status_static.argtypes = [V, P(ctypes.c_uint32)]
     lib.moe_device_status_static.restype = ctypes.c_int
+    lib.moe_pack_int4.argtypes = [V, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, V, V]
+    lib.moe_pack_int4.restype = ctypes.c_int
     lib.moe_set_wait_timeout_us.argtypes = [ctypes.c_uint32]
     lib.moe_set_wait_timeout_us.restype = ctypes.c_int
     lib.moe_synth_normal.argtypes = [V, ctypes.c_int32, ctypes.c_uint64, ctypes.c_uint64,
@@ -259,6 +261,26 @@ def moe_expert_ffn_mixed(hidden, w_gate, w_up, w_down, mixed: MixedExperts, d_ff
                                      ctypes.byref(routing.c()), _ptr(out), _ptr(workspace),
                                      workspace.numel(), _stream(stream))
     _check(st, "moe_expert_ffn_mixed")
+    return out
+
+
+def int4_image_bytes(rows: int, cols: int) -> int:
+    """Bytes of the packed INT4 image of a [rows][cols] matrix."""
+    return rows * cols // 2 + rows * (cols // 128) * 2
+
+
+def moe_pack_int4(w: torch.Tensor, rb: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Packed INT4 image (uint8) of the bf16 matrix w [rows][cols]."""
+    _need(w, torch.bfloat16, "w")
+    if w.dim() != 2:
+        raise ValueError("w must be a matrix")
+    rows, cols = w.shape
+    n = int4_image_bytes(rows, cols)
+    if out is None:
+        out = torch.empty(n, dtype=torch.uint8, device=w.device)
+    if not out.is_cuda or out.dtype != torch.uint8 or not out.is_contiguous() or out.numel() < n:
+        raise ValueError(f"out must be a contiguous CUDA uint8 tensor of at least {n} bytes")
+    _check(load().moe_pack_int4(_ptr(w), rows, cols, rb, _ptr(out), _stream(stream)), "moe_pack_int4")
     return out
 
 

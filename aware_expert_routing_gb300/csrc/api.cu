@@ -635,6 +635,17 @@ moe_status moe_synth_normal(void* dst, int32_t dtype, uint64_t n, uint64_t start
     return MOE_OK;
 }
 
+moe_status moe_pack_int4(const void* w, int32_t rows, int32_t cols, int32_t rb, void* out, moe_stream_t stream) {
+    if (!w || !out || !aligned(w, 16) || !aligned(out, 16))
+        return fail(MOE_ERR_ARG, "w and out must be non-NULL and 16-byte aligned");
+    if (rows < 1 || cols < 128 || cols % 128 != 0) return fail(MOE_ERR_ARG, "need rows >= 1 and cols a multiple of 128");
+    if (rb < 8 || rb % 8 != 0 || rows % rb != 0)
+        return fail(MOE_ERR_ARG, "rb=%d must be a multiple of 8 that divides rows=%d", rb, rows);
+    cudaError_t e = launch_pack_int4(w, rows, cols, rb, out, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "INT4 pack launch");
+    return MOE_OK;
+}
+
 moe_status moe_set_wait_timeout_us(uint32_t microseconds) {
     g_wait_us.store(microseconds ? microseconds : kDefaultWaitUs);
     return MOE_OK;

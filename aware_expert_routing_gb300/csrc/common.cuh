@@ -163,6 +163,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap* maps, int num_sms
 cudaError_t launch_ffn_f32(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_synth(void* dst, int dtype, uint64_t n, uint64_t start, uint64_t seed,
                          float scale, cudaStream_t s);
+cudaError_t launch_pack_int4(const void* w, int rows, int cols, int rb, void* out, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Device helpers.

@@ -50,9 +50,9 @@
 //     tcgen05.commit frees each stage when its MMAs have completed and marks
 //     a tile's accumulator full.
 //   * INT4 experts (DynaExq page, section 3.2): warp 4 bulk-copies the
-//     packed chunk of each K block of a stage into a raw ring of 4 to 16
-//     slots (the stage ring's unused tail holds all but 4) and arrives on
-//     the stage barrier without bytes; warps 7-14 decode each
+//     packed 128-column chunks of a stage's K blocks into a raw ring of up
+//     to 16 slots (the stage ring's unused tail holds all but one or two)
+//     and arrives on the stage barrier without bytes; warps 7-14 decode each
 //     chunk together (exact integer codes, times the row's group scale,
 //     rounded once to bf16) into the stage's 128-byte-swizzled A operand,
 //     fence it for the tensor core's async proxy, and after the stage's last
@@ -97,12 +97,12 @@ constexpr int kM = 128;                  // weight rows per tile (MMA M)
 constexpr int kNMax = 128;               // most token columns per tile (MMA N)
 constexpr int kWBytes = kM * 128;        // one K block: 128 rows x 64 bf16
 constexpr int kMaxStages = 12;
-constexpr int kRaw = 4;                  // packed INT4 chunks' worth of bytes after the stage ring
 constexpr int kRawMax = 16;              // raw slots (one stage's chunks each) at most; the ring's unused tail holds more
-constexpr int kQ4A = 64 * 32 + 64 * 2;   // INT4 chunk of W_gate / W_up: 64 rows x 64 columns + scales
-constexpr int kQ4B = 128 * 32 + 128 * 2; // INT4 chunk of W_down: 128 rows x 64 columns + scales
-constexpr int kRawBytes = 2 * kQ4A;      // a phase-A stage needs a W_gate and a W_up chunk
-static_assert(kRawBytes == kQ4B, "one raw slot fits either K block");
+constexpr int kQ4A = 64 * 64 + 64 * 2;   // INT4 chunk of W_gate / W_up: 64 rows x 128 columns (a scale group) + scales
+constexpr int kQ4B = 128 * 64 + 128 * 2; // INT4 chunk of W_down: 128 rows x 128 columns + scales
+constexpr int kRawPair = 2 * kQ4A;       // a W_gate and a W_up chunk (phase A), or a W_down chunk (phase B)
+static_assert(kRawPair == kQ4B, "one raw unit fits either phase");
+constexpr int kRawReserve = 2 * kRawPair;   // packed INT4 bytes kept after the stage ring
 constexpr int kQ = 16;                   // tile queue entries
 constexpr int kAcc = 4;                  // accumulator buffers
 constexpr uint32_t kTmemCols = kAcc * kNMax;   // fp32 columns (batches over 16 tokens)
@@ -157,7 +157,7 @@ __host__ __device__ constexpr size_t tabs_bytes(int N) {
 // Stage ring bytes left in `total` bytes of dynamic shared memory (whole KB).
 __host__ __device__ constexpr size_t ring_bytes_for(size_t total, int N, bool int4) {
     return (total - 1024 - ((sizeof(Smem) + 15) & ~size_t(15)) - tabs_bytes(N) -
-            (int4 ? (size_t)kRaw * kRawBytes : 0)) & ~size_t(1023);
+            (int4 ? (size_t)kRawReserve : 0)) & ~size_t(1023);
 }
 
 struct Tile {
@@ -316,13 +316,13 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
               const __grid_constant__ CUtensorMap tm_h4, const __grid_constant__ CUtensorMap tm_gu2,
               const __grid_constant__ CUtensorMap tm_down2) {
     extern __shared__ unsigned char smem_raw[];
-    // [stage ring][kRaw packed INT4 slots, with INT4 experts][Smem][tables]
+    // [stage ring][kRawReserve bytes of packed INT4 slots, with INT4 experts][Smem][tables]
     const bool has_q4 = A.n_cold > 0;
     const int ring_bytes = (int)ring_bytes_for((size_t)A.smem_bytes, A.N, has_q4);
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     unsigned char* raw = ring + ring_bytes;
-    Smem& S = *reinterpret_cast<Smem*>(raw + (has_q4 ? kRaw * kRawBytes : 0));
+    Smem& S = *reinterpret_cast<Smem*>(raw + (has_q4 ? kRawReserve : 0));
     Tabs X;
     X.chunk_off = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(&S) + ((sizeof(Smem) + 15) & ~size_t(15)));
     X.ex_info = reinterpret_cast<uint32_t*>(X.chunk_off + A.N + 1);
@@ -618,13 +618,16 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     const int slot_bytes = KB * (kWBytes + nmax * 128);
     const int obytes = nmax * 128;                  // one operand block
     const int nst = min(kMaxStages, ring_bytes / slot_bytes);
-    // Packed INT4 chunk slots: kRaw after the ring, more in the ring's tail
-    // that the whole stages leave unused (deeper raw rings keep more bytes in
-    // flight for the converter warps without costing a stage).
-    // A raw slot holds one stage's KB packed chunks (W_gate's, then W_up's,
-    // in phase A), each matrix's moved by one bulk copy.
-    const int rslot = KB * kRawBytes;
-    const int nraw_a = kRaw * kRawBytes / rslot;   // slots after the ring
+    // Packed INT4 chunk slots: kRawReserve bytes after the ring, more in the
+    // ring's tail that the whole stages leave unused (deeper raw rings keep
+    // more bytes in flight for the converter warps without costing a stage).
+    // A packed chunk spans 128 columns (two K blocks); a raw slot holds the
+    // chunks of one stage's KB blocks (W_gate's, then W_up's, in phase A),
+    // each matrix's moved by one bulk copy.  With KB = 1 a stage reads half
+    // of its chunk.
+    const int qch = KB > 1 ? KB / 2 : 1;           // packed chunks per matrix and stage
+    const int rslot = qch * kRawPair;
+    const int nraw_a = kRawReserve / rslot;        // slots after the ring
     const int nraw = nraw_a + min(kRawMax - nraw_a, (ring_bytes - nst * slot_bytes) / rslot);
     auto raw_slot = [&](int r) -> unsigned char* {
         return r < nraw_a ? raw + (size_t)r * rslot : ring + (size_t)nst * slot_bytes + (size_t)(r - nraw_a) * rslot;
@@ -636,8 +639,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const uint64_t pol_once = l2_evict_first_policy();
             const uint64_t pol_keep = l2_evict_normal_policy();
             RingPos rp, rq;   // stage ring, packed INT4 ring
-            const size_t q4_mat_a = (size_t)(F / 64) * (d / 64) * kQ4A;    // bytes of one INT4 W_gate / W_up
-            const size_t q4_mat_b = (size_t)(d / kM) * (F / 64) * kQ4B;    // bytes of one INT4 W_down
+            const size_t q4_mat_a = (size_t)(F / 64) * (d / 128) * kQ4A;   // bytes of one INT4 W_gate / W_up
+            const size_t q4_mat_b = (size_t)(d / kM) * (F / 128) * kQ4B;   // bytes of one INT4 W_down
             // CTA b starts with tile b; the next tile is claimed when this
             // one is posted, so the atomic's latency hides behind its stages
             int next0 = (int)blockIdx.x;
@@ -670,18 +673,19 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                         mbar_arrive(&S.full[slot]);
                         const int r = rq.slot;
                         if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
-                        S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u);
+                        // slot, phase A, and (KB = 1) which half of the chunk the stage reads
+                        S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u) | ((uint32_t)((s * KB) & 1) << 9);
                         unsigned char* rdst = raw_slot(r);
-                        const int kblk = s * KB;
+                        const int cg = s * KB / 2;   // the stage's first 128-column group
                         if (ph_a) {
-                            const size_t off = (size_t)c * q4_mat_a + ((size_t)T.rb * (d / 64) + kblk) * kQ4A;
-                            mbar_arrive_expect_tx(&S.raw_full[r], 2 * KB * kQ4A);
-                            bulk_load(rdst, A.q_gate + off, KB * kQ4A, &S.raw_full[r], pol);
-                            bulk_load(rdst + KB * kQ4A, A.q_up + off, KB * kQ4A, &S.raw_full[r], pol);
+                            const size_t off = (size_t)c * q4_mat_a + ((size_t)T.rb * (d / 128) + cg) * kQ4A;
+                            mbar_arrive_expect_tx(&S.raw_full[r], 2 * qch * kQ4A);
+                            bulk_load(rdst, A.q_gate + off, qch * kQ4A, &S.raw_full[r], pol);
+                            bulk_load(rdst + qch * kQ4A, A.q_up + off, qch * kQ4A, &S.raw_full[r], pol);
                         } else {
-                            const size_t off = (size_t)c * q4_mat_b + ((size_t)T.rb * (F / 64) + kblk) * kQ4B;
-                            mbar_arrive_expect_tx(&S.raw_full[r], KB * kQ4B);
-                            bulk_load(rdst, A.q_down + off, KB * kQ4B, &S.raw_full[r], pol);
+                            const size_t off = (size_t)c * q4_mat_b + ((size_t)T.rb * (F / 128) + cg) * kQ4B;
+                            mbar_arrive_expect_tx(&S.raw_full[r], qch * kQ4B);
+                            bulk_load(rdst, A.q_down + off, qch * kQ4B, &S.raw_full[r], pol);
                         }
                         rq.next(nraw);
                         continue;
@@ -883,21 +887,24 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 break;
             }
             const bool ph_a = (info >> 8) & 1u;
+            const int half1 = (info >> 9) & 1u;          // KB = 1: the stage's half of its chunk
             const int rows = ph_a ? 64 : kM;
             const unsigned char* src = raw_slot(r);
 #pragma unroll
             for (int kb = 0; kb < 4; ++kb) {
                 if (kb >= KB) break;
                 unsigned char* dstA = ring + (size_t)slot * slot_bytes + kb * kWBytes;
+                const int ci = kb >> 1;                           // chunk of this block within the stage
+                const int half = KB > 1 ? (kb & 1) : half1;       // 64-column half of that chunk
 #pragma unroll
                 for (int it = 0; it < 1024 / (kConvWarps * 32); ++it) {   // 128 rows x 8 units
                     const int k = it * (kConvWarps * 32) + ct;
                     const int i = k >> 3, u = k & 7;
-                    // phase A: W_gate's chunk kb, or W_up's (after W_gate's KB)
-                    const unsigned char* ch = ph_a ? src + (((i >> 3) & 1) * KB + kb) * kQ4A : src + kb * kQ4B;
+                    // phase A: W_gate's chunk ci, or W_up's (after W_gate's qch)
+                    const unsigned char* ch = ph_a ? src + (((i >> 3) & 1) * qch + ci) * kQ4A : src + ci * kQ4B;
                     const int srow = ph_a ? 8 * (i >> 4) + (i & 7) : i;
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(ch + srow * 32 + u * 4);
-                    const __nv_bfloat16 sc = *reinterpret_cast<const __nv_bfloat16*>(ch + rows * 32 + srow * 2);
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(ch + srow * 64 + half * 32 + u * 4);
+                    const __nv_bfloat16 sc = *reinterpret_cast<const __nv_bfloat16*>(ch + rows * 64 + srow * 2);
                     *reinterpret_cast<uint4*>(dstA + i * 128 + ((u ^ (i & 7)) << 4)) =
                         decode_q4_row8(w, __bfloat162bfloat162(sc));
                 }
@@ -1130,7 +1137,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
     // the ring must hold two stages of the largest slot this launch can use
     const int kb = a.gu_fused ? (a.B <= 16 ? a.kbs : a.kbl) : 1;
     const size_t slot = (size_t)kb * (kWBytes + (a.B <= 16 ? 16 : kNMax) * 128);
-    if ((size_t)a.smem_bytes < 4096 + tabs_bytes(a.N) + (size_t)kRaw * kRawBytes ||
+    if ((size_t)a.smem_bytes < 4096 + tabs_bytes(a.N) + (size_t)kRawReserve ||
         ring_bytes_for((size_t)a.smem_bytes, a.N, a.n_cold > 0) < 2 * slot)
         return cudaErrorInvalidConfiguration;
     // One CTA per SM (the shared-memory size allows no second one, so the

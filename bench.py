@@ -2,27 +2,42 @@
 """Benchmark of the OEA MoE decode layer on GB300.
 
 A step is one pass of the whole layer (router, routing, grouped SwiGLU
-experts, combine) over one decode batch.  Steps cycle through 8 layers with
-distinct seeded weights (about 1.2 GB of expert weights per layer at the
-Qwen3-30B-A3B shapes, far larger than the 126 MB L2), so every step streams
-its activated experts from HBM.
+experts, combine) over one decode batch, through one public call
+(moe_decode_layer, or moe_decode_layer_mixed for bf16/INT4 experts).  Steps
+cycle through 8 layers with distinct seeded weights (about 1.2 GB of expert
+weights per layer at the Qwen3-30B-A3B shapes, far larger than the 126 MB
+L2), so every step streams its activated experts from HBM.
 
-value     = algorithmic bytes / device time for the headline routing run
+Timed regions: exactly K steps back to back between a barrier +
+synchronize on both sides and one CUDA event pair on the launching stream,
+repeated until at least --min-seconds have been timed (so the clock sampler
+sees the run); ms_per_step = total time / (reps * K).
+
+value     = algorithmic bytes / device time of the headline routing run
             (whole job: summed over ranks, divided by the slowest rank's
-            time).  Algorithmic bytes per layer = T * 3*d*d_ff*2 (the
-            activated experts, read once) + the router weights
-            N*d*2 + activations (x read twice, scores, output).
+            time).  Algorithmic bytes per layer = T * expert bytes (the
+            activated experts, read once) + the router weights N*d*2 +
+            activations (x read twice, scores, output).
+modes     = every routing run of the headline workload.
+sweep     = the rest of the metric ("vs B, OEA vs top-k"): the Zipf-routed
+            30B workload at B = 1, 16, 64, the 235B workload at B = 64 and
+            the mixed bf16/INT4 30B workload at B = 32, OEA and top-8 each.
+router    = scoring + routing alone (moe_route back to back), its own
+            microseconds and GB/s.
 roofline  = the expert kernel alone: its algorithmic bytes per launch over
-            its mean launch time (CUDA events on the launching stream,
-            recorded around every launch in a second timed pass of the same
-            steps; the headline pass has events only at its two ends),
-            against the measured HBM copy bandwidth.
-e2e       = the same metric through moe_decode_layer with host buffers: the
-            step's hidden states are copied from pinned host memory and the
-            output read back inside the timed region.
+            its mean launch time (CUDA events on the launching stream
+            around every expert launch, in a separate pass of the same
+            steps), against the measured HBM copy bandwidth; `traffic` is
+            ncu's DRAM bytes per launch from profiles/, when the capture
+            matches the kernel source.
+e2e       = the same metric through the public call with host buffers:
+            every step's hidden states are copied in from pinned host
+            memory and its output copied back, on a copy stream with double
+            buffers (a step's input one step ahead, its output after an
+            event), all inside the timed region.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload NAME] [--sweep-out FILE]
+                [--workload NAME] [--no-sweep] [--sweep-out FILE]
 """
 from __future__ import annotations
 
@@ -30,8 +45,8 @@ import argparse
 import datetime
 import hashlib
 import json
-import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -48,9 +63,13 @@ import synth  # noqa: E402
 
 METRIC = "MoE decode layer µs & HBM GB/s (T·expert bytes roofline) vs B, OEA vs top-k"
 UNIT = "GB/s"
+SPEC_HBM_GBS = 8000.0   # the ~8 TB/s HBM3e figure the target is stated against
 DEFAULT_WORKLOAD = "qwen3_30b_a3b_uniform_b16"
 HEADLINE = {"qwen3_30b_a3b_uniform_b16": "oea_k0_3", "qwen3_30b_a3b_zipf_sweep": "oea_k0_5_p0.7",
             "qwen3_235b_a22b_zipf_b64": "oea_k0_5_p0.7", "qwen3_30b_a3b_mixed_int4_b32": "oea_k0_5"}
+# the rest of the metric in the default line: (workload, batch sizes)
+SWEEP = [("qwen3_30b_a3b_zipf_sweep", (1, 16, 64)), ("qwen3_235b_a22b_zipf_b64", (64,)),
+         ("qwen3_30b_a3b_mixed_int4_b32", (32,))]
 N_LAYERS = 8          # default rotation; --layers changes it
 
 
@@ -67,9 +86,13 @@ def expert_kernel_bytes(w: synth.Workload, B: int, T: float) -> float:
     return T * w.expert_bytes + 2 * B * w.d * 2
 
 
+def router_bytes(w: synth.Workload, B: int) -> float:
+    """Router weights once, hidden states in, scores out."""
+    return w.N * w.d * 2 + B * w.d * 2 + B * w.N * 4
+
+
 def layer_bytes(w: synth.Workload, B: int, T: float) -> float:
-    router = w.N * w.d * 2 + B * w.d * 2 + B * w.N * 4
-    return router + expert_kernel_bytes(w, B, T)
+    return router_bytes(w, B) + expert_kernel_bytes(w, B, T)
 
 
 def mixed_kernel_bytes(w: synth.Workload, B: int, n_hot_active: int, n_cold_active: int) -> float:
@@ -79,7 +102,7 @@ def mixed_kernel_bytes(w: synth.Workload, B: int, n_hot_active: int, n_cold_acti
 
 
 def mixed_layer_bytes(w: synth.Workload, B: int, n_hot_active: int, n_cold_active: int) -> float:
-    return w.N * w.d * 2 + B * w.d * 2 + B * w.N * 4 + mixed_kernel_bytes(w, B, n_hot_active, n_cold_active)
+    return router_bytes(w, B) + mixed_kernel_bytes(w, B, n_hot_active, n_cold_active)
 
 
 def measured_peaks() -> dict:
@@ -89,12 +112,6 @@ def measured_peaks() -> dict:
             d = json.load(f)
         return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
     return {"hbm_gbs": 6800.0, "source": "fallback"}
-
-
-def expert_kernel(w: synth.Workload) -> tuple:
-    """(kernel name, source file) of the expert kernel that runs the workload
-    (the tcgen05 kernel for bf16 and mixed bf16/INT4 experts)."""
-    return ("ffn_tc_kernel", "ffn_tc.cu")
 
 
 def kernel_source_hash(source: str = "ffn_tc.cu") -> str:
@@ -121,6 +138,29 @@ def recorded_traffic(workload: str, run: str, algo_bytes_per_launch: float, sour
     return round(e["dram_bytes"] * algo_bytes_per_launch / e["algorithmic_bytes"])
 
 
+def cpu_description() -> dict:
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine(),
+            "arch": platform.machine()}
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
@@ -133,6 +173,7 @@ class Clocks:
     def __init__(self, gpu_id: str):
         self.lines = []
         self.proc = None
+        self.windows = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -147,8 +188,8 @@ class Clocks:
             self.lines.append(line.strip())
 
     def window(self, t0, t1):
-        """Only samples taken between t0 and t1 (local wall clock) count."""
-        self.t0, self.t1 = t0, t1
+        """Samples taken between t0 and t1 (local wall clock) count."""
+        self.windows.append((t0, t1))
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -166,7 +207,7 @@ class Clocks:
                 continue
             try:
                 ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
-                if not (self.t0 <= ts <= self.t1):
+                if not any(a <= ts <= b for a, b in self.windows):
                     continue
             except (ValueError, AttributeError):
                 continue
@@ -246,12 +287,14 @@ def oracle_layer_time(w: synth.Workload, B: int, run: tuple, budget_s: float, in
 def cpu_baseline(w, B, run, budget_s, unit_bytes_fn):
     o = oracle_layer_time(w, B, run, budget_s)
     value = unit_bytes_fn(o["T"]) / o["seconds_per_layer"] / 1e9
+    cpu = cpu_description()
     return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": (f"{w.name} run {run[0]}: oracle router+routing on the full B={B} batch, then "
                        f"{o['pairs_timed']} single-token expert FFNs (8 experts cycled) timed for "
                        f"{budget_s:.0f} s and scaled to the layer's {o['pairs_per_layer']} (token, expert) "
-                       f"pairs; {o['seconds_per_layer'] * 1e3:.1f} ms per layer, single thread"),
-            "ms_per_layer": o["seconds_per_layer"] * 1e3}
+                       f"pairs; {o['seconds_per_layer'] * 1e3:.1f} ms per layer, single thread on 1 of "
+                       f"{cpu['nproc']} cores ({cpu['cpu_model']})"),
+            "ms_per_layer": o["seconds_per_layer"] * 1e3, **cpu}
 
 
 # ---------------------------------------------------------------------------
@@ -260,18 +303,17 @@ def cpu_baseline(w, B, run, budget_s, unit_bytes_fn):
 def build_mixed(moe, torch, w: synth.Workload, layer: int, D: dict, dev):
     """Hot set from a 200-step EMA trace of plain top-k on fresh seeded
     batches of 32 tokens; hot experts stay bf16 (device pool), cold experts
-    are generated on the device, packed to INT4 on the host and uploaded."""
-    bf = torch.bfloat16
+    are packed to INT4 on the device (moe_pack_int4)."""
     prm_t = moe.RouteParams(B=32, d=w.d, N=w.N, k=w.k)
     rt = moe.Routing(prm_t, dev)
     wst = moe.alloc_workspace(prm_t, 0, dev)
-    xt = torch.empty(32, w.d, dtype=bf, device=dev)
+    xt = torch.empty(32, w.d, dtype=torch.bfloat16, device=dev)
     counts = []
     for step in range(200):
         moe.moe_synth_normal(xt, synth.trace_seed(w, layer, step), float(synth.scale_f32(1.0)))
         moe.moe_route(xt, D["w_router"], D["bias"], prm_t, rt, wst)
-        counts.append(rt.counts.cpu().numpy())
-    hot = [int(e) for e in moe.ema_hot_set(np.array(counts), w.hot_n)]
+        counts.append(rt.counts.clone())
+    hot = [int(e) for e in moe.ema_hot_set(torch.stack(counts).cpu().numpy(), w.hot_n)]
     cold = [e for e in range(w.N) if e not in hot]
     slot = np.empty(w.N, np.int32)
     for i, e in enumerate(hot):
@@ -280,15 +322,15 @@ def build_mixed(moe, torch, w: synth.Workload, layer: int, D: dict, dev):
         slot[e] = -1 - i
     hot_idx = torch.tensor(hot, device=dev)
     pools = {k: D[k].index_select(0, hot_idx).contiguous() for k in ("w_gate", "w_up", "w_down")}
-    q = {k: [] for k in ("w_gate", "w_up", "w_down")}
-    for e in cold:
-        g, u, dn = (D[k][e].float().cpu().numpy() for k in ("w_gate", "w_up", "w_down"))
-        (pg, pu, pd), _ = synth.pack_int4_expert(g, u, dn)
-        q["w_gate"].append(pg)
-        q["w_up"].append(pu)
-        q["w_down"].append(pd)
-    qt = {k: torch.from_numpy(np.stack(v)).to(dev) for k, v in q.items()}
-    mixed = moe.MixedExperts(torch.from_numpy(slot).to(dev), qt["w_gate"], qt["w_up"], qt["w_down"],
+    u8 = dict(dtype=torch.uint8, device=dev)
+    q = {"w_gate": torch.empty(len(cold), moe.int4_image_bytes(w.F, w.d), **u8),
+         "w_up": torch.empty(len(cold), moe.int4_image_bytes(w.F, w.d), **u8),
+         "w_down": torch.empty(len(cold), moe.int4_image_bytes(w.d, w.F), **u8)}
+    for i, e in enumerate(cold):
+        moe.moe_pack_int4(D["w_gate"][e], 64, out=q["w_gate"][i])
+        moe.moe_pack_int4(D["w_up"][e], 64, out=q["w_up"][i])
+        moe.moe_pack_int4(D["w_down"][e], 128, out=q["w_down"][i])
+    mixed = moe.MixedExperts(torch.from_numpy(slot).to(dev), q["w_gate"], q["w_up"], q["w_down"],
                              len(hot), len(cold))
     for k in ("w_gate", "w_up", "w_down"):   # the full bf16 tensors are not needed any more
         D[k] = None
@@ -297,20 +339,18 @@ def build_mixed(moe, torch, w: synth.Workload, layer: int, D: dict, dev):
     D["is_hot"] = np.isin(np.arange(w.N), hot)
 
 
-def build_layers(moe, torch, w: synth.Workload, B: int, dev):
+def build_weights(moe, torch, w: synth.Workload, dev, nl: int):
+    """nl layers of router and expert weights, generated on the device."""
     bf = torch.bfloat16
     layers = []
-    for l in range(N_LAYERS):  # noqa: E741
+    for l in range(nl):  # noqa: E741
         D = {}
         for name, tid in (("w_router", synth.T_ROUTER), ("w_gate", synth.T_GATE), ("w_up", synth.T_UP),
                           ("w_down", synth.T_DOWN)):
-            t = torch.empty(synth.tensor_shape(w, tid, B), dtype=bf, device=dev)
+            t = torch.empty(synth.tensor_shape(w, tid), dtype=bf, device=dev)
             moe.moe_synth_normal(t, synth.tensor_seed(w.seed, l, tid),
                                  float(synth.scale_f32(synth.tensor_std(w, tid))))
             D[name] = t
-        x = torch.empty((B, w.d), dtype=bf, device=dev)
-        moe.moe_synth_normal(x, synth.tensor_seed(w.seed, l, synth.T_X), float(synth.scale_f32(1.0)))
-        D["x"] = x
         b = synth.make_bias(w, l)
         D["bias"] = torch.from_numpy(b).to(dev) if b is not None else None
         if w.int4_cold:
@@ -321,27 +361,90 @@ def build_layers(moe, torch, w: synth.Workload, B: int, dev):
     return layers
 
 
-def expert_call(moe, w, D, prm, routing, out, ws, stream, x=None):
+def with_batch(moe, torch, w: synth.Workload, weights: list, B: int, dev):
+    """The layers with hidden states of B tokens (seeded per layer)."""
+    out = []
+    for l, D in enumerate(weights):  # noqa: E741
+        x = torch.empty((B, w.d), dtype=torch.bfloat16, device=dev)
+        moe.moe_synth_normal(x, synth.tensor_seed(w.seed, l, synth.T_X), float(synth.scale_f32(1.0)))
+        out.append(dict(D, x=x))
+    torch.cuda.synchronize(dev)
+    return out
+
+
+def build_layers(moe, torch, w: synth.Workload, B: int, dev):
+    return with_batch(moe, torch, w, build_weights(moe, torch, w, dev, N_LAYERS), B, dev)
+
+
+def layer_call(moe, w, D, prm, routing, out, ws, stream, x=None):
+    """One whole layer through the public one-call API."""
     x = D["x"] if x is None else x
     if "mixed" in D:
         h = D["hot"]
-        moe.moe_expert_ffn_mixed(x, h["w_gate"], h["w_up"], h["w_down"], D["mixed"], w.F, prm, routing, out, ws,
-                                 stream)
+        moe.moe_decode_layer_mixed(x, D["w_router"], D["bias"], h["w_gate"], h["w_up"], h["w_down"], D["mixed"],
+                                   w.F, prm, routing, out, ws, stream)
     else:
-        moe.moe_expert_ffn(x, D["w_gate"], D["w_up"], D["w_down"], w.F, prm, routing, out, ws, stream)
+        moe.moe_decode_layer(x, D["w_router"], D["bias"], D["w_gate"], D["w_up"], D["w_down"], w.F, prm,
+                             routing, out, ws, stream)
 
 
-def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_for=None, detail_steps=2000):
+def expert_call(moe, w, D, prm, routing, out, ws, stream):
+    if "mixed" in D:
+        h = D["hot"]
+        moe.moe_expert_ffn_mixed(D["x"], h["w_gate"], h["w_up"], h["w_down"], D["mixed"], w.F, prm, routing, out,
+                                 ws, stream)
+    else:
+        moe.moe_expert_ffn(D["x"], D["w_gate"], D["w_up"], D["w_down"], w.F, prm, routing, out, ws, stream)
+
+
+def params_of(moe, w, B, run):
     label, mode, k0, p = run
-    prm = moe.RouteParams(B=B, d=w.d, N=w.N, k=w.k, mode=moe.MODE_OEA if mode == "oea" else moe.MODE_TOPK,
-                          k0=k0, p=p)
+    return moe.RouteParams(B=B, d=w.d, N=w.N, k=w.k, mode=moe.MODE_OEA if mode == "oea" else moe.MODE_TOPK,
+                           k0=k0, p=p)
+
+
+def timed_reps(torch, dev, stream, step, steps: int, min_seconds: float, first: int = 0,
+               clocks=None, max_reps: int = 100000):
+    """Exactly `steps` steps per timed region (barrier + synchronize on both
+    sides, one CUDA event pair on the stream), repeated until min_seconds
+    of device time; returns the per-region milliseconds and the steps
+    issued."""
+    reps_ms = []
+    i = first
+    total = 0.0
+    while True:
+        barrier(torch)
+        torch.cuda.synchronize(dev)
+        t0 = datetime.datetime.now()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            step(i)
+            i += 1
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = datetime.datetime.now()
+        barrier(torch)
+        if clocks:
+            clocks.window(t0, t1)
+        ms = a.elapsed_time(b)
+        reps_ms.append(ms)
+        total += ms
+        if total >= min_seconds * 1e3 or len(reps_ms) >= max_reps:
+            return reps_ms, i
+
+
+def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, min_seconds, clocks=None,
+             detail_steps=200):
+    nl = len(layers)
+    prm = params_of(moe, w, B, run)
     routing = moe.Routing(prm, dev)
     ws = moe.alloc_workspace(prm, w.F, dev)
     out = torch.empty((B, w.d), dtype=torch.bfloat16, device=dev)
 
     # T of each layer (routing is deterministic for fixed inputs), and for
     # mixed layers the active experts' formats
-    Ts, kbytes, lbytes = [], [], []
+    Ts, kbytes, lbytes, nhot = [], [], [], []
     with torch.cuda.stream(stream):
         for D in layers:
             moe.moe_route(D["x"], D["w_router"], D["bias"], prm, routing, ws, stream)
@@ -350,6 +453,7 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
             if "mixed" in D:
                 act = routing.active[:T].cpu().numpy()
                 nh = int(D["is_hot"][act].sum())
+                nhot.append(nh)
                 kbytes.append(mixed_kernel_bytes(w, B, nh, T - nh))
                 lbytes.append(mixed_layer_bytes(w, B, nh, T - nh))
             else:
@@ -359,131 +463,180 @@ def run_mode(moe, torch, w, B, layers, run, steps, warmup, dev, stream, clocks_f
     if flags:
         raise RuntimeError(f"device flags {flags:#x}")
 
-    def step(i, ev_pre=None, ev_post=None):
-        D = layers[i % N_LAYERS]
-        if ev_pre is None and "mixed" not in D:
-            # the whole layer through the public call (routing, then experts)
-            moe.moe_decode_layer(D["x"], D["w_router"], D["bias"], D["w_gate"], D["w_up"], D["w_down"], w.F, prm,
-                                 routing, out, ws, stream)
-            return
-        moe.moe_route(D["x"], D["w_router"], D["bias"], prm, routing, ws, stream)
-        if ev_pre is not None:
-            ev_pre.record(stream)
-        expert_call(moe, w, D, prm, routing, out, ws, stream)
-        if ev_post is not None:
-            ev_post.record(stream)
+    def step(i):
+        layer_call(moe, w, layers[i % nl], prm, routing, out, ws, stream)
 
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize(dev)
+    reps_ms, issued = timed_reps(torch, dev, stream, step, steps, min_seconds, first=warmup, clocks=clocks)
+    n_steps = len(reps_ms) * steps
+    total_ms = sum(reps_ms)
+    layer_b = sum(lbytes[i % nl] for i in range(warmup, issued))
 
-    # Timed region 1 (the headline): K steps back to back, one event pair
-    # around all of them, so consecutive kernels overlap their launch and
-    # prologue as they do in use.
-    clocks = Clocks(clocks_for) if clocks_for else None
-    if clocks:
-        time.sleep(0.5)          # nvidia-smi start-up
-    barrier(torch)
-    torch.cuda.synchronize(dev)
-    t_start = datetime.datetime.now()
-    ev_a, ev_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev_a.record(stream)
-    for i in range(steps):
-        step(i)
-    ev_b.record(stream)
-    torch.cuda.synchronize(dev)
-    t_end = datetime.datetime.now()
-    barrier(torch)
-    clk = None
-    if clocks:
-        time.sleep(0.2)
-        clocks.window(t_start, t_end)
-        clk = clocks.stop()
-    total_ms = ev_a.elapsed_time(ev_b)
-
-    # Timed region 2: the same steps with an event at every step boundary
-    # and around every expert-kernel launch (per-step percentiles and the
-    # expert kernel's launch duration for the roofline).  An event between
-    # two kernels keeps the second from starting early, so these steps run
-    # slower than region 1's.
-    n2 = min(steps, detail_steps)
-    ev_step = [torch.cuda.Event(enable_timing=True) for _ in range(n2 + 1)]
+    # The expert kernel alone: events around every expert launch (moe_route,
+    # then the expert call), in a separate pass.  An event between two
+    # kernels keeps the second from starting early, so these steps are
+    # slower than the timed regions'; only the expert kernel's duration is
+    # taken from here.
+    n2 = max(steps, detail_steps)
     ev_pre = [torch.cuda.Event(enable_timing=True) for _ in range(n2)]
     ev_post = [torch.cuda.Event(enable_timing=True) for _ in range(n2)]
     barrier(torch)
     torch.cuda.synchronize(dev)
-    ev_step[0].record(stream)
     for i in range(n2):
-        step(i, ev_pre[i], ev_post[i])
-        ev_step[i + 1].record(stream)
+        D = layers[i % nl]
+        moe.moe_route(D["x"], D["w_router"], D["bias"], prm, routing, ws, stream)
+        ev_pre[i].record(stream)
+        expert_call(moe, w, D, prm, routing, out, ws, stream)
+        ev_post[i].record(stream)
     torch.cuda.synchronize(dev)
     barrier(torch)
     flags = moe.moe_device_status(ws, stream)
     if flags:
         raise RuntimeError(f"device flags {flags:#x}")
-    step_us = [ev_step[i].elapsed_time(ev_step[i + 1]) * 1e3 for i in range(n2)]
     ffn_us = [ev_pre[i].elapsed_time(ev_post[i]) * 1e3 for i in range(n2)]
-    layer_b = sum(lbytes[i % N_LAYERS] for i in range(steps))
-    ffn_b = sum(kbytes[i % N_LAYERS] for i in range(n2))
+    ffn_b = sum(kbytes[i % nl] for i in range(n2))
+    per_step_reps = [ms * 1e3 / steps for ms in reps_ms]
     return {
-        "label": label, "T_mean": float(np.mean(Ts)), "T_per_layer": Ts, "layer_bytes": lbytes,
-        "total_ms": total_ms, "bytes": layer_b,
-        "us_per_layer": total_ms * 1e3 / steps,
-        "us_per_layer_p10_p50_p90": [float(np.percentile(step_us, q)) for q in (10, 50, 90)],
-        "us_per_layer_with_kernel_events": float(np.mean(step_us)),
+        "label": run[0], "T_mean": float(np.mean(Ts)), "T_per_layer": Ts, "layer_bytes": lbytes,
+        "hot_active_mean": float(np.mean(nhot)) if nhot else None,
+        "total_ms": total_ms, "bytes": layer_b, "reps": len(reps_ms), "steps_timed": n_steps,
+        "us_per_layer": total_ms * 1e3 / n_steps,
+        "us_per_layer_reps_p10_p50_p90": [float(np.percentile(per_step_reps, q)) for q in (10, 50, 90)],
         "gbs": layer_b / (total_ms * 1e-3) / 1e9,
-        "tokens_per_s": B * steps / (total_ms * 1e-3),
+        "tokens_per_s": B * n_steps / (total_ms * 1e-3),
         "ffn_us_mean": float(np.mean(ffn_us)),
         "ffn_gbs": ffn_b / (sum(ffn_us) * 1e-6) / 1e9,
         "ffn_bytes_per_launch": ffn_b / n2,
-        "clocks": clk, "launches": moe.moe_layer_launches(prm, w.F) * steps,
-        "objs": (prm, routing, ws, out),
+        "launches_per_region": moe.moe_layer_launches(prm, w.F) * steps,
     }
 
 
-def run_e2e(moe, torch, w, B, layers, run, steps, warmup, dev, stream, lbytes):
-    """moe_decode_layer with the hidden states copied in from pinned host
-    memory and the output copied back, every step, inside the timed region."""
-    label, mode, k0, p = run
-    prm = moe.RouteParams(B=B, d=w.d, N=w.N, k=w.k, mode=moe.MODE_OEA if mode == "oea" else moe.MODE_TOPK,
-                          k0=k0, p=p)
+def run_router(moe, torch, w, B, layers, run, steps, warmup, dev, stream, min_seconds):
+    """Scoring + routing alone (moe_route back to back)."""
+    nl = len(layers)
+    prm = params_of(moe, w, B, run)
     routing = moe.Routing(prm, dev)
-    ws = moe.alloc_workspace(prm, w.F, dev)
-    x_host = [D["x"].cpu().pin_memory() for D in layers]
-    out_host = torch.empty((B, w.d), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty((B, w.d), dtype=torch.bfloat16, device=dev)
-    out = torch.empty((B, w.d), dtype=torch.bfloat16, device=dev)
+    ws = moe.alloc_workspace(prm, 0, dev)
 
     def step(i):
-        D = layers[i % N_LAYERS]
-        with torch.cuda.stream(stream):
-            x_dev.copy_(x_host[i % N_LAYERS], non_blocking=True)
-            if "mixed" in D:
-                moe.moe_route(x_dev, D["w_router"], D["bias"], prm, routing, ws, stream)
-                expert_call(moe, w, D, prm, routing, out, ws, stream, x=x_dev)
-            else:
-                moe.moe_decode_layer(x_dev, D["w_router"], D["bias"], D["w_gate"], D["w_up"], D["w_down"],
-                                     w.F, prm, routing, out, ws, stream)
-            out_host.copy_(out, non_blocking=True)
+        D = layers[i % nl]
+        moe.moe_route(D["x"], D["w_router"], D["bias"], prm, routing, ws, stream)
 
     for i in range(warmup):
         step(i)
-    torch.cuda.synchronize(dev)
-    barrier(torch)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(torch)
-    ms = e0.elapsed_time(e1)
+    reps_ms, _ = timed_reps(torch, dev, stream, step, steps, min_seconds)
+    us = sum(reps_ms) * 1e3 / (len(reps_ms) * steps)
     flags = moe.moe_device_status(ws, stream)
     if flags:
         raise RuntimeError(f"device flags {flags:#x}")
-    b = sum(lbytes[i % N_LAYERS] for i in range(steps))
-    return {"value": b / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": B * w.d * 2,
-            "d2h_bytes_per_step": B * w.d * 2, "us_per_layer": ms * 1e3 / steps, "_bytes": b, "_ms": ms}
+    fused = moe.moe_layer_launches(prm, w.F) == 2
+    return {"workload": w.name, "B": B, "run": run[0],
+            "kernels": ["route_fused_kernel"] if fused else ["router_bf16_kernel", "route_kernel"],
+            "us": round(us, 2), "bytes": router_bytes(w, B),
+            "gbs": round(router_bytes(w, B) / (us * 1e-6) / 1e9, 1)}
+
+
+def run_e2e(moe, torch, w, B, layers, run, steps, warmup, dev, stream, lbytes, min_seconds):
+    """The public one-call layer with the hidden states copied in from
+    pinned host memory and the output copied back, every step, inside the
+    timed region.  The copies run on a copy stream with two device buffers
+    each: a step's input is copied one step ahead, its output after an
+    event, so they overlap the neighbouring layers."""
+    nl = len(layers)
+    prm = params_of(moe, w, B, run)
+    routing = moe.Routing(prm, dev)
+    ws = moe.alloc_workspace(prm, w.F, dev)
+    cs = torch.cuda.Stream(dev)
+    bf = torch.bfloat16
+    x_host = [D["x"].cpu().pin_memory() for D in layers]
+    out_host = [torch.empty((B, w.d), dtype=bf).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty((B, w.d), dtype=bf, device=dev) for _ in range(2)]
+    out_dev = [torch.empty((B, w.d), dtype=bf, device=dev) for _ in range(2)]
+    ev_h2d = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_d2h = [torch.cuda.Event() for _ in range(2)]
+
+    def h2d(i):   # step i's hidden states into x_dev[i % 2], once step i-2 has read that buffer
+        b = i % 2
+        cs.wait_event(ev_comp[b])
+        with torch.cuda.stream(cs):
+            x_dev[b].copy_(x_host[i % nl], non_blocking=True)
+        ev_h2d[b].record(cs)
+
+    def region(first: int, n: int):
+        h2d(first)
+        for i in range(first, first + n):
+            b = i % 2
+            if i + 1 < first + n:
+                h2d(i + 1)
+            stream.wait_event(ev_h2d[b])
+            stream.wait_event(ev_d2h[b])           # out_dev[b] copied out (step i-2)
+            layer_call(moe, w, layers[i % nl], prm, routing, out_dev[b], ws, stream, x=x_dev[b])
+            ev_comp[b].record(stream)
+            cs.wait_event(ev_comp[b])
+            with torch.cuda.stream(cs):
+                out_host[b].copy_(out_dev[b], non_blocking=True)
+            ev_d2h[b].record(cs)
+        stream.wait_event(ev_d2h[(first + n - 1) % 2])   # the last output is on the host
+
+    region(0, warmup)
+    torch.cuda.synchronize(dev)
+    reps_ms = []
+    i = warmup
+    while True:
+        barrier(torch)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        cs.wait_event(a)
+        region(i, steps)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(torch)
+        reps_ms.append(a.elapsed_time(b))
+        i += steps
+        if sum(reps_ms) >= min_seconds * 1e3:
+            break
+    ms = sum(reps_ms)
+    n_steps = len(reps_ms) * steps
+    flags = moe.moe_device_status(ws, stream)
+    if flags:
+        raise RuntimeError(f"device flags {flags:#x}")
+    byt = sum(lbytes[j % nl] for j in range(warmup, warmup + n_steps))
+    return {"value": byt / (ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": B * w.d * 2,
+            "d2h_bytes_per_step": B * w.d * 2, "us_per_layer": ms * 1e3 / n_steps,
+            "call": "moe_decode_layer_mixed" if "mixed" in layers[0] else "moe_decode_layer",
+            "_bytes": byt, "_ms": ms}
+
+
+def config_of(w: synth.Workload, B: int, head: tuple, runs: dict, world: int) -> dict:
+    """The workload named in the JSON line (the same for both arms)."""
+    return {"workload": w.name, "B": B, "N": w.N, "k": w.k, "d": w.d, "d_ff": w.F,
+            "routing": head[0], "layers_rotated": N_LAYERS, "runs": sorted(runs),
+            "l2": "inputs larger than L2: %d-layer rotation, %.2f GB of expert weights per layer"
+                  % (N_LAYERS, w.N * w.expert_bytes / 1e9),
+            "parallelism": f"replicas x{world}"}
+
+
+def mode_row(r: dict, peak: float) -> dict:
+    return {"T": round(r["T_mean"], 2), "us_per_layer": round(r["us_per_layer"], 2),
+            "us_reps_p10_p50_p90": [round(v, 2) for v in r["us_per_layer_reps_p10_p50_p90"]],
+            "gbs": round(r["gbs"], 1), "tokens_per_s": round(r["tokens_per_s"]),
+            "frac_of_measured_hbm": round(r["gbs"] / peak, 4),
+            "ffn_us": round(r["ffn_us_mean"], 2), "ffn_gbs": round(r["ffn_gbs"], 1),
+            "ffn_frac_of_measured_hbm": round(r["ffn_gbs"] / peak, 4),
+            "ffn_frac_of_8tbs": round(r["ffn_gbs"] / SPEC_HBM_GBS, 4),
+            **({"hot_active": round(r["hot_active_mean"], 2)} if r["hot_active_mean"] is not None else {})}
+
+
+def add_vs_topk(rows: dict):
+    if "topk" in rows:
+        for label, r in rows.items():
+            if label != "topk":
+                r["latency_vs_topk"] = round(r["us_per_layer"] / rows["topk"]["us_per_layer"], 4)
+                r["T_vs_topk"] = round(r["T"] / rows["topk"]["T"], 4)
 
 
 # ---------------------------------------------------------------------------
@@ -525,6 +678,29 @@ def reduce_sum(torch, dev, x: float) -> float:
     return float(t.item())
 
 
+def sweep_rows(moe, torch, args, dev, stream, peak):
+    """The metric's other workloads and batch sizes, OEA against top-8."""
+    rows = []
+    for wname, batches in SWEEP:
+        w = synth.WORKLOADS[wname]
+        weights = build_weights(moe, torch, w, dev, N_LAYERS)
+        for B in batches:
+            layers = with_batch(moe, torch, w, weights, B, dev)
+            res = {}
+            for run in w.runs:
+                r = run_mode(moe, torch, w, B, layers, run, args.steps, args.warmup, dev, stream,
+                             args.sweep_seconds, detail_steps=100)
+                res[run[0]] = dict(workload=wname, B=B, run=run[0], **mode_row(r, peak))
+            add_vs_topk(res)
+            rows += list(res.values())
+            for r in res.values():
+                log(json.dumps(r))
+            del layers
+        del weights
+        torch.cuda.empty_cache()
+    return rows
+
+
 def main_ours(args):
     import torch
     import aware_expert_routing_gb300 as moe
@@ -541,21 +717,33 @@ def main_ours(args):
     B = args.batch or w.B
     runs = {r[0]: r for r in w.runs}
     head = runs[HEADLINE.get(w.name, w.runs[-1][0])]
-    stream = torch.cuda.Stream(dev)
-    layers = build_layers(moe, torch, w, B, dev)
-    smi = gpu_smi_id(torch, dev)
-
-    results = {}
     if args.only_run:
         runs = {args.only_run: runs[args.only_run]}
         head = runs[args.only_run]
+    stream = torch.cuda.Stream(dev)
+    layers = build_layers(moe, torch, w, B, dev)
+    peaks = measured_peaks()
+
+    # the headline run first, with the clock sampler running
+    results = {}
+    clocks = Clocks(gpu_smi_id(torch, dev))
+    time.sleep(0.5)          # nvidia-smi start-up
+    results[head[0]] = run_mode(moe, torch, w, B, layers, head, args.steps, args.warmup, dev, stream,
+                                args.min_seconds, clocks=clocks)
+    time.sleep(0.2)
+    clk = clocks.stop()
     for label, run in runs.items():
-        res = run_mode(moe, torch, w, B, layers, run, args.steps, args.warmup, dev, stream,
-                       clocks_for=smi if label == head[0] else None)
-        res.pop("objs")
-        results[label] = res
+        if label != head[0]:
+            results[label] = run_mode(moe, torch, w, B, layers, run, args.steps, args.warmup, dev, stream,
+                                      args.min_seconds / 2)
     hr = results[head[0]]
-    e2e = run_e2e(moe, torch, w, B, layers, head, args.steps, args.warmup, dev, stream, hr["layer_bytes"])
+    e2e = run_e2e(moe, torch, w, B, layers, head, args.steps, args.warmup, dev, stream, hr["layer_bytes"],
+                  args.min_seconds / 2)
+    router = [run_router(moe, torch, w, B, layers, head, args.steps, args.warmup, dev, stream, 0.2)]
+    if B <= 32 and not args.no_sweep:   # the separate router and routing kernels (above 32 tokens)
+        l64 = with_batch(moe, torch, w, [{k: v for k, v in D.items() if k != "x"} for D in layers], 64, dev)
+        router.append(run_router(moe, torch, w, 64, l64, head, args.steps, args.warmup, dev, stream, 0.2))
+        del l64
 
     # whole job: bytes of all ranks / slowest rank
     t_max = reduce_max(torch, dev, hr["total_ms"])
@@ -565,14 +753,17 @@ def main_ours(args):
     e2e["value"] = round(reduce_sum(torch, dev, e2e.pop("_bytes")) / (e2e_ms * 1e-3) / 1e9, 1)
     e2e["us_per_layer"] = round(e2e["us_per_layer"], 2)
 
+    del layers
+    torch.cuda.empty_cache()
+    sweep = [] if args.no_sweep else sweep_rows(moe, torch, args, dev, stream, peaks["hbm_gbs"])
+
     if rank != 0:
         return
-    peaks = measured_peaks()
     ach = hr["ffn_gbs"]
     roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(ach / peaks["hbm_gbs"], 4),
-            "traffic": recorded_traffic(w.name, head[0], hr["ffn_bytes_per_launch"], expert_kernel(w)[1]),
-            "kernel": expert_kernel(w)[0], "peak_source": peaks["source"],
+            "frac": round(ach / peaks["hbm_gbs"], 4), "frac_of_8tbs_spec": round(ach / SPEC_HBM_GBS, 4),
+            "traffic": recorded_traffic(w.name, head[0], hr["ffn_bytes_per_launch"]),
+            "kernel": "ffn_tc_kernel", "peak_source": peaks["source"],
             "algorithmic_bytes_per_launch": round(hr["ffn_bytes_per_launch"]),
             "mean_launch_us": round(hr["ffn_us_mean"], 2)}
     base = None
@@ -580,54 +771,42 @@ def main_ours(args):
         mean_b = float(np.mean(hr["layer_bytes"]))
         base = cpu_baseline(w, B, head, args.cpu_budget,
                             (lambda T: mean_b) if w.int4_cold else (lambda T: layer_bytes(w, B, T)))
-    modes = {}
-    for label, r in results.items():
-        modes[label] = {"T": round(r["T_mean"], 2), "us_per_layer": round(r["us_per_layer"], 2),
-                        "us_p10_p50_p90": [round(v, 2) for v in r["us_per_layer_p10_p50_p90"]],
-                        "gbs": round(r["gbs"], 1), "tokens_per_s": round(r["tokens_per_s"]),
-                        "frac_of_measured_hbm": round(r["gbs"] / peaks["hbm_gbs"], 4),
-                        "us_per_layer_with_kernel_events": round(r["us_per_layer_with_kernel_events"], 2),
-                        "ffn_us": round(r["ffn_us_mean"], 2), "ffn_gbs": round(r["ffn_gbs"], 1)}
-    if "topk" in results:
-        for label, r in results.items():
-            if label != "topk":
-                modes[label]["latency_vs_topk"] = round(r["us_per_layer"] / results["topk"]["us_per_layer"], 4)
-                modes[label]["T_vs_topk"] = round(r["T_mean"] / results["topk"]["T_mean"], 4)
+    modes = {label: mode_row(r, peaks["hbm_gbs"]) for label, r in results.items()}
+    add_vs_topk(modes)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(t_max / args.steps, 5), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(t_max / hr["steps_timed"], 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded SplitMix64/Irwin-Hall weights and hidden states, random init",
-        "config": {"workload": w.name, "B": B, "N": w.N, "k": w.k, "d": w.d, "d_ff": w.F,
-                   "routing": head[0], "layers_rotated": N_LAYERS, "runs": sorted(runs),
-                   "l2": "inputs larger than L2: %d-layer rotation, %.2f GB of expert weights per layer"
-                         % (N_LAYERS, w.N * w.expert_bytes / 1e9),
-                   "parallelism": f"replicas x{world}"},
-        "modes": modes, "roofline": roof, "cpu_baseline": base, "e2e": e2e,
-        "clocks": hr["clocks"], "gpu_launches": hr["launches"],
+        "config": config_of(w, B, head, runs, world),
+        "timed_regions": hr["reps"], "steps_per_region": args.steps,
+        "modes": modes, "sweep": sweep, "router": router, "roofline": roof, "cpu_baseline": base, "e2e": e2e,
+        "clocks": clk, "gpu_launches": hr["launches_per_region"],
     }
     print(json.dumps(line), flush=True)
     if args.sweep_out:
-        sweep(moe, torch, w, dev, stream, args)
+        full_sweep(moe, torch, w, dev, stream, args)
     if args.linearity_out:
         linearity(moe, torch, w, dev, stream, args)
 
 
-def sweep(moe, torch, w, dev, stream, args):
-    """Per-B rows for the workload's batch sweep (written to a file)."""
+def full_sweep(moe, torch, w, dev, stream, args):
+    """Per-B rows for the workload's whole batch sweep (written to a file)."""
     rows = []
+    peak = measured_peaks()["hbm_gbs"]
+    weights = build_weights(moe, torch, w, dev, N_LAYERS)
     for B in (w.batch_sweep or (w.B,)):
-        layers = build_layers(moe, torch, w, B, dev)
+        layers = with_batch(moe, torch, w, weights, B, dev)
+        res = {}
         for run in w.runs:
-            r = run_mode(moe, torch, w, B, layers, run, max(50, args.steps // 4), args.warmup, dev, stream)
-            r.pop("objs")
-            rows.append({"workload": w.name, "B": B, "run": run[0], "T": r["T_mean"],
-                         "us_per_layer": r["us_per_layer"], "p10_p50_p90": r["us_per_layer_p10_p50_p90"],
-                         "tokens_per_s": r["tokens_per_s"], "gbs": r["gbs"], "ffn_us": r["ffn_us_mean"],
-                         "ffn_gbs": r["ffn_gbs"]})
-            log(json.dumps(rows[-1]))
+            r = run_mode(moe, torch, w, B, layers, run, args.steps, args.warmup, dev, stream,
+                         args.sweep_seconds)
+            res[run[0]] = dict(workload=w.name, B=B, run=run[0], **mode_row(r, peak))
+        add_vs_topk(res)
+        rows += list(res.values())
+        for r in res.values():
+            log(json.dumps(r))
         del layers
-        torch.cuda.empty_cache()
     with open(args.sweep_out, "w") as f:
         json.dump(rows, f, indent=1)
 
@@ -641,6 +820,18 @@ def linear_fit(X: np.ndarray, y: np.ndarray) -> dict:
     return {"coef": [float(b) for b in beta], "r2": 1.0 - ss_res / ss_tot if ss_tot > 0 else 1.0}
 
 
+def linearity_points(k: int, N: int, B: int) -> list:
+    """Forced union sizes T for one batch size: top-min(k, T) routing on T
+    experts, so only T <= k is possible for a single token (distinct
+    (B, k, T) points only)."""
+    pts = []
+    for Tt in (1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128):
+        if Tt > N or (B == 1 and Tt > k):
+            continue
+        pts.append(Tt)
+    return pts
+
+
 def linearity(moe, torch, w, dev, stream, args):
     """Latency against T (distinct activated experts) and sum(cnt_e) (token-
     expert pairs), the OEA page's cost model (section 4: latency grows with
@@ -648,44 +839,43 @@ def linearity(moe, torch, w, dev, stream, args):
     T experts drawn with a seeded generator (every token's top-k then lies
     among them) with top-min(k, T) routing, so sum(cnt_e) = B min(k, T);
     B in {1, 4, 16, 64} varies sum(cnt_e) independently of T.  Fits
-    us = a sum(cnt_e) + b T + c for the whole layer and the expert kernel;
-    b is the cost of one more activated expert, 3 d d_ff 2 / b its
-    streaming rate.  32 distinct layers rotate (1.2 GB of experts each at
-    the 30B shapes), so even T = 1 streams 300 MB per rotation, above the
-    126 MB L2."""
+    us = a sum(cnt_e) + b T + c for the whole layer and the expert kernel,
+    over all points and per batch size; b is the cost of one more
+    activated expert (a marginal cost, not a bandwidth).  32 distinct
+    layers rotate (1.2 GB of experts each at the 30B shapes), so even T = 1
+    streams 300 MB per rotation, above the 126 MB L2."""
     import dataclasses
-    global N_LAYERS
-    saved, N_LAYERS = N_LAYERS, 32
     rows = []
-    steps = max(100, args.steps // 20)
+    weights = build_weights(moe, torch, w, dev, 32)
     for B in (1, 4, 16, 64):
-        base = build_layers(moe, torch, w, B, dev)
-        for Tt in (1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128):
-            if Tt > w.N:
-                continue
+        base = with_batch(moe, torch, w, weights, B, dev)
+        for Tt in linearity_points(w.k, w.N, B):
             k = min(w.k, Tt)
             wk = dataclasses.replace(w, k=k)
             bias = np.zeros(w.N, np.float32)
             bias[np.random.default_rng(1000 + Tt).choice(w.N, Tt, replace=False)] = 20.0
             bias_d = torch.from_numpy(bias).to(dev)
             layers = [dict(D, bias=bias_d) for D in base]
-            r = run_mode(moe, torch, wk, B, layers, ("topk", "topk", k, 1.0), steps, args.warmup, dev, stream,
-                         detail_steps=steps)
-            r.pop("objs")
+            r = run_mode(moe, torch, wk, B, layers, ("topk", "topk", k, 1.0), args.steps, args.warmup, dev,
+                         stream, args.sweep_seconds, detail_steps=200)
             rows.append({"B": B, "k": k, "T_forced": Tt, "T": r["T_mean"], "sum_cnt": B * k,
                          "us_per_layer": r["us_per_layer"], "ffn_us": r["ffn_us_mean"]})
             log(json.dumps(rows[-1]))
         del base
-        torch.cuda.empty_cache()
-    N_LAYERS = saved
-    X = np.array([[r["sum_cnt"], r["T"], 1.0] for r in rows])
+    del weights
+    torch.cuda.empty_cache()
     out = {"workload": w.name, "model": "us = a * sum_cnt + b * T + c", "layers_rotated": 32, "rows": rows}
     for key, col in (("fit_layer", "us_per_layer"), ("fit_expert_kernel", "ffn_us")):
+        X = np.array([[r["sum_cnt"], r["T"], 1.0] for r in rows])
         f = linear_fit(X, np.array([r[col] for r in rows]))
         a, b, c = f["coef"]
-        out[key] = {"a_us_per_pair": a, "b_us_per_expert": b, "c_us": c, "r2": f["r2"],
-                    "expert_bytes": w.expert_bytes,
-                    "streaming_gbs_per_added_expert": w.expert_bytes / (b * 1e-6) / 1e9 if b > 0 else None}
+        out[key] = {"a_us_per_pair": a, "b_us_per_expert": b, "c_us": c, "r2": f["r2"]}
+        for Bq in (4, 16, 64):   # per batch size: us = b T + c (sum_cnt fixed for T >= k)
+            sel = [r for r in rows if r["B"] == Bq and r["T_forced"] >= w.k]
+            if len(sel) >= 3:
+                fb = linear_fit(np.array([[r["T"], 1.0] for r in sel]), np.array([r[col] for r in sel]))
+                out[key][f"B{Bq}_T_ge_k"] = {"b_us_per_expert": fb["coef"][0], "c_us": fb["coef"][1],
+                                             "r2": fb["r2"], "points": len(sel)}
     with open(args.linearity_out, "w") as f:
         json.dump(out, f, indent=1)
     log(json.dumps({k: v for k, v in out.items() if k.startswith("fit")}))
@@ -710,16 +900,16 @@ def main_reference(args):
             vals.append(o)
     sec = float(np.mean([o["seconds_per_layer"] for o in vals]))
     value = layer_bytes(w, B, vals[0]["T"]) / sec / 1e9
+    cpu = cpu_description()
     sample = (f"per step: oracle router+routing on the full B={B} batch and single-token expert FFNs "
               f"(8 experts cycled, at least one, for {budget:.3f} s), scaled to one layer's "
-              f"(token, expert) pairs; single thread")
+              f"(token, expert) pairs; single thread on 1 of {cpu['nproc']} cores ({cpu['cpu_model']})")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": w.name, "B": B, "N": w.N, "k": w.k, "d": w.d, "d_ff": w.F,
-                       "routing": head[0]},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "config": config_of(w, B, head, runs, 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample, **cpu},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -727,14 +917,18 @@ def main_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20, help="steps per timed region")
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="device time the headline run's timed regions add up to at least")
+    ap.add_argument("--sweep-seconds", type=float, default=0.25, help="the same for each sweep row")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sweep-out", default="")
+    ap.add_argument("--no-sweep", action="store_true", help="only the headline workload")
+    ap.add_argument("--sweep-out", default="", help="the workload's whole batch sweep, written to this file")
     ap.add_argument("--linearity-out", default="", help="latency-vs-T sweep and fit, written to this file")
     ap.add_argument("--layers", type=int, default=8, help="distinct layers rotated through")
     ap.add_argument("--only-run", default="", help="time only this routing run (profiling)")
@@ -743,6 +937,8 @@ def main():
     N_LAYERS = args.layers
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
     if args.impl == "reference":
         main_reference(args)
     else:

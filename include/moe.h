@@ -218,19 +218,20 @@ moe_status moe_expert_ffn(const void *hidden, const void *w_gate, const void *w_
  * weights in w_gate / w_up / w_down (laid out as for moe_expert_ffn, with
  * n_hot experts); cold experts are INT4 with one bf16 scale per row and
  * 128-column group of the contraction dimension (d for W_gate / W_up, d_ff
- * for W_down): w = q * s, q in -7..7.
+ * for W_down): w = q * s, q in -7..7.  An INT4 expert is
+ * 3 * (d * d_ff / 2 + d * d_ff / 64) bytes (moe_pack_int4 makes images).
  *   slot    [N] int32, device: for expert e, slot[e] >= 0 is its index among
  *           the bf16 experts, slot[e] < 0 means INT4 expert -1 - slot[e].
  *           An out-of-range slot raises MOE_FLAG_BAD_INDEX.
  *   q_gate, q_up  [n_cold] packed images of the [d_ff][d] matrices,
  *   q_down        [n_cold] packed images of the [d][d_ff] matrices.
  * Packed image of a matrix [rows][cols] with chunk height rb (64 for W_gate
- * and W_up, 128 for W_down): chunks of rb rows x 64 columns in row-block-
- * major, column-block order; a chunk is rb*32 bytes of codes then rb bf16
- * scales (one per row: the scale of the 128-column group holding the
- * chunk's columns).  In a chunk row, local column c is the 4-bit field at
- * bit 4*((c%8)/2) + 16*(c%2) of little-endian 32-bit word c/8 of the row's
- * 32 bytes, holding q + 8.
+ * and W_up, 128 for W_down): chunks of rb rows x 128 columns (one scale
+ * group) in row-block-major, column-group order; a chunk is rb*64 bytes of
+ * codes then rb bf16 scales (one per row: the row's scale of the group).
+ * In a chunk row, local column c is the 4-bit field at bit
+ * 4*((c%8)/2) + 16*(c%2) of little-endian 32-bit word c/8 of the row's 64
+ * bytes, holding q + 8.
  * Requirements: dtype bf16, d and d_ff multiples of 128, n_hot >= 1,
  * 16-byte aligned images.  Results as moe_expert_ffn; each INT4 weight is
  * decoded to q exactly and multiplied by its group scale with one rounding
@@ -249,6 +250,25 @@ moe_status moe_expert_ffn_mixed(const void *hidden, const void *w_gate, const vo
                                 const moe_mixed_experts *mixed, int32_t d_ff, const moe_route_params *params,
                                 const moe_routing *routing, void *out, void *workspace, size_t workspace_bytes,
                                 moe_stream_t stream);
+
+/*
+ * Makes the packed INT4 image of one bf16 matrix on the device: the 4-bit
+ * version of an expert matrix that moe_expert_ffn_mixed reads (DynaExq
+ * page, section 3.2, INT4 tier; section 2.4: a new version is prepared
+ * off the request path and only then published, here by writing the
+ * expert's slot).  Per row and 128-column group:
+ *   s = max|w| / 7, the quotient taken in double and rounded to nearest
+ *       even, first to fp32, then to bf16;
+ *   q = rint(w / s) in double (ties to even), clamped to -7..7; q = 0
+ *       where s = 0.
+ *   w     [rows][cols] bf16, device, 16-byte aligned.
+ *   rows  a multiple of rb.  cols: a multiple of 128.
+ *   rb    chunk height of the image: 64 for W_gate / W_up, 128 for W_down
+ *         (any multiple of 8 is accepted).
+ *   out   rows*cols/2 + rows*(cols/128)*2 bytes, device, 16-byte aligned.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+moe_status moe_pack_int4(const void *w, int32_t rows, int32_t cols, int32_t rb, void *out, moe_stream_t stream);
 
 /*
  * The whole layer with mixed-precision experts in one call: moe_route, then

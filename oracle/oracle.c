@@ -318,27 +318,27 @@ void oracle_moe_experts(const float *x, const float *w_gate, const float *w_up,
 
 /* INT4 group-wise dequantisation of one packed matrix [rows][cols]:
  * w[r][c] = q[r][c] * s[r][c / 128], symmetric codes q in -7..7.
- * Packed format (chunks of rb rows x 64 columns, in row-block-major then
- * column-block order; each chunk = rb*32 code bytes then rb bf16 scales):
- * within a chunk row r, local column c is the nibble at bit
- * 4*((c%8)/2) + 16*(c%2) of the little-endian 32-bit word c/8 of the row's
- * 32 bytes, stored as q + 8; the row's scale (of the 128-column group that
- * holds the chunk) follows all code bytes, at r*2 bytes. */
+ * Packed format (chunks of rb rows x 128 columns -- one scale group -- in
+ * row-block-major then column-group order; each chunk = rb*64 code bytes
+ * then rb bf16 scales): within a chunk row r, local column c is the nibble
+ * at bit 4*((c%8)/2) + 16*(c%2) of the little-endian 32-bit word c/8 of
+ * the row's 64 bytes, stored as q + 8; the row's scale of the group
+ * follows all code bytes, at r*2 bytes. */
 void oracle_dequant_int4(const uint8_t *packed, int rows, int cols, int rb, float *out)
 {
-    const int nkb = cols / 64;
-    const size_t chunk = (size_t)rb * 32 + (size_t)rb * 2;
+    const int nkb = cols / 128;
+    const size_t chunk = (size_t)rb * 64 + (size_t)rb * 2;
     for (int r = 0; r < rows; ++r)
         for (int c = 0; c < cols; ++c) {
-            const int rbi = r / rb, rr = r % rb, kb = c / 64, cl = c % 64;
+            const int rbi = r / rb, rr = r % rb, kb = c / 128, cl = c % 128;
             const uint8_t *ch = packed + ((size_t)rbi * nkb + kb) * chunk;
-            const uint8_t *wp = ch + (size_t)rr * 32 + (size_t)(cl / 8) * 4;
+            const uint8_t *wp = ch + (size_t)rr * 64 + (size_t)(cl / 8) * 4;
             uint32_t word = (uint32_t)wp[0] | ((uint32_t)wp[1] << 8) | ((uint32_t)wp[2] << 16) |
                             ((uint32_t)wp[3] << 24);
             const int o = cl % 8;
             const int bit = 4 * (o / 2) + 16 * (o % 2);
             const int q = (int)((word >> bit) & 0xFu) - 8;
-            const uint8_t *sp = ch + (size_t)rb * 32 + (size_t)rr * 2;   /* this row's group scale */
+            const uint8_t *sp = ch + (size_t)rb * 64 + (size_t)rr * 2;   /* this row's group scale */
             uint32_t sb = ((uint32_t)sp[0] | ((uint32_t)sp[1] << 8)) << 16;
             float sc;
             memcpy(&sc, &sb, sizeof sc);

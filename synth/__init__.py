@@ -222,7 +222,7 @@ def make_layer(w: Workload, layer: int = 0, B: int | None = None, step: int = 0)
 # INT4 cold-expert format (input preparation for the mixed-precision layer)
 # ---------------------------------------------------------------------------
 INT4_GROUP = 128     # scale group along the contraction dimension
-INT4_CHUNK = 64      # columns per tile chunk
+INT4_CHUNK = 128     # columns per tile chunk: one scale group
 INT4_RB_GATE_UP = 64  # rows per chunk of W_gate / W_up
 INT4_RB_DOWN = 128    # rows per chunk of W_down
 
@@ -246,33 +246,32 @@ def quantize_int4(w: np.ndarray):
 def pack_int4_tiles(q: np.ndarray, s: np.ndarray, rb: int) -> np.ndarray:
     """Tile-contiguous byte image of one quantised matrix.
 
-    The matrix is cut into chunks of `rb` rows x 64 columns, stored in the
-    order (row block, column block).  A chunk is rb*32 bytes of codes (32
-    per row) followed by rb bf16 scales (one per row: the scale of the
-    128-column group that holds the chunk's columns).  Codes are stored
-    offset by 8 (q + 8 in 0..15).  Within a row, column c = 8*h + o (word h,
-    offset o) is the nibble at bit 4*(o//2) + 16*(o%2) of 32-bit word h,
-    little endian: each 16-bit half of a word holds the codes of two
-    adjacent columns four bits apart.
+    The matrix is cut into chunks of `rb` rows x 128 columns (one scale
+    group), stored in the order (row block, column group).  A chunk is
+    rb*64 bytes of codes (64 per row) followed by rb bf16 scales (one per
+    row: the row's scale of that group).  Codes are stored offset by 8
+    (q + 8 in 0..15).  Within a row, column c = 8*h + o (word h, offset o)
+    is the nibble at bit 4*(o//2) + 16*(o%2) of 32-bit word h, little
+    endian: each 16-bit half of a word holds the codes of two adjacent
+    columns four bits apart.
     """
     R, K = q.shape
-    assert R % rb == 0 and K % INT4_CHUNK == 0 and K % INT4_GROUP == 0
+    assert R % rb == 0 and K % INT4_CHUNK == 0 and INT4_CHUNK == INT4_GROUP
     nrb, nkb = R // rb, K // INT4_CHUNK
     code = (q.astype(np.int16) + 8).astype(np.uint32).reshape(R, K // 8, 8)   # words of 8 columns
     shifts = np.array([0, 16, 4, 20, 8, 24, 12, 28], np.uint32)
     words = (code << shifts[None, None, :]).sum(axis=2, dtype=np.uint64).astype(np.uint32)   # [R][K/8]
-    words = words.reshape(nrb, rb, nkb, INT4_CHUNK // 8).transpose(0, 2, 1, 3)             # [nrb][nkb][rb][8]
-    code_bytes = np.ascontiguousarray(words).astype("<u4").view(np.uint8).reshape(nrb, nkb, rb * 32)
-    sg = np.repeat(np.asarray(s, np.float32), INT4_GROUP // INT4_CHUNK, axis=1)             # [R][K/64]
-    sb = to_bf16_bits(sg).reshape(nrb, rb, nkb).transpose(0, 2, 1)                          # [nrb][nkb][rb]
+    words = words.reshape(nrb, rb, nkb, INT4_CHUNK // 8).transpose(0, 2, 1, 3)             # [nrb][nkb][rb][16]
+    code_bytes = np.ascontiguousarray(words).astype("<u4").view(np.uint8).reshape(nrb, nkb, rb * 64)
+    sb = to_bf16_bits(np.asarray(s, np.float32)).reshape(nrb, rb, nkb).transpose(0, 2, 1)   # [nrb][nkb][rb]
     scale_bytes = np.ascontiguousarray(sb).astype("<u2").view(np.uint8).reshape(nrb, nkb, rb * 2)
     return np.concatenate([code_bytes, scale_bytes], axis=2).reshape(-1)
 
 
 def int4_expert_bytes(d: int, F: int) -> int:
-    """Bytes of one expert's three packed INT4 matrices: codes and one bf16
-    scale per row and 64-column chunk."""
-    return 3 * (d * F // 2 + d * F // INT4_CHUNK * 2)
+    """Bytes of one expert's three packed INT4 matrices: half a byte per
+    weight and one bf16 scale per row and 128-column group."""
+    return 3 * (d * F // 2 + d * F // INT4_GROUP * 2)
 
 
 def pack_int4_expert(w_gate: np.ndarray, w_up: np.ndarray, w_down: np.ndarray):

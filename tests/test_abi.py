@@ -112,6 +112,14 @@ def test_batch_size_policy_is_accepted(lib):
     assert lib.moe_num_slots(ctypes.byref(P(B=4, mode=moe.MODE_OEA, k0=0, kmax=4).c())) == -1   # k0 = 5 > kmax
 
 
+def test_int4_pack_checks_its_arguments(lib):
+    fake = ctypes.c_void_p(4096)
+    for rows, cols, rb, w, out in [(64, 100, 64, fake, fake), (64, 256, 48, fake, fake), (60, 256, 64, fake, fake),
+                                   (64, 256, 64, None, fake), (64, 256, 64, fake, ctypes.c_void_p(4104))]:
+        assert lib.moe_pack_int4(w, rows, cols, rb, out, None) == moe.MOE_ERR_ARG
+    assert moe.int4_image_bytes(768, 2048) == 768 * 2048 // 2 + 768 * 16 * 2
+
+
 def test_mixed_layer_checks_its_descriptor_before_launching(lib):
     """moe_decode_layer_mixed rejects a bad expert descriptor on the host,
     so not even the routing kernel is launched."""

@@ -20,3 +20,15 @@ def test_linear_fit_recovers_plane():
     assert abs(f["r2"] - 1.0) < 1e-12
     g = bench.linear_fit(X, y + rng.normal(0, 5.0, 40))
     assert 0.5 < g["r2"] < 1.0
+
+
+def test_linearity_points_are_distinct():
+    """One token keeps at most k experts, so at B = 1 only T <= k is a new
+    point: no (B, k, T) point repeats."""
+    for B in (1, 4, 16, 64):
+        pts = bench.linearity_points(8, 128, B)
+        assert len(set(pts)) == len(pts)
+        if B == 1:
+            assert max(pts) <= 8
+        else:
+            assert max(pts) == 128

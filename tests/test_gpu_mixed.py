@@ -36,7 +36,7 @@ def build_mixed(w, L, hot, active=None):
     for i, e in enumerate(cold):
         slot[e] = -1 - i
     eff = {k: L[k].copy() for k in ("w_gate", "w_up", "w_down")}
-    na, nd = F * d // 2 + F * (d // 64) * 2, d * F // 2 + d * (F // 64) * 2   # codes + a scale per 64-column chunk
+    na, nd = moe.int4_image_bytes(F, d), moe.int4_image_bytes(d, F)   # codes + a scale per 128-column group
     qg = np.zeros((len(cold), na), np.uint8)
     qu = np.zeros((len(cold), na), np.uint8)
     qd = np.zeros((len(cold), nd), np.uint8)
@@ -103,6 +103,22 @@ def test_mixed_small_batches(d, F, B):
     ref = oracle.moe_experts(L["x"], eff["w_gate"], eff["w_up"], eff["w_down"], g["expert_idx"],
                              g["weights"].astype(np.float64))
     gu.check_output(out, ref, True)
+
+
+@pytest.mark.parametrize("rows,cols,rb", [(64, 2048, 64), (256, 384, 128), (24, 128, 8)])
+def test_device_int4_pack_matches_host(rows, cols, rb):
+    """moe_pack_int4 writes the same bytes as the host packer: scales,
+    ties to even (w / s exactly k + 1/2), groups of zeros and the clamp."""
+    rng = np.random.default_rng(rows + cols)
+    w = synth.round_bf16(rng.standard_normal((rows, cols)).astype(np.float32) * 0.05)
+    w[0, :128] = 0.0                                    # s = 0: every code 0
+    w[1, :128] = np.float32(0.25) * np.resize(np.arange(-7.0, 7.5, 0.5), 128).astype(np.float32)
+    w[1, 0] = np.float32(1.75)                          # max 1.75: s = 0.25, w / s hits every half step
+    q, s = synth.quantize_int4(w)
+    want = synth.pack_int4_tiles(q, s, rb)
+    got = moe.moe_pack_int4(torch.from_numpy(w).to(gu.DEV).to(torch.bfloat16), rb)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), want)
 
 
 @pytest.mark.parametrize("mode,k0", [(TOPK, 2), (OEA, 1)])

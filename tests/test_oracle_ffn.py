@@ -97,25 +97,25 @@ def test_router_logits_match_library():
 
 def pack_by_definition(q, s, rb):
     """The packed format built byte by byte from its definition (a second,
-    independent construction): chunks of rb rows x 64 columns, codes then
-    one bf16 scale per row."""
+    independent construction): chunks of rb rows x 128 columns (one scale
+    group), codes then one bf16 scale per row."""
     R, K = q.shape
     out = bytearray()
     for rbi in range(R // rb):
-        for kb in range(K // 64):
-            codes = bytearray(rb * 32)
+        for kb in range(K // 128):
+            codes = bytearray(rb * 64)
             for rr in range(rb):
                 r = rbi * rb + rr
-                for cl in range(64):
+                for cl in range(128):
                     o = cl % 8
                     bit = 4 * (o // 2) + 16 * (o % 2)
-                    word_off = rr * 32 + (cl // 8) * 4
-                    v = (int(q[r, kb * 64 + cl]) + 8) << bit
+                    word_off = rr * 64 + (cl // 8) * 4
+                    v = (int(q[r, kb * 128 + cl]) + 8) << bit
                     for byte in range(4):
                         codes[word_off + byte] |= (v >> (8 * byte)) & 0xFF
             scales = bytearray()
             for rr in range(rb):
-                group = (kb * 64) // 128
+                group = kb
                 bits = int(synth.to_bf16_bits(np.array([s[rbi * rb + rr, group]], np.float32))[0])
                 scales += bytes([bits & 0xFF, bits >> 8])
             out += codes + scales
@@ -135,6 +135,18 @@ def test_dequant_int4_codes_and_layout():
     assert np.array_equal(packed, synth.pack_int4_tiles(q, s, rb))
     out = oracle.dequant_int4(packed, rows, cols, rb)
     assert np.array_equal(out, (q * np.repeat(s, 128, axis=1)).astype(np.float32))
+
+
+def test_int4_expert_bytes_are_half_a_byte_per_weight_plus_group_scales():
+    """One expert at the Qwen3-30B-A3B shapes: 3 d d_ff / 2 code bytes and
+    one bf16 scale per row and 128-column group, 2,433,024 bytes."""
+    d, F = 2048, 768
+    assert synth.int4_expert_bytes(d, F) == 3 * (d * F // 2 + d * F // 128 * 2) == 2_433_024
+    rng = np.random.default_rng(1)
+    g, u = (synth.round_bf16(rng.standard_normal((128, 256)).astype(np.float32)) for _ in range(2))
+    dn = synth.round_bf16(rng.standard_normal((256, 128)).astype(np.float32))
+    (pg, pu, pd), _ = synth.pack_int4_expert(g, u, dn)
+    assert pg.size + pu.size + pd.size == synth.int4_expert_bytes(256, 128)
 
 
 def test_int4_round_trip_within_half_step():

@@ -35,7 +35,7 @@ MUTANTS = {
     "max_depth_ignored": ("const int depth = maxP < N ? maxP : N;", "const int depth = N;"),
     "int4_nibble_pairs_swapped": ("const int bit = 4 * (o / 2) + 16 * (o % 2);",
                                   "const int bit = 16 * (o / 2 % 2) + 4 * (o % 2) + 8 * (o / 4);"),
-    "int4_scale_row_ignored": ("(size_t)rb * 32 + (size_t)rr * 2;", "(size_t)rb * 32;"),
+    "int4_scale_row_ignored": ("(size_t)rb * 64 + (size_t)rr * 2;", "(size_t)rb * 64;"),
     "int4_chunk_order_swapped": ("((size_t)rbi * nkb + kb) * chunk", "((size_t)kb * (rows / rb) + rbi) * chunk"),
     "given_baseline_sizes_ignored": ("nbase[i] = nbase_in[i];", "nbase[i] = k0;"),
     "policy_keeps_oea_for_one_token": ("if (B_valid <= 1) {", "if (B_valid < 1) {"),
