@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -147,31 +148,73 @@ struct MapKey {
 
 std::mutex g_map_mu;
 
-// Routing calls per workspace.  Each routing launch publishes its early
-// union of activated experts under a new epoch (never 0); the expert kernel
-// that follows on the same workspace waits for that epoch, so a union left
-// by an earlier call never passes for the current one.
-std::mutex g_epoch_mu;
-std::unordered_map<const void*, uint32_t> g_epoch;
+// Per workspace: the epoch of its last routing call, and whether the expert
+// kernel's counters are fresh (zeroed by that routing call and not used
+// since).  Each OEA routing launch of up to 32 tokens publishes its union of
+// activated experts under a new epoch (never 0, distinct across all
+// workspaces); the expert kernel that follows on the same workspace waits
+// for that epoch, so a union left by an earlier call never passes for the
+// current one.  Forgetting a workspace is safe: its next expert call then
+// clears the counters itself and waits for the whole routing.
+struct WsState {
+    uint32_t epoch = 0;    // 0: no routing call recorded
+    uint32_t routes = 0;   // routing calls recorded (their parity picks the counter sets)
+    bool fresh = false;    // the expert counters of the last routing call are unused
+    bool known = false;
+};
+std::mutex g_ws_mu;
+std::unordered_map<const void*, WsState> g_ws;
+uint32_t g_last_epoch = 0;
 
-// The epoch the next routing call on `ws` publishes under; recorded by
-// commit_epoch() once that call's kernel has been launched.
-uint32_t next_epoch(const void* ws) {
-    std::lock_guard<std::mutex> lk(g_epoch_mu);
-    const auto it = g_epoch.find(ws);
-    const uint32_t e = it == g_epoch.end() ? 0u : it->second;
-    return e + 1u == 0u ? 1u : e + 1u;
+// The epoch the next routing call publishes under (recorded by
+// routed() once that call's kernel has been launched).
+uint32_t next_epoch() {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    return g_last_epoch + 1u == 0u ? 1u : g_last_epoch + 1u;
 }
 
-void commit_epoch(const void* ws, uint32_t e) {
-    std::lock_guard<std::mutex> lk(g_epoch_mu);
-    g_epoch[ws] = e;
+// A routing kernel was launched on `ws` (epoch e, or 0: none published).
+void routed(const void* ws, uint32_t e) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    if (g_ws.size() >= 4096 && !g_ws.count(ws)) g_ws.clear();
+    WsState& st = g_ws[ws];
+    st.epoch = e;
+    st.routes += 1;
+    st.fresh = true;
+    st.known = true;
+    if (e) g_last_epoch = e;
 }
 
-uint32_t current_epoch(const void* ws) {   // 0: no routing call recorded for this workspace
-    std::lock_guard<std::mutex> lk(g_epoch_mu);
-    const auto it = g_epoch.find(ws);
-    return it == g_epoch.end() ? 0u : it->second;
+// The expert counter set used after routing call r (the one routing call
+// r zeroes is the other).
+int counter_set(uint32_t routes_before) { return (int)(routes_before & 1u); }
+
+// Zeroes counter set `set` (both, if set < 0) of the workspace on `s`.
+cudaError_t clear_counters(unsigned char* ws, const WsLayout& L, int set, cudaStream_t s) {
+    WsHeader* h = reinterpret_cast<WsHeader*>(ws + L.header);
+    for (int k = 0; k < 2; ++k) {
+        if (set >= 0 && k != set) continue;
+        cudaError_t e = cudaMemsetAsync(&h->next_tile[k], 0, sizeof(uint32_t), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(&h->gathered[k], 0, sizeof(uint32_t), s);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(ws + L.hdone + (size_t)k * kHdoneSet * sizeof(uint32_t), 0,
+                                (size_t)kHdoneSet * sizeof(uint32_t), s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+WsState ws_state(const void* ws) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    const auto it = g_ws.find(ws);
+    return it == g_ws.end() ? WsState{} : it->second;
+}
+
+// An expert kernel was launched on `ws`: its counters are used.
+void experts_launched(const void* ws) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    const auto it = g_ws.find(ws);
+    if (it != g_ws.end()) it->second.fresh = false;
 }
 
 // A row-major bf16 matrix [rows][cols] (cols a multiple of 64) viewed as 3D
@@ -418,8 +461,14 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     a.ycnt = reinterpret_cast<uint32_t*>(ws + L.ycnt);
     a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
     a.uwords = a.hdr->union_words;
-    // the early start serves OEA routing of batches of up to 16 tokens
-    a.epoch = P.B <= 16 && P.mode == MOE_MODE_OEA ? current_epoch(workspace) : 0u;
+    const WsState wst = ws_state(workspace);
+    // the early start serves OEA routing of batches of up to 16 tokens, right
+    // after the routing call (counters fresh)
+    a.epoch = P.B <= 16 && P.mode == MOE_MODE_OEA && wst.fresh ? wst.epoch : 0u;
+    const int cset = counter_set(wst.routes > 0 ? wst.routes - 1 : 0u);
+    a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone) + (size_t)cset * kHdoneSet;
+    a.next_tile = &a.hdr->next_tile[cset];
+    a.gathered = &a.hdr->gathered[cset];
     a.w_gate = w_gate;
     a.w_up = w_up;
     a.w_down = w_down;
@@ -443,6 +492,12 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
         return MOE_OK;
     }
     if (P.B == 0) return MOE_OK;   // nothing to compute or write
+    if (!wst.fresh) {
+        // another expert call used this counter set since the routing call
+        // (or no routing call is recorded): zero it here
+        if ((e = clear_counters(ws, L, cset, s)) != cudaSuccess)
+            return cuda_fail(e, "clearing the expert kernel's counters");
+    }
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     int sms = num_sms();
@@ -473,6 +528,7 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
         a.kbl = large_batch_blocks(P.d, d_ff);
         e = launch_ffn_tc(a, maps, sms, s);
         if (e != cudaSuccess) return cuda_fail(e, "expert kernel launch");
+        experts_launched(workspace);
         return MOE_OK;
     }
 
@@ -559,13 +615,22 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
     a.rbd = (P.d + 127) / 128;
     WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.header);
     a.flags = &hdr->flags;
+    const WsState wst = ws_state(workspace);
+    if (!wst.known) {   // the counter sets' state is not recorded: zero both
+        if ((e = clear_counters(ws, L, -1, s)) != cudaSuccess)
+            return cuda_fail(e, "clearing the expert kernel's counters");
+    }
+    const int clr = 1 - counter_set(wst.routes);   // the set the previous expert call used
+    a.clr_next = &hdr->next_tile[clr];
+    a.clr_gathered = &hdr->gathered[clr];
+    a.clr_hdone = reinterpret_cast<uint32_t*>(ws + L.hdone) + (size_t)clr * kHdoneSet;
     if (P.B <= 32 && P.mode == MOE_MODE_OEA) {   // one routing CTA: it publishes S_base after phase 1
         a.uwords = hdr->union_words;
-        a.epoch = next_epoch(workspace);
+        a.epoch = next_epoch();
     }
     e = fused ? launch_route_fused(ra, a, s) : launch_route(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
-    if (a.epoch) commit_epoch(workspace, a.epoch);   // an expert call on this workspace now waits for it
+    routed(workspace, a.epoch);   // an expert call on this workspace now waits for it
     return MOE_OK;
 }
 

@@ -22,17 +22,27 @@ constexpr uint32_t kFlagBadIndex = MOE_FLAG_BAD_INDEX;
 // ---------------------------------------------------------------------------
 struct WsHeader {
     uint32_t flags;        // MOE_FLAG_* raised by kernels
-    uint32_t ctas_done;    // expert kernel: CTAs finished (the last one resets the counters)
-    uint32_t next_tile;    // expert kernel: tiles claimed beyond each CTA's first
     uint32_t unused0;
-    uint32_t gathered;     // expert kernel: CTAs that copied their rows of the grouped hidden states
-    uint32_t pad[59];
+    // Two sets of the expert kernel's counters.  Routing call r on a
+    // workspace zeroes set (r + 1) % 2, which the expert call of routing
+    // r - 1 used, and the expert call of routing r uses set r % 2, which
+    // routing r - 1 zeroed (the host zeroes a set itself before an expert
+    // call that repeats one on the same routing).  So the expert kernel ends
+    // without a grid-wide reset, and the routing kernel's zeroing is not
+    // ordered against anything it publishes.
+    uint32_t next_tile[2]; // expert kernel: tiles claimed beyond each CTA's first
+    uint32_t gathered[2];  // expert kernel: CTAs that copied their rows of the grouped hidden states
+    uint32_t pad[58];
     // routing kernel (OEA, batches of up to 32): S_base, word j (experts
     // 32j ... 32j + 31, one bit each) in the low half and the epoch of the
     // routing call in the high half, each stored at once with release
     uint64_t union_words[32];
 };
 static_assert(sizeof(WsHeader) == 512, "the header is two 256-byte blocks");
+
+// Per-chunk counters of one set (hdone): at most N + B * kslots / 16 + 1
+// token chunks of the largest launch.
+constexpr int kHdoneSet = MOE_MAX_EXPERTS + MOE_MAX_TOKENS * MOE_MAX_SLOTS / 16 + 1;
 
 struct WsLayout {
     size_t header, hdone, exinfo, pos_of, nused, ycnt, logits, hbuf, ybuf, xperm, total;
@@ -48,7 +58,7 @@ inline WsLayout ws_layout(int B, int N, int d, int kslots, int F, int h_elt) {
     WsLayout L;
     size_t o = 0;
     L.header = o; o += align256(sizeof(WsHeader));
-    L.hdone = o;  o += align256(sizeof(uint32_t) * (N + (size_t)B * kslots / 16 + 1));   // per token chunk
+    L.hdone = o;  o += align256(sizeof(uint32_t) * 2 * (size_t)kHdoneSet);   // two sets, per token chunk
     L.exinfo = o; o += align256(sizeof(uint32_t) * 2 * N);   // per active expert: info, token mask
     L.pos_of = o; o += align256(sizeof(int32_t) * (size_t)B * kslots + 4);
     L.nused = o;  o += align256(sizeof(int32_t) * (size_t)B + 4);                  // kept slots per token
@@ -96,6 +106,11 @@ struct RouteArgs {
     // the activated experts' weights before the routing ends.
     uint64_t* uwords;       // [32] epoch << 32 | word, or null: not published
     uint32_t epoch;         // nonzero, distinct per routing call on this workspace
+    // the expert kernel's counter set this call zeroes (see WsHeader): the
+    // header's next_tile[s] and gathered[s], and hdone [kHdoneSet] of set s
+    uint32_t* clr_next;
+    uint32_t* clr_gathered;
+    uint32_t* clr_hdone;
 };
 
 struct FfnArgs {
@@ -113,7 +128,9 @@ struct FfnArgs {
     float* ybuf;            // [pairs][d]
     void* xperm;            // [pairs][d] hidden states grouped by expert
     void* out;              // [B][d]
-    uint32_t* hdone;        // [token chunks] phase-A tiles of the chunk whose h rows are written
+    uint32_t* hdone;        // [token chunks] phase-A tiles of the chunk whose h rows are written (this launch's set)
+    uint32_t* next_tile;    // this launch's set of the header counters
+    uint32_t* gathered;
     const int32_t* nused;   // [B] kept slots of each token (routing kernel)
     uint32_t* ycnt;         // [B][ceil(d / 128)] y slices still missing; the last writer combines
     WsHeader* hdr;
@@ -385,6 +402,13 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(raddr) : "memory");
     return v;
+}
+
+// Stores v at the address of `local` in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void st_dsmem_f32(float* local, uint32_t rank, float v) {
+    uint32_t raddr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
 }
 
 // Global memory ordering -------------------------------------------------------

@@ -138,7 +138,6 @@ struct Smem {
     int nmax;                            // tokens per chunk for this launch (multiple of 16)
     int tn;                              // activated experts (T)
     int abort_flag;
-    int last_flag;
     long long wait_cycles;               // bound of every wait (FfnArgs::wait_cycles)
 };
 
@@ -603,7 +602,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         }
         if (gt == 0) {
             __threadfence();
-            atomicAdd(&A.hdr->gathered, 1u);
+            atomicAdd(A.gathered, 1u);
         }
     }
 
@@ -652,7 +651,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 S.tq[q] = tile;
                 mbar_arrive(&S.tq_full[q]);
                 if (tile < 0) break;
-                next0 = (int)G + (int)atomicAdd(&A.hdr->next_tile, 1u);
+                next0 = (int)G + (int)atomicAdd(A.next_tile, 1u);
                 const bool ph_a = tile < TA;
                 const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;   // chunked experts are re-read from L2
@@ -738,7 +737,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
             if (ph_a && !gathered) {   // every CTA has copied its rows of the grouped hidden states
                 if (lane == 0) {
-                    wait_counter(&A.hdr->gathered, G, S, flags);
+                    wait_counter(A.gathered, G, S, flags);
                     fence_proxy_async_global();
                 }
                 __syncwarp();
@@ -1077,7 +1076,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         }
     }
 
-    // ---- release the tensor memory; the last CTA resets the counters ----
+    // ---- release the tensor memory ----
     // After a wait gave up, stages may have been issued that no MMA waited
     // for: give their TMA copies (a few, each landing within microseconds)
     // a bounded 20 us to land before the CTA's shared memory is released.
@@ -1087,24 +1086,16 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     }
     tmem_fence_before_sync();
     __syncthreads();
+    // This CTA is done with every counter and buffer of the workspace: the
+    // next kernel in the stream may be scheduled (it still waits for this
+    // grid's completion before it reads anything).  The counters are zeroed
+    // by the next routing kernel, so no grid-wide reset (and no fence under
+    // a memory system still saturated by other CTAs' streams) ends the
+    // kernel.
+    grid_launch_dependents();
     if (warp == kWarpM) {
         tmem_fence_after_sync();
         tmem_dealloc(tmem, tmem_cols);
-    }
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const uint32_t old = atomicAdd(&A.hdr->ctas_done, 1u);
-        S.last_flag = (old + 1 == G);
-    }
-    __syncthreads();
-    if (S.last_flag) {
-        __threadfence();
-        for (int k = threadIdx.x; k < X.chunk_off[Tn]; k += kThreads) A.hdone[k] = 0;
-    }
-    if (S.last_flag && threadIdx.x == 0) {
-        A.hdr->next_tile = 0;
-        A.hdr->gathered = 0;
-        A.hdr->ctas_done = 0;
     }
 }
 

@@ -143,7 +143,7 @@ __device__ __forceinline__ void finish_token(const RouteArgs& a, RouteSmem& sm, 
 // as soon as phase 1 is done: phase 2 only adds tokens to experts inside it,
 // and every expert in it keeps the token whose baseline put it there.  The
 // expert kernel, launched early, starts on those experts' weights from it
-// while phase 2 and the grouping run.  Warp 0 of a one-CTA launch.
+// while phase 2 and the grouping run.  The last warp of a one-CTA launch.
 __device__ __forceinline__ void publish_union(const RouteArgs& a, uint32_t word, int lane) {
     st_release_gpu_u64(&a.uwords[lane], ((uint64_t)a.epoch << 32) | (lane < (a.N + 31) / 32 ? word : 0u));
 }
@@ -176,6 +176,18 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
     for (int q = threadIdx.x; q < N; q += nthreads) sm.bits[q] = 0;
     grid_launch_dependents();    // the expert kernel may start its prologue
     grid_dependency_wait();      // scores come from the router kernel
+    if (rank == 0 && a.clr_hdone && warp < nwarps - 1) {
+        // Zero the counter set that the expert call after the previous
+        // routing call used (it has completed: dependency wait above); the
+        // expert call after the next routing call uses it.  The last warp,
+        // which publishes S_base with release stores, takes no part, so its
+        // stores wait for none of these.
+        for (int q = threadIdx.x; q < kHdoneSet; q += nthreads - 32) a.clr_hdone[q] = 0u;
+        if (threadIdx.x == 0) {
+            *a.clr_next = 0u;
+            *a.clr_gathered = 0u;
+        }
+    }
     __syncthreads();
 
     bool nonfinite = false;
@@ -194,7 +206,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
         if (i >= a.B_valid) {           // padding token: selects nothing
             if (lane == 0) {
                 sm.snb[il] = 0;
-                if (a.n_base) a.n_base[i] = 0;
+                if (a.n_base && !oea) a.n_base[i] = 0;   // OEA: after S_base is published
             }
             if (!oea) finish_token(a, sm, i, il, lane, 0, -1, 0.f);
             continue;
@@ -246,10 +258,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
             const uint32_t word = __ballot_sync(kFull, (taken >> j) & 1u);
             if (lane == 0 && word) atomicOr(&sm.sbase[j], word);
         }
-        if (lane == 0) {
-            sm.snb[il] = n;
-            if (a.n_base) a.n_base[i] = n;
-        }
+        if (lane == 0) sm.snb[il] = n;   // n_base is written after S_base is published
         taken1 = taken; n1 = n; myid1 = myid; myval1 = myval;
     }
 
@@ -270,7 +279,11 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
             sb = sm.sball;
         }
         __syncthreads();
-        if (ncta == 1 && a.uwords && warp == 0) publish_union(a, sb[lane], lane);   // S_base
+        // S_base, from the last warp: it has no global store pending that its
+        // release stores would have to wait for
+        if (ncta == 1 && a.uwords && warp == nwarps - 1) publish_union(a, sb[lane], lane);
+        if (a.n_base)
+            for (int i = tb + (int)threadIdx.x; i < te; i += nthreads) a.n_base[i] = sm.snb[i - tb];
         uint32_t notin = 0;
 #pragma unroll
         for (int j = 0; j < NPL; ++j)
@@ -430,10 +443,13 @@ __global__ void route_kernel(RouteArgs a) {
 // the whole hidden dimension: its 32 warps take the 64-column blocks w,
 // w + 32, ... with warp-level bf16 MMAs (the operand loads and the K-index
 // permutation of the separate router kernel), then sum their partial tiles
-// in warp order.  CTA 0 gathers every CTA's tile through distributed shared
-// memory and runs the routing above on the scores in its own shared memory,
-// so the scores never make a round trip through global memory between two
+// in warp order.  Each CTA stores its scores straight into CTA 0's score
+// array (distributed shared memory; one cluster barrier completes it), and
+// CTA 0 runs the routing above on the scores in its own shared memory, so
+// the scores never make a round trip through global memory between two
 // kernels (they are still written there, as the routing's logits output).
+// Each warp loads its first block of router weights before the dependency
+// wait: the weights do not come from the preceding kernel.
 constexpr int kFusedWarps = 32;
 
 // Opt-in dynamic shared memory per block of the current device.
@@ -457,11 +473,11 @@ __host__ __device__ constexpr size_t route_smem_bytes(int N, int kslots) {
     return 4 * 32 * 4 + 3 * (size_t)N * 4 + 32 * (size_t)kslots * 4;
 }
 
-// Shared memory of the fused kernel: the routing's, the gathered scores
-// [32][N], the warps' partial tiles [32][512] and the CTA's tile [32][16].
+// Shared memory of the fused kernel: the routing's, the scores [32][N]
+// (complete in CTA 0) and the warps' partial tiles [32][512].
 __host__ __device__ constexpr size_t fused_smem_bytes(int N, int kslots) {
     return ((route_smem_bytes(N, kslots) + 15) & ~size_t(15)) + 32 * (size_t)N * 4 +
-           (size_t)kFusedWarps * 512 * 4 + 512 * 4;
+           (size_t)kFusedWarps * 512 * 4;
 }
 
 template <int NPL>
@@ -470,9 +486,6 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_fused_kernel(Router
     const size_t rsm = (route_smem_bytes(a.N, a.kslots) + 15) & ~size_t(15);
     float* lg = reinterpret_cast<float*>(smem_raw + rsm);             // [32][N] scores (CTA 0)
     float* red = lg + 32 * a.N;                                        // [32 warps][512] partial tiles
-    float* lt = red + kFusedWarps * 512;                               // [32 tokens][16 experts] this CTA's tile
-    grid_launch_dependents();    // the expert kernel may start its prologue
-    grid_dependency_wait();      // hidden states come from the preceding kernel
     const uint32_t rank = cluster_ctarank();   // the whole grid is one cluster
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
@@ -481,18 +494,30 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_fused_kernel(Router
     const int kbtot = r.d / 64;
     const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(r.x);
     const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(r.w);
+    const int r0 = e0 + g, r1 = e0 + g + 8;
+    // The router weights do not come from the preceding kernel: the warp's
+    // first K block is loaded before the dependency wait.
+    auto load_w = [&](int kb, uint4& wa0, uint4& wa1, uint4& wb0, uint4& wb1) {
+        const int col = kb * 64 + 16 * t;
+        wa0 = make_uint4(0, 0, 0, 0), wa1 = wa0, wb0 = wa0, wb1 = wa0;
+        if (kb >= kbtot) return;
+        if (r0 < r.N) { wa0 = ldg16(w + (size_t)r0 * r.d + col); wa1 = ldg16(w + (size_t)r0 * r.d + col + 8); }
+        if (r1 < r.N) { wb0 = ldg16(w + (size_t)r1 * r.d + col); wb1 = ldg16(w + (size_t)r1 * r.d + col + 8); }
+    };
+    uint4 pa0, pa1, pb0, pb1;
+    load_w(warp, pa0, pa1, pb0, pb1);
+    grid_launch_dependents();    // the expert kernel may start its prologue
+    grid_dependency_wait();      // hidden states come from the preceding kernel
 
     float acc[4][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[j][q] = 0.f;
-    const int r0 = e0 + g, r1 = e0 + g + 8;
     for (int kb = warp; kb < kbtot; kb += kFusedWarps) {
         const int col = kb * 64 + 16 * t;
-        uint4 wa0 = make_uint4(0, 0, 0, 0), wa1 = wa0, wb0 = wa0, wb1 = wa0;
-        if (r0 < r.N) { wa0 = ldg16(w + (size_t)r0 * r.d + col); wa1 = ldg16(w + (size_t)r0 * r.d + col + 8); }
-        if (r1 < r.N) { wb0 = ldg16(w + (size_t)r1 * r.d + col); wb1 = ldg16(w + (size_t)r1 * r.d + col + 8); }
+        uint4 wa0 = pa0, wa1 = pa1, wb0 = pb0, wb1 = pb1;
+        if (kb != warp) load_w(kb, wa0, wa1, wb0, wb1);
         const uint32_t A0[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
         const uint32_t A1[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
 #pragma unroll
@@ -507,7 +532,9 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_fused_kernel(Router
                 mma_bf16_16816(acc[j], A0[2 * s], A1[2 * s], A0[2 * s + 1], A1[2 * s + 1], X[2 * s], X[2 * s + 1]);
         }
     }
-    // the warps' partial tiles (fragment-linear), summed in warp order
+    // the warps' partial tiles (fragment-linear), summed in warp order; each
+    // score goes straight into CTA 0's score array (distributed shared
+    // memory), so one cluster barrier completes the [B][N] scores there
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -524,20 +551,12 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_fused_kernel(Router
         if (tok < r.B && e < r.N) {
             if (r.bias) sum += r.bias[e];
             r.logits[(size_t)tok * r.N + e] = sum;
+            float* dst = &lg[tok * r.N + e];
+            if (rank == 0) *dst = sum; else st_dsmem_f32(dst, 0u, sum);
         }
-        lt[tok * 16 + row] = sum;
     }
     const bool clustered = gridDim.x > 1;   // one CTA (N <= 16) is launched without a cluster
-    if (clustered) cluster_sync(); else __syncthreads();   // every CTA's tile is complete
-    if (rank == 0) {
-        for (int q = threadIdx.x; q < r.B * r.N; q += blockDim.x) {
-            const int tok = q / r.N, e = q - tok * r.N;
-            const uint32_t src = (uint32_t)(e >> 4);
-            const float* p = &lt[tok * 16 + (e & 15)];
-            lg[q] = src == 0 ? *p : ld_dsmem_f32(p, src);
-        }
-    }
-    if (clustered) cluster_sync(); else __syncthreads();   // CTA 0 has read every tile: the others may leave
+    if (clustered) cluster_sync(); else __syncthreads();   // CTA 0 holds every score
     if (rank != 0) return;
     RouteArgs ra = a;
     ra.logits = lg;
