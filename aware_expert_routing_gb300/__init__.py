@@ -27,7 +27,9 @@ MAX_TOKENS, MAX_EXPERTS, MAX_SLOTS = 256, 1024, 32
 
 EXPORTED = ["moe_num_slots", "moe_layer_launches", "moe_workspace_bytes", "moe_route", "moe_expert_ffn",
             "moe_expert_ffn_mixed", "moe_pack_int4", "moe_decode_layer", "moe_decode_layer_mixed", "moe_decode_layer_static",
-            "moe_device_status", "moe_device_status_static", "moe_set_wait_timeout_us", "moe_synth_normal", "moe_status_string", "moe_last_error"]
+            "moe_device_status", "moe_device_status_static", "moe_set_wait_timeout_us",
+            "moe_residency_create", "moe_residency_observe", "moe_residency_flush", "moe_residency_query",
+            "moe_residency_destroy", "moe_residency_select", "moe_synth_normal", "moe_status_string", "moe_last_error"]
 STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -47,6 +49,14 @@ class _Params(ctypes.Structure):
 class _Mixed(ctypes.Structure):
     _fields_ = [("slot", ctypes.c_void_p), ("q_gate", ctypes.c_void_p), ("q_up", ctypes.c_void_p),
                 ("q_down", ctypes.c_void_p), ("n_hot", ctypes.c_int32), ("n_cold", ctypes.c_int32)]
+
+
+class _ResidencyConfig(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int32), ("n_hot", ctypes.c_int32), ("d", ctypes.c_int32), ("d_ff", ctypes.c_int32),
+                ("alpha", ctypes.c_double), ("margin", ctypes.c_double), ("update_every", ctypes.c_int32),
+                ("max_inflight", ctypes.c_int32)] + \
+               [(n, ctypes.c_void_p) for n in ("slot", "counts_acc", "snapshot", "hot_gate", "hot_up", "hot_down",
+                                              "host_gate", "host_up", "host_down")]
 
 
 class _Routing(ctypes.Structure):
@@ -97,6 +107,18 @@ def load(path: str | None = None):
     lib.moe_device_status_static.restype = ctypes.c_int
     lib.moe_pack_int4.argtypes = [V, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, V, V]
     lib.moe_pack_int4.restype = ctypes.c_int
+    lib.moe_residency_create.argtypes = [P(_ResidencyConfig), V, P(V), V]
+    lib.moe_residency_create.restype = ctypes.c_int
+    lib.moe_residency_observe.argtypes = [V, V, V]
+    lib.moe_residency_observe.restype = ctypes.c_int
+    lib.moe_residency_flush.argtypes = [V, V]
+    lib.moe_residency_flush.restype = ctypes.c_int
+    lib.moe_residency_query.argtypes = [V, V, V, V]
+    lib.moe_residency_query.restype = ctypes.c_int
+    lib.moe_residency_destroy.argtypes = [V]
+    lib.moe_residency_destroy.restype = ctypes.c_int
+    lib.moe_residency_select.argtypes = [V, ctypes.c_int32, ctypes.c_double, V, V, V]
+    lib.moe_residency_select.restype = ctypes.c_int32
     lib.moe_set_wait_timeout_us.argtypes = [ctypes.c_uint32]
     lib.moe_set_wait_timeout_us.restype = ctypes.c_int
     lib.moe_synth_normal.argtypes = [V, ctypes.c_int32, ctypes.c_uint64, ctypes.c_uint64,
@@ -282,6 +304,90 @@ def moe_pack_int4(w: torch.Tensor, rb: int, out: torch.Tensor | None = None, str
         raise ValueError(f"out must be a contiguous CUDA uint8 tensor of at least {n} bytes")
     _check(load().moe_pack_int4(_ptr(w), rows, cols, rb, _ptr(out), _stream(stream)), "moe_pack_int4")
     return out
+
+
+MOE_RESIDENT_LO, MOE_RESIDENT_HI, MOE_PROMOTING = 0, 1, 2
+
+
+def moe_residency_select(S, in_hot, margin: float):
+    """The library's selection step on the host: returns (in_hot after the
+    swaps, promoted, demoted)."""
+    import numpy as np
+    S = np.ascontiguousarray(S, dtype=np.float64)
+    h = np.ascontiguousarray(in_hot, dtype=np.uint8).copy()
+    pro = np.empty(S.size, np.int32)
+    dem = np.empty(S.size, np.int32)
+    n = load().moe_residency_select(S.ctypes.data, S.size, margin, h.ctypes.data, pro.ctypes.data, dem.ctypes.data)
+    if n < 0:
+        raise MoeError(MOE_ERR_ARG, "moe_residency_select", "bad arguments")
+    return h.astype(bool), [int(x) for x in pro[:n]], [int(x) for x in dem[:n]]
+
+
+class Residency:
+    """moe_residency: which experts keep their bf16 version, changed while
+    the layer runs (see include/moe.h).  The caller's buffers: the bf16 pool
+    (hot_gate/hot_up/hot_down, n_hot slots, filled with the initial experts
+    in order), INT4 images of all N experts, and pinned host bf16 weights of
+    all experts (the promotion sources).  The handle table, the count
+    accumulator and the pinned snapshot are allocated here with torch."""
+
+    def __init__(self, N: int, d: int, d_ff: int, initial_hot, hot: dict, q: dict, host: dict, alpha: float = 0.9,
+                 margin: float = 0.0, update_every: int = 1, max_inflight: int = 4, stream=None):
+        import numpy as np
+        dev = hot["w_gate"].device
+        for t in list(hot.values()):
+            _need(t, torch.bfloat16, "bf16 pool")
+        for t in host.values():
+            if t.is_cuda or not t.is_pinned() or t.dtype != torch.bfloat16 or not t.is_contiguous():
+                raise ValueError("host weights must be contiguous pinned bf16 CPU tensors")
+        self.N, self.n_hot = N, len(initial_hot)
+        self.slot = torch.empty(N, dtype=torch.int32, device=dev)
+        self.acc = torch.zeros(N, dtype=torch.int32, device=dev)
+        self.snapshot = torch.zeros(N, dtype=torch.int32).pin_memory()
+        self.hot, self.q, self.host = hot, q, host
+        self._cfg = _ResidencyConfig(N, self.n_hot, d, d_ff, alpha, margin, update_every, max_inflight,
+                                     self.slot.data_ptr(), self.acc.data_ptr(), self.snapshot.data_ptr(),
+                                     hot["w_gate"].data_ptr(), hot["w_up"].data_ptr(), hot["w_down"].data_ptr(),
+                                     host["w_gate"].data_ptr(), host["w_up"].data_ptr(), host["w_down"].data_ptr())
+        init = np.ascontiguousarray(initial_hot, dtype=np.int32)
+        self._init = init
+        h = ctypes.c_void_p()
+        _check(load().moe_residency_create(ctypes.byref(self._cfg), init.ctypes.data, ctypes.byref(h),
+                                           _stream(stream)), "moe_residency_create")
+        self._h = h
+
+    def mixed(self) -> "MixedExperts":
+        """The expert descriptor for the mixed layer calls."""
+        return MixedExperts(self.slot, self.q["w_gate"], self.q["w_up"], self.q["w_down"], self.n_hot, self.N)
+
+    def observe(self, counts: torch.Tensor, stream=None):
+        _need(counts, torch.int32, "counts")
+        _check(load().moe_residency_observe(self._h, _ptr(counts), _stream(stream)), "moe_residency_observe")
+
+    def flush(self, stream=None):
+        _check(load().moe_residency_flush(self._h, _stream(stream)), "moe_residency_flush")
+
+    def query(self):
+        """(state [N], scores [N], stats dict)."""
+        import numpy as np
+        st = np.empty(self.N, np.int32)
+        sc = np.empty(self.N, np.float64)
+        stats = np.empty(5, np.uint64)
+        _check(load().moe_residency_query(self._h, st.ctypes.data, sc.ctypes.data, stats.ctypes.data),
+               "moe_residency_query")
+        keys = ("calls", "updates", "promotions", "demotions", "pending")
+        return st, sc, {k: int(v) for k, v in zip(keys, stats)}
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().moe_residency_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def ema_hot_set(counts, n_hot: int, alpha: float = 0.9) -> "np.ndarray":

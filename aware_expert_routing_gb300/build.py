@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libaware_moe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "router.cu", "route.cu", "ffn_tc.cu", "ffn_f32.cu", "synth.cu", "pack.cu", "static_scratch.cu"]
+SOURCES = ["api.cu", "router.cu", "route.cu", "ffn_tc.cu", "ffn_f32.cu", "synth.cu", "pack.cu", "residency.cu",
+           "static_scratch.cu"]
 
 
 def nvcc() -> str:

@@ -291,6 +291,101 @@ moe_status moe_decode_layer_mixed(const void *hidden, const void *w_router, cons
                                   const moe_route_params *params, const moe_routing *routing, void *out,
                                   void *workspace, size_t workspace_bytes, moe_stream_t stream);
 
+/*
+ * Expert residency at run time (DynaExq page, sections 2.2-2.5 and 3.2-3.5):
+ * which experts of one layer keep their bf16 version, decided from the
+ * routing as the layer runs, and changed without stopping it.
+ *   - Handles: `slot` is the table moe_expert_ffn_mixed / moe_decode_layer_mixed
+ *     read (pass it as moe_mixed_experts.slot with n_hot = n_hot, n_cold = N
+ *     and INT4 images of all N experts, image i = expert i).  The kernels
+ *     resolve every activated expert through it at every call.
+ *   - Pools: the caller's bf16 pool of n_hot slots (fixed budget) and INT4
+ *     images of all experts, which stay resident as the version every handle
+ *     can fall back to.
+ *   - Hotness (section 2.5): moe_residency_observe adds a call's per-expert
+ *     counts (moe_routing.counts) on the device; every update_every calls the
+ *     interval's counts c are copied to `snapshot` (pinned host memory) and
+ *     cleared, without waiting; when they have arrived,
+ *     S_e <- alpha S_e + (1 - alpha) c_e (S starts at 0).
+ *   - Selection with hysteresis (section 3.5): while the best expert outside
+ *     the bf16 set (highest S, ties to the lower id) scores more than
+ *     `margin` above the weakest member (lowest S, ties to the higher id),
+ *     the two swap places (moe_residency_select).  A selection runs only
+ *     when no transition is pending.
+ *   - Transitions (sections 2.4, 3.4): a demotion redirects the handle to
+ *     the INT4 image on the caller's stream, then the freed slot receives
+ *     the promoted expert's bf16 weights: an asynchronous copy from the
+ *     caller's pinned host memory on the residency's own migration stream,
+ *     which waits for the redirect.  The handle is pointed at the new slot
+ *     only after that copy's completion event has been seen (by a later
+ *     observe or flush), so no kernel reads a partly copied version; until
+ *     then the expert runs in INT4.  At most max_inflight copies are in
+ *     flight; further swaps wait in a queue.
+ * The library allocates no device memory for this: the accumulator and the
+ * snapshot are the caller's.  Not thread-safe; calls on one residency must
+ * use one stream.
+ * Reading of the page: the update interval is counted in routing calls
+ * (the page uses a time interval); the INT4 images of all experts stay on
+ * the device, so a demotion moves no data.
+ */
+typedef struct {
+    int32_t N;             /* experts, 2..MOE_MAX_EXPERTS                          */
+    int32_t n_hot;         /* bf16 slots (the budget), 1..N-1                      */
+    int32_t d, d_ff;       /* multiples of 128                                     */
+    double alpha;          /* weight of the old score, 0 <= alpha < 1              */
+    double margin;         /* hysteresis margin, in selections per interval, >= 0 */
+    int32_t update_every;  /* routing calls per update interval, >= 1             */
+    int32_t max_inflight;  /* promotion copies in flight at once, >= 1            */
+    int32_t *slot;         /* [N] device: the handle table                         */
+    uint32_t *counts_acc;  /* [N] device: counts of the current interval           */
+    uint32_t *snapshot;    /* [N] pinned host: counts of the last interval         */
+    void *hot_gate;        /* device bf16 pool: [n_hot][d_ff][d]                   */
+    void *hot_up;          /*                   [n_hot][d_ff][d]                   */
+    void *hot_down;        /*                   [n_hot][d][d_ff]                   */
+    const void *host_gate; /* pinned host bf16 weights of all experts: [N][d_ff][d] */
+    const void *host_up;   /*                                          [N][d_ff][d] */
+    const void *host_down; /*                                          [N][d][d_ff] */
+} moe_residency_config;
+
+typedef struct moe_residency moe_residency;
+
+/* Residency states reported by moe_residency_query. */
+#define MOE_RESIDENT_LO 0
+#define MOE_RESIDENT_HI 1
+#define MOE_PROMOTING 2
+
+/*
+ * Creates a residency whose bf16 set starts as initial_hot[n_hot] (expert
+ * initial_hot[k] in slot k; the caller has filled the pool accordingly).
+ * Writes the handle table and clears the accumulator on `stream` and waits
+ * for them.
+ */
+moe_status moe_residency_create(const moe_residency_config *cfg, const int32_t *initial_hot,
+                                moe_residency **out, moe_stream_t stream);
+
+/* After a routing call on `stream`: adds its counts[N] (device), publishes
+ * completed promotions, updates the scores when a snapshot has arrived,
+ * selects and issues transitions.  Never waits for the GPU. */
+moe_status moe_residency_observe(moe_residency *r, const int32_t *counts, moe_stream_t stream);
+
+/* Waits for every queued and in-flight transition and publishes it. */
+moe_status moe_residency_flush(moe_residency *r, moe_stream_t stream);
+
+/* Host copies of the per-expert state (MOE_RESIDENT_*, nullable [N]), the
+ * scores S (nullable [N]) and, in stats[5] (nullable): routing calls seen,
+ * score updates, promotions, demotions, transitions queued or in flight. */
+moe_status moe_residency_query(const moe_residency *r, int32_t *state, double *scores, uint64_t *stats);
+
+moe_status moe_residency_destroy(moe_residency *r);
+
+/*
+ * The selection step alone, on the host: in_hot[N] (0/1) is updated in
+ * place and the swaps are written to promote / demote (nullable, [N]) in
+ * the order they are made.  Returns their number, or -1 for bad arguments.
+ */
+int32_t moe_residency_select(const double *S, int32_t N, double margin, uint8_t *in_hot, int32_t *promote,
+                             int32_t *demote);
+
 /* moe_route followed by moe_expert_ffn on the same stream. */
 moe_status moe_decode_layer(const void *hidden, const void *w_router, const float *router_bias,
                             const void *w_gate, const void *w_up, const void *w_down,

@@ -57,6 +57,10 @@ def _load():
             lib.oracle_moe_experts.restype = None
             lib.oracle_dequant_int4.argtypes = [P, i, i, i, P]
             lib.oracle_dequant_int4.restype = None
+            lib.oracle_ema_update.argtypes = [P, P, i, ctypes.c_double]
+            lib.oracle_ema_update.restype = None
+            lib.oracle_hot_select.argtypes = [P, i, ctypes.c_double, P, P, P]
+            lib.oracle_hot_select.restype = i
             _lib = lib
     return _lib
 
@@ -169,3 +173,25 @@ def moe_layer(x, w_router, w_gate, w_up, w_down, bias, mode, k, k0=None, p=1.0,
     r["logits"] = lg
     r["out"] = moe_experts(x, w_gate, w_up, w_down, r["idx"], r["w"])
     return r
+
+
+def ema_update(S, counts, alpha: float) -> np.ndarray:
+    """One hotness update S <- alpha S + (1 - alpha) c (DynaExq page,
+    section 2.5); returns the new scores."""
+    S = np.array(S, dtype=np.float64)
+    c = np.ascontiguousarray(counts, dtype=np.float64)
+    _load().oracle_ema_update(_ptr(S), _ptr(c), S.size, alpha)
+    return S
+
+
+def hot_select(S, in_hot, margin: float):
+    """The high-precision set after one selection with hysteresis (DynaExq
+    page, sections 2.5 and 3.5): returns (new in_hot [N] bool, promoted,
+    demoted), the swaps in the order they are made."""
+    S = np.ascontiguousarray(S, dtype=np.float64)
+    h = np.ascontiguousarray(in_hot, dtype=np.uint8).copy()
+    N = S.size
+    pro = np.empty(N, np.int32)
+    dem = np.empty(N, np.int32)
+    n = _load().oracle_hot_select(_ptr(S), N, margin, _ptr(h), _ptr(pro), _ptr(dem))
+    return h.astype(bool), [int(x) for x in pro[:n]], [int(x) for x in dem[:n]]

@@ -345,3 +345,48 @@ void oracle_dequant_int4(const uint8_t *packed, int rows, int cols, int rb, floa
             out[(size_t)r * cols + c] = (float)q * sc;
         }
 }
+
+/*
+ * Hotness and the high-precision set (DynaExq page, section 2.5 / 3.5):
+ *   - EMA hotness per expert over update intervals:
+ *       S_e <- alpha * S_e + (1 - alpha) * c_e,
+ *     c_e = the times the router selected expert e in the interval;
+ *   - the high-precision set has a fixed size (the layer's budget);
+ *   - hysteresis: an expert outside the set is promoted only if its score
+ *     exceeds the score of the lowest-ranked expert inside the set by the
+ *     margin, and an expert inside is demoted only if its score is below
+ *     that of the highest-ranked expert outside by the same margin.
+ * With a fixed set size, every promotion pairs with a demotion: the best
+ * outsider (highest score, ties to the lower id) replaces the weakest
+ * insider (lowest score, ties to the higher id) while the outsider's score
+ * exceeds the insider's by more than the margin.
+ */
+void oracle_ema_update(double *S, const double *c, int N, double alpha)
+{
+    for (int e = 0; e < N; ++e)
+        S[e] = alpha * S[e] + (1.0 - alpha) * c[e];
+}
+
+/* in_hot[N] (0/1) is updated in place; promote[] / demote[] receive the
+ * swaps in the order they are made; returns their number. */
+int oracle_hot_select(const double *S, int N, double margin, unsigned char *in_hot,
+                      int *promote, int *demote)
+{
+    int n = 0;
+    for (;;) {
+        int o = -1, i = -1;
+        for (int e = 0; e < N; ++e) {
+            if (!in_hot[e] && (o < 0 || S[e] > S[o]))
+                o = e;                        /* first maximum: the lower id */
+            if (in_hot[e] && (i < 0 || S[e] <= S[i]))
+                i = e;                        /* last minimum: the higher id */
+        }
+        if (o < 0 || i < 0 || !(S[o] > S[i] + margin))
+            return n;
+        in_hot[o] = 1;
+        in_hot[i] = 0;
+        promote[n] = o;
+        demote[n] = i;
+        ++n;
+    }
+}

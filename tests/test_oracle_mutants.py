@@ -10,6 +10,7 @@ import pytest
 
 import test_oracle_ffn as FFN
 import test_oracle_routing as R
+import test_residency as RES
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -39,6 +40,9 @@ MUTANTS = {
     "int4_chunk_order_swapped": ("((size_t)rbi * nkb + kb) * chunk", "((size_t)kb * (rows / rb) + rbi) * chunk"),
     "given_baseline_sizes_ignored": ("nbase[i] = nbase_in[i];", "nbase[i] = k0;"),
     "policy_keeps_oea_for_one_token": ("if (B_valid <= 1) {", "if (B_valid < 1) {"),
+    "hysteresis_margin_ignored": ("!(S[o] > S[i] + margin)", "!(S[o] > S[i])"),
+    "ema_weights_swapped": ("S[e] = alpha * S[e] + (1.0 - alpha) * c[e];", "S[e] = (1.0 - alpha) * S[e] + alpha * c[e];"),
+    "selection_ties_to_higher_outsider": ("(o < 0 || S[e] > S[o])", "(o < 0 || S[e] >= S[o])"),
     "policy_smaller_k0_at_small_batches": ("if (B_valid < 16)\n        return (5 * k + 7) / 8;",
                                            "if (B_valid < 16)\n        return (3 * k + 7) / 8;"),
 }
@@ -59,6 +63,9 @@ def pins():
         out.append(lambda d=d, F=F: FFN.test_expert_matches_library_fp64(d, F))
     out.append(lambda: R.test_union_size_monte_carlo(16, R.OEA, 3))
     out += [lambda s=s: R.test_given_baseline_sizes_follow_the_definitions(s, 2, 12, 4) for s in range(3)]
+    out += [RES.test_ema_closed_form, RES.test_margin_zero_gives_the_top_n, RES.test_worked_example_and_hysteresis,
+            RES.test_every_member_set_on_tiny_cases]
+    out += [lambda s=s, m=m: RES.test_selection_matches_pairing(s, m) for s in range(6) for m in (0.0, 2.0)]
     return out
 
 
@@ -81,6 +88,7 @@ def test_pins_catch_planted_mistake(name, tmp_path, monkeypatch):
     mod = load_mutant(tmp_path, name, *MUTANTS[name])
     monkeypatch.setattr(R, "oracle", mod)
     monkeypatch.setattr(FFN, "oracle", mod)
+    monkeypatch.setattr(RES, "oracle", mod)
     caught = 0
     for pin in pins():
         try:
