@@ -333,9 +333,10 @@ moe_status tc_expert_maps(const void* g, const void* u, const void* dn, int N, i
 }
 
 // Workspace maps of the tcgen05 kernel: expert-grouped hidden states and h
-// (16-row boxes), and the hidden states themselves (16-row boxes: the whole
-// batch of up to 16 tokens; rows past B read as zeros); then the hidden
-// states and h with boxes kb blocks wide (batches of up to 16 tokens).
+// (16-row boxes), and the hidden states themselves (one box holds the whole
+// batch of up to 64 tokens, rounded up to 16 rows; rows past B read as
+// zeros); then the hidden states with boxes as wide as the launch's stages
+// and h with boxes kb blocks wide (batches of up to 16 tokens).
 struct TcOpEntry {
     const void* ws;
     const void* hidden;
@@ -366,8 +367,12 @@ moe_status tc_operand_maps(unsigned char* ws, const WsLayout& L, const void* hid
     e.F = F;
     e.dev = dev;
     const uint32_t kb = (uint32_t)small_batch_blocks(d, F);
+    // the whole batch of up to 64 tokens as one box (rows past B read as
+    // zeros), as wide as the launch's stages
+    const uint32_t nwb = B <= 64 ? (uint32_t)(B <= 16 ? 16 : (B + 15) & ~15) : 16u;
+    const uint32_t kbw = B <= 16 ? kb : (uint32_t)large_batch_blocks(d, F);
     if (!encode_3d(&e.maps[0], ws + L.xperm, d, pairs, 16, 1) || !encode_3d(&e.maps[1], ws + L.hbuf, F, pairs, 16, 1) ||
-        !encode_3d(&e.maps[2], hidden, d, B, 16, 1) || !encode_3d(&e.maps[3], hidden, d, B, 16, kb) ||
+        !encode_3d(&e.maps[2], hidden, d, B, nwb, 1) || !encode_3d(&e.maps[3], hidden, d, B, nwb, kbw) ||
         !encode_3d(&e.maps[4], ws + L.hbuf, F, pairs, 16, kb))
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (operands)");
     e.used = true;
@@ -462,9 +467,9 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     a.hdr = reinterpret_cast<WsHeader*>(ws + L.header);
     a.uwords = a.hdr->union_words;
     const WsState wst = ws_state(workspace);
-    // the early start serves OEA routing of batches of up to 16 tokens, right
+    // the early start serves OEA routing of batches of up to 64 tokens, right
     // after the routing call (counters fresh)
-    a.epoch = P.B <= 16 && P.mode == MOE_MODE_OEA && wst.fresh ? wst.epoch : 0u;
+    a.epoch = P.B <= 64 && P.mode == MOE_MODE_OEA && wst.fresh ? wst.epoch : 0u;
     const int cset = counter_set(wst.routes > 0 ? wst.routes - 1 : 0u);
     a.hdone = reinterpret_cast<uint32_t*>(ws + L.hdone) + (size_t)cset * kHdoneSet;
     a.next_tile = &a.hdr->next_tile[cset];
@@ -624,7 +629,7 @@ moe_status moe_route(const void* hidden, const void* w_router, const float* rout
     a.clr_next = &hdr->next_tile[clr];
     a.clr_gathered = &hdr->gathered[clr];
     a.clr_hdone = reinterpret_cast<uint32_t*>(ws + L.hdone) + (size_t)clr * kHdoneSet;
-    if (P.B <= 32 && P.mode == MOE_MODE_OEA) {   // one routing CTA: it publishes S_base after phase 1
+    if (P.B <= 64 && P.mode == MOE_MODE_OEA) {   // it publishes S_base after phase 1 (and the cluster's union)
         a.uwords = hdr->union_words;
         a.epoch = next_epoch();
     }

@@ -59,7 +59,7 @@ inline WsLayout ws_layout(int B, int N, int d, int kslots, int F, int h_elt) {
     size_t o = 0;
     L.header = o; o += align256(sizeof(WsHeader));
     L.hdone = o;  o += align256(sizeof(uint32_t) * 2 * (size_t)kHdoneSet);   // two sets, per token chunk
-    L.exinfo = o; o += align256(sizeof(uint32_t) * 2 * N);   // per active expert: info, token mask
+    L.exinfo = o; o += align256(sizeof(uint32_t) * 3 * N);   // per active expert: info, token mask (2 words)
     L.pos_of = o; o += align256(sizeof(int32_t) * (size_t)B * kslots + 4);
     L.nused = o;  o += align256(sizeof(int32_t) * (size_t)B + 4);                  // kept slots per token
     L.ycnt = o;   o += align256(sizeof(uint32_t) * (size_t)B * ((d + 127) / 128) + 4);   // per (token, 128 rows of d)
@@ -96,12 +96,12 @@ struct RouteArgs {
     int32_t* perm;          // [B*kslots]
     int32_t* pos_of;        // [B*kslots]
     int32_t* n_base;        // [B] or null
-    uint32_t* exinfo;       // [2][N]: active expert a -> id | cnt << 10 | first pair << 19; tokens (B <= 32)
+    uint32_t* exinfo;       // [3][N]: active expert a -> id | cnt << 10 | first pair << 19; tokens 0-31, 32-63 (B <= 64)
     int32_t* nused;         // [B] kept slots of each token
     uint32_t* ycnt;         // [B][rbd] set to nused: the expert kernel counts each row block's y slices down
     int rbd;                // row blocks of 128 in d
     uint32_t* flags;
-    // OEA, batches of up to 32 tokens: S_base (one bit per expert), published
+    // OEA, batches of up to 64 tokens: S_base (one bit per expert), published
     // with `epoch` once phase 1 is done, so the expert kernel can start on
     // the activated experts' weights before the routing ends.
     uint64_t* uwords;       // [32] epoch << 32 | word, or null: not published
@@ -121,7 +121,7 @@ struct FfnArgs {
     const int32_t* offsets;
     const int32_t* perm;
     const int32_t* pos_of;
-    const uint32_t* exinfo; // [2][N] written by the routing kernel
+    const uint32_t* exinfo; // [3][N] written by the routing kernel
     const int32_t* idx;     // [B][kslots] routing experts
     const float* w;         // [B][kslots] routing weights
     void* hbuf;             // [pairs][F]
@@ -148,7 +148,7 @@ struct FfnArgs {
     int kbs;                // tcgen05 kernel: 64-column blocks per stage for batches of up to 16 tokens
     int kbl;                // tcgen05 kernel: 64-column blocks per stage for larger batches
     int smem_bytes;         // tcgen05 kernel: dynamic shared memory of the launch (set by the launcher)
-    // OEA, batches of up to 16 tokens: the routing kernel's early S_base
+    // OEA, batches of up to 64 tokens: the routing kernel's early S_base
     // (RouteArgs::uwords) and the epoch of the routing call that this launch
     // follows; epoch 0: wait for the whole routing instead.
     const uint64_t* uwords;
@@ -171,10 +171,11 @@ bool route_fused_supported(int dtype, int B, int N, int kslots);
 cudaError_t launch_route_fused(const RouterArgs& r, const RouteArgs& a, cudaStream_t s);
 // tcgen05 expert kernel (bf16 weights).  maps[0..6]: W_gate/W_up
 // interleaved 8 rows at a time (5D, gu_fused) or W_gate and W_up alone
-// (8-row boxes), W_down (128-row boxes), gathered hidden states, h and the
-// hidden states (16-row boxes), all one 64-column block wide; maps[7..10]:
-// the 5D gate/up map, W_down, the hidden states and h with boxes kbs blocks
-// wide (batches of up to 16 tokens); maps[11..12]: the 5D gate/up map and
+// (8-row boxes), W_down (128-row boxes), gathered hidden states and h
+// (16-row boxes) and the hidden states (the whole batch of up to 64 tokens
+// in one box), all one 64-column block wide; maps[7..10]: the 5D gate/up
+// map, W_down, the hidden states (as wide as the launch's stages) and h
+// with boxes kbs blocks wide (batches of up to 16 tokens); maps[11..12]: the 5D gate/up map and
 // W_down with boxes kbl blocks wide (larger batches).
 cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s);
 cudaError_t launch_ffn_f32(const FfnArgs& a, cudaStream_t s);

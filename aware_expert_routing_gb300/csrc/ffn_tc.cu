@@ -15,10 +15,15 @@
 //     d_ff indices, interleaved 8 rows at a time (rows 16g..16g+7 = gate
 //     rows 8g..8g+7, rows 16g+8..16g+15 = the up rows), form the 128-row A
 //     operand of a tcgen05 MMA with M = 128; the chunk's token rows are the
-//     N operand (N = the chunk's tokens rounded up to 16; a chunk holds the
-//     whole batch of up to 16 tokens, else up to nmax = the largest expert's
-//     token count rounded up to 16, at most 128, so most experts' weights
-//     are streamed once); K = d.  Phase-B tile (expert a, 128 rows of d,
+//     N operand; K = d.  Batches of up to 64 tokens: one chunk per expert
+//     whose phase-A operand is the whole batch (N = the batch rounded up to
+//     16; the tensor pipe is nearly idle at decode, so multiplying tokens
+//     that the expert does not serve costs nothing, and the epilogue keeps
+//     the expert's own by a 64-bit token mask).  Larger batches: chunks of
+//     up to nmax = the largest expert's token count rounded up to 16, at
+//     most 128, rows of an expert-grouped copy of the hidden states (N = the
+//     chunk's tokens rounded up to 16), so most experts' weights are
+//     streamed once.  Phase-B tile (expert a, 128 rows of d,
 //     chunk c): W_down rows times the chunk's h rows, K = d_ff.  The list
 //     holds every phase-A tile, then every phase-B tile, each in active-
 //     expert order; CTA b starts with tile b and claims each next tile (one
@@ -31,13 +36,13 @@
 //     grows with the bytes of each operation, so batches of up to 16 tokens
 //     use KB = 4 (64 KB per operation) where d and d_ff allow it, larger
 //     batches KB = 2 where both are even.  Warp 5 streams the token rows of
-//     each stage (16-row boxes): the whole batch of up to 16 tokens
-//     straight from the hidden states, or rows of the expert-grouped copy
-//     of the hidden states, or (phase B) rows of h once every phase-A tile
+//     each stage: the whole batch of up to 64 tokens straight from the
+//     hidden states (one box), or rows of the expert-grouped copy of the
+//     hidden states (16-row boxes), or (phase B) rows of h once every phase-A tile
 //     of the chunk has written them (a per-chunk counter).  The stage ring takes the shared memory
 //     that the barriers and per-expert tables leave (3 stages of 72 KB at
 //     KB = 4; 3 to 6 stages at KB = 2, by the chunk width).  For batches of
-//     up to 16 tokens warp 4 also loads the first tile's first stages (token
+//     up to 64 tokens warp 4 also loads the first tile's first stages (token
 //     rows, then weights) as soon as the activated experts are known: with
 //     OEA routing, from the S_base that the routing kernel publishes after
 //     phase 1 (the early start: the weights stream while phase 2 and the
@@ -45,8 +50,9 @@
 //     once the routing kernel has completed), else after it ends.
 //   * Warp 6, lane 0, issues the MMAs: four K=16 steps per stage straight
 //     from the swizzled shared memory (no register staging), fp32
-//     accumulators in tensor memory, four accumulator buffers (16 columns
-//     each for batches of up to 16 tokens, else 128).
+//     accumulators in tensor memory, four accumulator buffers (the batch
+//     rounded up to 16 columns each for batches of up to 64 tokens, else
+//     128).
 //     tcgen05.commit frees each stage when its MMAs have completed and marks
 //     a tile's accumulator full.
 //   * INT4 experts (DynaExq page, section 3.2): warp 4 bulk-copies the
@@ -105,8 +111,8 @@ static_assert(kRawPair == kQ4B, "one raw unit fits either phase");
 constexpr int kRawReserve = 2 * kRawPair;   // packed INT4 bytes kept after the stage ring
 constexpr int kQ = 16;                   // tile queue entries
 constexpr int kAcc = 4;                  // accumulator buffers
-constexpr uint32_t kTmemCols = kAcc * kNMax;   // fp32 columns (batches over 16 tokens)
-constexpr uint32_t kTmemColsSmall = kAcc * 16;  // batches of up to 16 tokens
+constexpr uint32_t kTmemCols = kAcc * kNMax;   // fp32 columns (batches over kWholeMax tokens)
+constexpr int kWholeMax = 64;            // batches up to this size use the whole batch as the phase-A operand
 constexpr uint32_t kBarGather = 2;       // named barrier of the warps that copy grouped rows
 constexpr int kGatherThreads = (kEpiWarps + kConvWarps + 1) * 32;   // warps 0-3 and 7-15
 constexpr int kGatherRows = 64;          // grouped rows per pass
@@ -143,14 +149,14 @@ struct Smem {
 
 // Per-expert tables in shared memory, after Smem, sized by N at launch.
 struct Tabs {
+    uint64_t* tokmask;    // [N] active index -> tokens routed to it (batches of up to kWholeMax)
     int* chunk_off;       // [N + 1] first token chunk of each active expert
     uint32_t* ex_info;    // [N] active index -> id | cnt << 10 | first pair << 19
     int* ex_slot;         // [N] active index -> bf16 expert (>= 0) or -1 - INT4 expert
-    uint16_t* tokmask;    // [N] active index -> tokens routed to it (batches of <= 16)
 };
 
 __host__ __device__ constexpr size_t tabs_bytes(int N) {
-    return (((size_t)(N + 1) * 4 + (size_t)N * 4 + (size_t)N * 4 + (size_t)N * 2) + 15) & ~size_t(15);
+    return (((size_t)N * 8 + (size_t)(N + 1) * 4 + (size_t)N * 4 + (size_t)N * 4) + 15) & ~size_t(15);
 }
 
 // Stage ring bytes left in `total` bytes of dynamic shared memory (whole KB).
@@ -236,7 +242,7 @@ __device__ __forceinline__ void wait_zero(const uint32_t* p, Smem& S, uint32_t* 
     }
 }
 
-// Early start (batches of up to 16): waits (bounded) until the routing call
+// Early start (whole batches): waits (bounded) until the routing call
 // that this launch follows has published its activated experts, then
 // returns word `lane` of that union (bit b: expert 32 * lane + b).  Each
 // lane polls its own word, which carries the epoch in its high half; the
@@ -323,10 +329,10 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     unsigned char* raw = ring + ring_bytes;
     Smem& S = *reinterpret_cast<Smem*>(raw + (has_q4 ? kRawReserve : 0));
     Tabs X;
-    X.chunk_off = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(&S) + ((sizeof(Smem) + 15) & ~size_t(15)));
+    X.tokmask = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(&S) + ((sizeof(Smem) + 15) & ~size_t(15)));
+    X.chunk_off = reinterpret_cast<int*>(X.tokmask + A.N);
     X.ex_info = reinterpret_cast<uint32_t*>(X.chunk_off + A.N + 1);
     X.ex_slot = reinterpret_cast<int*>(X.ex_info + A.N);
-    X.tokmask = reinterpret_cast<uint16_t*>(X.ex_slot + A.N);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int d = A.d, F = A.F;
@@ -336,7 +342,13 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // weights, since the TMA unit's rate per SM grows with the size of each
     // operation: A.kbs (up to 4) for batches of up to 16 tokens, A.kbl (up to
     // 2) for larger batches, whose token rows share the ring.
-    const bool small_b = A.B <= 16;                 // phase-A operand: the whole batch
+    const bool small_b = A.B <= 16;                 // 4-block stages where d and d_ff allow them
+    // Batches of up to kWholeMax tokens: the phase-A operand is the whole
+    // batch (nwb rows, the batch rounded up to 16; the tensor pipe is nearly
+    // idle at decode, so multiplying every token costs nothing), each expert
+    // is one token chunk, and h is stored for the expert's own tokens only.
+    const bool whole = A.B <= kWholeMax;
+    const int nwb = max(16, (A.B + 15) & ~15);
     const int KB = A.gu_fused ? (small_b ? A.kbs : A.kbl) : 1;
     const CUtensorMap* const m_gu = KB == 1 ? &tm_gu : small_b ? &tm_gu4 : &tm_gu2;       // weight maps, KB wide
     const CUtensorMap* const m_down = KB == 1 ? &tm_down : small_b ? &tm_down4 : &tm_down2;
@@ -374,12 +386,12 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         S.wait_cycles = A.wait_cycles;
         for (int i = 0; i < 32; ++i) S.uw[i] = 0u;   // read as "no expert" if a wait gives up first
     }
-    // accumulator buffers: kAcc x nmax columns, nmax = 16 for batches of up to 16
-    const uint32_t tmem_cols = small_b ? kTmemColsSmall : kTmemCols;
-    const int acc_stride = small_b ? 16 : kNMax;
+    // accumulator buffers: kAcc x nwb columns for whole batches, else kAcc x kNMax
+    const int acc_stride = whole ? nwb : kNMax;
+    const uint32_t tmem_cols = whole ? (kAcc * nwb <= 64 ? 64u : kAcc * nwb <= 128 ? 128u : 256u) : kTmemCols;
     if (warp == kWarpM) tmem_alloc(&S.tmem_base, tmem_cols);
     __syncthreads();             // barriers initialised (this overlaps the routing kernel)
-    // Early start (OEA routing of batches of up to 16 tokens, whose routing
+    // Early start (OEA routing of whole batches, whose routing
     // call publishes S_base after phase 1): the activated experts are fixed
     // before the routing kernel ends, and they are all that phase A needs (its operand
     // is the whole batch; the token masks and first pairs are read only by
@@ -389,7 +401,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // first pairs and token masks once the routing kernel has completed.
     // Every warp that reads the routing's other outputs waits for its
     // completion first.
-    const bool early = small_b && A.epoch != 0u;
+    const bool early = whole && A.epoch != 0u;
     int Tn = 0;
     if (!early) {
         grid_dependency_wait();      // routing comes from the preceding kernel
@@ -399,12 +411,12 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             Tn = 0;
         }
     }
-    // Batches of up to 16 tokens: the CTA's first tile is phase-A tile
-    // blockIdx.x of a one-chunk-per-expert list, so the weight warp starts
-    // its stages now (each stage's token rows first, then its weights), while
-    // warp 0 builds the per-expert records.
+    // Whole batches: the CTA's first tile is phase-A tile blockIdx.x of a
+    // one-chunk-per-expert list, so the weight warp starts its stages now
+    // (each stage's token rows first, then its weights), while warp 0 builds
+    // the per-expert records.
     int fast_stages = 0;
-    if (warp == kWarpW && small_b) {
+    if (warp == kWarpW && whole) {
         const int rbA0 = F / 64, t0 = (int)blockIdx.x;
         int e = -1;   // expert of phase-A tile t0 (active index t0 / rbA0), if there is one
         if (early) {
@@ -440,12 +452,12 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             if (sl >= 0 && sl < A.n_hot) {
                 const uint64_t pol = l2_evict_first_policy();
                 const int row0 = sl * F + 64 * (t0 % rbA0);
-                const int sb = KB * (kWBytes + 16 * 128);   // the slot size of this launch (nmax = 16)
+                const int sb = KB * (kWBytes + nwb * 128);   // the slot size of this launch (nmax = nwb)
                 fast_stages = min(d / 64 / KB, min(kMaxStages, ring_bytes / sb));
                 const uint64_t pol_x = l2_evict_last_policy();
                 for (int s = 0; s < fast_stages; ++s) {
                     unsigned char* dst = ring + (size_t)s * sb;
-                    mbar_arrive_expect_tx(&S.full[s], KB * 2048);   // rows past B read as zeros
+                    mbar_arrive_expect_tx(&S.full[s], KB * nwb * 128);   // rows past B read as zeros
                     tma_load_3d(dst + KB * kWBytes, KB > 1 ? &tm_hid4 : &tm_hid, 0, 0, s * KB, &S.full[s], pol_x);
                     mbar_arrive_expect_tx(&S.full[s], KB * kWBytes);
                     if (A.gu_fused) {
@@ -483,13 +495,13 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 sl = A.n_hot > 0 ? 0 : -1;
             }
             X.ex_info[a] = (uint32_t)e;   // the count and first pair follow with the routing's completion
-            X.tokmask[a] = 0;
+            X.tokmask[a] = 0ull;
             X.ex_slot[a] = sl;
             X.chunk_off[a] = a;
         }
         if (lane == 0) {
             X.chunk_off[tot] = tot;
-            S.nmax = 16;
+            S.nmax = nwb;
             S.tn = tot;
         }
     } else if (warp == 0) {   // per-expert records, chunk width and chunk offsets of the active experts
@@ -498,7 +510,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         for (int a = lane; a < Tn; a += 32) {
             const uint32_t info = A.exinfo[a];   // written by the routing kernel
             X.ex_info[a] = info;
-            X.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
+            X.tokmask[a] = (uint64_t)A.exinfo[A.N + a] | ((uint64_t)A.exinfo[2 * A.N + a] << 32);
             maxcnt = max(maxcnt, (int)((info >> 10) & 511u));
             const int e = info & 1023u;
             int sl = A.slot ? A.slot[e] : e;
@@ -509,9 +521,9 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             X.ex_slot[a] = sl;
         }
         maxcnt = __reduce_max_sync(0xffffffffu, maxcnt);
-        // a chunk holds up to nmax tokens: the whole batch for batches of up to
-        // 16, else the largest expert's tokens rounded up to 16, at most 128
-        const int nmax = small_b ? 16 : min(kNMax, max(16, (maxcnt + 15) & ~15));
+        // a chunk holds up to nmax tokens: the whole batch for whole batches,
+        // else the largest expert's tokens rounded up to 16, at most 128
+        const int nmax = whole ? nwb : min(kNMax, max(16, (maxcnt + 15) & ~15));
         if (lane == 0) S.nmax = nmax;
         __syncwarp();
         int run = 0;
@@ -536,9 +548,9 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         prefetch_tensormap(m_down);
     }
     if (warp == kWarpO && lane == 0) {
-        if (small_b) {
+        if (whole) {
             prefetch_tensormap(KB > 1 ? &tm_hid4 : &tm_hid);
-            prefetch_tensormap(KB > 1 ? &tm_h4 : &tm_h);
+            prefetch_tensormap(small_b && KB > 1 ? &tm_h4 : &tm_h);
         } else {
             prefetch_tensormap(&tm_x);
             prefetch_tensormap(&tm_h);
@@ -558,18 +570,18 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const uint32_t info = A.exinfo[a];
             if ((info & 1023u) != X.ex_info[a]) raise_flag(flags, kFlagBadIndex);
             X.ex_info[a] = info;
-            X.tokmask[a] = (uint16_t)A.exinfo[A.N + a];
+            X.tokmask[a] = (uint64_t)A.exinfo[A.N + a] | ((uint64_t)A.exinfo[2 * A.N + a] << 32);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.meta_full);
     }
 
-    // Batches over 16 tokens: the expert-grouped copy of the hidden states.
+    // Batches over kWholeMax tokens: the expert-grouped copy of the hidden states.
     // Warps 0-3 and 7-15 copy this CTA's rows b, b+G, ... (their tokens
     // first, so that every 16-byte load depends on shared memory only), then
     // one thread counts the CTA in; the operand warp starts phase A once all
     // CTAs have.
-    if (!small_b && (warp < kEpiWarps || warp >= kWarpC)) {
+    if (!whole && (warp < kEpiWarps || warp >= kWarpC)) {
         const int gt = warp < kEpiWarps ? (int)threadIdx.x : (int)threadIdx.x - (kWarpC - kEpiWarps) * 32;
         const int P = A.offsets[A.N];
         const int vpr = d / 8;   // 16-byte vectors per row
@@ -721,7 +733,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         RingPos rp;
         const int fast_ops = S.fast_ops;   // stages of the first tile already loaded by warp 4
         for (int s = 0; s < fast_ops; ++s) rp.next(nst);
-        bool gathered = small_b;
+        bool gathered = whole;
         bool meta = !early;   // the tables hold the counts and first pairs
         for (int n = 0;; ++n) {
             const int q = n % kQ;
@@ -748,14 +760,16 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     wait_counter(&A.hdone[X.chunk_off[T.a] + T.c], (uint32_t)rbA, S, flags);
                     fence_proxy_async_global();
                 }
-                // Batches of up to 16 tokens: one 16-row box of KB blocks, which
-                // lands as KB consecutive [16 rows][64] operand blocks.  Larger
-                // batches: one 16-row box per 16 tokens and block, block kb at
-                // kb x nmax rows.
-                const CUtensorMap* map = ph_a ? (small_b ? (KB > 1 ? &tm_hid4 : &tm_hid) : &tm_x)
+                // Phase A of whole batches: one box of nwb rows and KB blocks,
+                // which lands as KB consecutive [nwb rows][64] operand blocks.
+                // Phase B of batches of up to 16 tokens: one 16-row box of KB
+                // blocks.  Otherwise: one 16-row box per 16 tokens and block,
+                // block kb at kb x nmax rows.
+                const bool wide = ph_a && whole;
+                const CUtensorMap* map = ph_a ? (whole ? (KB > 1 ? &tm_hid4 : &tm_hid) : &tm_x)
                                               : (small_b && KB > 1 ? &tm_h4 : &tm_h);
-                const int row = (ph_a && small_b) ? 0 : T.off + nmax * T.c;
-                const int nb = (ph_a && small_b) ? 1 : (T.ntok + 15) >> 4;   // 16-row boxes = MMA N / 16
+                const int row = wide ? 0 : T.off + nmax * T.c;
+                const int nb = wide ? nwb >> 4 : (T.ntok + 15) >> 4;   // 16-row boxes = MMA N / 16
                 const int ns = ph_a ? SA : SB;
                 for (int s = n == 0 ? fast_ops : 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
@@ -763,7 +777,9 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     if (aborted(S)) break;
                     mbar_arrive_expect_tx(&S.full[slot], nb * 2048 * KB);   // rows past the end read as zeros
                     unsigned char* dst = ring + (size_t)slot * slot_bytes + KB * kWBytes;
-                    if (small_b) {
+                    if (wide) {
+                        tma_load_3d(dst, map, 0, 0, s * KB, &S.full[slot], pol);
+                    } else if (small_b) {
                         for (int j = 0; j < nb; ++j)
                             tma_load_3d(dst + j * 2048, map, 0, row + 16 * j, s * KB, &S.full[slot], pol);
                     } else {
@@ -781,6 +797,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         if (lane == 0) {
             RingPos rp;
             uint32_t cpar = 0;   // per ring slot: parity of its next cfull phase (INT4 stages)
+            bool meta = !early;  // the tables hold the counts
             for (int n = 0;; ++n) {
                 const int q = n % kQ;
                 wait_bar(&S.tq_full[q], (n / kQ) & 1, S, flags);
@@ -788,11 +805,21 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 const int tile = S.tq[q];
                 if (tile < 0) break;
                 const bool ph_a = tile < TA;
-                int ntile = 16;   // MMA N: batches of up to 16 always use 16 columns
+                // MMA N: every token (phase A of whole batches; phase B of
+                // batches of up to 16, whose chunks hold at most 16), else the
+                // chunk's tokens rounded up to 16, read once the routing has
+                // completed (before that an early table holds no counts)
+                const bool by_count = !small_b && !(whole && ph_a);
+                if (by_count && !meta) {
+                    wait_bar(&S.meta_full, 0, S, flags);
+                    if (aborted(S)) break;
+                    meta = true;
+                }
+                int ntile = nwb;
                 bool q4 = false;  // INT4 expert: the converter warps write the A operand
-                if (!small_b || A.n_cold > 0) {
+                if (by_count || A.n_cold > 0) {
                     const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
-                    if (!small_b) ntile = (T.ntok + 15) & ~15;
+                    if (by_count) ntile = max(16, (T.ntok + 15) & ~15);
                     q4 = X.ex_slot[T.a] < 0;
                 }
                 const uint32_t idesc = umma_idesc_bf16(kM, ntile);
@@ -944,7 +971,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const bool ph_a = tile < TA;
             const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
             const int b = n % kAcc;
-            const int ngroups = (ph_a && small_b) ? 1 : (T.ntok + 15) >> 4;   // 16-column groups of D
+            const int ngroups = (ph_a && whole) ? nwb >> 4 : (T.ntok + 15) >> 4;   // 16-column groups of D
             wait_bar(&S.acc_full[b], (n / kAcc) & 1, S, flags);
             if (aborted(S)) break;
             tmem_fence_after_sync();
@@ -954,7 +981,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 // the partner row is 8 lanes away in the same warp.
                 const int m = (i >> 3) & 1;
                 const int frow = 64 * T.rb + 8 * (i >> 4) + (i & 7);
-                const uint32_t tmask = small_b ? X.tokmask[T.a] : 0u;
+                const uint64_t tmask = whole ? X.tokmask[T.a] : 0ull;
                 const bool swap = A.gu_swap && X.ex_slot[T.a] >= 0;   // INT4 stages hold the gate rows first
                 for (int cg = 0; cg < ngroups; ++cg) {
                     float v[16];
@@ -970,11 +997,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                         const float other = __shfl_down_sync(0xffffffffu, v[jj], 8);
                         const float gs = swap ? other : v[jj];
                         const float us = swap ? v[jj] : other;
-                        // column j: batch token j (small batches) or the chunk's j-th pair
-                        const bool keep = small_b ? ((tmask >> j) & 1u) != 0 : j < T.ntok;
+                        // column j: batch token j (whole batches) or the chunk's j-th pair
+                        const bool keep = whole ? ((tmask >> j) & 1ull) != 0 : j < T.ntok;
                         if (m == 0 && keep) {
-                            const size_t pos = small_b ? (size_t)T.off + __popc(tmask & ((1u << j) - 1u))
-                                                       : (size_t)T.off + nmax * T.c + j;
+                            const size_t pos = whole ? (size_t)T.off + __popcll(tmask & ((1ull << j) - 1ull))
+                                                     : (size_t)T.off + nmax * T.c + j;
                             hb[pos * F + frow] = __float2bfloat16_rn(silu_f(gs) * us);
                         }
                     }
@@ -1127,7 +1154,8 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
     a.smem_bytes = smem_optin[dev];
     // the ring must hold two stages of the largest slot this launch can use
     const int kb = a.gu_fused ? (a.B <= 16 ? a.kbs : a.kbl) : 1;
-    const size_t slot = (size_t)kb * (kWBytes + (a.B <= 16 ? 16 : kNMax) * 128);
+    const int nwb = a.B <= 16 ? 16 : (a.B + 15) & ~15;
+    const size_t slot = (size_t)kb * (kWBytes + (a.B <= kWholeMax ? nwb : kNMax) * 128);
     if ((size_t)a.smem_bytes < 4096 + tabs_bytes(a.N) + (size_t)kRawReserve ||
         ring_bytes_for((size_t)a.smem_bytes, a.N, a.n_cold > 0) < 2 * slot)
         return cudaErrorInvalidConfiguration;

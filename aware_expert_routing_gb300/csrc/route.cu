@@ -29,10 +29,11 @@
 // earlier CTAs, which give each pair's position directly (tokens ascending
 // within an expert).  CTA 0 writes the per-expert arrays.
 //
-// With OEA and one CTA (up to 32 tokens), S_base is published to the
-// workspace as soon as phase 1 is done, each word with the routing call's
-// epoch: the expert kernel, already resident, starts on the activated
-// experts' weights while phase 2 and the grouping run.
+// With OEA and up to 64 tokens (one or two CTAs), S_base is published to
+// the workspace as soon as phase 1 (and the cluster's union) is done, each
+// word with the routing call's epoch: the expert kernel, already resident,
+// starts on the activated experts' weights while phase 2 and the grouping
+// run.
 //
 // For bf16 batches of up to 32 tokens with N <= 128, route_fused_kernel
 // also computes the router scores (page section 2 Q1/Q2: every token scores
@@ -279,9 +280,9 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
             sb = sm.sball;
         }
         __syncthreads();
-        // S_base, from the last warp: it has no global store pending that its
-        // release stores would have to wait for
-        if (ncta == 1 && a.uwords && warp == nwarps - 1) publish_union(a, sb[lane], lane);
+        // S_base (over the cluster), from CTA 0's last warp: it has no global
+        // store pending that its release stores would have to wait for
+        if (rank == 0 && a.uwords && warp == nwarps - 1) publish_union(a, sb[lane], lane);
         if (a.n_base)
             for (int i = tb + (int)threadIdx.x; i < te; i += nthreads) a.n_base[i] = sm.snb[i - tb];
         uint32_t notin = 0;
@@ -344,11 +345,13 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
     const int nblk = (N + 31) >> 5;
     int cnt_r[kBlkPerWarp];
     uint32_t inc_r[kBlkPerWarp];
+    uint32_t m0_r[kBlkPerWarp], m1_r[kBlkPerWarp];   // tokens 0-31 and 32-63 of expert e (batches of up to 64)
 #pragma unroll
     for (int u = 0; u < kBlkPerWarp; ++u) {
         const int b = warp + u * nwarps;
         cnt_r[u] = 0;
         inc_r[u] = 0;
+        m0_r[u] = m1_r[u] = 0u;
         if (b < nblk) {
             const int e = (b << 5) + lane;
             int c = 0;
@@ -362,6 +365,8 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
                     if (r == (int)rank) sm.pre[e] = c;
                     c += __popc(w[r]);
                 }
+                m0_r[u] = w[0];
+                m1_r[u] = kMaxCtas > 1 ? w[1] : 0u;
             }
             uint32_t v = (uint32_t)c | ((uint32_t)(c > 0) << 26);
 #pragma unroll
@@ -398,7 +403,9 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
                     if (act) {
                         a.active[ex2] = e;
                         a.exinfo[ex2] = (uint32_t)e | ((uint32_t)c << 10) | ((uint32_t)ex1 << 19);
-                        a.exinfo[N + ex2] = B <= 32 ? sm.bits[e] : 0u;   // one CTA: its words are all tokens'
+                        // the expert's tokens (batches of up to 64: the first two CTAs' words)
+                        a.exinfo[N + ex2] = B <= 64 ? m0_r[u] : 0u;
+                        a.exinfo[2 * N + ex2] = B <= 64 ? m1_r[u] : 0u;
                     }
                 }
             }
@@ -414,6 +421,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
                 a.active[q] = -1;
                 a.exinfo[q] = 0;
                 a.exinfo[N + q] = 0;
+                a.exinfo[2 * N + q] = 0;
             }
         }
     }

@@ -190,7 +190,7 @@ moe_status moe_route(const void *hidden, const void *w_router, const float *rout
  * workspace, so no other call may use that workspace in between.  A
  * completed call leaves them as it found them, so it may be repeated on the
  * same routing.  Reads only activated experts, each expert's three
- * matrices once from HBM.  With OEA routing of up to 16 tokens, the call
+ * matrices once from HBM.  With OEA routing of up to 64 tokens, the call
  * starts on the activated experts' weights as soon as the preceding
  * moe_route() on this workspace and stream has fixed them (its phase 1),
  * before that routing call's kernel ends; it recognises that call's
@@ -281,7 +281,7 @@ moe_status moe_pack_int4(const void *w, int32_t rows, int32_t cols, int32_t rb, 
  * expert's version by rewriting its slot (and image) between calls.
  * Arguments, layouts and results as moe_route and moe_expert_ffn_mixed;
  * every argument, the descriptor included, is checked before anything is
- * launched.  With OEA routing of up to 16 tokens the expert kernel starts
+ * launched.  With OEA routing of up to 64 tokens the expert kernel starts
  * on the activated experts before the routing kernel ends, as for
  * moe_expert_ffn.
  */
