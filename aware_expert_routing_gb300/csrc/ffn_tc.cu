@@ -249,7 +249,7 @@ __device__ __forceinline__ void wait_zero(const uint32_t* p, Smem& S, uint32_t* 
 // whole warp calls this.
 __device__ __forceinline__ uint32_t early_union_word(const FfnArgs& A, int lane, Smem& S, uint32_t* flags) {
     const long long t0 = clock64();
-    uint64_t v = ld_acquire_gpu_u64(&A.uwords[lane]);
+    uint64_t v = ld_relaxed_gpu_u64(&A.uwords[lane]);
     while (!__all_sync(0xffffffffu, (uint32_t)(v >> 32) == A.epoch)) {
         if (__any_sync(0xffffffffu, *(volatile int*)&S.abort_flag != 0)) return 0u;
         if (__any_sync(0xffffffffu, clock64() - t0 > S.wait_cycles)) {
@@ -257,7 +257,7 @@ __device__ __forceinline__ uint32_t early_union_word(const FfnArgs& A, int lane,
             return 0u;
         }
         __nanosleep(64);
-        v = ld_acquire_gpu_u64(&A.uwords[lane]);
+        v = ld_relaxed_gpu_u64(&A.uwords[lane]);
     }
     return (uint32_t)v;
 }
@@ -353,6 +353,23 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     const CUtensorMap* const m_gu = KB == 1 ? &tm_gu : small_b ? &tm_gu4 : &tm_gu2;       // weight maps, KB wide
     const CUtensorMap* const m_down = KB == 1 ? &tm_down : small_b ? &tm_down4 : &tm_down2;
 
+    // The tensor maps' descriptors, fetched while the barriers are set up:
+    // the first copies (which the early start issues the moment the
+    // activated experts are known) then find them cached.
+    if (warp == kWarpW && lane == 0) {
+        prefetch_tensormap(A.gu_fused ? m_gu : &tm_gate);
+        if (!A.gu_fused) prefetch_tensormap(&tm_up);
+        prefetch_tensormap(m_down);
+    }
+    if (warp == kWarpO && lane == 0) {
+        if (whole) {
+            prefetch_tensormap(KB > 1 ? &tm_hid4 : &tm_hid);
+            prefetch_tensormap(small_b && KB > 1 ? &tm_h4 : &tm_h);
+        } else {
+            prefetch_tensormap(&tm_x);
+            prefetch_tensormap(&tm_h);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&S.full[i], 2);          // weight producer + operand producer
@@ -540,20 +557,6 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             }
             if (a < Tn) X.chunk_off[a + 1] = run + inc;
             run += __shfl_sync(0xffffffffu, inc, 31);
-        }
-    }
-    if (warp == kWarpW && lane == 0) {
-        prefetch_tensormap(A.gu_fused ? m_gu : &tm_gate);
-        if (!A.gu_fused) prefetch_tensormap(&tm_up);
-        prefetch_tensormap(m_down);
-    }
-    if (warp == kWarpO && lane == 0) {
-        if (whole) {
-            prefetch_tensormap(KB > 1 ? &tm_hid4 : &tm_hid);
-            prefetch_tensormap(small_b && KB > 1 ? &tm_h4 : &tm_h);
-        } else {
-            prefetch_tensormap(&tm_x);
-            prefetch_tensormap(&tm_h);
         }
     }
     tmem_fence_before_sync();

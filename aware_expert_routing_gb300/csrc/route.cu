@@ -139,14 +139,14 @@ __device__ __forceinline__ void finish_token(const RouteArgs& a, RouteSmem& sm, 
 }
 
 // Publishes the OEA union S_base: lane j stores word j (bit b: expert
-// 32j + b) together with the call's epoch, at once and with release
-// semantics, so a reader that sees the epoch sees the word.  The activated set is S_base
-// as soon as phase 1 is done: phase 2 only adds tokens to experts inside it,
-// and every expert in it keeps the token whose baseline put it there.  The
+// 32j + b) together with the call's epoch in one 64-bit store, so a reader
+// that sees the epoch sees the word.  The activated set is S_base as soon
+// as phase 1 is done: phase 2 only adds tokens to experts inside it, and
+// every expert in it keeps the token whose baseline put it there.  The
 // expert kernel, launched early, starts on those experts' weights from it
-// while phase 2 and the grouping run.  The last warp of a one-CTA launch.
+// while phase 2 and the grouping run.  CTA 0's last warp.
 __device__ __forceinline__ void publish_union(const RouteArgs& a, uint32_t word, int lane) {
-    st_release_gpu_u64(&a.uwords[lane], ((uint64_t)a.epoch << 32) | (lane < (a.N + 31) / 32 ? word : 0u));
+    st_relaxed_gpu_u64(&a.uwords[lane], ((uint64_t)a.epoch << 32) | (lane < (a.N + 31) / 32 ? word : 0u));
 }
 
 // The routing of tokens [32 rank, 32 rank + 32) by one CTA of `ncta` in a
@@ -181,8 +181,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
         // Zero the counter set that the expert call after the previous
         // routing call used (it has completed: dependency wait above); the
         // expert call after the next routing call uses it.  The last warp,
-        // which publishes S_base with release stores, takes no part, so its
-        // stores wait for none of these.
+        // which publishes S_base, takes no part.
         for (int q = threadIdx.x; q < kHdoneSet; q += nthreads - 32) a.clr_hdone[q] = 0u;
         if (threadIdx.x == 0) {
             *a.clr_next = 0u;
@@ -280,8 +279,11 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
             sb = sm.sball;
         }
         __syncthreads();
-        // S_base (over the cluster), from CTA 0's last warp: it has no global
-        // store pending that its release stores would have to wait for
+        // S_base (over the cluster), from CTA 0's last warp.  Each word holds
+        // the routing call's epoch in the same 64-bit store, and the expert
+        // kernel reads everything else of this kernel's only after its
+        // completion, so the stores are relaxed: no fence, which would wait
+        // for this CTA's earlier stores (1.8 us measured).
         if (rank == 0 && a.uwords && warp == nwarps - 1) publish_union(a, sb[lane], lane);
         if (a.n_base)
             for (int i = tb + (int)threadIdx.x; i < te; i += nthreads) a.n_base[i] = sm.snb[i - tb];
