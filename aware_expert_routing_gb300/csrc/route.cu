@@ -149,9 +149,32 @@ __device__ __forceinline__ void publish_union(const RouteArgs& a, uint32_t word,
     st_relaxed_gpu_u64(&a.uwords[lane], ((uint64_t)a.epoch << 32) | (lane < (a.N + 31) / 32 ? word : 0u));
 }
 
+// Zeroes the shared union and per-expert token words of route_body's layout
+// and, in CTA 0, the counter set that the expert call after the previous
+// routing call used (it has completed: the caller has waited for the
+// preceding kernel); the expert call after the next routing call uses it.
+// The last warp, which publishes S_base, takes no part in the clearing.
+// The caller synchronises the CTA before route_body reads them.
+__device__ __forceinline__ void route_prepare(const RouteArgs& a, unsigned char* smem_raw, const uint32_t rank) {
+    const int nthreads = blockDim.x;
+    const int warp = threadIdx.x >> 5, nwarps = nthreads >> 5;
+    uint32_t* sbase = reinterpret_cast<uint32_t*>(smem_raw);
+    uint32_t* bits = reinterpret_cast<uint32_t*>(smem_raw + 4 * 32 * 4 + 2 * (size_t)a.N * 4);
+    if (threadIdx.x < 32) sbase[threadIdx.x] = 0;
+    for (int q = threadIdx.x; q < a.N; q += nthreads) bits[q] = 0;
+    if (rank == 0 && a.clr_hdone && warp < nwarps - 1) {
+        for (int q = threadIdx.x; q < kHdoneSet; q += nthreads - 32) a.clr_hdone[q] = 0u;
+        if (threadIdx.x == 0) {
+            *a.clr_next = 0u;
+            *a.clr_gathered = 0u;
+        }
+    }
+}
+
 // The routing of tokens [32 rank, 32 rank + 32) by one CTA of `ncta` in a
-// cluster; a.logits may point to shared memory.
-template <int NPL>
+// cluster; a.logits may point to shared memory.  Prepared: the caller has
+// run route_prepare and synchronised the CTA after its dependency wait.
+template <int NPL, bool kPrepared>
 __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* smem_raw, const uint32_t rank,
                                            const uint32_t ncta) {
     const int nthreads = blockDim.x;
@@ -173,22 +196,12 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
     sm.bits = reinterpret_cast<uint32_t*>(p); p += (size_t)N * 4;
     sm.sidx = reinterpret_cast<int*>(p);
 
-    if (threadIdx.x < 32) sm.sbase[threadIdx.x] = 0;
-    for (int q = threadIdx.x; q < N; q += nthreads) sm.bits[q] = 0;
-    grid_launch_dependents();    // the expert kernel may start its prologue
-    grid_dependency_wait();      // scores come from the router kernel
-    if (rank == 0 && a.clr_hdone && warp < nwarps - 1) {
-        // Zero the counter set that the expert call after the previous
-        // routing call used (it has completed: dependency wait above); the
-        // expert call after the next routing call uses it.  The last warp,
-        // which publishes S_base, takes no part.
-        for (int q = threadIdx.x; q < kHdoneSet; q += nthreads - 32) a.clr_hdone[q] = 0u;
-        if (threadIdx.x == 0) {
-            *a.clr_next = 0u;
-            *a.clr_gathered = 0u;
-        }
+    if (!kPrepared) {
+        grid_launch_dependents();    // the expert kernel may start its prologue
+        grid_dependency_wait();      // scores come from the router kernel
+        route_prepare(a, smem_raw, rank);
+        __syncthreads();
     }
-    __syncthreads();
 
     bool nonfinite = false;
     const bool oea = a.mode == MOE_MODE_OEA;
@@ -445,7 +458,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
 template <int NPL>
 __global__ void route_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    route_body<NPL>(a, smem_raw, cluster_ctarank(), gridDim.x);   // the whole grid is one cluster
+    route_body<NPL, false>(a, smem_raw, cluster_ctarank(), gridDim.x);   // the whole grid is one cluster
 }
 
 // ---- scores and routing in one cluster (bf16, up to 32 tokens, N <= 128) ----
@@ -518,6 +531,9 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_fused_kernel(Router
     load_w(warp, pa0, pa1, pb0, pb1);
     grid_launch_dependents();    // the expert kernel may start its prologue
     grid_dependency_wait();      // hidden states come from the preceding kernel
+    // CTA 0's routing state, set up while the token rows load; the cluster
+    // barrier after the scores orders it before the routing reads it
+    if (rank == 0) route_prepare(a, smem_raw, 0u);
 
     float acc[4][4];
 #pragma unroll
@@ -570,7 +586,7 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_fused_kernel(Router
     if (rank != 0) return;
     RouteArgs ra = a;
     ra.logits = lg;
-    route_body<NPL>(ra, smem_raw, 0u, 1u);
+    route_body<NPL, true>(ra, smem_raw, 0u, 1u);
 }
 
 template <int NPL>
