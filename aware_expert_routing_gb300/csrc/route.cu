@@ -172,11 +172,12 @@ __device__ __forceinline__ void route_prepare(const RouteArgs& a, unsigned char*
 }
 
 // The routing of tokens [32 rank, 32 rank + 32) by one CTA of `ncta` in a
-// cluster; a.logits may point to shared memory.  Prepared: the caller has
-// run route_prepare and synchronised the CTA after its dependency wait.
+// cluster, from the scores at `logits` (global or shared memory).  Prepared:
+// the caller has run route_prepare and synchronised the CTA after its
+// dependency wait.
 template <int NPL, bool kPrepared>
-__device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* smem_raw, const uint32_t rank,
-                                           const uint32_t ncta) {
+__device__ __forceinline__ void route_body(const RouteArgs& a, const float* logits, unsigned char* smem_raw,
+                                           const uint32_t rank, const uint32_t ncta) {
     const int nthreads = blockDim.x;
     const int nwarps = nthreads >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -215,7 +216,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
     // ---- plain top-k, or OEA phase 1 (baseline and union) ------------------
     for (int i = tb + warp; i < te; i += nwarps) {
         const int il = i - tb;
-        load_keys<NPL>(a.logits + (size_t)i * N, N, lane, kv, nonfinite);
+        load_keys<NPL>(logits + (size_t)i * N, N, lane, kv, nonfinite);
         if (i >= a.B_valid) {           // padding token: selects nothing
             if (lane == 0) {
                 sm.snb[il] = 0;
@@ -313,7 +314,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
                 taken = taken1; cnt = n1; r0 = n1; myid = myid1; myval = myval1;
             } else {
                 bool dummy = false;
-                load_keys<NPL>(a.logits + (size_t)i * N, N, lane, kv, dummy);
+                load_keys<NPL>(logits + (size_t)i * N, N, lane, kv, dummy);
             }
             if (a.maxP >= N) {
                 // the in-union experts in rank order; the first n_i are the baseline
@@ -458,7 +459,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, unsigned char* sm
 template <int NPL>
 __global__ void route_kernel(RouteArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    route_body<NPL, false>(a, smem_raw, cluster_ctarank(), gridDim.x);   // the whole grid is one cluster
+    route_body<NPL, false>(a, a.logits, smem_raw, cluster_ctarank(), gridDim.x);   // the whole grid is one cluster
 }
 
 // ---- scores and routing in one cluster (bf16, up to 32 tokens, N <= 128) ----
@@ -584,9 +585,9 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_fused_kernel(Router
     const bool clustered = gridDim.x > 1;   // one CTA (N <= 16) is launched without a cluster
     if (clustered) cluster_sync(); else __syncthreads();   // CTA 0 holds every score
     if (rank != 0) return;
-    RouteArgs ra = a;
-    ra.logits = lg;
-    route_body<NPL, true>(ra, smem_raw, 0u, 1u);
+    // the routing reads every argument from the kernel's parameters and the
+    // scores from shared memory
+    route_body<NPL, true>(a, lg, smem_raw, 0u, 1u);
 }
 
 template <int NPL>
