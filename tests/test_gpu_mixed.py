@@ -67,7 +67,8 @@ def run_mixed(w, L, D, hot_w, mixed, prm):
     return r, out
 
 
-@pytest.mark.parametrize("mode,k0,p,B", [(TOPK, 4, 1.0, 20), (OEA, 2, 0.7, 20), (OEA, 3, 1.0, 37)])
+@pytest.mark.parametrize("mode,k0,p,B", [(TOPK, 4, 1.0, 20), (OEA, 2, 0.7, 20), (OEA, 3, 1.0, 37),
+                                         (OEA, 4, 1.0, 64), (TOPK, 4, 1.0, 64), (OEA, 3, 1.0, 65)])
 def test_mixed_layer_parity(mode, k0, p, B):
     w = synth.Workload("t_mixed", N=32, k=4, d=512, F=256, B=B, seed=41, zipf=True)
     L = synth.make_layer(w, 0, B)

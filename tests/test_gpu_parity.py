@@ -93,6 +93,19 @@ def test_bf16_ragged_batches(B):
     run_case(w, B, TOPK)
 
 
+@pytest.mark.parametrize("B", [16, 17, 32, 33, 48, 64, 65])
+def test_whole_batch_boundaries(B):
+    # Up to 64 tokens the whole batch is the phase-A operand: one chunk per
+    # expert, each expert's tokens from the routing's two 32-token words,
+    # and with OEA the early start.  65 tokens take the expert-grouped copy.
+    # N = 512 keeps the routing kernel busy long enough for phase-B tiles to
+    # be posted before it completes, when their MMA width (the chunk's token
+    # count) is not yet known; Zipf routing gives chunks of many tokens.
+    w = W("t_whole", N=512, k=8, d=512, F=256, seed=100 + B, zipf=True)
+    run_case(w, B, OEA, 4, 1.0)
+    run_case(w, B, TOPK)
+
+
 @pytest.mark.parametrize("N,k,d,F", [(16, 4, 64, 64), (160, 6, 320, 192), (1024, 8, 128, 64),
                                      (256, 16, 192, 320), (32, 32, 64, 128)])
 def test_bf16_shapes(N, k, d, F):
