@@ -99,6 +99,7 @@ constexpr int kConvWarps = 8;
 constexpr int kWarpN = kWarpC + kConvWarps;   // warp 15: counts finished y slices down
 constexpr int kThreads = (kWarpN + 1) * 32;
 constexpr int kNQ = 8;                   // phase-B tiles handed to warp 15
+static_assert(MOE_MAX_TOKENS <= 256, "a handed-over tile's tokens are kept as bytes");
 constexpr int kM = 128;                  // weight rows per tile (MMA M)
 constexpr int kNMax = 128;               // most token columns per tile (MMA N)
 constexpr int kWBytes = kM * 128;        // one K block: 128 rows x 64 bf16
@@ -133,6 +134,7 @@ struct Smem {
     uint64_t nt_full[kNQ];               // the four epilogue warps stored a phase-B tile's y rows
     uint64_t nt_empty[kNQ];              // warp 15 has counted them down
     int4 nt_info[kNQ];                   // first pair, pairs (-1: no more tiles), row block
+    uint8_t nt_tok[kNQ][kNMax];          // the tile's tokens (batches of at most 256), looked up by the epilogue
     uint64_t raw_full[kRawMax];          // packed INT4 chunks landed (bulk copies)
     uint64_t raw_empty[kRawMax];         // the converter warps have read them
     uint64_t cfull[kMaxStages];          // each converter warp wrote its rows of a stage's blocks (INT4 stages)
@@ -864,11 +866,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         __syncwarp();
     } else if (warp == kWarpN) {
         // ----------------------------- count-down warp ----------------------------
-        // Each finished phase-B tile's tokens (at most kNMax, four per lane)
-        // count down their counters for the tile's 128 rows of d: all the
-        // tokens are looked up at once, then one fence (after the acquire of
-        // the epilogue warps' barrier) makes their y stores visible before
-        // the plain atomic subtractions -- a release.
+        // Each finished phase-B tile's tokens (at most kNMax, four per lane,
+        // looked up by the epilogue warps while the tile's MMAs ran) count
+        // down their counters for the tile's 128 rows of d: one fence (after
+        // the acquire of the epilogue warps' barrier) makes their y stores
+        // visible before the plain atomic subtractions -- a release.
         if (early) grid_dependency_wait();   // the pairs and counters come from the routing kernel
         for (uint32_t p = 0;; ++p) {
             const int slot = (int)(p % kNQ);
@@ -880,7 +882,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
 #pragma unroll
             for (int u = 0; u < kNMax / 32; ++u) {
                 const int j = lane + 32 * u;
-                tk[u] = j < inf.y ? A.perm[inf.x + j] / A.kslots : -1;
+                tk[u] = j < inf.y ? (int)S.nt_tok[slot][j] : -1;   // written by the epilogue warps
             }
             __threadfence();
 #pragma unroll
@@ -949,17 +951,23 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     } else {
         // ------------------------------- epilogue --------------------------------
         const int tid = threadIdx.x;   // 0..127
-        if (early) wait_bar(&S.meta_full, 0, S, flags);   // token masks and first pairs
+        if (early) {
+            wait_bar(&S.meta_full, 0, S, flags);   // token masks and first pairs
+            grid_dependency_wait();                // the pairs' tokens come from the routing kernel
+        }
 
         __nv_bfloat16* hb = static_cast<__nv_bfloat16*>(A.hbuf);
         const int i = 32 * warp + lane;                    // this thread's D row (tensor-memory lane)
         const uint32_t lane_addr = (uint32_t)(32 * warp) << 16;
         uint32_t nm = 0;   // meetings of the four warps so far (parity of epi_bar)
         uint32_t np = 0;   // phase-B tiles handed to warp 15
-        // hands a finished phase-B tile (or the end, ntok = -1) to warp 15
-        auto hand_over = [&](int pair0, int ntok, int rb) {
+        // hands a finished phase-B tile (or the end, ntok = -1) to warp 15,
+        // with the token of the tile's pair `tid` (looked up before the tile's
+        // accumulator was ready, so warp 15 need not wait for the lookup)
+        auto hand_over = [&](int pair0, int ntok, int rb, int tok) {
             const int slot = (int)(np % kNQ);
             if (np >= kNQ) wait_bar(&S.nt_empty[slot], ((np / kNQ) - 1) & 1, S, flags);
+            if (tid < ntok) S.nt_tok[slot][tid] = (uint8_t)tok;
             if (tid == 0) S.nt_info[slot] = make_int4(pair0, ntok, rb, 0);
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.nt_full[slot]);
@@ -975,6 +983,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
             const int b = n % kAcc;
             const int ngroups = (ph_a && whole) ? nwb >> 4 : (T.ntok + 15) >> 4;   // 16-column groups of D
+            // phase B: the token of pair `tid` of the tile, loaded while the MMAs run
+            const int my_tok = !ph_a && tid < T.ntok ? A.perm[T.off + nmax * T.c + tid] / A.kslots : -1;
             wait_bar(&S.acc_full[b], (n / kAcc) & 1, S, flags);
             if (aborted(S)) break;
             tmem_fence_after_sync();
@@ -1033,12 +1043,12 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     }
                 }
                 // the tile's y rows are stored: warp 15 counts its tokens down
-                hand_over(T.off + nmax * T.c, T.ntok, T.rb);
+                hand_over(T.off + nmax * T.c, T.ntok, T.rb, my_tok);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&S.tq_empty[q]);
         }
-        hand_over(0, -1, 0);   // no more tiles
+        hand_over(0, -1, 0, -1);   // no more tiles
     }
 
     // ---- combine: one warp per (token, 128 rows of d) ----
