@@ -341,6 +341,7 @@ struct TcOpEntry {
     const void* ws;
     const void* hidden;
     int pairs, B, d, F, dev;
+    bool q4;   // a launch with INT4 experts: stages of kbl blocks at every batch size
     CUtensorMap maps[5];
     bool used;
 };
@@ -348,11 +349,11 @@ TcOpEntry g_tc_ops[32];
 int g_tc_ops_next = 0;
 
 moe_status tc_operand_maps(unsigned char* ws, const WsLayout& L, const void* hidden, int pairs, int B, int d, int F,
-                           int dev, CUtensorMap* out) {
+                           int dev, bool q4, CUtensorMap* out) {
     std::lock_guard<std::mutex> lk(g_map_mu);
     for (auto& e : g_tc_ops)
         if (e.used && e.ws == ws && e.hidden == hidden && e.pairs == pairs && e.B == B && e.d == d && e.F == F &&
-            e.dev == dev) {
+            e.dev == dev && e.q4 == q4) {
             memcpy(out, e.maps, sizeof e.maps);
             return MOE_OK;
         }
@@ -366,11 +367,12 @@ moe_status tc_operand_maps(unsigned char* ws, const WsLayout& L, const void* hid
     e.d = d;
     e.F = F;
     e.dev = dev;
+    e.q4 = q4;
     const uint32_t kb = (uint32_t)small_batch_blocks(d, F);
     // the whole batch of up to 64 tokens as one box (rows past B read as
     // zeros), as wide as the launch's stages
     const uint32_t nwb = B <= 64 ? (uint32_t)(B <= 16 ? 16 : (B + 15) & ~15) : 16u;
-    const uint32_t kbw = B <= 16 ? kb : (uint32_t)large_batch_blocks(d, F);
+    const uint32_t kbw = B <= 16 && !q4 ? kb : (uint32_t)large_batch_blocks(d, F);
     if (!encode_3d(&e.maps[0], ws + L.xperm, d, pairs, 16, 1) || !encode_3d(&e.maps[1], ws + L.hbuf, F, pairs, 16, 1) ||
         !encode_3d(&e.maps[2], hidden, d, B, nwb, 1) || !encode_3d(&e.maps[3], hidden, d, B, nwb, kbw) ||
         !encode_3d(&e.maps[4], ws + L.hbuf, F, pairs, 16, kb))
@@ -513,7 +515,8 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
         bool fused = false, swap = false;
         CUtensorMap wm[7], om[5];
         if ((st = tc_expert_maps(w_gate, w_up, w_down, n_hot, d_ff, P.d, dev, wm, &fused, &swap)) != MOE_OK) return st;
-        if ((st = tc_operand_maps(ws, L, hidden, P.B * P.kslots, P.B, P.d, d_ff, dev, om)) != MOE_OK) return st;
+        if ((st = tc_operand_maps(ws, L, hidden, P.B * P.kslots, P.B, P.d, d_ff, dev, a.n_cold > 0, om)) != MOE_OK)
+            return st;
         maps[0] = wm[0];                       // gate/up 5D, or W_gate
         maps[1] = wm[0];                       // W_gate (8-row boxes; read when not fused)
         maps[2] = wm[1];                       // W_up

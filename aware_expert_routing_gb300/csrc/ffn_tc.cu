@@ -344,16 +344,20 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // weights, since the TMA unit's rate per SM grows with the size of each
     // operation: A.kbs (up to 4) for batches of up to 16 tokens, A.kbl (up to
     // 2) for larger batches, whose token rows share the ring.
-    const bool small_b = A.B <= 16;                 // 4-block stages where d and d_ff allow them
+    const bool small_b = A.B <= 16;
+    // Stages of A.kbs blocks (4 where d and d_ff allow them) for bf16 batches
+    // of up to 16 tokens.  Launches with INT4 experts keep the packed slots'
+    // reserve, which leaves room for only two such stages: they use A.kbl.
+    const bool kbs_stages = small_b && A.n_cold == 0;
     // Batches of up to kWholeMax tokens: the phase-A operand is the whole
     // batch (nwb rows, the batch rounded up to 16; the tensor pipe is nearly
     // idle at decode, so multiplying every token costs nothing), each expert
     // is one token chunk, and h is stored for the expert's own tokens only.
     const bool whole = A.B <= kWholeMax;
     const int nwb = max(16, (A.B + 15) & ~15);
-    const int KB = A.gu_fused ? (small_b ? A.kbs : A.kbl) : 1;
-    const CUtensorMap* const m_gu = KB == 1 ? &tm_gu : small_b ? &tm_gu4 : &tm_gu2;       // weight maps, KB wide
-    const CUtensorMap* const m_down = KB == 1 ? &tm_down : small_b ? &tm_down4 : &tm_down2;
+    const int KB = A.gu_fused ? (kbs_stages ? A.kbs : A.kbl) : 1;
+    const CUtensorMap* const m_gu = KB == 1 ? &tm_gu : kbs_stages ? &tm_gu4 : &tm_gu2;       // weight maps, KB wide
+    const CUtensorMap* const m_down = KB == 1 ? &tm_down : kbs_stages ? &tm_down4 : &tm_down2;
 
     // The tensor maps' descriptors, fetched while the barriers are set up:
     // the first copies (which the early start issues the moment the
@@ -366,7 +370,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     if (warp == kWarpO && lane == 0) {
         if (whole) {
             prefetch_tensormap(KB > 1 ? &tm_hid4 : &tm_hid);
-            prefetch_tensormap(small_b && KB > 1 ? &tm_h4 : &tm_h);
+            prefetch_tensormap(kbs_stages && KB > 1 ? &tm_h4 : &tm_h);
         } else {
             prefetch_tensormap(&tm_x);
             prefetch_tensormap(&tm_h);
@@ -772,7 +776,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 // block kb at kb x nmax rows.
                 const bool wide = ph_a && whole;
                 const CUtensorMap* map = ph_a ? (whole ? (KB > 1 ? &tm_hid4 : &tm_hid) : &tm_x)
-                                              : (small_b && KB > 1 ? &tm_h4 : &tm_h);
+                                              : (kbs_stages && KB > 1 ? &tm_h4 : &tm_h);
                 const int row = wide ? 0 : T.off + nmax * T.c;
                 const int nb = wide ? nwb >> 4 : (T.ntok + 15) >> 4;   // 16-row boxes = MMA N / 16
                 const int ns = ph_a ? SA : SB;
@@ -784,7 +788,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     unsigned char* dst = ring + (size_t)slot * slot_bytes + KB * kWBytes;
                     if (wide) {
                         tma_load_3d(dst, map, 0, 0, s * KB, &S.full[slot], pol);
-                    } else if (small_b) {
+                    } else if (kbs_stages) {
                         for (int j = 0; j < nb; ++j)
                             tma_load_3d(dst + j * 2048, map, 0, row + 16 * j, s * KB, &S.full[slot], pol);
                     } else {
@@ -1166,7 +1170,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
     FfnArgs a = a_in;
     a.smem_bytes = smem_optin[dev];
     // the ring must hold two stages of the largest slot this launch can use
-    const int kb = a.gu_fused ? (a.B <= 16 ? a.kbs : a.kbl) : 1;
+    const int kb = a.gu_fused ? (a.B <= 16 && a.n_cold == 0 ? a.kbs : a.kbl) : 1;
     const int nwb = a.B <= 16 ? 16 : (a.B + 15) & ~15;
     const size_t slot = (size_t)kb * (kWBytes + (a.B <= kWholeMax ? nwb : kNMax) * 128);
     if ((size_t)a.smem_bytes < 4096 + tabs_bytes(a.N) + (size_t)kRawReserve ||
