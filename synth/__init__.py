@@ -161,7 +161,8 @@ WORKLOADS = {
                  batch_sweep=(16, 64, 256)),
         Workload("qwen3_30b_a3b_mixed_int4_b32", N=128, k=8, d=2048, F=768, B=32,
                  seed=32, zipf=True, layers=1, int4_cold=True, hot_n=32,
-                 runs=(("topk", "topk", 8, 1.0), ("oea_k0_5", "oea", 5, 1.0))),
+                 runs=(("topk", "topk", 8, 1.0), ("oea_k0_5", "oea", 5, 1.0)),
+                 batch_sweep=(8, 16, 32)),
     ]
 }
 
