@@ -114,6 +114,8 @@ constexpr int kQ = 16;                   // tile queue entries
 constexpr int kAcc = 4;                  // accumulator buffers
 constexpr uint32_t kTmemCols = kAcc * kNMax;   // fp32 columns (batches over kWholeMax tokens)
 constexpr int kWholeMax = 64;            // batches up to this size use the whole batch as the phase-A operand
+constexpr uint32_t kTmA = 256;           // first TMEM column of the INT4 A buffers (whole batches)
+constexpr uint32_t kTmAStride = 128;     // columns of one A buffer: up to 4 blocks of 64 bf16
 constexpr uint32_t kBarGather = 2;       // named barrier of the warps that copy grouped rows
 constexpr int kGatherThreads = (kEpiWarps + kConvWarps + 1) * 32;   // warps 0-3 and 7-15
 constexpr int kGatherRows = 64;          // grouped rows per pass
@@ -126,6 +128,7 @@ struct Smem {
     uint64_t acc_empty[kAcc];            // the four epilogue warps
     uint64_t tq_full[kQ];                // tile queue entry posted by the weight warp
     uint64_t tq_empty[kQ];               // entry released by the four epilogue warps
+    uint64_t tma_empty[2];               // the MMAs have read a TMEM A buffer (INT4 stages of whole batches)
     uint64_t mma_done;                   // every MMA issued has completed
     uint64_t meta_full;                  // early start: counts, first pairs and token masks are in the tables
     uint64_t union_full;                 // early start: warp 4 has put the union's words in uw
@@ -358,6 +361,18 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     const int KB = A.gu_fused ? (kbs_stages ? A.kbs : A.kbl) : 1;
     const CUtensorMap* const m_gu = KB == 1 ? &tm_gu : kbs_stages ? &tm_gu4 : &tm_gu2;       // weight maps, KB wide
     const CUtensorMap* const m_down = KB == 1 ? &tm_down : kbs_stages ? &tm_down4 : &tm_down2;
+    // Batches of up to 48 tokens with INT4 experts: an INT4 stage spans
+    // KBq = 2 KB blocks and its ring slot holds the token rows of those
+    // blocks, then their packed chunks (2 KB x 128 x nwb + KB x 16.5 KB
+    // bytes, within the slot's KB x (16 KB + 128 x nwb) while nwb <= 48).
+    // The converter warps write the decoded A operand into one of two
+    // tensor-memory buffers (columns kTmA and kTmA + kTmAStride) that the
+    // MMAs read.  A ring slot's cycle is set by the token rows' TMA load,
+    // which queues behind the HBM stream, so twice the K per slot doubles the
+    // INT4 stages' rate, and the bf16 stages keep the whole ring.
+    const bool q4t = has_q4 && whole && KB <= 2 && nwb * 128 + kRawPair <= kWBytes &&
+                     (d / 64) % (2 * KB) == 0 && (F / 64) % (2 * KB) == 0;
+    const int KBq = q4t ? 2 * KB : KB;   // blocks of an INT4 stage
 
     // The tensor maps' descriptors, fetched while the barriers are set up:
     // the first copies (which the early start issues the moment the
@@ -390,6 +405,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             mbar_init(&S.tq_empty[i], kEpiWarps);
         }
         mbar_init(&S.mma_done, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&S.tma_empty[i], 1);
         mbar_init(&S.meta_full, 1);
         mbar_init(&S.union_full, 1);
         mbar_init(&S.epi_bar, kEpiWarps);
@@ -411,7 +427,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     }
     // accumulator buffers: kAcc x nwb columns for whole batches, else kAcc x kNMax
     const int acc_stride = whole ? nwb : kNMax;
-    const uint32_t tmem_cols = whole ? (kAcc * nwb <= 64 ? 64u : kAcc * nwb <= 128 ? 128u : 256u) : kTmemCols;
+    const uint32_t tmem_cols = q4t ? 512u : whole ? (kAcc * nwb <= 64 ? 64u : kAcc * nwb <= 128 ? 128u : 256u)
+                                                  : kTmemCols;
     if (warp == kWarpM) tmem_alloc(&S.tmem_base, tmem_cols);
     __syncthreads();             // barriers initialised (this overlaps the routing kernel)
     // Early start (OEA routing of whole batches, whose routing
@@ -645,12 +662,18 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // chunks of one stage's KB blocks (W_gate's, then W_up's, in phase A),
     // each matrix's moved by one bulk copy.  With KB = 1 a stage reads half
     // of its chunk.
-    const int qch = KB > 1 ? KB / 2 : 1;           // packed chunks per matrix and stage
+    // With q4t the packed chunks sit in the stage's ring slot (after its
+    // KBq operand blocks) and a raw slot is only the converters' queue entry.
+    const int qch = KBq > 1 ? KBq / 2 : 1;         // packed chunks per matrix and stage
     const int rslot = qch * kRawPair;
     const int nraw_a = kRawReserve / rslot;        // slots after the ring
-    const int nraw = nraw_a + min(kRawMax - nraw_a, (ring_bytes - nst * slot_bytes) / rslot);
+    const int nraw = q4t ? kRawMax : nraw_a + min(kRawMax - nraw_a, (ring_bytes - nst * slot_bytes) / rslot);
     auto raw_slot = [&](int r) -> unsigned char* {
         return r < nraw_a ? raw + (size_t)r * rslot : ring + (size_t)nst * slot_bytes + (size_t)(r - nraw_a) * rslot;
+    };
+    // q4t: the packed chunks of the INT4 stage in ring slot `slot`
+    auto packed_in_slot = [&](int slot) -> unsigned char* {
+        return ring + (size_t)slot * slot_bytes + (size_t)KBq * obytes;
     };
 
     if (warp == kWarpW) {
@@ -678,7 +701,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;   // chunked experts are re-read from L2
                 const int sl = X.ex_slot[T.a];                          // bf16 expert, or -1 - INT4 expert
                 const int row0 = ph_a ? sl * F + 64 * T.rb : sl * d + kM * T.rb;
-                const int ns = ph_a ? SA : SB;
+                const int ns = (ph_a ? SA : SB) / (q4t && sl < 0 ? 2 : 1);   // INT4 stages of KBq blocks
                 for (int s = n == 0 ? fast_stages : 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
@@ -695,8 +718,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                         if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
                         // slot, phase A, and (KB = 1) which half of the chunk the stage reads
                         S.raw_info[r] = (uint32_t)slot | (ph_a ? 256u : 0u) | ((uint32_t)((s * KB) & 1) << 9);
-                        unsigned char* rdst = raw_slot(r);
-                        const int cg = s * KB / 2;   // the stage's first 128-column group
+                        unsigned char* rdst = q4t ? packed_in_slot(slot) : raw_slot(r);
+                        const int cg = s * KBq / 2;   // the stage's first 128-column group
                         if (ph_a) {
                             const size_t off = (size_t)c * q4_mat_a + ((size_t)T.rb * (d / 128) + cg) * kQ4A;
                             mbar_arrive_expect_tx(&S.raw_full[r], 2 * qch * kQ4A);
@@ -779,13 +802,28 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                                               : (kbs_stages && KB > 1 ? &tm_h4 : &tm_h);
                 const int row = wide ? 0 : T.off + nmax * T.c;
                 const int nb = wide ? nwb >> 4 : (T.ntok + 15) >> 4;   // 16-row boxes = MMA N / 16
-                const int ns = ph_a ? SA : SB;
+                // an INT4 stage of a q4t launch: KBq operand blocks at the slot's start
+                const bool pk = q4t && X.ex_slot[T.a] < 0;
+                const int ns = (ph_a ? SA : SB) / (pk ? 2 : 1);
                 for (int s = n == 0 ? fast_ops : 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
                     if (aborted(S)) break;
+                    unsigned char* dst = ring + (size_t)slot * slot_bytes + (pk ? 0 : KB * kWBytes);
+                    if (pk) {
+                        mbar_arrive_expect_tx(&S.full[slot], nb * 2048 * KBq);
+                        if (wide) {   // KBq / KB boxes of KB blocks
+                            for (int h = 0; h < KBq; h += KB)
+                                tma_load_3d(dst + h * obytes, map, 0, 0, s * KBq + h, &S.full[slot], pol);
+                        } else {
+                            for (int kb = 0; kb < KBq; ++kb)
+                                for (int j = 0; j < nb; ++j)
+                                    tma_load_3d(dst + kb * obytes + j * 2048, map, 0, row + 16 * j, s * KBq + kb,
+                                                &S.full[slot], pol);
+                        }
+                        continue;
+                    }
                     mbar_arrive_expect_tx(&S.full[slot], nb * 2048 * KB);   // rows past the end read as zeros
-                    unsigned char* dst = ring + (size_t)slot * slot_bytes + KB * kWBytes;
                     if (wide) {
                         tma_load_3d(dst, map, 0, 0, s * KB, &S.full[slot], pol);
                     } else if (kbs_stages) {
@@ -806,6 +844,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         if (lane == 0) {
             RingPos rp;
             uint32_t cpar = 0;   // per ring slot: parity of its next cfull phase (INT4 stages)
+            uint32_t q4n = 0;    // INT4 stages of a q4t launch so far (TMEM A buffer q4n & 1)
             bool meta = !early;  // the tables hold the counts
             for (int n = 0;; ++n) {
                 const int q = n % kQ;
@@ -832,7 +871,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     q4 = X.ex_slot[T.a] < 0;
                 }
                 const uint32_t idesc = umma_idesc_bf16(kM, ntile);
-                const int ns = ph_a ? SA : SB;
+                const bool pk = q4 && q4t;   // A from tensor memory, KBq blocks per stage
+                const int ns = (ph_a ? SA : SB) / (pk ? 2 : 1);
                 const int b = n % kAcc;
                 if (n >= kAcc) {   // the epilogue has read this accumulator's previous tile
                     wait_bar(&S.acc_empty[b], ((n / kAcc) - 1) & 1, S, flags);
@@ -849,6 +889,20 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     if (aborted(S)) break;   // the stage may not have landed: issue nothing more
                     tmem_fence_after_sync();
                     const uint32_t a0 = smem_u32(ring + (size_t)slot * slot_bytes);
+                    if (pk) {
+                        const uint32_t ta = tmem + kTmA + (q4n & 1u) * kTmAStride;
+#pragma unroll 1
+                        for (int kb = 0; kb < KBq; ++kb) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)   // 8 columns of A, 32 bytes of the swizzled B row
+                                umma_bf16_tmem_a(dt, ta + 32 * kb + 8 * k, umma_sdesc_sw128(a0 + kb * obytes + 32 * k),
+                                                 idesc, (s | kb | k) ? 1u : 0u);
+                        }
+                        umma_commit(&S.empty[slot]);
+                        umma_commit(&S.tma_empty[q4n & 1u]);   // the converters may refill this A buffer
+                        ++q4n;
+                        continue;
+                    }
                     const uint32_t b0 = a0 + KB * kWBytes;
 #pragma unroll 1
                     for (int kb = 0; kb < KB; ++kb) {
@@ -906,6 +960,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         // slot and on the stage.
         const int ct = threadIdx.x - kWarpC * 32;   // 0..kConvWarps*32-1
         RingPos rq;
+        uint32_t cq = 0;   // INT4 stages decoded so far (q4t launches)
         for (;;) {
             if (A.n_cold == 0) break;                  // no INT4 experts in this launch
             const int r = rq.slot;
@@ -924,6 +979,56 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
             const bool ph_a = (info >> 8) & 1u;
             const int half1 = (info >> 9) & 1u;          // KB = 1: the stage's half of its chunk
             const int rows = ph_a ? 64 : kM;
+            if (q4t) {
+                // The stage's KBq blocks go to tensor-memory A buffer cq & 1:
+                // row i (this warp's lane quarter) in lane i, block kb at
+                // column 32 kb, the K pair (2j, 2j + 1) of a block in its
+                // column j.  Warps 7-10 and 11-14 each cover the four lane
+                // quarters, for the first and the second half of the blocks.
+                const unsigned char* src = packed_in_slot(slot);
+                const int qd = warp & 3;                  // lane quarter this warp may access
+                const int i = 32 * qd + lane;             // A row
+                const int grp = (warp - kWarpC) >> 2;
+                if (cq >= 2) {   // the MMAs have read what this buffer held two stages ago
+                    wait_bar(&S.tma_empty[cq & 1u], ((cq >> 1) - 1) & 1u, S, flags);
+                    if (*(volatile int*)&S.abort_flag) break;
+                    tmem_fence_after_sync();
+                }
+                const int srow = ph_a ? 8 * (i >> 4) + (i & 7) : i;
+                const uint32_t tb = tmem + ((uint32_t)(32 * qd) << 16) + kTmA + (cq & 1u) * kTmAStride;
+#pragma unroll 1
+                for (int h = 0; h < KBq / 2; ++h) {
+                    const int kb = grp * (KBq / 2) + h;
+                    const int ci = kb >> 1, half = kb & 1;   // chunk of the block, 64-column half of it
+                    // phase A: W_gate's chunk ci, or W_up's (after W_gate's qch)
+                    const unsigned char* ch = ph_a ? src + (((i >> 3) & 1) * qch + ci) * kQ4A : src + ci * kQ4B;
+                    const uint4 c0 = *reinterpret_cast<const uint4*>(ch + srow * 64 + half * 32);
+                    const uint4 c1 = *reinterpret_cast<const uint4*>(ch + srow * 64 + half * 32 + 16);
+                    const __nv_bfloat162 sc =
+                        __bfloat162bfloat162(*reinterpret_cast<const __nv_bfloat16*>(ch + rows * 64 + srow * 2));
+                    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    uint32_t o[32];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {   // 8 columns of the block per code word
+                        const uint4 v = decode_q4_row8(w[u], sc);
+                        o[4 * u] = v.x;
+                        o[4 * u + 1] = v.y;
+                        o[4 * u + 2] = v.z;
+                        o[4 * u + 3] = v.w;
+                    }
+                    tmem_st32(tb + 32 * kb, o);
+                }
+                tmem_wait_st();
+                tmem_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&S.raw_empty[r]);
+                    mbar_arrive(&S.cfull[slot]);
+                }
+                ++cq;
+                rq.next(nraw);
+                continue;
+            }
             const unsigned char* src = raw_slot(r);
 #pragma unroll
             for (int kb = 0; kb < 4; ++kb) {
