@@ -317,6 +317,41 @@ struct RingPos {
     }
 };
 
+// One converter warp, q4t stages: decodes block kb of a stage's packed
+// chunks at src (qch chunks per matrix) for A row i (a row of this warp's
+// lane quarter) and stores its 64 bf16 as 32 columns of tensor memory from
+// tb + 32 kb (the K pair (2j, 2j + 1) in column j, the lower K in the low
+// half).  Phase A: row i = (2g + m) 8 + r is row 8g + r of W_gate (m = 0)
+// or W_up (m = 1).
+__device__ __forceinline__ void q4_block_to_tmem(const unsigned char* src, uint32_t tb, int i, int kb, int qch, bool ph_a) {
+    const int ci = kb >> 1, half = kb & 1;   // chunk of the block, 64-column half of it
+    const int srow = ph_a ? 8 * (i >> 4) + (i & 7) : i;
+    const int rows = ph_a ? 64 : kM;
+    // phase A: W_gate's chunk ci, or W_up's (after W_gate's qch)
+    const unsigned char* ch = ph_a ? src + (((i >> 3) & 1) * qch + ci) * kQ4A : src + ci * kQ4B;
+    const __nv_bfloat162 sc = __bfloat162bfloat162(*reinterpret_cast<const __nv_bfloat16*>(ch + rows * 64 + srow * 2));
+#pragma unroll 1
+    for (int g = 0; g < 2; ++g) {   // 32 columns of the block: 4 code words of 8
+        const uint4 c = *reinterpret_cast<const uint4*>(ch + srow * 64 + half * 32 + 16 * g);
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+        uint32_t o[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint4 v = decode_q4_row8(w[u], sc);
+            o[4 * u] = v.x;
+            o[4 * u + 1] = v.y;
+            o[4 * u + 2] = v.z;
+            o[4 * u + 3] = v.w;
+        }
+        tmem_st16(tb + 32 * kb + 16 * g, o);
+    }
+}
+
+// kInt4: launches with INT4 experts (the packed slots, the converter warps,
+// INT4 stages).  Launches with bf16 experts only run the instantiation
+// without that code, whose warps keep the registers and the instruction
+// footprint that the bf16 stages alone need.
+template <bool kInt4>
 __global__ void __launch_bounds__(kThreads, 1)
 ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const __grid_constant__ CUtensorMap tm_gate,
               const __grid_constant__ CUtensorMap tm_up, const __grid_constant__ CUtensorMap tm_down,
@@ -327,7 +362,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
               const __grid_constant__ CUtensorMap tm_down2) {
     extern __shared__ unsigned char smem_raw[];
     // [stage ring][kRawReserve bytes of packed INT4 slots, with INT4 experts][Smem][tables]
-    const bool has_q4 = A.n_cold > 0;
+    const bool has_q4 = kInt4 && A.n_cold > 0;
     const int ring_bytes = (int)ring_bytes_for((size_t)A.smem_bytes, A.N, has_q4);
     unsigned char* ring = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -351,7 +386,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // Stages of A.kbs blocks (4 where d and d_ff allow them) for bf16 batches
     // of up to 16 tokens.  Launches with INT4 experts keep the packed slots'
     // reserve, which leaves room for only two such stages: they use A.kbl.
-    const bool kbs_stages = small_b && A.n_cold == 0;
+    const bool kbs_stages = small_b && !has_q4;
     // Batches of up to kWholeMax tokens: the phase-A operand is the whole
     // batch (nwb rows, the batch rounded up to 16; the tensor pipe is nearly
     // idle at decode, so multiplying every token costs nothing), each expert
@@ -701,13 +736,13 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 const uint64_t pol = T.nch > 1 ? pol_keep : pol_once;   // chunked experts are re-read from L2
                 const int sl = X.ex_slot[T.a];                          // bf16 expert, or -1 - INT4 expert
                 const int row0 = ph_a ? sl * F + 64 * T.rb : sl * d + kM * T.rb;
-                const int ns = (ph_a ? SA : SB) / (q4t && sl < 0 ? 2 : 1);   // INT4 stages of KBq blocks
+                const int ns = (ph_a ? SA : SB) >> (q4t && sl < 0 ? 1 : 0);   // INT4 stages of KBq blocks
                 for (int s = n == 0 ? fast_stages : 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
                     if (aborted(S)) break;
                     unsigned char* dst = ring + (size_t)slot * slot_bytes;
-                    if (sl < 0) {
+                    if (has_q4 && sl < 0) {
                         // INT4 expert: the packed chunks of the stage's KB blocks are
                         // contiguous per matrix and go to one raw slot; the converter
                         // warps write the bf16 blocks and each arrives on the stage's
@@ -749,7 +784,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     }
                 }
             }
-            {   // no more INT4 chunks: the converter warps stop
+            if (has_q4) {   // no more INT4 chunks: the converter warps stop
                 const int r = rq.slot;
                 if (rq.wrapped) wait_bar(&S.raw_empty[r], rq.phase ^ 1u, S, flags);
                 S.raw_info[r] = ~0u;
@@ -804,7 +839,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 const int nb = wide ? nwb >> 4 : (T.ntok + 15) >> 4;   // 16-row boxes = MMA N / 16
                 // an INT4 stage of a q4t launch: KBq operand blocks at the slot's start
                 const bool pk = q4t && X.ex_slot[T.a] < 0;
-                const int ns = (ph_a ? SA : SB) / (pk ? 2 : 1);
+                const int ns = (ph_a ? SA : SB) >> (pk ? 1 : 0);
                 for (int s = n == 0 ? fast_ops : 0; s < ns; ++s, rp.next(nst)) {
                     const int slot = rp.slot;
                     if (rp.wrapped) wait_bar(&S.empty[slot], rp.phase ^ 1u, S, flags);
@@ -865,14 +900,14 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                 }
                 int ntile = nwb;
                 bool q4 = false;  // INT4 expert: the converter warps write the A operand
-                if (by_count || A.n_cold > 0) {
+                if (by_count || has_q4) {
                     const Tile T = decode_tile(ph_a ? tile : tile - TA, ph_a ? rbA : rbB, X, Tn, nmax);
                     if (by_count) ntile = max(16, (T.ntok + 15) & ~15);
-                    q4 = X.ex_slot[T.a] < 0;
+                    q4 = has_q4 && X.ex_slot[T.a] < 0;
                 }
                 const uint32_t idesc = umma_idesc_bf16(kM, ntile);
                 const bool pk = q4 && q4t;   // A from tensor memory, KBq blocks per stage
-                const int ns = (ph_a ? SA : SB) / (pk ? 2 : 1);
+                const int ns = (ph_a ? SA : SB) >> (pk ? 1 : 0);
                 const int b = n % kAcc;
                 if (n >= kAcc) {   // the epilogue has read this accumulator's previous tile
                     wait_bar(&S.acc_empty[b], ((n / kAcc) - 1) & 1, S, flags);
@@ -962,7 +997,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
         RingPos rq;
         uint32_t cq = 0;   // INT4 stages decoded so far (q4t launches)
         for (;;) {
-            if (A.n_cold == 0) break;                  // no INT4 experts in this launch
+            if (!has_q4) break;                        // no INT4 experts in this launch
             const int r = rq.slot;
             wait_bar(&S.raw_full[r], rq.phase, S, flags);
             if (*(volatile int*)&S.abort_flag) break;
@@ -994,30 +1029,10 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     if (*(volatile int*)&S.abort_flag) break;
                     tmem_fence_after_sync();
                 }
-                const int srow = ph_a ? 8 * (i >> 4) + (i & 7) : i;
                 const uint32_t tb = tmem + ((uint32_t)(32 * qd) << 16) + kTmA + (cq & 1u) * kTmAStride;
 #pragma unroll 1
-                for (int h = 0; h < KBq / 2; ++h) {
-                    const int kb = grp * (KBq / 2) + h;
-                    const int ci = kb >> 1, half = kb & 1;   // chunk of the block, 64-column half of it
-                    // phase A: W_gate's chunk ci, or W_up's (after W_gate's qch)
-                    const unsigned char* ch = ph_a ? src + (((i >> 3) & 1) * qch + ci) * kQ4A : src + ci * kQ4B;
-                    const uint4 c0 = *reinterpret_cast<const uint4*>(ch + srow * 64 + half * 32);
-                    const uint4 c1 = *reinterpret_cast<const uint4*>(ch + srow * 64 + half * 32 + 16);
-                    const __nv_bfloat162 sc =
-                        __bfloat162bfloat162(*reinterpret_cast<const __nv_bfloat16*>(ch + rows * 64 + srow * 2));
-                    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                    uint32_t o[32];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {   // 8 columns of the block per code word
-                        const uint4 v = decode_q4_row8(w[u], sc);
-                        o[4 * u] = v.x;
-                        o[4 * u + 1] = v.y;
-                        o[4 * u + 2] = v.z;
-                        o[4 * u + 3] = v.w;
-                    }
-                    tmem_st32(tb + 32 * kb, o);
-                }
+                for (int h = 0; h < KBq / 2; ++h)
+                    q4_block_to_tmem(src, tb, i, grp * (KBq / 2) + h, qch, ph_a);
                 tmem_wait_st();
                 tmem_fence_before_sync();
                 __syncwarp();
@@ -1261,15 +1276,16 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
     if (!smem_optin[dev]) {
         int v = 0;
         if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
-        if ((e = cudaFuncSetAttribute(ffn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, v)) != cudaSuccess)
-            return e;
-        // The CTAs wait for one another, so the grid (one CTA per SM) must be
-        // able to be resident at once: one CTA of this size has to fit an SM.
-        int per_sm = 0;
-        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_tc_kernel, kThreads, (size_t)v)) !=
-            cudaSuccess)
-            return e;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        for (auto* kern : {ffn_tc_kernel<false>, ffn_tc_kernel<true>}) {
+            if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, v)) != cudaSuccess)
+                return e;
+            // The CTAs wait for one another, so the grid (one CTA per SM) must
+            // be able to be resident at once: one CTA of this size has to fit an SM.
+            int per_sm = 0;
+            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, (size_t)v)) != cudaSuccess)
+                return e;
+            if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        }
         smem_optin[dev] = v;
     }
     FfnArgs a = a_in;
@@ -1294,7 +1310,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_tc_kernel, a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+    return cudaLaunchKernelEx(&cfg, a.n_cold > 0 ? ffn_tc_kernel<true> : ffn_tc_kernel<false>, a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
                               maps[6], maps[7], maps[8], maps[9], maps[10], maps[11], maps[12]);
 }
 
