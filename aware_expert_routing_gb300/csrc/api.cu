@@ -280,9 +280,11 @@ int large_batch_blocks(int d, int F) { return ((d / 64) % 2 == 0 && (F / 64) % 2
 struct TcMapEntry {
     MapKey key;
     // gate/up 5D (or W_gate 8-row boxes), W_up 8-row boxes, W_down 128-row boxes
-    // (one block wide); gate/up 5D and W_down as many blocks wide as small
-    // batches use, then as many as larger batches use
-    CUtensorMap maps[7];
+    // (one block wide); gate/up 5D (or W_gate 8-row boxes) and W_down as many
+    // blocks wide as small batches use, then as many as larger batches use;
+    // W_up 8-row boxes as wide as small, then as larger batches use (read
+    // when W_gate and W_up cannot share the 5D map)
+    CUtensorMap maps[9];
     bool fused, swap, used;
 };
 TcMapEntry g_tc_maps[64];
@@ -313,18 +315,22 @@ moe_status tc_expert_maps(const void* g, const void* u, const void* dn, int N, i
     if (!encode_3d(&e.maps[1], u, d, (uint64_t)N * F, 8, 1) || !encode_3d(&e.maps[2], dn, F, (uint64_t)N * d, 128, 1))
         return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_up / W_down)");
     const uint32_t kb = (uint32_t)small_batch_blocks(d, F);
-    e.maps[3] = e.maps[0];
-    bool swap4 = false;
-    if (e.fused && !encode_gate_up_5d(&e.maps[3], g, u, d, (uint64_t)N * F, &swap4, kb))
-        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_gate / W_up, wide boxes)");
-    if (!encode_3d(&e.maps[4], dn, F, (uint64_t)N * d, 128, kb))
-        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_down, wide boxes)");
     const uint32_t kbl = (uint32_t)large_batch_blocks(d, F);
-    e.maps[5] = e.maps[0];
-    if (e.fused && !encode_gate_up_5d(&e.maps[5], g, u, d, (uint64_t)N * F, &swap4, kbl))
-        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_gate / W_up, 2-block boxes)");
-    if (!encode_3d(&e.maps[6], dn, F, (uint64_t)N * d, 128, kbl))
-        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_down, 2-block boxes)");
+    bool swap4 = false;
+    if (e.fused) {
+        if (!encode_gate_up_5d(&e.maps[3], g, u, d, (uint64_t)N * F, &swap4, kb) ||
+            !encode_gate_up_5d(&e.maps[5], g, u, d, (uint64_t)N * F, &swap4, kbl))
+            return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_gate / W_up, wide boxes)");
+        e.maps[7] = e.maps[1];   // not read
+        e.maps[8] = e.maps[1];
+    } else if (!encode_3d(&e.maps[3], g, d, (uint64_t)N * F, 8, kb) ||
+               !encode_3d(&e.maps[5], g, d, (uint64_t)N * F, 8, kbl) ||
+               !encode_3d(&e.maps[7], u, d, (uint64_t)N * F, 8, kb) ||
+               !encode_3d(&e.maps[8], u, d, (uint64_t)N * F, 8, kbl)) {
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_gate / W_up, 8-row wide boxes)");
+    }
+    if (!encode_3d(&e.maps[4], dn, F, (uint64_t)N * d, 128, kb) || !encode_3d(&e.maps[6], dn, F, (uint64_t)N * d, 128, kbl))
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (W_down, wide boxes)");
     e.used = true;
     memcpy(out, e.maps, sizeof e.maps);
     *fused = e.fused;
@@ -511,9 +517,9 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
     if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the SM count");
     if (sms > kMaxGrid) sms = kMaxGrid;
     {   // the tcgen05 expert kernel (bf16 experts, and INT4 experts through its converter warps)
-        CUtensorMap maps[13];
+        CUtensorMap maps[15];
         bool fused = false, swap = false;
-        CUtensorMap wm[7], om[5];
+        CUtensorMap wm[9], om[5];
         if ((st = tc_expert_maps(w_gate, w_up, w_down, n_hot, d_ff, P.d, dev, wm, &fused, &swap)) != MOE_OK) return st;
         if ((st = tc_operand_maps(ws, L, hidden, P.B * P.kslots, P.B, P.d, d_ff, dev, a.n_cold > 0, om)) != MOE_OK)
             return st;
@@ -530,6 +536,8 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
         maps[10] = om[4];                      // h, kb blocks wide
         maps[11] = wm[5];                      // gate/up 5D, 2 blocks wide (larger batches)
         maps[12] = wm[6];                      // W_down, 2 blocks wide (larger batches)
+        maps[13] = wm[7];                      // W_up 8-row boxes, kb blocks wide (read when not fused)
+        maps[14] = wm[8];                      // W_up 8-row boxes, 2 blocks wide (read when not fused)
         a.gu_fused = fused ? 1 : 0;
         a.gu_swap = swap ? 1 : 0;
         a.kbs = small_batch_blocks(P.d, d_ff);

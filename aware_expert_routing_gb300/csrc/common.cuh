@@ -170,13 +170,16 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 bool route_fused_supported(int dtype, int B, int N, int kslots);
 cudaError_t launch_route_fused(const RouterArgs& r, const RouteArgs& a, cudaStream_t s);
 // tcgen05 expert kernel (bf16 weights).  maps[0..6]: W_gate/W_up
-// interleaved 8 rows at a time (5D, gu_fused) or W_gate and W_up alone
-// (8-row boxes), W_down (128-row boxes), gathered hidden states and h
-// (16-row boxes) and the hidden states (the whole batch of up to 64 tokens
-// in one box), all one 64-column block wide; maps[7..10]: the 5D gate/up
-// map, W_down, the hidden states (as wide as the launch's stages) and h
-// with boxes kbs blocks wide (batches of up to 16 tokens); maps[11..12]: the 5D gate/up map and
-// W_down with boxes kbl blocks wide (larger batches).
+// interleaved 8 rows at a time (5D, gu_fused) or W_gate alone (8-row
+// boxes), the same again (not read), W_up (8-row boxes), W_down (128-row
+// boxes), gathered hidden states and h (16-row boxes) and the hidden states
+// (the whole batch of up to 64 tokens in one box), all one 64-column block
+// wide; maps[7..10]: the 5D gate/up map (or W_gate's 8-row map), W_down,
+// the hidden states (as wide as the launch's stages) and h with boxes kbs
+// blocks wide (batches of up to 16 tokens); maps[11..12]: the 5D gate/up
+// map (or W_gate's) and W_down with boxes kbl blocks wide (larger batches);
+// maps[13..14]: W_up's 8-row map kbs, then kbl blocks wide (read when
+// W_gate and W_up cannot share the 5D map).
 cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap* maps, int num_sms, cudaStream_t s);
 cudaError_t launch_ffn_f32(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_synth(void* dst, int dtype, uint64_t n, uint64_t start, uint64_t seed,
@@ -293,6 +296,14 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, i
 // row is added to the start address.
 __device__ __forceinline__ uint64_t umma_sdesc_sw128(uint32_t saddr) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// The same with the 8-row groups `sbo` bytes apart (a multiple of 1024
+// below 256 KB): an operand whose 1024-byte swizzle atoms are interleaved
+// with those of other K blocks.
+__device__ __forceinline__ uint64_t umma_sdesc_sw128_sbo(uint32_t saddr, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 

@@ -317,6 +317,23 @@ struct RingPos {
     }
 };
 
+// Phase-A weights of one stage when W_gate and W_up have separate maps
+// (8-row boxes, kb blocks wide): for each of the tile's 8 row groups g, the
+// g-th 8 rows of W_gate then of W_up, each box landing as kb consecutive
+// 1024-byte swizzle atoms (one per K block).  Atom (j, b) of row-group slot
+// j = 2g + m (m = 0: W_gate, 1: W_up) and block b sits at (j kb + b) x 1024,
+// so block b's 128 A rows are 8-row groups kb x 1024 apart, in the same
+// interleaved row order as the 5D map's.
+__device__ __forceinline__ void load_gate_up_groups(unsigned char* dst, const CUtensorMap* m_gate,
+                                                    const CUtensorMap* m_up, int row0, int blk, int kb,
+                                                    uint64_t* bar, uint64_t pol) {
+#pragma unroll 1
+    for (int g = 0; g < 8; ++g) {
+        tma_load_3d(dst + (2 * g) * kb * 1024, m_gate, 0, row0 + 8 * g, blk, bar, pol);
+        tma_load_3d(dst + (2 * g + 1) * kb * 1024, m_up, 0, row0 + 8 * g, blk, bar, pol);
+    }
+}
+
 // One converter warp, q4t stages: decodes block kb of a stage's packed
 // chunks at src (qch chunks per matrix) for A row i (a row of this warp's
 // lane quarter) and stores its 64 bf16 as 32 columns of tensor memory from
@@ -359,7 +376,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
               const __grid_constant__ CUtensorMap tm_hid, const __grid_constant__ CUtensorMap tm_gu4,
               const __grid_constant__ CUtensorMap tm_down4, const __grid_constant__ CUtensorMap tm_hid4,
               const __grid_constant__ CUtensorMap tm_h4, const __grid_constant__ CUtensorMap tm_gu2,
-              const __grid_constant__ CUtensorMap tm_down2) {
+              const __grid_constant__ CUtensorMap tm_down2, const __grid_constant__ CUtensorMap tm_up4,
+              const __grid_constant__ CUtensorMap tm_up2) {
     extern __shared__ unsigned char smem_raw[];
     // [stage ring][kRawReserve bytes of packed INT4 slots, with INT4 experts][Smem][tables]
     const bool has_q4 = kInt4 && A.n_cold > 0;
@@ -393,8 +411,11 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // is one token chunk, and h is stored for the expert's own tokens only.
     const bool whole = A.B <= kWholeMax;
     const int nwb = max(16, (A.B + 15) & ~15);
-    const int KB = A.gu_fused ? (kbs_stages ? A.kbs : A.kbl) : 1;
-    const CUtensorMap* const m_gu = KB == 1 ? &tm_gu : kbs_stages ? &tm_gu4 : &tm_gu2;       // weight maps, KB wide
+    const int KB = kbs_stages ? A.kbs : A.kbl;
+    // weight maps, KB blocks wide: the 5D gate/up map (or, when W_gate and
+    // W_up cannot share one, W_gate's and W_up's 8-row maps) and W_down's
+    const CUtensorMap* const m_gu = KB == 1 ? &tm_gu : kbs_stages ? &tm_gu4 : &tm_gu2;
+    const CUtensorMap* const m_up = KB == 1 ? &tm_up : kbs_stages ? &tm_up4 : &tm_up2;
     const CUtensorMap* const m_down = KB == 1 ? &tm_down : kbs_stages ? &tm_down4 : &tm_down2;
     // Batches of up to 48 tokens with INT4 experts: an INT4 stage spans
     // KBq = 2 KB blocks and its ring slot holds the token rows of those
@@ -413,8 +434,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
     // the first copies (which the early start issues the moment the
     // activated experts are known) then find them cached.
     if (warp == kWarpW && lane == 0) {
-        prefetch_tensormap(A.gu_fused ? m_gu : &tm_gate);
-        if (!A.gu_fused) prefetch_tensormap(&tm_up);
+        prefetch_tensormap(m_gu);
+        if (!A.gu_fused) prefetch_tensormap(m_up);
         prefetch_tensormap(m_down);
     }
     if (warp == kWarpO && lane == 0) {
@@ -538,10 +559,7 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     if (A.gu_fused) {
                         tma_load_5d(dst, m_gu, 0, 0, 0, row0 / 8, s * KB, &S.full[s], pol);
                     } else {
-                        for (int g = 0; g < 8; ++g) {
-                            tma_load_3d(dst + (2 * g) * 1024, &tm_gate, 0, row0 + 8 * g, s, &S.full[s], pol);
-                            tma_load_3d(dst + (2 * g + 1) * 1024, &tm_up, 0, row0 + 8 * g, s, &S.full[s], pol);
-                        }
+                        load_gate_up_groups(dst, m_gu, m_up, row0, s * KB, KB, &S.full[s], pol);
                     }
                 }
                 S.fast_ops = fast_stages;   // read by the operand warp after the barrier below
@@ -775,12 +793,8 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                     } else if (A.gu_fused) {
                         // 8 row groups x {8 rows of the lower matrix, 8 rows of the other}
                         tma_load_5d(dst, m_gu, 0, 0, 0, row0 / 8, s * KB, &S.full[slot], pol);
-                    } else {   // KB = 1
-#pragma unroll 1
-                        for (int g = 0; g < 8; ++g) {
-                            tma_load_3d(dst + (2 * g) * 1024, &tm_gate, 0, row0 + 8 * g, s, &S.full[slot], pol);
-                            tma_load_3d(dst + (2 * g + 1) * 1024, &tm_up, 0, row0 + 8 * g, s, &S.full[slot], pol);
-                        }
+                    } else {
+                        load_gate_up_groups(dst, m_gu, m_up, row0, s * KB, KB, &S.full[slot], pol);
                     }
                 }
             }
@@ -939,11 +953,18 @@ ffn_tc_kernel(const FfnArgs A, const __grid_constant__ CUtensorMap tm_gu, const 
                         continue;
                     }
                     const uint32_t b0 = a0 + KB * kWBytes;
+                    // bf16 phase-A stages of separate W_gate / W_up maps hold
+                    // their K blocks' swizzle atoms interleaved (see
+                    // load_gate_up_groups): block kb at kb x 1024, 8-row
+                    // groups KB x 1024 apart
+                    const bool grouped = ph_a && !q4 && !A.gu_fused;
+                    const uint32_t a_blk = grouped ? 1024u : (uint32_t)kWBytes;
+                    const uint32_t a_sbo = grouped ? 1024u * KB : 1024u;
 #pragma unroll 1
                     for (int kb = 0; kb < KB; ++kb) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)   // K = 16 per step: 32 bytes along the swizzled row
-                            umma_bf16(dt, umma_sdesc_sw128(a0 + kb * kWBytes + 32 * k),
+                            umma_bf16(dt, umma_sdesc_sw128_sbo(a0 + kb * a_blk + 32 * k, a_sbo),
                                       umma_sdesc_sw128(b0 + kb * obytes + 32 * k), idesc, (s | kb | k) ? 1u : 0u);
                     }
                     umma_commit(&S.empty[slot]);   // the stage is free once these MMAs are done
@@ -1291,7 +1312,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
     FfnArgs a = a_in;
     a.smem_bytes = smem_optin[dev];
     // the ring must hold two stages of the largest slot this launch can use
-    const int kb = a.gu_fused ? (a.B <= 16 && a.n_cold == 0 ? a.kbs : a.kbl) : 1;
+    const int kb = a.B <= 16 && a.n_cold == 0 ? a.kbs : a.kbl;
     const int nwb = a.B <= 16 ? 16 : (a.B + 15) & ~15;
     const size_t slot = (size_t)kb * (kWBytes + (a.B <= kWholeMax ? nwb : kNMax) * 128);
     if ((size_t)a.smem_bytes < 4096 + tabs_bytes(a.N) + (size_t)kRawReserve ||
@@ -1311,7 +1332,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a_in, const CUtensorMap* maps, int num_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, a.n_cold > 0 ? ffn_tc_kernel<true> : ffn_tc_kernel<false>, a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
-                              maps[6], maps[7], maps[8], maps[9], maps[10], maps[11], maps[12]);
+                              maps[6], maps[7], maps[8], maps[9], maps[10], maps[11], maps[12], maps[13], maps[14]);
 }
 
 }  // namespace moe

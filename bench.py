@@ -321,7 +321,12 @@ def build_mixed(moe, torch, w: synth.Workload, layer: int, D: dict, dev):
     for i, e in enumerate(cold):
         slot[e] = -1 - i
     hot_idx = torch.tensor(hot, device=dev)
-    pools = {k: D[k].index_select(0, hot_idx).contiguous() for k in ("w_gate", "w_up", "w_down")}
+    # W_gate's and W_up's pools as the two halves of one buffer (one tensor
+    # map then reads both; see w_up in include/moe.h)
+    gu = torch.empty((2, len(hot)) + tuple(D["w_gate"].shape[1:]), dtype=D["w_gate"].dtype, device=dev)
+    torch.index_select(D["w_gate"], 0, hot_idx, out=gu[0])
+    torch.index_select(D["w_up"], 0, hot_idx, out=gu[1])
+    pools = {"w_gate": gu[0], "w_up": gu[1], "w_down": D["w_down"].index_select(0, hot_idx).contiguous()}
     u8 = dict(dtype=torch.uint8, device=dev)
     q = {"w_gate": torch.empty(len(cold), moe.int4_image_bytes(w.F, w.d), **u8),
          "w_up": torch.empty(len(cold), moe.int4_image_bytes(w.F, w.d), **u8),

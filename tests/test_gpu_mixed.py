@@ -24,9 +24,11 @@ def built():
     moe.load()
 
 
-def build_mixed(w, L, hot, active=None):
+def build_mixed(w, L, hot, active=None, alias_up=False):
     """Device buffers of a mixed layer and the oracle's effective weights.
-    Cold experts outside `active` (if given) get zero images (never read)."""
+    Cold experts outside `active` (if given) get zero images (never read).
+    alias_up: the hot experts' W_up is their W_gate buffer (separate 8-row
+    gate/up maps in the kernel); L's w_up must then equal its w_gate."""
     N, d, F = w.N, w.d, w.F
     hot = list(hot)
     cold = [e for e in range(N) if e not in hot]
@@ -51,6 +53,9 @@ def build_mixed(w, L, hot, active=None):
     bf = torch.bfloat16
     dev = gu.DEV
     hot_w = {k: torch.from_numpy(L[k][hot]).to(dev).to(bf).contiguous() for k in ("w_gate", "w_up", "w_down")}
+    if alias_up:
+        assert np.array_equal(L["w_up"], L["w_gate"])
+        hot_w["w_up"] = hot_w["w_gate"]
     mixed = moe.MixedExperts(torch.from_numpy(slot).to(dev),
                              torch.from_numpy(qg).to(dev), torch.from_numpy(qu).to(dev),
                              torch.from_numpy(qd).to(dev), len(hot), len(cold))
@@ -86,6 +91,27 @@ def test_mixed_layer_parity(mode, k0, p, B):
     ref_bf16 = oracle.moe_experts(L["x"], L["w_gate"], L["w_up"], L["w_down"], g["expert_idx"],
                                   g["weights"].astype(np.float64))
     assert np.abs(ref - ref_bf16).max() > 1e-3 * np.abs(ref_bf16).max()
+
+
+@pytest.mark.parametrize("mode,B", [(OEA, 8), (TOPK, 32), (OEA, 64), (TOPK, 80)])
+def test_mixed_separate_gate_up_maps(mode, B):
+    # Hot experts whose W_gate and W_up cannot share one 5D map (W_up passed
+    # as W_gate's buffer): their stages load 8-row groups of each, K blocks
+    # per load; INT4 stages are unchanged (decoded into shared or tensor
+    # memory).
+    w = synth.Workload("t_mixed_sep", N=32, k=4, d=512, F=256, B=B, seed=43 + B, zipf=True)
+    L = synth.make_layer(w, 0, B)
+    L = dict(L, w_up=L["w_gate"].copy())
+    hot = [0, 3, 4, 9, 10, 11, 17, 20, 25, 31]
+    hot_w, mixed, eff = build_mixed(w, L, hot, alias_up=True)
+    D = gu.device_inputs(L, True)
+    prm = gu.params_for(w, B, mode, 3 if mode == OEA else 4, 1.0)
+    r, out = run_mixed(w, L, D, hot_w, mixed, prm)
+    g = gu.to_np(r)
+    gu.check_routing(g, prm, B)
+    ref = oracle.moe_experts(L["x"], eff["w_gate"], eff["w_up"], eff["w_down"], g["expert_idx"],
+                             g["weights"].astype(np.float64))
+    gu.check_output(out, ref, True)
 
 
 @pytest.mark.parametrize("d,F,B", [(512, 256, 8), (384, 128, 16), (512, 256, 1), (256, 384, 5)])

@@ -35,9 +35,13 @@ def W(name, **kw):
     return synth.Workload(name, **base)
 
 
-def run_case(w, B, mode, k0=None, p=1.0, maxP=0, kmax=0, B_valid=-1, L=None, check_e2e=True):
+def run_case(w, B, mode, k0=None, p=1.0, maxP=0, kmax=0, B_valid=-1, L=None, check_e2e=True, alias_up=False):
     L = L if L is not None else synth.make_layer(w, 0, B)
+    if alias_up:   # W_up is W_gate's own device buffer
+        L = dict(L, w_up=L["w_gate"])
     D = gu.device_inputs(L, w.bf16)
+    if alias_up:
+        D["w_up"] = D["w_gate"]
     prm = gu.params_for(w, B, mode, k0, p, maxP, kmax, B_valid)
     r, out, ws, flags = gu.run_layer(w, D, prm)
     assert flags == 0, f"device flags {flags:#x}"
@@ -104,6 +108,21 @@ def test_whole_batch_boundaries(B):
     w = W("t_whole", N=512, k=8, d=512, F=256, seed=100 + B, zipf=True)
     run_case(w, B, OEA, 4, 1.0)
     run_case(w, B, TOPK)
+
+
+@pytest.mark.parametrize("B,d,F", [(8, 512, 256), (16, 384, 128), (32, 512, 256), (48, 256, 384), (65, 512, 256),
+                                   (130, 320, 192)])
+def test_separate_gate_up_maps(B, d, F):
+    # W_gate and W_up share one interleaving 5D tensor map when they lie
+    # less than 2^40 bytes apart and not at the same address; otherwise
+    # (separate allocations in distant address ranges, or here W_up passed
+    # as W_gate's own buffer) the kernel loads each 8-row group of both
+    # through 8-row maps, all of a stage's K blocks per load.  Stages of 4
+    # (B=8), 2 and 1 (d=320, F=192) blocks; whole batches and the
+    # expert-grouped copy.
+    w = W("t_sep_gu", N=64, k=8, d=d, F=F, seed=300 + B, zipf=True)
+    run_case(w, B, OEA, 3, 1.0, alias_up=True)
+    run_case(w, B, TOPK, alias_up=True)
 
 
 @pytest.mark.parametrize("N,k,d,F", [(16, 4, 64, 64), (160, 6, 320, 192), (1024, 8, 128, 64),
