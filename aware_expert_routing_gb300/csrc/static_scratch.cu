@@ -11,7 +11,6 @@
 // allocating library routine.
 #include <cstddef>
 #include <cstdio>
-#include <mutex>
 
 #include "common.cuh"
 
@@ -26,24 +25,15 @@ namespace {
 constexpr size_t kScratchBytes = MOE_STATIC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-// Device address of g_scratch, looked up once per device (with that device
-// current).  In host code the symbol is only a host-side stand-in.
-std::mutex g_mu;
-void* g_scratch_ptr[64] = {};
-
+// Device address of g_scratch on the current device (in host code the
+// symbol is only a host-side stand-in).  Looked up on every call: the lookup
+// allocates nothing, and an address kept across calls would be stale after
+// the device's context is reset and the module loaded again.
 moe_status scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return moe::report_error(MOE_ERR_CUDA, cudaGetErrorString(e));
-    if (dev < 0 || dev >= 64) return moe::report_error(MOE_ERR_UNSUPPORTED, "device index above 63");
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess) return moe::report_error(MOE_ERR_CUDA, cudaGetErrorString(e));
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return MOE_OK;
 }
 

@@ -412,12 +412,11 @@ moe_status moe_decode_layer(const void *hidden, const void *w_router, const floa
  *   - A batch whose workspace (moe_workspace_bytes) exceeds
  *     MOE_STATIC_SCRATCH_BYTES is rejected with MOE_ERR_WORKSPACE before
  *     anything is launched.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current) and keeps it for the life of
- *     the process; make that first call before any stream capture, and do
- *     not use this call across a reset of the device (cudaDeviceReset, or
- *     the primary context torn down and recreated), after which the kept
- *     address no longer names the array.
+ *   - Every call looks up the array's device address on the current device
+ *     (no allocation).  The first call on a device may load the library's
+ *     device code, so make it before any stream capture.  After a reset of
+ *     the device (cudaDeviceReset, or the primary context torn down and
+ *     recreated) the next call finds the array again, zeroed.
  *   - All calls on a device share its array, which keeps the last call's
  *     contents; the counters at its front are cleared on `stream` at every
  *     call.  Calls that overlap on the GPU (for example on two streams) race
