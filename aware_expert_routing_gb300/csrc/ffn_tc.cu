@@ -32,7 +32,8 @@
 //   * Warp 4 claims the tiles, posts them to a 16-entry shared-memory queue
 //     and streams the weights: one TMA operation per stage of KB blocks of
 //     128 rows x 64 columns (128-byte swizzle; the gate/up interleave comes
-//     from one 5D tensor map over both matrices).  A TMA unit's rate per SM
+//     from one 5D tensor map over both matrices, or, where the two cannot
+//     share one, from 16 copies of 8-row groups, KB blocks each).  A TMA unit's rate per SM
 //     grows with the bytes of each operation, so batches of up to 16 tokens
 //     use KB = 4 (64 KB per operation) where d and d_ff allow it, larger
 //     batches KB = 2 where both are even.  Warp 5 streams the token rows of
@@ -55,15 +56,19 @@
 //     128).
 //     tcgen05.commit frees each stage when its MMAs have completed and marks
 //     a tile's accumulator full.
-//   * INT4 experts (DynaExq page, section 3.2): warp 4 bulk-copies the
-//     packed 128-column chunks of a stage's K blocks into a raw ring of up
-//     to 16 slots (the stage ring's unused tail holds all but one or two)
-//     and arrives on the stage barrier without bytes; warps 7-14 decode each
-//     chunk together (exact integer codes, times the row's group scale,
-//     rounded once to bf16) into the stage's 128-byte-swizzled A operand,
-//     fence it for the tensor core's async proxy, and after the stage's last
-//     block each arrives on the stage's cfull barrier, which the MMA thread
-//     waits on besides the stage barrier.
+//   * INT4 experts (DynaExq page, section 3.2; compiled into the kInt4
+//     instantiation only): warp 4 bulk-copies the packed 128-column chunks
+//     of a stage's K blocks into a raw ring of up to 16 slots (the stage
+//     ring's unused tail holds all but one or two) and arrives on the stage
+//     barrier without bytes; warps 7-14 decode each chunk together (exact
+//     integer codes, times the row's group scale, rounded once to bf16)
+//     into the stage's 128-byte-swizzled A operand, fence it for the tensor
+//     core's async proxy, and after the stage's last block each arrives on
+//     the stage's cfull barrier, which the MMA thread waits on besides the
+//     stage barrier.  Batches of up to 48 tokens: an INT4 stage spans twice
+//     the K blocks, its packed chunks land in its own ring slot after the
+//     token rows, and the converters write the decoded A operand into one of
+//     two tensor-memory buffers, from which the MMAs read it.
 //   * Warps 0-3 (tensor-memory lanes 32w..32w+31, one D row per thread)
 //     read a finished accumulator with tcgen05.ld and free it; phase A:
 //     the lane holding gate row r takes the matching up row from the lane
@@ -80,8 +85,9 @@
 //     the y rows in slot order, writes the output rows and restores the
 //     counter for the next launch.
 //   * All phase-A tiles precede all phase-B tiles in the list and wait on
-//     nothing later, so every wait ends.  The last CTA to finish resets the
-//     tile and chunk counters for the next launch.
+//     nothing later, so every wait ends.  Nothing is reset at the end: the
+//     routing call that precedes the next launch zeroes the tile and chunk
+//     counters of the set that launch uses.
 // Every wait is bounded; a wait that gives up raises MOE_FLAG_WAIT_TIMEOUT
 // and the CTA runs to its end without waiting again.
 #include "common.cuh"

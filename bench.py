@@ -114,11 +114,38 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments (string and character literals
+    kept as they are), whitespace runs collapsed to one space."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(source: str = "ffn_tc.cu") -> str:
+    """Hash of the expert kernel's code (its source and common.cuh, comments
+    and layout left out): an ncu record taken from other code is not used."""
     h = hashlib.sha256()
     for f in (source, "common.cuh"):
-        with open(os.path.join(ROOT, "aware_expert_routing_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "aware_expert_routing_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -32,3 +32,16 @@ def test_linearity_points_are_distinct():
             assert max(pts) <= 8
         else:
             assert max(pts) == 128
+
+
+def test_strip_comments_keeps_code_and_literals():
+    """The ncu record's source hash ignores comments and layout but not
+    code: comment markers inside string or character literals are code."""
+    src = ('int a = 1;  // one\n/* two\n   lines */ const char* s = "x // y /* z */";\n'
+           "char q = '/'; char e = '\\''; const char* t = \"esc \\\" // still\";\n")
+    got = bench.strip_comments(src)
+    assert got == ('int a = 1; const char* s = "x // y /* z */"; char q = \'/\'; char e = \'\\\'\'; '
+                   'const char* t = "esc \\" // still";')
+    assert bench.strip_comments("a  =\n b; // c") == bench.strip_comments("a =  b;")
+    assert bench.strip_comments("a = b;") != bench.strip_comments("a = c;")
+    assert "record" not in bench.strip_comments("x = 1; // record\ny = 2;")
