@@ -524,7 +524,7 @@ moe_status expert_ffn_impl(const void* hidden, const void* w_gate, const void* w
         if ((st = tc_operand_maps(ws, L, hidden, P.B * P.kslots, P.B, P.d, d_ff, dev, a.n_cold > 0, om)) != MOE_OK)
             return st;
         maps[0] = wm[0];                       // gate/up 5D, or W_gate
-        maps[1] = wm[0];                       // W_gate (8-row boxes; read when not fused)
+        maps[1] = wm[0];                       // not read (the kernel takes W_gate's 8-row map from maps[0])
         maps[2] = wm[1];                       // W_up
         maps[3] = wm[2];                       // W_down
         maps[4] = om[0];                       // grouped hidden states
